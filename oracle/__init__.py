@@ -1,0 +1,130 @@
+"""Oracle for the hierarchical beam-search step: TEST INFRASTRUCTURE ONLY.
+
+Only the tests, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline /
+reference legs may import this package.  The product path (the CUDA library and
+its binding in ``serving_ls_beam_gb300``) never imports it and shares no code
+with it.
+
+The arithmetic lives in ``ls_beam_oracle.c`` (plain single-threaded C, fp64),
+which restates the naive decoding definition from the LightSeq inference
+article (31duo.com, itemid-283120, section on the hierarchical rewrite of
+decoding).  This module only compiles it with gcc and marshals numpy arrays.
+
+Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
+(brute force, closed forms, invariants, library routines).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ls_beam_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2}
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no FMA contraction, so x86 and Arm agree)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.run(
+            ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"],
+            check=True,
+        )
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            vp, ip = ctypes.c_void_p, ctypes.c_int
+            lib.oracle_beam_step.argtypes = [vp, ip, vp, vp, vp, ip, ip, ip, ip, ip, vp, vp, vp, vp, vp]
+            lib.oracle_beam_step.restype = ip
+            lib.oracle_rtopk_stats.argtypes = [vp, ip, vp, ip, ip, ip, ip, vp, vp, vp]
+            lib.oracle_rtopk_stats.restype = ip
+            lib.oracle_cache_reorder.argtypes = [vp, vp, ip, vp, ip, ip, ip, ip, ip, ip, ip]
+            lib.oracle_cache_reorder.restype = ip
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _logit_code(logits: np.ndarray, dtype: str | None) -> tuple[np.ndarray, int]:
+    if logits.dtype == np.float32:
+        return np.ascontiguousarray(logits), DTYPE_CODES["f32"]
+    if logits.dtype == np.float16:
+        return np.ascontiguousarray(logits).view(np.uint16), DTYPE_CODES["f16"]
+    if logits.dtype == np.uint16 and dtype in ("f16", "bf16"):
+        return np.ascontiguousarray(logits), DTYPE_CODES[dtype]
+    raise TypeError(f"unsupported logits dtype {logits.dtype} / {dtype}")
+
+
+def beam_step(logits, beam_scores, *, bias=None, finished=None, eos_id=0, m_out=None, dtype=None):
+    """Naive beam step.  Returns dict of per-batch sorted lists of length m_out (default k):
+    token, parent (int32), score (float64), finished (uint8), and lse [batch, k] (float64)."""
+    lib = _load()
+    lg, code = _logit_code(np.asarray(logits), dtype)
+    batch, k, vocab = lg.shape
+    m_out = k if m_out is None else int(m_out)
+    bs = np.ascontiguousarray(beam_scores, dtype=np.float32).reshape(batch, k)
+    bi = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32).reshape(vocab)
+    fin = None if finished is None else np.ascontiguousarray(finished, dtype=np.uint8).reshape(batch, k)
+    tok = np.empty((batch, m_out), np.int32)
+    par = np.empty((batch, m_out), np.int32)
+    sc = np.empty((batch, m_out), np.float64)
+    of = np.empty((batch, m_out), np.uint8)
+    lse = np.empty((batch, k), np.float64)
+    rc = lib.oracle_beam_step(_ptr(lg), code, _ptr(bi), _ptr(bs), _ptr(fin), batch, k, vocab, int(eos_id),
+                              m_out, _ptr(tok), _ptr(par), _ptr(sc), _ptr(of), _ptr(lse))
+    if rc != 0:
+        raise ValueError(f"oracle_beam_step failed ({rc})")
+    return {"token": tok, "parent": par, "score": sc, "finished": of, "lse": lse}
+
+
+def rtopk_stats(logits, k, *, groups=None, bias=None, dtype=None):
+    """Per-row first-traversal diagnostics: R (k-th largest of group maxima), true k-th largest, count x >= R."""
+    lib = _load()
+    lg, code = _logit_code(np.asarray(logits), dtype)
+    vocab = lg.shape[-1]
+    rows = lg.size // vocab
+    groups = k if groups is None else int(groups)
+    bi = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32).reshape(vocab)
+    R = np.empty(rows, np.float64)
+    kth = np.empty(rows, np.float64)
+    nc = np.empty(rows, np.int64)
+    rc = lib.oracle_rtopk_stats(_ptr(lg), code, _ptr(bi), rows, int(k), vocab, groups, _ptr(R), _ptr(kth), _ptr(nc))
+    if rc != 0:
+        raise ValueError(f"oracle_rtopk_stats failed ({rc})")
+    return {"R": R, "kth": kth, "ncand": nc}
+
+
+def cache_reorder(src, parent, length, dst=None):
+    """Gather of the [layers, batch*k, heads, max_len, head_dim] cache by parent beam (positions < length)."""
+    lib = _load()
+    src = np.ascontiguousarray(src)
+    layers, rows, heads, max_len, head_dim = src.shape
+    par = np.ascontiguousarray(parent, dtype=np.int32)
+    batch, k = par.shape
+    if batch * k != rows:
+        raise ValueError("parent shape does not match cache rows")
+    out = np.zeros_like(src) if dst is None else dst
+    rc = lib.oracle_cache_reorder(_ptr(src), _ptr(out), src.dtype.itemsize, _ptr(par), layers, batch, k, heads,
+                                  max_len, int(length), head_dim)
+    if rc != 0:
+        raise ValueError(f"oracle_cache_reorder failed ({rc})")
+    return out
