@@ -1,0 +1,522 @@
+#!/usr/bin/env python3
+"""Benchmark of the hierarchical beam-search step + cache refresh on GB300.
+
+Default workload (c5): 64 autoregressive decode steps, batch 256, beam 4, vocab 40000,
+fp16 logits N(0,2) + a per-step offset, KV cache [6, 1024, 16, 64(max_len), 64] fp16
+refreshed by parent beam each step (len = step).  One benchmark "step" is the whole
+64-step decode of one batch of synthetic input; `value` is decode steps per second
+(every decode step covers all 256 x 4 beams), measured with all inputs resident in
+HBM (5.24 GB of logits, larger than L2, so no flush is needed), the 64 steps replayed
+as one CUDA graph.  `e2e` repeats it through the same C ABI with the logits copied
+from pinned host memory every decode step and the step's outputs read back.
+
+--impl reference times the oracle (single-threaded fp64 C, the naive definition) on
+a bounded sample of the same workload on the host cores.
+
+Launch: python bench.py [--gpus N --steps K --warmup W]; for N > 1 under
+torch.distributed.run (one process per GPU, independent batches per rank: weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "beam-search decode steps/s and logit GB/s vs GB300 HBM roofline (1 GPU)"
+UNIT = "decode steps/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="c5", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ distributed plumbing
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def shard_seed(base_seed: int, rank: int) -> int:
+    """Each rank gets its own independent batches (weak scaling, no data-path collective)."""
+    return base_seed + 1000003 * rank
+
+
+def shard_workload(w: synth.Workload, rank: int) -> synth.Workload:
+    if rank == 0:
+        return w
+    from dataclasses import replace
+
+    return replace(w, seed=shard_seed(w.seed, rank))
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ peaks, clocks, profiles
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "serving_ls_beam_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, fn), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes from the committed ncu summary, or None if absent or stale."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    try:
+        with open(path) as f:
+            for ln in f:
+                if ln.startswith("#") or not ln.strip():
+                    continue
+                parts = ln.split()
+                if len(parts) >= 4 and parts[0] == kernel and parts[1] == workload:
+                    return float(parts[2]) if parts[3] == source_hash() else None
+    except OSError:
+        return None
+    return None
+
+
+# ------------------------------------------------------------------ oracle (CPU) timing
+def time_oracle_sample(w: synth.Workload, batches, steps_list, with_cache: bool):
+    """Run the oracle on `batches` for the given decode steps (own trajectory); returns (seconds, batch_steps)."""
+    import oracle
+
+    oracle.build()
+    k = w.k
+    o_beam = synth.beam_scores(w, 0)[batches].copy()
+    o_fin = np.zeros((len(batches), k), np.uint8)
+    cache = None
+    if with_cache and w.kv_shape is not None:
+        layers, heads, max_len, head_dim = w.kv_shape
+        shape = (layers, w.rows, heads, max_len, head_dim)
+        rows = [b * k + j for b in batches for j in range(k)]
+        cache = [synth.kv_cache_rows(shape, w.seed, rows, which=i) for i in range(2)]
+    inputs = [synth.logits(w, t, batches) for t in steps_list]
+    cur = 0
+    t0 = time.perf_counter()
+    for lg, t in zip(inputs, steps_list):
+        r = oracle.beam_step(lg, o_beam, bias=synth.bias(w), finished=o_fin, eos_id=w.eos_id)
+        if cache is not None:
+            cache[1 - cur] = oracle.cache_reorder(cache[cur], r["parent"], t, dst=cache[1 - cur])
+            cur = 1 - cur
+        o_beam = r["score"].astype(np.float32)
+        o_fin = r["finished"]
+    dt = time.perf_counter() - t0
+    return dt, len(batches) * len(steps_list)
+
+
+def cpu_baseline(w: synth.Workload, target_s: float = 12.0):
+    # calibrate on one batch-step, then size the sample to roughly target_s seconds
+    dt1, n1 = time_oracle_sample(w, [0], [1], True)
+    per = dt1 / n1
+    n = max(2, int(target_s / max(per, 1e-4)))
+    steps = min(w.steps, max(1, n // 8))
+    nb = max(1, min(w.batch, n // steps))
+    batches = list(range(nb))
+    dt, bs = time_oracle_sample(w, batches, list(range(1, steps + 1)), True)
+    per = dt / bs
+    value = 1.0 / (per * w.batch)
+    return {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{nb} batches x {steps} decode steps of {w.name} (beam step + cache refresh), single thread; "
+                      f"{per * 1e3:.1f} ms per batch-step, scaled to all {w.batch} batches"}
+
+
+# ------------------------------------------------------------------ GPU arm
+def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
+    import torch
+
+    import serving_ls_beam_gb300 as lsb
+    from serving_ls_beam_gb300 import _build
+    from serving_ls_beam_gb300.loop import BeamSearchLoop
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    _build.build()
+    lsb.load_library()
+    wr = shard_workload(w, rank)
+    T = wr.steps
+    B, K, V = wr.batch, wr.k, wr.vocab
+    es = 2 if wr.dtype in ("f16", "bf16") else 4
+    tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[wr.dtype]
+
+    # ---- inputs, resident in HBM
+    t0 = time.time()
+    host_logits = np.empty((T, B, K, V), np.float16 if wr.dtype == "f16" else np.float32)
+    for t in range(T):
+        host_logits[t] = synth.logits(wr, t + 1 if T > 1 else 0)
+    d_logits = torch.from_numpy(host_logits).to(dev)
+    bias_np = synth.bias(wr)
+    d_bias = None if bias_np is None else torch.from_numpy(bias_np).to(dev)
+    beam0 = torch.from_numpy(synth.beam_scores(wr, 0)).to(dev)
+    fin_np = synth.finished(wr)
+    fin0 = None if fin_np is None else torch.from_numpy(fin_np).to(dev)
+    caches = None
+    if wr.kv_shape is not None:
+        layers, heads, max_len, head_dim = wr.kv_shape
+        shape = (layers, wr.rows, heads, max_len, head_dim)
+        caches = [torch.from_numpy(synth.kv_cache(shape, wr.seed, which=i)).to(dev) for i in range(2)]
+    loop = BeamSearchLoop(B, K, V, wr.eos_id, kv_shape=wr.kv_shape, device=dev, caches=caches)
+    setup_s = time.time() - t0
+
+    def lens(t):  # cache positions refreshed at decode step t (1-based)
+        return t if T > 1 else (wr.kv_shape[2] if wr.kv_shape else 0)
+
+    stream = torch.cuda.Stream(device=dev)
+    try:  # events inside a captured graph must be "external" record nodes to be timed
+        ev_k = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)] for _ in range(T)]
+        graph_events = True
+    except TypeError:
+        ev_k = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(T)]
+        graph_events = False
+
+    def run_all(instrument: bool):
+        loop.reset(beam0, fin0)
+        for t in range(T):
+            if instrument:
+                ev_k[t][0].record()
+            s, n = loop.cur, 1 - loop.cur
+            lsb.check(lsb.ls_beam_step(d_logits[t], d_bias, loop.scores[s], loop.finished[s], wr.eos_id,
+                                       loop.token[n], loop.parent[n], loop.scores[n], loop.finished[n],
+                                       loop.workspace), "ls_beam_step")
+            if instrument:
+                ev_k[t][1].record()
+            if loop.cache is not None:
+                lsb.check(lsb.ls_cache_reorder(loop.cache[s], loop.cache[n], loop.parent[n], lens(t + 1)),
+                          "ls_cache_reorder")
+            if instrument:
+                ev_k[t][2].record()
+            loop.cur = n
+
+    # warm the library's per-device setup outside capture, then capture both graphs
+    with torch.cuda.stream(stream):
+        run_all(False)
+    torch.cuda.synchronize()
+    lsb.check(lsb.ls_read_status(loop.workspace, stream), "device status")
+    g_plain, g_inst = torch.cuda.CUDAGraph(), None
+    with torch.cuda.graph(g_plain, stream=stream):
+        run_all(False)
+    if graph_events:
+        g_inst = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_inst, stream=stream):
+            run_all(True)
+    torch.cuda.synchronize()
+
+    launches_per_step = T * (2 if loop.cache is not None else 1)
+    for _ in range(args.warmup):
+        g_plain.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record()
+            for _ in range(args.steps):
+                g_plain.replay()
+            e1.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        ms_plain = e0.elapsed_time(e1)
+        # per-kernel durations: the same graph with an event around each kernel
+        k1_ms, k4_ms = 0.0, 0.0
+        reps = max(1, min(args.steps, 3))
+        with torch.cuda.stream(stream):
+            for _ in range(reps):
+                if g_inst is not None:
+                    g_inst.replay()
+                else:
+                    run_all(True)
+                torch.cuda.synchronize()
+                for t in range(T):
+                    k1_ms += ev_k[t][0].elapsed_time(ev_k[t][1])
+                    if loop.cache is not None:
+                        k4_ms += ev_k[t][1].elapsed_time(ev_k[t][2])
+    lsb.check(lsb.ls_read_status(loop.workspace, stream), "device status")
+    k1_ms /= reps
+    k4_ms /= reps
+    ms_total = max_over_ranks(ms_plain, world, dev)
+    ms_per_step = ms_total / args.steps
+    decode_steps = T * args.steps * world
+    value = decode_steps / (ms_total / 1e3)
+
+    # ---- algorithmic bytes
+    fin_rows = 0 if fin_np is None else int(fin_np.sum())
+    logit_bytes_launch = (wr.rows - fin_rows) * V * es + (V * 4 if bias_np is not None else 0) + wr.rows * 13
+    k1_bytes = logit_bytes_launch * T
+    k4_bytes = 0
+    if loop.cache is not None:
+        layers, heads, max_len, head_dim = wr.kv_shape
+        for t in range(1, T + 1):
+            k4_bytes += 2 * layers * wr.rows * heads * lens(t) * head_dim * 2
+    peak, peak_src = hbm_peak()
+    k1_gbs = k1_bytes / (k1_ms / 1e3) / 1e9
+    kern = {"beam_step": {"bound": "hbm", "achieved": k1_gbs, "peak": peak, "unit": "GB/s", "frac": k1_gbs / peak,
+                          "traffic": recorded_traffic("beam_step", wr.name),
+                          "us_per_launch": k1_ms * 1e3 / T,
+                          "algorithmic_bytes_per_launch": k1_bytes / T}}
+    if loop.cache is not None:
+        k4_gbs = k4_bytes / (k4_ms / 1e3) / 1e9
+        kern["cache_reorder"] = {"bound": "hbm", "achieved": k4_gbs, "peak": peak, "unit": "GB/s",
+                                 "frac": k4_gbs / peak, "traffic": recorded_traffic("cache_reorder", wr.name),
+                                 "us_per_launch": k4_ms * 1e3 / T, "algorithmic_bytes_per_launch": k4_bytes / T}
+    dominant = max(kern, key=lambda n: kern[n]["us_per_launch"])
+    roof = {key: kern[dominant][key] for key in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
+    roof["kernel"] = dominant
+    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback"
+    step_gbs = (k1_bytes + k4_bytes) / (ms_plain / args.steps / 1e3) / 1e9
+
+    # ---- end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = bench_e2e(args, wr, loop, host_logits, bias_np, beam0, fin0, lens, dev, world)
+
+    clocks = clk.summary()
+    cfg = {"workload": f"{wr.name}: batch {B}, beam {K}, vocab {V}, {wr.dtype} logits, "
+                       f"{T} decode step(s)" + (f", KV cache {[wr.kv_shape[0], wr.rows, *wr.kv_shape[1:]]} fp16 "
+                                                f"refreshed by parent (len = step)" if wr.kv_shape else ""),
+           "batch": B, "beam": K, "vocab": V, "logit_dtype": wr.dtype, "decode_steps_per_step": T,
+           "l2": f"inputs larger than L2: {host_logits.nbytes / 1e9:.2f} GB of logits per benchmark step",
+           "graph": f"one CUDA graph of the {T}-step loop", "parallelism": f"replicas x{world} (independent batches)"}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": wr.dtype, "data": "synthetic (seeded generators, workload recipe in synth/)", "config": cfg,
+        "logit_gbs": k1_gbs, "step_gbs": step_gbs, "step_roofline_frac": step_gbs / peak,
+        "roofline": roof, "roofline_kernels": kern, "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks, "e2e": e2e, "setup_s": round(setup_s, 1),
+    }
+    return line
+
+
+def bench_e2e(args, wr, loop, host_logits, bias_np, beam0, fin0, lens, dev, world):
+    """Logits copied from pinned host memory each decode step (copy stream, double-buffered),
+    outputs read back each step; the all-finished stop is checked one step behind."""
+    import torch
+
+    import serving_ls_beam_gb300 as lsb
+
+    T = host_logits.shape[0]
+    pinned = torch.from_numpy(host_logits).pin_memory()
+    bufs = [torch.empty(pinned.shape[1:], dtype=pinned.dtype, device=dev) for _ in range(2)]
+    d_bias = None if bias_np is None else torch.from_numpy(bias_np).to(dev)
+    out_host = {key: torch.empty((T,) + tuple(loop.token[0].shape), dtype=dt).pin_memory()
+                for key, dt in (("token", torch.int32), ("parent", torch.int32), ("score", torch.float32),
+                                ("finished", torch.uint8))}
+    comp = torch.cuda.current_stream(dev)
+    copy = torch.cuda.Stream(device=dev)
+    h2d_done = [torch.cuda.Event() for _ in range(2)]
+    buf_free = [torch.cuda.Event() for _ in range(2)]
+    d2h_done = [torch.cuda.Event() for _ in range(T)]
+
+    def one_run():
+        loop.reset(beam0, fin0)
+        stop = T
+        for t in range(T):
+            i = t % 2
+            with torch.cuda.stream(copy):
+                if t >= 2:
+                    copy.wait_event(buf_free[i])
+                bufs[i].copy_(pinned[t], non_blocking=True)
+                h2d_done[i].record(copy)
+            comp.wait_event(h2d_done[i])
+            idx = loop.step(bufs[i], lens(t + 1), bias=d_bias)
+            buf_free[i].record(comp)
+            o = loop.outputs(idx)
+            for key in out_host:
+                out_host[key][t].copy_(o[key], non_blocking=True)
+            d2h_done[t].record(comp)
+            if t >= 1:
+                d2h_done[t - 1].synchronize()
+                if bool(out_host["finished"][t - 1].all()):
+                    stop = t
+                    break
+        torch.cuda.synchronize()
+        return stop
+
+    for _ in range(max(1, args.warmup)):
+        one_run()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    steps_done = 0
+    for _ in range(args.e2e_steps):
+        steps_done += one_run()
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    dt = max_over_ranks(dt, world, dev)
+    lsb.check(lsb.ls_read_status(loop.workspace), "device status")
+    h2d = int(pinned[0].numel() * pinned.element_size())
+    d2h = int(sum(v[0].numel() * v.element_size() for v in out_host.values()))
+    return {"value": steps_done * world / dt, "unit": UNIT, "h2d_bytes_per_step": h2d * T, "d2h_bytes_per_step": d2h * T,
+            "decode_steps_run": steps_done, "note": "per benchmark step (all decode steps): logits H2D from pinned "
+            "memory every decode step, outputs D2H every decode step, wall clock"}
+
+
+def bench_reference(args, w: synth.Workload):
+    """The oracle timed on the host cores; each benchmark step = one bounded sample (2 batch-steps)."""
+    import oracle
+
+    oracle.build()
+    T = w.steps
+    for i in range(args.warmup):
+        time_oracle_sample(w, [i % w.batch], [1], True)
+    total, bs = 0.0, 0
+    for i in range(args.steps):
+        dt, n = time_oracle_sample(w, [(2 * i) % w.batch, (2 * i + 1) % w.batch], [1 + (i % T)], True)
+        total += dt
+        bs += n
+    per = total / bs
+    value = 1.0 / (per * w.batch)
+    sample = (f"{args.steps} samples of 2 batches x 1 decode step of {w.name} (beam step + cache refresh), "
+              f"single thread; {per * 1e3:.1f} ms per batch-step, scaled to all {w.batch} batches")
+    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": per * w.batch * T * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic (seeded generators)", "impl": "reference",
+            "config": {"workload": w.name, "batch": w.batch, "beam": w.k, "vocab": w.vocab},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_env()
+    w = synth.WORKLOADS[args.workload]
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            if rank == 0:
+                print(json.dumps(bench_reference(args, w)))
+            return
+        line = bench_gpu(args, w, world, rank, local)
+        if rank == 0:
+            if not args.no_cpu_baseline:
+                line["cpu_baseline"] = cpu_baseline(w)
+            print(json.dumps(line))
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

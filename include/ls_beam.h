@@ -1,0 +1,148 @@
+/*
+ * ls_beam — hierarchical ("coarse-select, then fine-rank") beam-search step and
+ * beam-cache refresh for NVIDIA GB300 (sm_103a).
+ *
+ * Method: LightSeq inference article (31duo.com, itemid-283120), section on the
+ * hierarchical rewrite of decoding.  Per beam, a first traversal of the logits
+ * computes log_sum_exp and an "R-top-k" threshold (split the logits into groups,
+ * take each group's max, the k-th largest of those maxima never exceeds the true
+ * k-th largest logit).  A second traversal keeps the logits at or above R-top-k,
+ * rescores them as beam_score + logit - log_sum_exp and queues them on the device;
+ * one sort of that short queue per batch yields the exact top-k (token, parent
+ * beam, score) of every sequence.  The article then refreshes the cache by parent
+ * beam (its latency breakdown figure puts that at 10% / 6% of inference).
+ *
+ * Conventions for every entry point:
+ *  - All array pointers are DEVICE pointers unless the argument says "host".
+ *    The caller owns every buffer; the library allocates nothing.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *    Calls are stream-ordered and return once the work is enqueued; nothing here
+ *    synchronises except ls_read_status / ls_read_row_stats.
+ *  - Argument errors are found on the host before anything is enqueued and return
+ *    LS_ERR_INVALID_ARG.  A failed CUDA launch returns LS_ERR_CUDA.  Conditions the
+ *    GPU detects (a bounded wait that ran out, an out-of-range parent index) set a
+ *    status word in the workspace, read with ls_read_status.
+ *  - Buffer extents cannot be checked through this interface: each array must hold
+ *    at least the elements its comment states.
+ */
+#ifndef LS_BEAM_H
+#define LS_BEAM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define LS_API __attribute__((visibility("default")))
+#else
+#define LS_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LS_OK = 0,
+  LS_ERR_INVALID_ARG = 1, /* bad argument, found on the host; nothing enqueued */
+  LS_ERR_UNSUPPORTED = 2, /* valid request outside what this build supports */
+  LS_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+  LS_ERR_TIMEOUT = 4,     /* a bounded device wait ran out (reported by ls_read_status) */
+  LS_ERR_INTERNAL = 5     /* device-detected inconsistency, e.g. a parent index out of range */
+} ls_status;
+
+typedef enum { LS_DTYPE_F32 = 0, LS_DTYPE_F16 = 1, LS_DTYPE_BF16 = 2 } ls_dtype;
+
+/* Largest beam width supported. */
+#define LS_MAX_K 64
+
+/*
+ * Bytes of device workspace ls_beam_step needs for (batch, k, vocab).  Host-only,
+ * needs no GPU.  Returns 0 for arguments ls_beam_step would reject.
+ * Follows the article's memory-reuse rule (every dynamic shape gets a static
+ * maximum and buffers are allocated once, at start-up): allocate the workspace once
+ * for the largest shape served and reuse it for every step of that or a smaller shape.
+ */
+LS_API size_t ls_beam_step_workspace_size(int batch, int k, int vocab);
+
+/*
+ * Zero-fill a workspace (enqueued on `stream`).  Required once before the first
+ * ls_beam_step on it, and again after any call reported a device error.
+ * workspace: device, workspace_bytes long.
+ */
+LS_API ls_status ls_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * One beam-search step (article: hierarchical decoding — first traversal, second
+ * traversal into the candidate queue, then one sort of the queue per batch).
+ *
+ *  logits      [batch, k, vocab] row-major, logit_dtype (f32, f16 or bf16), device.
+ *              Any address aligned to the element size; 16-byte alignment is fastest.
+ *  bias        [vocab] f32 or NULL; added to every beam's logits before anything else.
+ *  beam_scores [batch, k] f32 accumulated log-probabilities of the live beams.
+ *  finished    [batch, k] uint8 0/1 or NULL (= none finished).  A finished beam
+ *              contributes exactly one candidate, (eos_id, its beam score unchanged),
+ *              and its logits are not read.
+ *  eos_id      in [0, vocab).
+ *  k           beam width, 1 <= k <= LS_MAX_K, k <= vocab; k * vocab < 2^31.
+ *  out_token, out_parent  [batch, k] int32: token id in [0, vocab) and parent beam in [0, k).
+ *  out_score   [batch, k] f32: beam_score[parent] + x - lse[parent], x = logit + bias.
+ *  out_finished [batch, k] uint8 or NULL: finished[parent] || token == eos_id.
+ *  Per batch the k outputs are the exact top-k of all k*vocab (beam, token) pairs,
+ *  sorted by descending score; equal scores are ordered by parent beam, then by the
+ *  larger logit, then by the smaller token id.  A beam whose scores are all -inf
+ *  (beam score -inf, or every logit -inf) offers tokens 0, 1, ... with score -inf.
+ *  NaN or +inf inputs are not supported (no fault; the result is unspecified).
+ *  workspace   device buffer of at least ls_beam_step_workspace_size(batch, k, vocab)
+ *              bytes, zero-filled once by ls_workspace_init.  Calls that share a
+ *              workspace must be ordered (same stream, or synchronised).
+ *  batch == 0 is a no-op.
+ */
+LS_API ls_status ls_beam_step(const void* logits, ls_dtype logit_dtype, const float* bias,
+                       const float* beam_scores, const uint8_t* finished, int batch, int k,
+                       int vocab, int eos_id, int32_t* out_token, int32_t* out_parent,
+                       float* out_score, uint8_t* out_finished, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/*
+ * Beam-cache refresh by parent beam (article: "update the cache" after selection):
+ *   dst[l, b*k+j, h, p, :] = src[l, b*k + parent[b*k+j], h, p, :]   for p < len.
+ * Layout [layers, batch*k, heads, max_len, head_dim], element size from dtype
+ * (the copy is bitwise).  Positions p >= len of dst are not written.
+ * src and dst must not overlap (ping-pong buffers).  parent [batch, k] int32 in [0, k);
+ * an out-of-range parent leaves that row of dst unwritten and, when `workspace` is
+ * not NULL, sets LS_ERR_INTERNAL in its status word.  workspace: NULL or a workspace
+ * initialised by ls_workspace_init (only its status word is used).
+ * len == 0 or an empty shape is a no-op.
+ */
+LS_API ls_status ls_cache_reorder(const void* src, void* dst, ls_dtype dtype, const int32_t* parent,
+                           int layers, int batch, int k, int heads, int max_len, int len,
+                           int head_dim, void* workspace, void* stream);
+
+/*
+ * Synchronise `stream`, return the status the device recorded in `workspace` since
+ * the last read, and clear it.  LS_OK when nothing was recorded.
+ */
+LS_API ls_status ls_read_status(void* workspace, void* stream);
+
+/* Static description of a status code. */
+LS_API const char* ls_status_string(ls_status status);
+
+/*
+ * Diagnostic readback of the last ls_beam_step on `workspace` (synchronises `stream`).
+ * All outputs are HOST arrays, each may be NULL:
+ *   lse      [batch*k] f32 log_sum_exp of each live beam (NaN for finished beams)
+ *   rtopk    [batch*k] f32 the beam's R-top-k threshold (the k-th largest of its
+ *            group maxima; -inf when fewer than k groups hold a value)
+ *   ncand    [batch*k] int32 candidates of that beam that entered the final sort
+ *            (-1 when the batch took the exact fallback)
+ *   path     [batch]   int32 0 = candidate queue, 1 = exact fallback (queue overflow),
+ *            2 = exact fallback (forced for testing), 3 = exact fallback (large queue)
+ */
+LS_API ls_status ls_read_row_stats(const void* workspace, int batch, int k, int vocab, float* lse,
+                            float* rtopk, int32_t* ncand, int32_t* path, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LS_BEAM_H */

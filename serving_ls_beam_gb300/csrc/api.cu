@@ -1,0 +1,343 @@
+// C-ABI entry points (include/ls_beam.h): argument checks on the host, launch plans,
+// and the enqueue of the kernels on the caller's stream.  The library holds no state
+// besides per-device properties cached on first use.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "ls_beam.h"
+#include "ls_internal.h"
+
+using namespace lsb;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr long long kDefaultSpinNs = 2000000000LL;  // 2 s per bounded wait
+
+struct DeviceInfo {
+  bool ready = false;
+  int sms = 0;
+  // beam-step occupancy per [dtype][bias][vpt index]; 0 = not configured yet
+  int step_occ[3][2][3] = {};
+  int copy_occ[5] = {};
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+int vpt_index(int vpt) { return vpt == 4 ? 0 : (vpt == 6 ? 1 : (vpt == 8 ? 2 : -1)); }
+int unit_index(int unit) { return unit == 16 ? 0 : unit == 8 ? 1 : unit == 4 ? 2 : unit == 2 ? 3 : 4; }
+
+struct Debug {
+  int flags = 0;
+  long long spin_ns = kDefaultSpinNs;
+  int vpt = 0;  // 0 = plan's choice
+  bool check_ptrs = true;
+};
+
+// LS_BEAM_DEBUG: comma-separated "exact", "spin=<ns>", "vpt=<4|6|8>", "nocheck".
+Debug read_debug() {
+  Debug d;
+  const char* env = std::getenv("LS_BEAM_DEBUG");
+  if (!env || !*env) return d;
+  char buf[256];
+  std::strncpy(buf, env, sizeof buf - 1);
+  buf[sizeof buf - 1] = 0;
+  for (char* tok = std::strtok(buf, ","); tok; tok = std::strtok(nullptr, ",")) {
+    if (!std::strcmp(tok, "exact")) d.flags |= kFlagForceExact;
+    else if (!std::strncmp(tok, "spin=", 5)) d.spin_ns = std::atoll(tok + 5);
+    else if (!std::strncmp(tok, "vpt=", 4)) d.vpt = std::atoi(tok + 4);
+    else if (!std::strcmp(tok, "nocheck")) d.check_ptrs = false;
+  }
+  if (d.spin_ns < 0) d.spin_ns = 0;
+  if (vpt_index(d.vpt) < 0) d.vpt = 0;
+  return d;
+}
+
+ls_status cuda_fail(cudaError_t e) {
+  (void)e;
+  cudaGetLastError();  // clear a non-sticky error so later calls start clean
+  return LS_ERR_CUDA;
+}
+
+DeviceInfo* device_info(int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  *dev_out = dev;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& di = g_dev[dev];
+  if (!di.ready) {
+    if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return nullptr;
+    di.ready = true;
+  }
+  return &di;
+}
+
+int step_occupancy(DeviceInfo* di, int dtype, bool bias, int vpt) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int& occ = di->step_occ[dtype][bias ? 1 : 0][vpt_index(vpt)];
+  if (occ == 0) {
+    int o = 0;
+    if (beam_step_config(dtype, bias, vpt, beam_step_smem_bytes(vpt), &o) != cudaSuccess || o < 1) return 0;
+    occ = o;
+  }
+  return occ;
+}
+
+int copy_occupancy(DeviceInfo* di, int unit) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int& occ = di->copy_occ[unit_index(unit)];
+  if (occ == 0) {
+    int o = 0;
+    if (cache_reorder_occupancy(unit, &o) != cudaSuccess || o < 1) return 0;
+    occ = o;
+  }
+  return occ;
+}
+
+// Device-reachable memory: device, managed, or registered host memory.
+bool device_reachable(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged || a.type == cudaMemoryTypeHost;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int dtype_bytes(ls_dtype d) { return d == LS_DTYPE_F32 ? 4 : 2; }
+bool dtype_ok(ls_dtype d) { return d == LS_DTYPE_F32 || d == LS_DTYPE_F16 || d == LS_DTYPE_BF16; }
+
+// Granlund-Montgomery round-up multiplier for division by d (1 <= d < 2^31).
+void make_divisor(uint32_t d, uint32_t* magic, int* shift) {
+  int s = 0;
+  while ((1ull << s) < d) ++s;
+  const unsigned long long m = ((1ull << 32) * ((1ull << s) - d)) / d + 1;
+  *magic = (uint32_t)m;
+  *shift = s;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ls_beam_step_workspace_size(int batch, int k, int vocab) {
+  if (batch < 0 || k < 1 || k > LS_MAX_K || vocab < k) return 0;
+  if ((long long)k * vocab >= (1ll << 31)) return 0;
+  return ws_layout(batch, k, vocab).total;
+}
+
+ls_status ls_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+  if (!workspace || workspace_bytes == 0) return LS_ERR_INVALID_ARG;
+  cudaError_t e = cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? LS_OK : cuda_fail(e);
+}
+
+ls_status ls_beam_step(const void* logits, ls_dtype logit_dtype, const float* bias, const float* beam_scores,
+                       const uint8_t* finished, int batch, int k, int vocab, int eos_id, int32_t* out_token,
+                       int32_t* out_parent, float* out_score, uint8_t* out_finished, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  if (batch < 0 || k < 1 || k > LS_MAX_K || vocab < k) return LS_ERR_INVALID_ARG;
+  if ((long long)k * vocab >= (1ll << 31)) return LS_ERR_INVALID_ARG;
+  if (eos_id < 0 || eos_id >= vocab) return LS_ERR_INVALID_ARG;
+  if (!dtype_ok(logit_dtype)) return LS_ERR_INVALID_ARG;
+  if (batch == 0) return LS_OK;
+  if (!logits || !beam_scores || !out_token || !out_parent || !out_score || !workspace) return LS_ERR_INVALID_ARG;
+  const WsLayout wl = ws_layout(batch, k, vocab);
+  if (wl.total == 0 || workspace_bytes < wl.total) return LS_ERR_INVALID_ARG;
+  const int es = dtype_bytes(logit_dtype);
+  if (!aligned(logits, es) || (bias && !aligned(bias, 4)) || !aligned(beam_scores, 4) || !aligned(out_token, 4) ||
+      !aligned(out_parent, 4) || !aligned(out_score, 4) || !aligned(workspace, 256))
+    return LS_ERR_INVALID_ARG;
+  const Debug dbg = read_debug();
+  if (dbg.check_ptrs) {
+    const void* ptrs[] = {logits, bias, beam_scores, finished, out_token, out_parent, out_score, out_finished,
+                          workspace};
+    for (const void* q : ptrs)
+      if (q && !device_reachable(q)) return LS_ERR_INVALID_ARG;
+  }
+  int dev = 0;
+  DeviceInfo* di = device_info(&dev);
+  if (!di) return cuda_fail(cudaErrorUnknown);
+
+  const int dtype = (int)logit_dtype;
+  const int vec = 16 / es;
+  const int vpt = dbg.vpt ? dbg.vpt : 6;
+  const int occ = step_occupancy(di, dtype, bias != nullptr, vpt);
+  if (occ < 1) return cuda_fail(cudaErrorUnknown);
+  const long long rows = (long long)batch * k;
+  const long long grid_full = (long long)di->sms * occ;
+  const int lmax = vpt * kThreads * vec;
+  const int nc0 = (vocab + lmax - 1) / lmax;
+  int nc_hi = nc0 + 8;
+  if (nc_hi > vocab / 512) nc_hi = vocab / 512;
+  if (nc_hi < nc0) nc_hi = nc0;
+  // pick the chunk count that minimises (waves of units) x (time per unit ~ 1/nc)
+  int best_nc = nc0;
+  long long best_waves = (rows * nc0 + grid_full - 1) / grid_full;
+  for (int nc = nc0 + 1; nc <= nc_hi; ++nc) {
+    const long long waves = (rows * nc + grid_full - 1) / grid_full;
+    if (waves * best_nc < best_waves * nc) {
+      best_nc = nc;
+      best_waves = waves;
+    }
+  }
+  int chunk_len = (vocab + best_nc - 1) / best_nc;
+  chunk_len = (chunk_len + vec - 1) / vec * vec;
+  const int nc = (vocab + chunk_len - 1) / chunk_len;
+  if (nc > wl.nc_max) return LS_ERR_INTERNAL;
+
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  StepParams p;
+  p.logits = logits;
+  p.bias = bias;
+  p.beam = beam_scores;
+  p.finished = finished;
+  p.out_token = out_token;
+  p.out_parent = out_parent;
+  p.out_score = out_score;
+  p.out_finished = out_finished;
+  p.status = reinterpret_cast<uint32_t*>(ws + wl.status_off);
+  p.done = reinterpret_cast<uint32_t*>(ws + wl.done_off);
+  p.rec = ws + wl.rec_off;
+  p.slots = reinterpret_cast<CandSlot*>(ws + wl.slot_off);
+  p.rowstat = reinterpret_cast<RowStat*>(ws + wl.rowstat_off);
+  p.bstat = reinterpret_cast<int32_t*>(ws + wl.bstat_off);
+  p.batch = batch;
+  p.k = k;
+  p.vocab = vocab;
+  p.eos = eos_id;
+  p.rows = (int)rows;
+  p.nc = nc;
+  p.chunk_len = chunk_len;
+  p.groups = wl.groups;
+  p.slot_cap = wl.slot_cap;
+  p.rec_stride = wl.rec_stride;
+  p.flags = dbg.flags;
+  p.units = rows * nc;
+  p.spin_limit_ns = dbg.spin_ns;
+  const long long grid = p.units < grid_full ? p.units : grid_full;
+  cudaError_t e = launch_beam_step(p, dtype, vpt, (int)grid, beam_step_smem_bytes(vpt),
+                                   static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? LS_OK : cuda_fail(e);
+}
+
+ls_status ls_cache_reorder(const void* src, void* dst, ls_dtype dtype, const int32_t* parent, int layers, int batch,
+                           int k, int heads, int max_len, int len, int head_dim, void* workspace, void* stream) {
+  if (layers < 0 || batch < 0 || k < 1 || heads < 0 || max_len < 0 || len < 0 || len > max_len || head_dim < 0)
+    return LS_ERR_INVALID_ARG;
+  if (!dtype_ok(dtype)) return LS_ERR_INVALID_ARG;
+  if (layers == 0 || batch == 0 || heads == 0 || len == 0 || head_dim == 0) return LS_OK;
+  if (!src || !dst || !parent) return LS_ERR_INVALID_ARG;
+  if (workspace && !aligned(workspace, 256)) return LS_ERR_INVALID_ARG;
+  const long long es = dtype_bytes(dtype);
+  const long long rows = (long long)batch * k;
+  const long long slab_stride = (long long)max_len * head_dim * es;
+  const long long row_stride = slab_stride * heads;
+  const long long layer_stride = row_stride * rows;
+  const long long total = layer_stride * layers;
+  const uintptr_t s0 = reinterpret_cast<uintptr_t>(src), d0 = reinterpret_cast<uintptr_t>(dst);
+  if (s0 < d0 + (uintptr_t)total && d0 < s0 + (uintptr_t)total) return LS_ERR_INVALID_ARG;  // overlap
+  if (!aligned(parent, 4)) return LS_ERR_INVALID_ARG;
+  const Debug dbg = read_debug();
+  if (dbg.check_ptrs) {
+    if (!device_reachable(src) || !device_reachable(dst) || !device_reachable(parent)) return LS_ERR_INVALID_ARG;
+    if (workspace && !device_reachable(workspace)) return LS_ERR_INVALID_ARG;
+  }
+  const long long slab_bytes = (long long)len * head_dim * es;
+  int unit = 16;
+  while (unit > 1 && ((s0 % unit) || (d0 % unit) || (slab_bytes % unit) || (slab_stride % unit))) unit >>= 1;
+  const long long slab_units = slab_bytes / unit;
+  if (slab_units * heads >= (1ll << 30) || rows >= (1ll << 31)) return LS_ERR_UNSUPPORTED;
+  int dev = 0;
+  DeviceInfo* di = device_info(&dev);
+  if (!di) return cuda_fail(cudaErrorUnknown);
+  const int occ = copy_occupancy(di, unit);
+  if (occ < 1) return cuda_fail(cudaErrorUnknown);
+
+  ReorderParams p;
+  p.src = static_cast<const unsigned char*>(src);
+  p.dst = static_cast<unsigned char*>(dst);
+  p.parent = parent;
+  p.status = workspace ? reinterpret_cast<uint32_t*>(workspace) : nullptr;
+  p.slab_stride = slab_stride;
+  p.row_stride = row_stride;
+  p.layer_stride = layer_stride;
+  p.rows = (int)rows;
+  p.k = k;
+  p.heads = heads;
+  p.layers = layers;
+  p.slab_units = (int)slab_units;
+  make_divisor((uint32_t)slab_units, &p.div_units_magic, &p.div_units_shift);
+  p.pairs = (long long)layers * rows;
+  const long long grid_full = (long long)di->sms * occ;
+  const long long grid = p.pairs < grid_full ? p.pairs : grid_full;
+  cudaError_t e = launch_cache_reorder(p, unit, (int)grid, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? LS_OK : cuda_fail(e);
+}
+
+ls_status ls_read_status(void* workspace, void* stream) {
+  if (!workspace) return LS_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, workspace, sizeof word, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, sizeof word, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (word & kDevTimeout) return LS_ERR_TIMEOUT;
+  if (word & (kDevBadParent | kDevInternal)) return LS_ERR_INTERNAL;
+  return LS_OK;
+}
+
+const char* ls_status_string(ls_status status) {
+  switch (status) {
+    case LS_OK: return "ok";
+    case LS_ERR_INVALID_ARG: return "invalid argument";
+    case LS_ERR_UNSUPPORTED: return "unsupported request";
+    case LS_ERR_CUDA: return "CUDA runtime error";
+    case LS_ERR_TIMEOUT: return "bounded device wait timed out";
+    case LS_ERR_INTERNAL: return "device-detected internal error (e.g. parent index out of range)";
+    default: return "unknown status";
+  }
+}
+
+ls_status ls_read_row_stats(const void* workspace, int batch, int k, int vocab, float* lse, float* rtopk,
+                            int32_t* ncand, int32_t* path, void* stream) {
+  if (!workspace || batch < 0 || k < 1 || k > LS_MAX_K || vocab < k) return LS_ERR_INVALID_ARG;
+  if (batch == 0) return LS_OK;
+  const WsLayout wl = ws_layout(batch, k, vocab);
+  const size_t rows = (size_t)batch * k;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const unsigned char* ws = static_cast<const unsigned char*>(workspace);
+  RowStat* tmp = static_cast<RowStat*>(std::malloc(rows * sizeof(RowStat)));
+  int32_t* bs = static_cast<int32_t*>(std::malloc((size_t)batch * sizeof(int32_t)));
+  if (!tmp || !bs) {
+    std::free(tmp);
+    std::free(bs);
+    return LS_ERR_INTERNAL;
+  }
+  cudaError_t e = cudaMemcpyAsync(tmp, ws + wl.rowstat_off, rows * sizeof(RowStat), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(bs, ws + wl.bstat_off, (size_t)batch * sizeof(int32_t), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess) {
+    for (size_t r = 0; r < rows; ++r) {
+      if (lse) lse[r] = tmp[r].lse;
+      if (rtopk) rtopk[r] = tmp[r].rtopk;
+      if (ncand) ncand[r] = tmp[r].ncand;
+    }
+    if (path) std::memcpy(path, bs, (size_t)batch * sizeof(int32_t));
+  }
+  std::free(tmp);
+  std::free(bs);
+  return e == cudaSuccess ? LS_OK : cuda_fail(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,118 @@
+// Device helpers: inline PTX for mbarriers, bulk (TMA) copies, timers, and the
+// order-preserving float keys used by the fine rank.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace lsb {
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Make barrier initialisation visible to the async (bulk-copy) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the barrier phase with the given parity; give up after limit_ns.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, long long limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((long long)(global_timer_ns() - t0) > limit_ns) return false;
+  }
+}
+
+// L2 policy: the logits are read exactly once, so let them leave L2 first.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// 1-D bulk copy global -> shared, completion counted in bytes on `bar`.
+// dst, src and bytes must all be multiples of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                          uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Order-preserving map of a float onto uint32 (ascending).  -0 is folded onto +0.
+__device__ __forceinline__ uint32_t float_ord(float f) {
+  uint32_t u = __float_as_uint(f + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float ord_float(uint32_t o) {
+  uint32_t u = (o & 0x80000000u) ? (o & 0x7fffffffu) : ~o;
+  return __uint_as_float(u);
+}
+
+// Key of one candidate for the fine rank; the smaller key ranks first.
+// Order: score descending, then parent beam ascending, then logit descending,
+// then token id ascending.  For a score of -inf the logit is left out (all such
+// candidates are an exact tie broken by the flattened index).
+struct Key {
+  unsigned long long hi;  // ~ord(score) << 32 | parent
+  unsigned long long lo;  // ~ord(x) << 32 | token   (x part zero when score is -inf)
+};
+
+__device__ __forceinline__ Key make_key(float s, int parent, float x, int token) {
+  Key k;
+  const uint32_t so = ~float_ord(s);
+  const uint32_t xo = (s == -INFINITY) ? 0u : ~float_ord(x);
+  k.hi = ((unsigned long long)so << 32) | (uint32_t)parent;
+  k.lo = ((unsigned long long)xo << 32) | (uint32_t)token;
+  return k;
+}
+__device__ __forceinline__ bool key_less(const Key& a, const Key& b) {
+  return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo);
+}
+__device__ __forceinline__ float key_score(const Key& k) { return ord_float(~(uint32_t)(k.hi >> 32)); }
+__device__ __forceinline__ int key_parent(const Key& k) { return (int)(uint32_t)(k.hi & 0xffffffffu); }
+__device__ __forceinline__ int key_token(const Key& k) { return (int)(uint32_t)(k.lo & 0xffffffffu); }
+
+}  // namespace lsb

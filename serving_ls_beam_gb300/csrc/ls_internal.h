@@ -1,0 +1,135 @@
+// Internal definitions shared by the host entry points (api.cu) and the kernels.
+// Nothing here is part of the public interface (include/ls_beam.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace lsb {
+
+// ---------------------------------------------------------------- kernel shape constants
+// Beam-step kernel: one CTA is a group of kThreads threads that owns one chunk of one
+// row at a time; the chunk sits in shared memory (bulk-copied) while the threads hold
+// it in registers, kVpt 16-byte vectors each.
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxK = 64;
+constexpr int kSelCap = 512;   // candidates the in-CTA fine rank holds in shared memory
+constexpr int kVptMin = 4;     // smallest vectors-per-thread variant built
+constexpr int kMinChunkElems = kVptMin * kThreads * 4;  // fp32: 4 elements per vector
+
+// Device status bits (workspace word 0).
+constexpr uint32_t kDevTimeout = 1u << 0;
+constexpr uint32_t kDevBadParent = 1u << 1;
+constexpr uint32_t kDevInternal = 1u << 2;
+
+// Debug flags (LS_BEAM_DEBUG).
+constexpr int kFlagForceExact = 1;
+
+// ---------------------------------------------------------------- workspace layout
+struct alignas(16) RowStat {
+  float lse;
+  float rtopk;
+  int32_t ncand;
+  int32_t pad;
+};
+
+struct CandSlot {
+  float x;    // logit (+ bias) of the candidate
+  int32_t v;  // token id within the row
+};
+
+struct WsLayout {
+  size_t status_off, done_off, rec_off, slot_off, rowstat_off, bstat_off, total;
+  int nc_max;      // most chunks per row any plan may use
+  int groups;      // G: number of R-top-k groups (power of two >= k)
+  int slot_cap;    // C: candidate slots per chunk
+  int rec_stride;  // bytes per chunk record
+};
+
+__host__ __device__ inline int pow2_ceil(int x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Returns total == 0 for unsupported shapes.
+inline WsLayout ws_layout(int batch, int k, int vocab) {
+  WsLayout w{};
+  if (batch < 0 || k < 1 || k > kMaxK || vocab < k) return w;
+  const size_t rows = (size_t)batch * (size_t)k;
+  w.groups = pow2_ceil(k);
+  w.slot_cap = (int)align_up((size_t)(4 * k + 32), 8);
+  w.rec_stride = (int)align_up((size_t)(16 + 4 * w.groups), 16);
+  w.nc_max = (vocab + kMinChunkElems - 1) / kMinChunkElems + 8;
+  size_t off = 0;
+  w.status_off = off;
+  off += 256;
+  w.done_off = off;
+  off = align_up(off + (size_t)batch * 4, 256);
+  w.rec_off = off;
+  off = align_up(off + rows * w.nc_max * w.rec_stride, 256);
+  w.slot_off = off;
+  off = align_up(off + rows * w.nc_max * w.slot_cap * sizeof(CandSlot), 256);
+  w.rowstat_off = off;
+  off = align_up(off + rows * sizeof(RowStat), 256);
+  w.bstat_off = off;
+  off = align_up(off + (size_t)batch * 4, 256);
+  w.total = off;
+  return w;
+}
+
+// ---------------------------------------------------------------- kernel parameters
+struct StepParams {
+  const void* logits;
+  const float* bias;
+  const float* beam;
+  const uint8_t* finished;
+  int32_t* out_token;
+  int32_t* out_parent;
+  float* out_score;
+  uint8_t* out_finished;
+  uint32_t* status;
+  uint32_t* done;
+  unsigned char* rec;
+  CandSlot* slots;
+  RowStat* rowstat;
+  int32_t* bstat;
+  int batch, k, vocab, eos;
+  int rows;
+  int nc;         // chunks per row
+  int chunk_len;  // elements per chunk (multiple of the 16-byte vector width)
+  int groups;
+  int slot_cap;
+  int rec_stride;
+  int flags;
+  long long units;  // rows * nc
+  long long spin_limit_ns;
+};
+
+struct ReorderParams {
+  const unsigned char* src;
+  unsigned char* dst;
+  const int32_t* parent;
+  uint32_t* status;  // may be null
+  long long slab_stride;  // bytes between consecutive (l, row, h) slabs = max_len * head_dim * es
+  long long row_stride;   // bytes between rows = heads * slab_stride
+  long long layer_stride; // bytes between layers = rows * row_stride
+  int rows, k, heads, layers;
+  int slab_units;   // copy units (of UNIT bytes) per slab = len * head_dim * es / UNIT
+  uint32_t div_units_magic;  // fast division by slab_units
+  int div_units_shift;
+  long long pairs;  // layers * rows
+};
+
+// Launchers (defined next to their kernels).
+cudaError_t launch_beam_step(const StepParams& p, int dtype, int vpt, int grid, size_t smem,
+                             cudaStream_t stream);
+cudaError_t beam_step_config(int dtype, bool bias, int vpt, size_t smem, int* occupancy);
+size_t beam_step_smem_bytes(int vpt);
+cudaError_t launch_cache_reorder(const ReorderParams& p, int unit, int grid, cudaStream_t stream);
+cudaError_t cache_reorder_occupancy(int unit, int* occupancy);
+
+}  // namespace lsb

@@ -1,0 +1,73 @@
+"""Device-resident autoregressive beam-search loop over the C ABI.
+
+One decode step is ``ls_beam_step`` (select the k best (token, parent) pairs of
+every batch from that step's logits) followed by ``ls_cache_reorder`` (gather
+the KV cache rows by parent beam, positions [0, t)), with the step's scores and
+finished flags becoming the next step's beam state.  Everything stays on the
+GPU: the beam state and the two cache buffers alternate between two sets
+(ping-pong), so a run of steps can be captured in one CUDA graph.
+
+Follows the LightSeq inference article (31duo.com, itemid-283120): decoding =
+vocab softmax + beam selection + cache refresh per step, with every buffer
+allocated once at its static maximum (memory-reuse section).
+"""
+from __future__ import annotations
+
+import torch
+
+from . import check, ls_beam_step, ls_beam_step_workspace_size, ls_cache_reorder, ls_workspace_init
+
+
+class BeamSearchLoop:
+    def __init__(self, batch: int, k: int, vocab: int, eos_id: int, kv_shape=None, kv_dtype=torch.float16,
+                 device="cuda", caches=None):
+        """kv_shape = (layers, heads, max_len, head_dim) or None for no cache refresh.
+        caches: optional pair of preallocated [layers, batch*k, heads, max_len, head_dim] tensors."""
+        self.batch, self.k, self.vocab, self.eos_id = batch, k, vocab, eos_id
+        self.device = torch.device(device)
+        dev = self.device
+        self.workspace = torch.empty(ls_beam_step_workspace_size(batch, k, vocab), dtype=torch.uint8, device=dev)
+        check(ls_workspace_init(self.workspace), "ls_workspace_init")
+        # two sets of beam state: set s is read by a step, set 1-s written by it
+        self.scores = [torch.zeros(batch, k, dtype=torch.float32, device=dev) for _ in range(2)]
+        self.finished = [torch.zeros(batch, k, dtype=torch.uint8, device=dev) for _ in range(2)]
+        self.token = [torch.zeros(batch, k, dtype=torch.int32, device=dev) for _ in range(2)]
+        self.parent = [torch.zeros(batch, k, dtype=torch.int32, device=dev) for _ in range(2)]
+        self.kv_shape = kv_shape
+        if kv_shape is not None:
+            layers, heads, max_len, head_dim = kv_shape
+            shape = (layers, batch * k, heads, max_len, head_dim)
+            if caches is None:
+                caches = [torch.zeros(shape, dtype=kv_dtype, device=dev) for _ in range(2)]
+            self.cache = list(caches)
+        else:
+            self.cache = None
+        self.cur = 0
+
+    def reset(self, beam_scores=None, finished=None):
+        """Start a new search: beam state set 0 from the given tensors (default: scores 0, none finished)."""
+        self.cur = 0
+        if beam_scores is None:
+            self.scores[0].zero_()
+        else:
+            self.scores[0].copy_(beam_scores)
+        if finished is None:
+            self.finished[0].zero_()
+        else:
+            self.finished[0].copy_(finished)
+
+    def step(self, logits: torch.Tensor, t: int, bias=None, stream=None) -> int:
+        """Decode step t (1-based): beam step on `logits` [batch, k, vocab], then the cache refresh of
+        positions [0, t).  Returns the index of the state set holding this step's outputs."""
+        s, n = self.cur, 1 - self.cur
+        check(ls_beam_step(logits, bias, self.scores[s], self.finished[s], self.eos_id, self.token[n], self.parent[n],
+                           self.scores[n], self.finished[n], self.workspace, stream), "ls_beam_step")
+        if self.cache is not None:
+            check(ls_cache_reorder(self.cache[s], self.cache[n], self.parent[n], t, stream=stream), "ls_cache_reorder")
+        self.cur = n
+        return n
+
+    def outputs(self, idx: int | None = None):
+        i = self.cur if idx is None else idx
+        return {"token": self.token[i], "parent": self.parent[i], "score": self.scores[i],
+                "finished": self.finished[i]}

@@ -1,0 +1,75 @@
+"""64-step autoregressive workload c5 (batch 256, beam 4, vocab 40000, fp16, cache
+[6, 1024, 16, 64, 64]) on the GPU against the oracle's own trajectory.
+
+The GPU runs every batch; the oracle runs a sample of batches, each step feeding
+its own outputs (beam scores, finished flags, parents) into the next one, so no
+oracle input ever comes from the GPU.  Batches are independent, so a sampled
+batch is compared at every step until the oracle shows a near-tie (two scores
+within 1e-4 among its first k+1 candidates), after which the two trajectories may
+legitimately part; that batch is then dropped from the comparison.  At the end
+the cache rows of every batch still in the comparison must match bitwise.
+"""
+import numpy as np
+import pytest
+
+import synth
+from parity import GAP_TOL, boundary_gaps, compare_step
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import serving_ls_beam_gb300 as lsb  # noqa: E402
+from serving_ls_beam_gb300.loop import BeamSearchLoop  # noqa: E402
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    lsb.load_library()
+    return torch.device("cuda:0")
+
+
+def test_c5_trajectory_sampled(dev, oracle_mod):
+    w = synth.WORKLOADS["c5"]
+    layers, heads, max_len, head_dim = w.kv_shape
+    shape = (layers, w.rows, heads, max_len, head_dim)
+    steps = w.steps
+    sample = [0, 37, 101, 128, 200, 255]
+    caches = [torch.from_numpy(synth.kv_cache(shape, w.seed, which=i)).to(dev) for i in range(2)]
+    loop = BeamSearchLoop(w.batch, w.k, w.vocab, w.eos_id, kv_shape=w.kv_shape, device=dev, caches=caches)
+    loop.reset(torch.from_numpy(synth.beam_scores(w, 0)).to(dev))
+    # oracle state for the sampled batches
+    rows = [b * w.k + j for b in sample for j in range(w.k)]
+    o_cache = [synth.kv_cache_rows(shape, w.seed, rows, which=i) for i in range(2)]
+    o_beam = synth.beam_scores(w, 0)[sample].copy()
+    o_fin = np.zeros((len(sample), w.k), np.uint8)
+    alive = set(range(len(sample)))
+    cur = 0
+    compared = 0
+    for t in range(1, steps + 1):
+        lg = synth.logits(w, t)
+        idx = loop.step(torch.from_numpy(lg).to(dev), t)
+        out = {key: v.cpu().numpy() for key, v in loop.outputs(idx).items()}
+        ora = oracle_mod.beam_step(lg[sample], o_beam, finished=o_fin, eos_id=w.eos_id, m_out=w.k + 8)
+        gaps = boundary_gaps(ora, w.k)
+        gpu_s = {key: v[sample] for key, v in out.items()}
+        for i in sorted(alive):
+            compare_step(gpu_s, ora, w.k, w.dtype, finished=o_fin, eos_id=w.eos_id, batches=[i])
+            if gaps[i] < GAP_TOL:
+                alive.discard(i)
+            else:
+                assert (gpu_s["token"][i] == ora["token"][i, : w.k]).all()
+                assert (gpu_s["parent"][i] == ora["parent"][i, : w.k]).all()
+                compared += 1
+        # the oracle's next state comes from its own outputs
+        n = 1 - cur
+        o_cache[n] = oracle_mod.cache_reorder(o_cache[cur], ora["parent"][:, : w.k], t, dst=o_cache[n])
+        cur = n
+        o_beam = ora["score"][:, : w.k].astype(np.float32)
+        o_fin = ora["finished"][:, : w.k].astype(np.uint8)
+    assert compared >= len(sample) * steps // 2
+    final = loop.cache[loop.cur][:, rows].cpu().numpy()
+    for i in sorted(alive):
+        sl = slice(i * w.k, (i + 1) * w.k)
+        assert np.array_equal(final[:, sl].view(np.int16), o_cache[cur][:, sl].view(np.int16))
