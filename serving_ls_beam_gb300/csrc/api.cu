@@ -168,7 +168,7 @@ ls_status ls_beam_step(const void* logits, ls_dtype logit_dtype, const float* bi
 
   const int dtype = (int)logit_dtype;
   const int vec = 16 / es;
-  const int vpt = dbg.vpt ? dbg.vpt : 6;
+  const int vpt = dbg.vpt ? dbg.vpt : (es == 2 ? 4 : 6);
   const int occ = step_occupancy(di, dtype, bias != nullptr, vpt);
   if (occ < 1) return cuda_fail(cudaErrorUnknown);
   const long long rows = (long long)batch * k;

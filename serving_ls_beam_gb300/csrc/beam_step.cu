@@ -108,6 +108,8 @@ struct __align__(16) Smem {
   int cnt;
   int last;
   int abort;
+  int refilter;
+  float thrmax[kThreads];
   // fine rank
   int nsel, big, ovf, nbest, nrl;
   int wc[kWarps];
@@ -629,17 +631,18 @@ __global__ void __launch_bounds__(kThreads, 3) beam_step_kernel(const StepParams
 #pragma unroll
         for (int e = 0; e < VEC; ++e) mt = fmaxf(mt, x[e]);
       }
+      // exp(x - m) as 2^((x - m) * log2 e): the difference is exact for the terms that
+      // dominate the sum (x within a factor 2 of m), so large logits keep full precision
       float st = 0.0f;
       if (mt != -INFINITY) {
-        const float mb = mt * kLog2e;
 #pragma unroll
         for (int r = 0; r < VPT; ++r) {
           float x[VEC];
           values(r, x);
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) st += fast_exp2(fmaf(x[e], kLog2e, -mb));
+          for (int e = 0; e < VEC; ++e) st += fast_exp2((x[e] - mt) * kLog2e);
         }
-        if (has_x) st += fast_exp2(fmaf(xe, kLog2e, -mb));
+        if (has_x) st += fast_exp2((xe - mt) * kLog2e);
       }
       // warp: combine (max, sum) and the group maxima (group = thread index mod G)
       float m = mt, ssum = st;
@@ -693,52 +696,86 @@ __global__ void __launch_bounds__(kThreads, 3) beam_step_kernel(const StepParams
         }
       }
       __syncthreads();  // BAR2: chunk threshold known
-      // second traversal: keep x >= R-top-k (only threads whose max reaches it can hold one)
-      const float rt = sm.rthr;
+      // second traversal: keep x >= threshold (only threads whose max reaches it can hold one)
       CandSlot* slots = p.slots + (size_t)u * C;
-      bool wrote = false;
-      if (mt >= rt) {
+      auto filter = [&](float thr) {
+        bool wrote = false;
+        if (mt >= thr) {
 #pragma unroll
-        for (int r = 0; r < VPT; ++r) {
-          const int iv = tid + r * kThreads;
-          if (iv < q.n_vec) {
-            float x[VEC];
-            values(r, x);
+          for (int r = 0; r < VPT; ++r) {
+            const int iv = tid + r * kThreads;
+            if (iv < q.n_vec) {
+              float x[VEC];
+              values(r, x);
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-              if (x[e] >= rt) {
-                const int pos = atomicAdd(&sm.cnt, 1);
-                if (pos < C) {
-                  CandSlot cs;
-                  cs.x = x[e];
-                  cs.v = vbase + iv * VEC + e;
-                  slots[pos] = cs;
-                  wrote = true;
+              for (int e = 0; e < VEC; ++e) {
+                if (x[e] >= thr) {
+                  const int pos = atomicAdd(&sm.cnt, 1);
+                  if (pos < C) {
+                    CandSlot cs;
+                    cs.x = x[e];
+                    cs.v = vbase + iv * VEC + e;
+                    slots[pos] = cs;
+                    wrote = true;
+                  }
                 }
               }
             }
           }
-        }
-        if (has_x && xe >= rt) {
-          const int pos = atomicAdd(&sm.cnt, 1);
-          if (pos < C) {
-            CandSlot cs;
-            cs.x = xe;
-            cs.v = q.e0 + ve;
-            slots[pos] = cs;
-            wrote = true;
+          if (has_x && xe >= thr) {
+            const int pos = atomicAdd(&sm.cnt, 1);
+            if (pos < C) {
+              CandSlot cs;
+              cs.x = xe;
+              cs.v = q.e0 + ve;
+              slots[pos] = cs;
+              wrote = true;
+            }
           }
         }
-      }
-      if (wrote) __threadfence();
-      __syncthreads();  // BAR3: all candidates of the chunk written
-      if (tid == 0) {
+        if (wrote) __threadfence();
+      };
+      auto publish = [&]() {  // thread 0: chunk count, then arrival on the batch counter
         reinterpret_cast<int*>(rec)[0] = sm.cnt;
         sm.cnt = 0;
         __threadfence();
         cuda::atomic_ref<unsigned int, cuda::thread_scope_device> done(p.done[b]);
         const unsigned int old = done.fetch_add(1u, cuda::std::memory_order_acq_rel);
         sm.last = (old == (unsigned int)(K * nc - 1)) ? 1 : 0;
+      };
+      filter(sm.rthr);
+      __syncthreads();  // BAR3: all candidates of the chunk written
+      if (tid == 0) {
+        sm.refilter = sm.cnt > C;
+        if (!sm.refilter) publish();
+      }
+      __syncthreads();  // BAR4: last-arrival (or refilter) flag visible
+      if (sm.refilter) {
+        // Too many survivors for the chunk's slots (heavy tails or ties with k groups):
+        // tighten to the k-th largest of the per-thread maxima (kThreads disjoint groups,
+        // still a lower bound on the chunk's k-th largest) and filter again.
+        sm.thrmax[tid] = mt;
+        if (tid == 0) sm.cnt = 0;
+        __syncthreads();
+        if (warp == 0) {
+          float res = -INFINITY;
+          for (int g = lane; g < kThreads; g += 32) {
+            const float v = sm.thrmax[g];
+            int rank = 0;
+            for (int q2 = 0; q2 < kThreads; ++q2) {
+              const float w2 = sm.thrmax[q2];
+              rank += (w2 > v) || (w2 == v && q2 < g);
+            }
+            if (rank == K - 1) res = v;
+          }
+          res = warp_max(res);
+          if (lane == 0) sm.rthr = res;
+        }
+        __syncthreads();
+        filter(sm.rthr);
+        __syncthreads();
+        if (tid == 0) publish();
+        __syncthreads();  // last-arrival flag visible
       }
       ++n_cons;
     } else {
@@ -747,8 +784,8 @@ __global__ void __launch_bounds__(kThreads, 3) beam_step_kernel(const StepParams
         const unsigned int old = done.fetch_add(1u, cuda::std::memory_order_acq_rel);
         sm.last = (old == (unsigned int)(K * nc - 1)) ? 1 : 0;
       }
+      __syncthreads();  // last-arrival flag visible
     }
-    __syncthreads();  // BAR4: last-arrival flag visible
     if (sm.last) {
       __threadfence();
       select_batch<DT, BIAS>(p, sm, b);

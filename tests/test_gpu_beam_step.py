@@ -105,7 +105,11 @@ def test_workload_parity(dev, oracle_mod, name):
     live = np.ones((w.batch, w.k), bool) if inp["finished"] is None else inp["finished"] == 0
     tol = 1e-5 if w.dtype == "f32" else 2e-3
     np.testing.assert_allclose(lse[live], ora["lse"][live], rtol=0, atol=tol)
-    st = oracle_mod.rtopk_stats(inp["logits"], w.k, bias=inp["bias"], dtype=w.dtype)
+    # the kernel works on x = fp32(logit + bias); its R-top-k must not exceed the k-th largest of those
+    x32 = inp["logits"].astype(np.float32)
+    if inp["bias"] is not None:
+        x32 = x32 + inp["bias"][None, None, :]
+    st = oracle_mod.rtopk_stats(x32, w.k)
     kth = st["kth"].reshape(w.batch, w.k)
     assert (rtopk[live].astype(np.float64) <= kth[live]).all()
     assert (path == 0).all()
