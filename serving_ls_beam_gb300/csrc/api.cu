@@ -21,25 +21,25 @@ constexpr long long kDefaultSpinNs = 2000000000LL;  // 2 s per bounded wait
 struct DeviceInfo {
   bool ready = false;
   int sms = 0;
-  // beam-step occupancy per [dtype][bias][vpt index]; 0 = not configured yet
-  int step_occ[3][2][3] = {};
+  // K1 occupancy per [dtype][bias][vpl index]; 0 = not configured yet
+  int step_occ[3][2][2] = {};
   int copy_occ[5] = {};
 };
 
 std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
 
-int vpt_index(int vpt) { return vpt == 4 ? 0 : (vpt == 6 ? 1 : (vpt == 8 ? 2 : -1)); }
+int vpl_index(int vpl) { return vpl == 4 ? 0 : (vpl == 8 ? 1 : -1); }
 int unit_index(int unit) { return unit == 16 ? 0 : unit == 8 ? 1 : unit == 4 ? 2 : unit == 2 ? 3 : 4; }
 
 struct Debug {
   int flags = 0;
   long long spin_ns = kDefaultSpinNs;
-  int vpt = 0;  // 0 = plan's choice
+  int vpl = 0;  // 0 = plan's choice
   bool check_ptrs = true;
 };
 
-// LS_BEAM_DEBUG: comma-separated "exact", "spin=<ns>", "vpt=<4|6|8>", "nocheck".
+// LS_BEAM_DEBUG: comma-separated "exact", "spin=<ns>", "vpl=<4|8>", "nocheck".
 Debug read_debug() {
   Debug d;
   const char* env = std::getenv("LS_BEAM_DEBUG");
@@ -50,11 +50,11 @@ Debug read_debug() {
   for (char* tok = std::strtok(buf, ","); tok; tok = std::strtok(nullptr, ",")) {
     if (!std::strcmp(tok, "exact")) d.flags |= kFlagForceExact;
     else if (!std::strncmp(tok, "spin=", 5)) d.spin_ns = std::atoll(tok + 5);
-    else if (!std::strncmp(tok, "vpt=", 4)) d.vpt = std::atoi(tok + 4);
+    else if (!std::strncmp(tok, "vpl=", 4)) d.vpl = std::atoi(tok + 4);
     else if (!std::strcmp(tok, "nocheck")) d.check_ptrs = false;
   }
   if (d.spin_ns < 0) d.spin_ns = 0;
-  if (vpt_index(d.vpt) < 0) d.vpt = 0;
+  if (vpl_index(d.vpl) < 0) d.vpl = 0;
   return d;
 }
 
@@ -77,12 +77,12 @@ DeviceInfo* device_info(int* dev_out) {
   return &di;
 }
 
-int step_occupancy(DeviceInfo* di, int dtype, bool bias, int vpt) {
+int step_occupancy(DeviceInfo* di, int dtype, bool bias, int vpl) {
   std::lock_guard<std::mutex> lk(g_mu);
-  int& occ = di->step_occ[dtype][bias ? 1 : 0][vpt_index(vpt)];
+  int& occ = di->step_occ[dtype][bias ? 1 : 0][vpl_index(vpl)];
   if (occ == 0) {
     int o = 0;
-    if (beam_step_config(dtype, bias, vpt, beam_step_smem_bytes(vpt), &o) != cudaSuccess || o < 1) return 0;
+    if (beam_rows_config(dtype, bias, vpl, &o) != cudaSuccess || o < 1) return 0;
     occ = o;
   }
   return occ;
@@ -129,7 +129,8 @@ extern "C" {
 
 size_t ls_beam_step_workspace_size(int batch, int k, int vocab) {
   if (batch < 0 || k < 1 || k > LS_MAX_K || vocab < k) return 0;
-  if ((long long)k * vocab >= (1ll << 31)) return 0;
+  if ((long long)k * vocab >= (1ll << 31) || vocab > (1 << 28)) return 0;
+  if ((long long)batch * k * ws_layout(batch, k, vocab).nc_max >= (1ll << 31)) return 0;
   return ws_layout(batch, k, vocab).total;
 }
 
@@ -144,7 +145,7 @@ ls_status ls_beam_step(const void* logits, ls_dtype logit_dtype, const float* bi
                        int32_t* out_parent, float* out_score, uint8_t* out_finished, void* workspace,
                        size_t workspace_bytes, void* stream) {
   if (batch < 0 || k < 1 || k > LS_MAX_K || vocab < k) return LS_ERR_INVALID_ARG;
-  if ((long long)k * vocab >= (1ll << 31)) return LS_ERR_INVALID_ARG;
+  if ((long long)k * vocab >= (1ll << 31) || vocab > (1 << 28)) return LS_ERR_INVALID_ARG;
   if (eos_id < 0 || eos_id >= vocab) return LS_ERR_INVALID_ARG;
   if (!dtype_ok(logit_dtype)) return LS_ERR_INVALID_ARG;
   if (batch == 0) return LS_OK;
@@ -167,31 +168,19 @@ ls_status ls_beam_step(const void* logits, ls_dtype logit_dtype, const float* bi
   if (!di) return cuda_fail(cudaErrorUnknown);
 
   const int dtype = (int)logit_dtype;
-  const int vec = 16 / es;
-  const int vpt = dbg.vpt ? dbg.vpt : (es == 2 ? 4 : 6);
-  const int occ = step_occupancy(di, dtype, bias != nullptr, vpt);
+  const int vpl = dbg.vpl ? dbg.vpl : 8;
+  const int occ = step_occupancy(di, dtype, bias != nullptr, vpl);
   if (occ < 1) return cuda_fail(cudaErrorUnknown);
   const long long rows = (long long)batch * k;
-  const long long grid_full = (long long)di->sms * occ;
-  const int lmax = vpt * kThreads * vec;
-  const int nc0 = (vocab + lmax - 1) / lmax;
-  int nc_hi = nc0 + 8;
-  if (nc_hi > vocab / 512) nc_hi = vocab / 512;
-  if (nc_hi < nc0) nc_hi = nc0;
-  // pick the chunk count that minimises (waves of units) x (time per unit ~ 1/nc)
-  int best_nc = nc0;
-  long long best_waves = (rows * nc0 + grid_full - 1) / grid_full;
-  for (int nc = nc0 + 1; nc <= nc_hi; ++nc) {
-    const long long waves = (rows * nc + grid_full - 1) / grid_full;
-    if (waves * best_nc < best_waves * nc) {
-      best_nc = nc;
-      best_waves = waves;
-    }
-  }
-  int chunk_len = (vocab + best_nc - 1) / best_nc;
-  chunk_len = (chunk_len + vec - 1) / vec * vec;
-  const int nc = (vocab + chunk_len - 1) / chunk_len;
+  // a row spans at most ceil((15 + vocab * es) / 16) aligned 16-byte vectors
+  const long long nv_max = (15 + (long long)vocab * es + 15) / 16;
+  const int cv = 32 * vpl;
+  const int nc = (int)((nv_max + cv - 1) / cv);
   if (nc > wl.nc_max) return LS_ERR_INTERNAL;
+  const long long units = rows * nc;
+  const long long grid_full = (long long)di->sms * occ;
+  const long long grid_need = (units + kRowWarps - 1) / kRowWarps;
+  const long long grid = grid_need < grid_full ? grid_need : grid_full;
 
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   StepParams p;
@@ -215,16 +204,15 @@ ls_status ls_beam_step(const void* logits, ls_dtype logit_dtype, const float* bi
   p.eos = eos_id;
   p.rows = (int)rows;
   p.nc = nc;
-  p.chunk_len = chunk_len;
   p.groups = wl.groups;
   p.slot_cap = wl.slot_cap;
   p.rec_stride = wl.rec_stride;
   p.flags = dbg.flags;
-  p.units = rows * nc;
+  p.units = units;
   p.spin_limit_ns = dbg.spin_ns;
-  const long long grid = p.units < grid_full ? p.units : grid_full;
-  cudaError_t e = launch_beam_step(p, dtype, vpt, (int)grid, beam_step_smem_bytes(vpt),
-                                   static_cast<cudaStream_t>(stream));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_beam_rows(p, dtype, vpl, (int)grid, st);
+  if (e == cudaSuccess) e = launch_beam_select(p, dtype, st);
   return e == cudaSuccess ? LS_OK : cuda_fail(e);
 }
 

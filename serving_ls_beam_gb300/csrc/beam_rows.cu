@@ -1,0 +1,385 @@
+// Beam-step kernel K1: the first and second traversal of every beam's logits, one
+// chunk at a time, each chunk owned by a single warp.
+//
+// Method: LightSeq inference article (31duo.com, itemid-283120), hierarchical decoding
+// section.  First traversal: split a beam's logits into k groups, take each group's
+// max; the k-th largest of those maxima (their min when there are exactly k groups)
+// is the R-top-k bound, never above the true k-th largest; log_sum_exp in the same
+// pass.  Second traversal: keep the logits at or above R-top-k as candidates.
+//
+// GB300 design:
+//  * Work unit = one chunk of 32 x VPL 16-byte vectors of one beam's row.  Every warp
+//    is an independent pipeline: lane 0 keeps a two-stage shared-memory ring full with
+//    1-D bulk (TMA) copies completed on per-warp mbarriers, the warp reads the chunk
+//    into registers and works on it while the next chunk lands.  No CTA barrier, no
+//    fence and no global atomic on the streaming path; the logits are read from HBM
+//    exactly once (L2 evict-first).
+//  * Row boundaries need not be 16-byte aligned: a chunk is copied as whole aligned
+//    vectors and the bytes outside the row are masked to -inf.
+//  * Per chunk: (max, sum of exp) and the group maxima (group = lane mod G, G = the
+//    power of two >= k; with G = 64 the two halves of a lane's vectors are two groups)
+//    by warp shuffles; R-top-k of the chunk = k-th largest group max.  Any element of
+//    the row's top-k lying in the chunk is in the chunk's own top-k, hence >= the
+//    chunk's R-top-k, so the chunk's survivors can be taken before the row is complete.
+//    They go to the chunk's own slot range (the batch's "queue" is the set of its
+//    chunks' ranges), so no atomics are needed; a chunk with more survivors than slots
+//    tightens its bound to the k-th largest of its 32 per-lane maxima and filters again.
+//  * The chunk record (count, max, sum, group maxima) lets the fine-rank kernel rebuild
+//    each beam's log_sum_exp and its row-level R-top-k (the article's k-group bound).
+#include "ls_device.cuh"
+#include "ls_dtype.cuh"
+#include "ls_internal.h"
+
+namespace lsb {
+namespace {
+
+constexpr int kStages = 2;
+constexpr long long kDrainLimitNs = 2000000000LL;  // 2 s for copies already in flight
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// k-th largest (1-based) of the values held by lanes [0, n), n <= 32; all lanes get it.
+__device__ __forceinline__ float warp_kth_of_lanes(float v, int n, int k) {
+  const int lane = threadIdx.x & 31;
+  int rank = 0;
+  for (int q = 0; q < n; ++q) {
+    const float w = __shfl_sync(0xffffffffu, v, q);
+    rank += (w > v) || (w == v && q < lane);
+  }
+  const unsigned hit = __ballot_sync(0xffffffffu, lane < n && rank == k - 1);
+  return __shfl_sync(0xffffffffu, v, __ffs(hit) - 1);
+}
+
+// k-th largest of 64 values, a = group lane, b = group lane + 32; all lanes get it.
+__device__ __forceinline__ float warp_kth_of_64(float a, float b, int k) {
+  const int lane = threadIdx.x & 31;
+  int ra = 0, rb = 0;
+  for (int q = 0; q < 32; ++q) {
+    const float wa = __shfl_sync(0xffffffffu, a, q);
+    const float wb = __shfl_sync(0xffffffffu, b, q);
+    ra += (wa > a) || (wa == a && q < lane);
+    ra += (wb > a);
+    rb += (wa >= b);
+    rb += (wb > b) || (wb == b && q < lane);
+  }
+  const bool ha = ra == k - 1, hb = rb == k - 1;
+  const unsigned hit = __ballot_sync(0xffffffffu, ha || hb);
+  const float mine = ha ? a : b;
+  return __shfl_sync(0xffffffffu, mine, __ffs(hit) - 1);
+}
+
+template <int DT, bool BIAS, int VPL>
+__global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepParams p) {
+  constexpr int VEC = Traits<DT>::kVec;
+  constexpr int ES = Traits<DT>::kBytes;
+  constexpr int CV = 32 * VPL;  // vectors per chunk
+  constexpr uint32_t kStageBytes = CV * 16;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned long long* bars = reinterpret_cast<unsigned long long*>(smem_raw) + warp * kStages;
+  unsigned char* stages = smem_raw + kRowBarBytes + (size_t)warp * kStages * kStageBytes;
+
+  const int K = p.k, V = p.vocab, nc = p.nc, G = p.groups, C = p.slot_cap;
+  const int units = (int)p.units;
+  const int nwarps = gridDim.x * kRowWarps;
+  const int gw = blockIdx.x * kRowWarps + warp;
+  const int n_mine = gw < units ? (units - gw + nwarps - 1) / nwarps : 0;
+  const unsigned char* logits = static_cast<const unsigned char*>(p.logits);
+  const int row_bytes = V * ES;
+
+  if (lane == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(smem_addr(&bars[s]), 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+
+  auto live = [&](int u) -> bool { return !(p.finished && p.finished[u / nc]); };
+  struct Geo {
+    const unsigned char* rb;  // 16-byte aligned start of the row's first vector
+    int lead;                 // bytes of that vector before the row starts
+    int j0;                   // first vector of the chunk within the row
+    int nvec;                 // vectors in the chunk
+  };
+  auto geometry = [&](int u) -> Geo {
+    Geo g;
+    const int row = u / nc;
+    const int c = u - row * nc;
+    const unsigned char* rowp = logits + (size_t)row * row_bytes;
+    g.lead = (int)(reinterpret_cast<uintptr_t>(rowp) & 15);
+    g.rb = rowp - g.lead;
+    const int nv = (g.lead + row_bytes + 15) >> 4;
+    g.j0 = c * CV;
+    g.nvec = max(0, min(CV, nv - g.j0));
+    return g;
+  };
+
+  // producer state (lane 0)
+  int iss_i = 0, n_iss = 0;
+  uint64_t policy = 0;
+  if (lane == 0) policy = l2_evict_first_policy();
+  auto fill = [&](int n_done) {
+    while (n_iss - n_done < kStages && iss_i < n_mine) {
+      const int u = gw + iss_i * nwarps;
+      if (live(u)) {
+        const Geo g = geometry(u);
+        const int s = n_iss % kStages;
+        const uint32_t bar = smem_addr(&bars[s]);
+        const uint32_t bytes = (uint32_t)g.nvec * 16u;
+        mbar_arrive_expect_tx(bar, bytes);
+        if (bytes)
+          bulk_load(smem_addr(stages + (size_t)s * kStageBytes), g.rb + (size_t)g.j0 * 16, bytes, bar, policy);
+        ++n_iss;
+      }
+      ++iss_i;
+    }
+  };
+  if (lane == 0) fill(0);
+
+  int n_cons = 0;
+  bool aborted = false;
+  for (int i = 0; i < n_mine; ++i) {
+    const int u = gw + i * nwarps;
+    if (!live(u)) continue;
+    const Geo g = geometry(u);
+    const int s = n_cons % kStages;
+    const bool ok = mbar_wait_bounded(smem_addr(&bars[s]), (uint32_t)((n_cons / kStages) & 1), p.spin_limit_ns);
+    if (!__all_sync(0xffffffffu, ok)) {
+      aborted = true;
+      break;
+    }
+    // the chunk into registers; bytes outside the row become -inf
+    const uint4* sv = reinterpret_cast<const uint4*>(stages + (size_t)s * kStageBytes);
+    uint4 d[VPL];
+#pragma unroll
+    for (int r = 0; r < VPL; ++r) {
+      const int jl = lane + 32 * r;
+      if (jl < g.nvec) {
+        d[r] = sv[jl];
+        const int base_b = (g.j0 + jl) * 16 - g.lead;  // row byte offset of element 0
+        if (base_b < 0 || base_b + 16 > row_bytes) {
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) {
+            const int eb = base_b + e * ES;
+            if (eb < 0 || eb >= row_bytes) set_neg_inf<DT>(d[r], e);
+          }
+        }
+      } else {
+        const uint32_t w = Traits<DT>::kNegInfWord;
+        d[r] = make_uint4(w, w, w, w);
+      }
+    }
+    __syncwarp();
+    ++n_cons;
+    if (lane == 0) fill(n_cons);  // the stage just read is free again
+
+    auto values = [&](int r, float (&x)[VEC]) {
+      unpack<DT>(d[r], x);
+      if constexpr (BIAS) {
+        const int jl = lane + 32 * r;
+        if (jl < g.nvec) {
+          const int base_b = (g.j0 + jl) * 16 - g.lead;
+          const int v0 = base_b / ES;  // token id of element 0 (negative before the row start)
+          const bool interior = base_b >= 0 && base_b + 16 <= row_bytes;
+          if (interior && ((reinterpret_cast<uintptr_t>(p.bias + v0) & 15) == 0)) {
+#pragma unroll
+            for (int e = 0; e < VEC; e += 4) {
+              const float4 bb = __ldg(reinterpret_cast<const float4*>(p.bias + v0 + e));
+              x[e] += bb.x;
+              x[e + 1] += bb.y;
+              x[e + 2] += bb.z;
+              x[e + 3] += bb.w;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+              const int v = v0 + e;
+              if (v >= 0 && v < V) x[e] += __ldg(p.bias + v);
+            }
+          }
+        }
+      }
+    };
+
+    // first traversal: max per lane (per lane half for 64 groups), then sum of exp
+    float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < VPL; ++r) {
+      float x[VEC];
+      values(r, x);
+      float mr = x[0];
+#pragma unroll
+      for (int e = 1; e < VEC; ++e) mr = fmaxf(mr, x[e]);
+      if (r & 1)
+        m1 = fmaxf(m1, mr);
+      else
+        m0 = fmaxf(m0, mr);
+    }
+    const float mt = fmaxf(m0, m1);
+    float st = 0.0f;
+    if (mt != -INFINITY) {
+#pragma unroll
+      for (int r = 0; r < VPL; ++r) {
+        float x[VEC];
+        values(r, x);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) st += fast_exp2((x[e] - mt) * kLog2e);
+      }
+    }
+    // chunk (max, sum) by shuffles
+    float m = mt, ssum = st;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float mo = __shfl_xor_sync(0xffffffffu, m, o);
+      const float so = __shfl_xor_sync(0xffffffffu, ssum, o);
+      const float M = fmaxf(m, mo);
+      ssum = (M == -INFINITY) ? 0.0f : ssum * fast_exp2((m - M) * kLog2e) + so * fast_exp2((mo - M) * kLog2e);
+      m = M;
+    }
+    // group maxima and the chunk's R-top-k
+    float* rec = reinterpret_cast<float*>(p.rec + (size_t)u * p.rec_stride);
+    float rt;
+    if (G <= 32) {
+      float gmv = mt;
+      for (int o = 16; o >= G; o >>= 1) gmv = fmaxf(gmv, __shfl_xor_sync(0xffffffffu, gmv, o));
+      if (lane < G) rec[4 + lane] = gmv;
+      rt = warp_kth_of_lanes(gmv, G, K);
+    } else {
+      rec[4 + lane] = m0;
+      rec[4 + 32 + lane] = m1;
+      rt = warp_kth_of_64(m0, m1, K);
+    }
+    // second traversal: survivors x >= rt, positions by a warp prefix sum
+    auto count = [&](float thr) -> int {
+      int c = 0;
+      if (mt >= thr) {
+#pragma unroll
+        for (int r = 0; r < VPL; ++r) {
+          const int jl = lane + 32 * r;
+          if (jl < g.nvec) {
+            float x[VEC];
+            values(r, x);
+            const int base_b = (g.j0 + jl) * 16 - g.lead;
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+              const int eb = base_b + e * ES;
+              c += (x[e] >= thr && eb >= 0 && eb < row_bytes) ? 1 : 0;
+            }
+          }
+        }
+      }
+      return c;
+    };
+    int cnt = count(rt);
+    int total = __reduce_add_sync(0xffffffffu, (unsigned)cnt);
+    if (total > C && K <= 32) {
+      // tighter bound: k-th largest of the 32 per-lane maxima (32 disjoint groups)
+      rt = fmaxf(rt, warp_kth_of_lanes(mt, 32, K));
+      cnt = count(rt);
+      total = __reduce_add_sync(0xffffffffu, (unsigned)cnt);
+    }
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (cnt) {
+      int pos = incl - cnt;
+      CandSlot* slots = p.slots + (size_t)u * C;
+#pragma unroll
+      for (int r = 0; r < VPL; ++r) {
+        const int jl = lane + 32 * r;
+        if (jl < g.nvec) {
+          float x[VEC];
+          values(r, x);
+          const int base_b = (g.j0 + jl) * 16 - g.lead;
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) {
+            const int eb = base_b + e * ES;
+            if (x[e] >= rt && eb >= 0 && eb < row_bytes) {
+              if (pos < C) {
+                CandSlot cs;
+                cs.x = x[e];
+                cs.v = eb / ES;
+                slots[pos] = cs;
+              }
+              ++pos;
+            }
+          }
+        }
+      }
+    }
+    if (lane == 0) {
+      reinterpret_cast<int*>(rec)[0] = total;
+      rec[1] = m;
+      rec[2] = ssum;
+    }
+  }
+
+  if (aborted && lane == 0) {
+    // a wait ran out: record it, then let every copy this warp issued land before exit
+    atomicOr(p.status, kDevTimeout);
+    for (int n = n_cons; n < n_iss; ++n)
+      mbar_wait_bounded(smem_addr(&bars[n % kStages]), (uint32_t)((n / kStages) & 1), kDrainLimitNs);
+  }
+  __syncwarp();
+}
+
+template <int DT, bool BIAS, int VPL>
+cudaError_t launch_t(const StepParams& p, int grid, cudaStream_t stream) {
+  const size_t smem = beam_rows_smem_bytes(VPL);
+  beam_rows_kernel<DT, BIAS, VPL><<<grid, kRowThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int DT, bool BIAS, int VPL>
+cudaError_t config_t(int* occ) {
+  auto fn = beam_rows_kernel<DT, BIAS, VPL>;
+  const size_t smem = beam_rows_smem_bytes(VPL);
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, fn, kRowThreads, smem);
+}
+
+template <int DT, bool BIAS>
+cudaError_t dispatch_vpl(bool launch, const StepParams* p, int vpl, int grid, cudaStream_t stream, int* occ) {
+  switch (vpl) {
+    case 4: return launch ? launch_t<DT, BIAS, 4>(*p, grid, stream) : config_t<DT, BIAS, 4>(occ);
+    case 8: return launch ? launch_t<DT, BIAS, 8>(*p, grid, stream) : config_t<DT, BIAS, 8>(occ);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t dispatch(bool launch, const StepParams* p, int dtype, bool bias, int vpl, int grid, cudaStream_t stream,
+                     int* occ) {
+  switch (dtype) {
+    case DT_F32:
+      return bias ? dispatch_vpl<DT_F32, true>(launch, p, vpl, grid, stream, occ)
+                  : dispatch_vpl<DT_F32, false>(launch, p, vpl, grid, stream, occ);
+    case DT_F16:
+      return bias ? dispatch_vpl<DT_F16, true>(launch, p, vpl, grid, stream, occ)
+                  : dispatch_vpl<DT_F16, false>(launch, p, vpl, grid, stream, occ);
+    case DT_BF16:
+      return bias ? dispatch_vpl<DT_BF16, true>(launch, p, vpl, grid, stream, occ)
+                  : dispatch_vpl<DT_BF16, false>(launch, p, vpl, grid, stream, occ);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+size_t beam_rows_smem_bytes(int vpl) { return kRowBarBytes + (size_t)kRowWarps * kStages * 32 * vpl * 16; }
+
+cudaError_t beam_rows_config(int dtype, bool bias, int vpl, int* occupancy) {
+  return dispatch(false, nullptr, dtype, bias, vpl, 0, nullptr, occupancy);
+}
+
+cudaError_t launch_beam_rows(const StepParams& p, int dtype, int vpl, int grid, cudaStream_t stream) {
+  return dispatch(true, &p, dtype, p.bias != nullptr, vpl, grid, stream, nullptr);
+}
+
+}  // namespace lsb

@@ -1,0 +1,424 @@
+// Beam-step kernel K2: the fine rank.  One CTA per batch merges the chunk records of
+// that batch's beams, re-applies each beam's row-level R-top-k, rescores the surviving
+// candidates and ranks them; the k best are the step's output.
+//
+// Method: LightSeq inference article (31duo.com, itemid-283120), hierarchical decoding
+// section: candidates above R-top-k are rescored as beam_score + logit - log_sum_exp
+// and one sort of that short queue per batch gives the exact top-k of every sequence.
+//
+// GB300 design: launched with programmatic dependent launch behind K1, so its launch
+// and prologue overlap K1's last wave; `griddepcontrol.wait` orders it after K1's
+// writes.  The queue is short (about a dozen survivors per beam for k = 4), so instead
+// of a sort each survivor's rank is counted against all the others in shared memory,
+// O(n^2 / threads), and the k with rank < k are written.  A batch whose chunk slots
+// overflowed, or with more than kSelCap survivors, takes an exact path that needs no
+// queue: a per-beam radix select of the top-k logits, merged across beams.
+#include "ls_device.cuh"
+#include "ls_dtype.cuh"
+#include "ls_internal.h"
+
+namespace lsb {
+namespace {
+
+enum { ROW_LIVE = 0, ROW_FIN = 1, ROW_DEAD = 2 };
+
+struct RowSel {
+  double c;  // beam_score - log_sum_exp
+  float rtopk;
+  float lse;
+  int kind;
+  int ncand;
+};
+
+struct __align__(16) SelSmem {
+  int nsel, big, ovf, nbest, nrl;
+  int wc[kSelWarps];
+  unsigned int hist[256];
+  unsigned int prefix, pmask;
+  int need;
+  RowSel row[kMaxK];
+  float selg[kSelWarps][64];
+  Key sel[kSelCap];
+  Key mg[2 * kMaxK];
+  Key best[kMaxK];
+  Key rl[kMaxK];
+};
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// k-th largest (1-based) of vals[0..n), n <= 64, by one warp; all lanes return it.
+__device__ __forceinline__ float warp_kth_largest(const float* vals, int n, int k) {
+  const int lane = threadIdx.x & 31;
+  float res = -INFINITY;
+  for (int g = lane; g < n; g += 32) {
+    const float v = vals[g];
+    int rank = 0;
+    for (int q = 0; q < n; ++q) {
+      const float w = vals[q];
+      rank += (w > v) || (w == v && q < g);
+    }
+    if (rank == k - 1) res = v;
+  }
+  return warp_max(res);  // exactly one lane holds it, the others hold -inf
+}
+
+__device__ __forceinline__ const float* rec_ptr(const StepParams& p, long long u) {
+  return reinterpret_cast<const float*>(p.rec + (size_t)u * p.rec_stride);
+}
+
+__device__ __forceinline__ void write_output(const StepParams& p, int b, int r, const Key& key) {
+  const int o = b * p.k + r;
+  const int parent = key_parent(key);
+  const int token = key_token(key);
+  p.out_token[o] = token;
+  p.out_parent[o] = parent;
+  p.out_score[o] = key_score(key);
+  if (p.out_finished) {
+    const bool fin = p.finished && p.finished[b * p.k + parent];
+    p.out_finished[o] = (fin || token == p.eos) ? 1 : 0;
+  }
+}
+
+__device__ __forceinline__ void write_row_stats(const StepParams& p, const SelSmem& sm, int b, bool exact) {
+  for (int j = threadIdx.x; j < p.k; j += kSelThreads) {
+    const RowSel rs = sm.row[j];
+    RowStat st;
+    st.lse = rs.kind == ROW_FIN ? __int_as_float(0x7fc00000) : rs.lse;
+    st.rtopk = rs.rtopk;
+    st.ncand = exact ? -1 : rs.ncand;
+    st.pad = 0;
+    p.rowstat[b * p.k + j] = st;
+  }
+}
+
+// Sort a[0..n) ascending by key (n a power of two); all threads call it.
+__device__ void bitonic_sort(Key* a, int n) {
+  for (int size = 2; size <= n; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < n; i += kSelThreads) {
+        const int q = i ^ stride;
+        if (q > i) {
+          const bool up = (i & size) == 0;
+          const Key x = a[i], y = a[q];
+          if (key_less(y, x) == up) {
+            a[i] = y;
+            a[q] = x;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// Merge sm.rl[0..nrl) into sm.best[0..nbest), keeping the K smallest keys.
+__device__ void merge_into_best(SelSmem& sm, int K) {
+  const int nb = sm.nbest, nr = sm.nrl;
+  const int tot = nb + nr;
+  int n = 1;
+  while (n < tot) n <<= 1;
+  for (int i = threadIdx.x; i < n; i += kSelThreads) {
+    Key k;
+    if (i < nb) {
+      k = sm.best[i];
+    } else if (i < tot) {
+      k = sm.rl[i - nb];
+    } else {
+      k.hi = ~0ull;
+      k.lo = ~0ull;
+    }
+    sm.mg[i] = k;
+  }
+  __syncthreads();
+  bitonic_sort(sm.mg, n);
+  const int keep = tot < K ? tot : K;
+  for (int i = threadIdx.x; i < keep; i += kSelThreads) sm.best[i] = sm.mg[i];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    sm.nbest = keep;
+    sm.nrl = 0;
+  }
+  __syncthreads();
+}
+
+// Exact fine rank of batch b without the candidate queue: per live beam, a radix select
+// of its top-K logits (order: larger x first, then smaller token id), merged across beams.
+template <int DT, bool BIAS>
+__device__ void exact_select(const StepParams& p, SelSmem& sm, int b, int path) {
+  constexpr int ES = Traits<DT>::kBytes;
+  const int K = p.k, V = p.vocab;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    sm.nbest = 0;
+    sm.nrl = 0;
+  }
+  __syncthreads();
+  for (int j = 0; j < K; ++j) {
+    const RowSel rs = sm.row[j];
+    const int row = b * K + j;
+    if (rs.kind == ROW_FIN) {
+      if (tid == 0) {
+        sm.rl[0] = make_key(p.beam[row], j, 0.0f, p.eos);
+        sm.nrl = 1;
+      }
+      __syncthreads();
+      merge_into_best(sm, K);
+      continue;
+    }
+    if (rs.kind == ROW_DEAD) {
+      for (int v = tid; v < K; v += kSelThreads) sm.rl[v] = make_key(-INFINITY, j, 0.0f, v);
+      if (tid == 0) sm.nrl = K;
+      __syncthreads();
+      merge_into_best(sm, K);
+      continue;
+    }
+    const unsigned char* rowp = static_cast<const unsigned char*>(p.logits) + (size_t)row * V * ES;
+    auto load_x = [&](int v) -> float {
+      float x = load_elem<DT>(rowp + (size_t)v * ES);
+      if constexpr (BIAS) x += __ldg(p.bias + v);
+      return x;
+    };
+    // radix select of the K-th largest order key, 8 bits at a time from the top
+    if (tid == 0) {
+      sm.prefix = 0;
+      sm.pmask = 0;
+      sm.need = K;
+    }
+    __syncthreads();
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int i = tid; i < 256; i += kSelThreads) sm.hist[i] = 0;
+      __syncthreads();
+      const uint32_t prefix = sm.prefix, pmask = sm.pmask;
+      for (int v = tid; v < V; v += kSelThreads) {
+        const uint32_t o = float_ord(load_x(v));
+        if ((o & pmask) == prefix) atomicAdd(&sm.hist[(o >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      if (tid == 0) {
+        const int need = sm.need;
+        unsigned int cum = 0;
+        int dgt = 255;
+        for (; dgt > 0; --dgt) {
+          if (cum + sm.hist[dgt] >= (unsigned)need) break;
+          cum += sm.hist[dgt];
+        }
+        sm.need = need - (int)cum;
+        sm.prefix = prefix | ((uint32_t)dgt << shift);
+        sm.pmask = pmask | (255u << shift);
+      }
+      __syncthreads();
+    }
+    const uint32_t tkey = sm.prefix;
+    const int need_eq = sm.need;  // elements equal to the threshold to take, in token order
+    for (int v = tid; v < V; v += kSelThreads) {
+      const float x = load_x(v);
+      if (float_ord(x) > tkey) {
+        const int pos = atomicAdd(&sm.nrl, 1);
+        if (pos < kMaxK) sm.rl[pos] = make_key((float)(rs.c + (double)x), j, x, v);
+      }
+    }
+    __syncthreads();
+    int taken = 0;
+    for (int base = 0; base < V && taken < need_eq; base += kSelThreads) {
+      const int v = base + tid;
+      float x = 0.0f;
+      bool eq = false;
+      if (v < V) {
+        x = load_x(v);
+        eq = float_ord(x) == tkey;
+      }
+      const unsigned ballot = __ballot_sync(0xffffffffu, eq);
+      if (lane == 0) sm.wc[warp] = __popc(ballot);
+      __syncthreads();
+      int before = 0, total = 0;
+      for (int w = 0; w < kSelWarps; ++w) {
+        before += (w < warp) ? sm.wc[w] : 0;
+        total += sm.wc[w];
+      }
+      const int off = taken + before + __popc(ballot & ((1u << lane) - 1u));
+      if (eq && off < need_eq) {
+        const int pos = atomicAdd(&sm.nrl, 1);
+        if (pos < kMaxK) sm.rl[pos] = make_key((float)(rs.c + (double)x), j, x, v);
+      }
+      taken += total;
+      __syncthreads();
+    }
+    if (tid == 0 && sm.nrl > kMaxK) sm.nrl = kMaxK;  // greater + ties == K, cannot exceed
+    __syncthreads();
+    merge_into_best(sm, K);
+  }
+  for (int r = tid; r < K && r < sm.nbest; r += kSelThreads) write_output(p, b, r, sm.best[r]);
+  write_row_stats(p, sm, b, true);
+  if (tid == 0) p.bstat[b] = path;
+}
+
+template <int DT, bool BIAS>
+__global__ void __launch_bounds__(kSelThreads) beam_select_kernel(const StepParams p) {
+  __shared__ SelSmem sm;
+  const int K = p.k, nc = p.nc, G = p.groups, C = p.slot_cap;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = blockIdx.x;
+  if (tid == 0) {
+    sm.nsel = 0;
+    sm.big = 0;
+    sm.ovf = 0;
+  }
+  grid_dependency_wait();  // K1's records and slots are complete and visible
+  __syncthreads();
+  // 1. per beam: log_sum_exp, the row-level R-top-k and the score offset
+  for (int j = warp; j < K; j += kSelWarps) {
+    const int row = b * K + j;
+    const bool fin = p.finished && p.finished[row];
+    const float beam = p.beam[row];
+    if (fin) {
+      if (lane == 0) {
+        RowSel rs;
+        rs.c = 0.0;
+        rs.rtopk = __int_as_float(0x7fc00000);
+        rs.lse = __int_as_float(0x7fc00000);
+        rs.kind = ROW_FIN;
+        rs.ncand = 1;
+        sm.row[j] = rs;
+      }
+      continue;
+    }
+    const long long u0 = (long long)row * nc;
+    float M = -INFINITY;
+    for (int c = lane; c < nc; c += 32) M = fmaxf(M, rec_ptr(p, u0 + c)[1]);
+    M = warp_max(M);
+    float S = 0.0f;
+    bool ovf = false;
+    for (int c = lane; c < nc; c += 32) {
+      const float* r = rec_ptr(p, u0 + c);
+      const float mc = r[1];
+      const float sc = r[2];
+      const int cnt = reinterpret_cast<const int*>(r)[0];
+      if (mc != -INFINITY) S += sc * exp2f((mc - M) * kLog2e);
+      ovf |= cnt > C;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+    ovf = __any_sync(0xffffffffu, ovf);
+    for (int g = lane; g < G; g += 32) {
+      float gm = -INFINITY;
+      for (int c = 0; c < nc; ++c) gm = fmaxf(gm, rec_ptr(p, u0 + c)[4 + g]);
+      sm.selg[warp][g] = gm;
+    }
+    __syncwarp();
+    const float rt = warp_kth_largest(sm.selg[warp], G, K);
+    if (lane == 0) {
+      RowSel rs;
+      rs.rtopk = rt;
+      rs.ncand = 0;
+      if (M == -INFINITY || beam == -INFINITY) {
+        rs.kind = ROW_DEAD;
+        rs.c = -(double)INFINITY;
+        rs.lse = M == -INFINITY ? -INFINITY : M + logf(S);
+      } else {
+        const float log_s = logf(S);
+        rs.kind = ROW_LIVE;
+        rs.c = (double)beam - (double)M - (double)log_s;  // beam - lse, lse = M + log S
+        rs.lse = (float)((double)M + (double)log_s);
+      }
+      sm.row[j] = rs;
+      if (ovf) sm.ovf = 1;
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  int path = 0;
+  if (sm.ovf) path = 1;
+  if (p.flags & kFlagForceExact) path = 2;
+  if (path == 0) {
+    // 2. survivors of the row-level R-top-k, rescored: beam_score + x - lse
+    for (int pair = warp; pair < K * nc; pair += kSelWarps) {
+      const int j = pair / nc;
+      const RowSel& rs = sm.row[j];
+      if (rs.kind != ROW_LIVE) continue;
+      const long long u = (long long)(b * K + j) * nc + (pair - j * nc);
+      const int cnt = min(reinterpret_cast<const int*>(rec_ptr(p, u))[0], C);
+      const float rt = rs.rtopk;
+      const double cj = rs.c;
+      for (int q = lane; q < cnt; q += 32) {
+        const int2 raw = *reinterpret_cast<const int2*>(p.slots + (size_t)u * C + q);
+        const float x = __int_as_float(raw.x);
+        if (x >= rt) {
+          const Key key = make_key((float)(cj + (double)x), j, x, raw.y);
+          const int pos = atomicAdd(&sm.nsel, 1);
+          if (pos < kSelCap)
+            sm.sel[pos] = key;
+          else
+            sm.big = 1;
+          atomicAdd(&sm.row[j].ncand, 1);
+        }
+      }
+    }
+    for (int idx = tid; idx < K * K; idx += kSelThreads) {
+      const int j = idx / K, v = idx - (idx / K) * K;
+      const int kind = sm.row[j].kind;
+      if (kind == ROW_FIN && v == 0) {
+        const int pos = atomicAdd(&sm.nsel, 1);
+        if (pos < kSelCap)
+          sm.sel[pos] = make_key(p.beam[b * K + j], j, 0.0f, p.eos);
+        else
+          sm.big = 1;
+      } else if (kind == ROW_DEAD) {
+        const int pos = atomicAdd(&sm.nsel, 1);
+        if (pos < kSelCap)
+          sm.sel[pos] = make_key(-INFINITY, j, 0.0f, v);
+        else
+          sm.big = 1;
+        if (v == 0) sm.row[j].ncand = K;
+      }
+    }
+    __syncthreads();
+    if (sm.big) path = 3;
+  }
+  if (path != 0) {
+    exact_select<DT, BIAS>(p, sm, b, path);
+    return;
+  }
+  // 3. rank of every survivor among the survivors; ranks 0..K-1 are the output
+  const int n = sm.nsel;
+  for (int i = tid; i < n; i += kSelThreads) {
+    const Key ki = sm.sel[i];
+    int rank = 0;
+    for (int q = 0; q < n; ++q) rank += key_less(sm.sel[q], ki);
+    if (rank < K) write_output(p, b, rank, ki);
+  }
+  write_row_stats(p, sm, b, false);
+  if (tid == 0) p.bstat[b] = 0;
+}
+
+template <int DT, bool BIAS>
+cudaError_t launch_t(const StepParams& p, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.batch);
+  cfg.blockDim = dim3(kSelThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, beam_select_kernel<DT, BIAS>, p);
+}
+
+}  // namespace
+
+cudaError_t launch_beam_select(const StepParams& p, int dtype, cudaStream_t stream) {
+  const bool bias = p.bias != nullptr;
+  switch (dtype) {
+    case DT_F32: return bias ? launch_t<DT_F32, true>(p, stream) : launch_t<DT_F32, false>(p, stream);
+    case DT_F16: return bias ? launch_t<DT_F16, true>(p, stream) : launch_t<DT_F16, false>(p, stream);
+    case DT_BF16: return bias ? launch_t<DT_BF16, true>(p, stream) : launch_t<DT_BF16, false>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace lsb

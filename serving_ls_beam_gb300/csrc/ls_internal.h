@@ -9,15 +9,17 @@
 namespace lsb {
 
 // ---------------------------------------------------------------- kernel shape constants
-// Beam-step kernel: one CTA is a group of kThreads threads that owns one chunk of one
-// row at a time; the chunk sits in shared memory (bulk-copied) while the threads hold
-// it in registers, kVpt 16-byte vectors each.
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
+// K1 (beam_rows.cu): CTAs of kRowWarps independent warps; a warp owns one chunk of
+// 32 x VPL 16-byte vectors at a time, streamed through its own 2-stage shared ring.
+constexpr int kRowThreads = 256;
+constexpr int kRowWarps = kRowThreads / 32;
+constexpr int kRowBarBytes = 128;  // per-warp mbarriers at the start of shared memory
+constexpr int kVplMin = 4;         // smallest vectors-per-lane variant built
+// K2 (beam_select.cu): one CTA per batch.
+constexpr int kSelThreads = 256;
+constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kMaxK = 64;
-constexpr int kSelCap = 512;   // candidates the in-CTA fine rank holds in shared memory
-constexpr int kVptMin = 4;     // smallest vectors-per-thread variant built
-constexpr int kMinChunkElems = kVptMin * kThreads * 4;  // fp32: 4 elements per vector
+constexpr int kSelCap = 512;  // survivors the fine rank holds in shared memory
 
 // Device status bits (workspace word 0).
 constexpr uint32_t kDevTimeout = 1u << 0;
@@ -63,7 +65,9 @@ inline WsLayout ws_layout(int batch, int k, int vocab) {
   w.groups = pow2_ceil(k);
   w.slot_cap = (int)align_up((size_t)(4 * k + 32), 8);
   w.rec_stride = (int)align_up((size_t)(16 + 4 * w.groups), 16);
-  w.nc_max = (vocab + kMinChunkElems - 1) / kMinChunkElems + 8;
+  // chunks of 32 x kVplMin vectors over a row of up to 4-byte elements (+ 15 bytes of lead)
+  const long long nv_max = (15 + 4ll * vocab + 15) / 16;
+  w.nc_max = (int)((nv_max + 32 * kVplMin - 1) / (32 * kVplMin));
   size_t off = 0;
   w.status_off = off;
   off += 256;
@@ -100,7 +104,6 @@ struct StepParams {
   int batch, k, vocab, eos;
   int rows;
   int nc;         // chunks per row
-  int chunk_len;  // elements per chunk (multiple of the 16-byte vector width)
   int groups;
   int slot_cap;
   int rec_stride;
@@ -125,10 +128,10 @@ struct ReorderParams {
 };
 
 // Launchers (defined next to their kernels).
-cudaError_t launch_beam_step(const StepParams& p, int dtype, int vpt, int grid, size_t smem,
-                             cudaStream_t stream);
-cudaError_t beam_step_config(int dtype, bool bias, int vpt, size_t smem, int* occupancy);
-size_t beam_step_smem_bytes(int vpt);
+size_t beam_rows_smem_bytes(int vpl);
+cudaError_t beam_rows_config(int dtype, bool bias, int vpl, int* occupancy);
+cudaError_t launch_beam_rows(const StepParams& p, int dtype, int vpl, int grid, cudaStream_t stream);
+cudaError_t launch_beam_select(const StepParams& p, int dtype, cudaStream_t stream);
 cudaError_t launch_cache_reorder(const ReorderParams& p, int unit, int grid, cudaStream_t stream);
 cudaError_t cache_reorder_occupancy(int unit, int* occupancy);
 
