@@ -114,15 +114,6 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 int dtype_bytes(ls_dtype d) { return d == LS_DTYPE_F32 ? 4 : 2; }
 bool dtype_ok(ls_dtype d) { return d == LS_DTYPE_F32 || d == LS_DTYPE_F16 || d == LS_DTYPE_BF16; }
 
-// Granlund-Montgomery round-up multiplier for division by d (1 <= d < 2^31).
-void make_divisor(uint32_t d, uint32_t* magic, int* shift) {
-  int s = 0;
-  while ((1ull << s) < d) ++s;
-  const unsigned long long m = ((1ull << 32) * ((1ull << s) - d)) / d + 1;
-  *magic = (uint32_t)m;
-  *shift = s;
-}
-
 }  // namespace
 
 extern "C" {
@@ -168,7 +159,8 @@ ls_status ls_beam_step(const void* logits, ls_dtype logit_dtype, const float* bi
   if (!di) return cuda_fail(cudaErrorUnknown);
 
   const int dtype = (int)logit_dtype;
-  const int vpl = dbg.vpl ? dbg.vpl : 8;
+  // 8 vectors per lane (4 KB chunks) unless 16-bit logits with a bias (register pressure)
+  const int vpl = dbg.vpl ? dbg.vpl : ((es == 2 && bias) ? 4 : 8);
   const int occ = step_occupancy(di, dtype, bias != nullptr, vpl);
   if (occ < 1) return cuda_fail(cudaErrorUnknown);
   const long long rows = (long long)batch * k;
@@ -204,6 +196,7 @@ ls_status ls_beam_step(const void* logits, ls_dtype logit_dtype, const float* bi
   p.eos = eos_id;
   p.rows = (int)rows;
   p.nc = nc;
+  make_divisor((uint32_t)nc, &p.nc_magic, &p.nc_shift);
   p.groups = wl.groups;
   p.slot_cap = wl.slot_cap;
   p.rec_stride = wl.rec_stride;

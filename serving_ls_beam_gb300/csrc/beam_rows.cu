@@ -72,6 +72,22 @@ __device__ __forceinline__ float warp_kth_of_64(float a, float b, int k) {
   return __shfl_sync(0xffffffffu, mine, __ffs(hit) - 1);
 }
 
+// Max of the VEC values of a 16-byte vector (values before any bias).
+template <int DT>
+__device__ __forceinline__ float vec_max(const uint4& d) {
+  if constexpr (DT == DT_F32) {
+    return fmaxf(fmaxf(__uint_as_float(d.x), __uint_as_float(d.y)), fmaxf(__uint_as_float(d.z), __uint_as_float(d.w)));
+  } else if constexpr (DT == DT_F16) {
+    const __half2* h = reinterpret_cast<const __half2*>(&d);
+    const __half2 m = __hmax2(__hmax2(h[0], h[1]), __hmax2(h[2], h[3]));
+    return fmaxf(__low2float(m), __high2float(m));
+  } else {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&d);
+    const __nv_bfloat162 m = __hmax2(__hmax2(h[0], h[1]), __hmax2(h[2], h[3]));
+    return fmaxf(__low2float(m), __high2float(m));
+  }
+}
+
 template <int DT, bool BIAS, int VPL>
 __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepParams p) {
   constexpr int VEC = Traits<DT>::kVec;
@@ -90,6 +106,7 @@ __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepPar
   const int n_mine = gw < units ? (units - gw + nwarps - 1) / nwarps : 0;
   const unsigned char* logits = static_cast<const unsigned char*>(p.logits);
   const int row_bytes = V * ES;
+  const unsigned long long kL2 = pack2(kLog2e, kLog2e);
 
   if (lane == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(smem_addr(&bars[s]), 1);
@@ -97,7 +114,8 @@ __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepPar
   }
   __syncwarp();
 
-  auto live = [&](int u) -> bool { return !(p.finished && p.finished[u / nc]); };
+  auto row_of = [&](int u) -> int { return (int)fast_div((uint32_t)u, p.nc_magic, p.nc_shift); };
+  auto live = [&](int u) -> bool { return !(p.finished && p.finished[row_of(u)]); };
   struct Geo {
     const unsigned char* rb;  // 16-byte aligned start of the row's first vector
     int lead;                 // bytes of that vector before the row starts
@@ -106,7 +124,7 @@ __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepPar
   };
   auto geometry = [&](int u) -> Geo {
     Geo g;
-    const int row = u / nc;
+    const int row = row_of(u);
     const int c = u - row * nc;
     const unsigned char* rowp = logits + (size_t)row * row_bytes;
     g.lead = (int)(reinterpret_cast<uintptr_t>(rowp) & 15);
@@ -176,6 +194,7 @@ __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepPar
     ++n_cons;
     if (lane == 0) fill(n_cons);  // the stage just read is free again
 
+    // x = logit (+ bias) of vector r
     auto values = [&](int r, float (&x)[VEC]) {
       unpack<DT>(d[r], x);
       if constexpr (BIAS) {
@@ -204,41 +223,50 @@ __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepPar
       }
     };
 
-    // first traversal: max per lane (per lane half for 64 groups), then sum of exp
-    float m0 = -INFINITY, m1 = -INFINITY;
+    // first traversal, part 1: per-vector maxima (packed 16-bit max when there is no bias)
+    float vmax[VPL];
 #pragma unroll
     for (int r = 0; r < VPL; ++r) {
-      float x[VEC];
-      values(r, x);
-      float mr = x[0];
+      if constexpr (BIAS) {
+        float x[VEC];
+        values(r, x);
+        float mr = x[0];
 #pragma unroll
-      for (int e = 1; e < VEC; ++e) mr = fmaxf(mr, x[e]);
-      if (r & 1)
-        m1 = fmaxf(m1, mr);
-      else
-        m0 = fmaxf(m0, mr);
+        for (int e = 1; e < VEC; ++e) mr = fmaxf(mr, x[e]);
+        vmax[r] = mr;
+      } else {
+        vmax[r] = vec_max<DT>(d[r]);
+      }
+    }
+    float m0 = -INFINITY, m1 = -INFINITY;  // even / odd vectors (the two groups of a lane when G = 64)
+#pragma unroll
+    for (int r = 0; r < VPL; r += 2) {
+      m0 = fmaxf(m0, vmax[r]);
+      if (r + 1 < VPL) m1 = fmaxf(m1, vmax[r + 1]);
     }
     const float mt = fmaxf(m0, m1);
-    float st = 0.0f;
-    if (mt != -INFINITY) {
+    const float M = warp_max(mt);
+    // first traversal, part 2: sum of exp(x - M) = 2^((x - M) log2 e), packed fp32x2;
+    // x - M is exact for the terms that dominate the sum, so large logits keep precision
+    float ssum = 0.0f;
+    if (M != -INFINITY) {
+      const unsigned long long m2 = pack2(M, M);
+      unsigned long long acc = pack2(0.0f, 0.0f);
 #pragma unroll
       for (int r = 0; r < VPL; ++r) {
         float x[VEC];
         values(r, x);
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) st += fast_exp2((x[e] - mt) * kLog2e);
+        for (int e = 0; e < VEC; e += 2) {
+          const float2 t = unpack2(mul2(sub2(pack2(x[e], x[e + 1]), m2), kL2));
+          acc = add2(acc, pack2(fast_exp2(t.x), fast_exp2(t.y)));
+        }
       }
+      const float2 a = unpack2(acc);
+      ssum = a.x + a.y;
     }
-    // chunk (max, sum) by shuffles
-    float m = mt, ssum = st;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float mo = __shfl_xor_sync(0xffffffffu, m, o);
-      const float so = __shfl_xor_sync(0xffffffffu, ssum, o);
-      const float M = fmaxf(m, mo);
-      ssum = (M == -INFINITY) ? 0.0f : ssum * fast_exp2((m - M) * kLog2e) + so * fast_exp2((mo - M) * kLog2e);
-      m = M;
-    }
+    for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
     // group maxima and the chunk's R-top-k
     float* rec = reinterpret_cast<float*>(p.rec + (size_t)u * p.rec_stride);
     float rt;
@@ -252,12 +280,12 @@ __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepPar
       rec[4 + 32 + lane] = m1;
       rt = warp_kth_of_64(m0, m1, K);
     }
-    // second traversal: survivors x >= rt, positions by a warp prefix sum
+    // second traversal: survivors x >= rt; only vectors whose max reaches rt are opened
     auto count = [&](float thr) -> int {
       int c = 0;
-      if (mt >= thr) {
 #pragma unroll
-        for (int r = 0; r < VPL; ++r) {
+      for (int r = 0; r < VPL; ++r) {
+        if (vmax[r] >= thr) {
           const int jl = lane + 32 * r;
           if (jl < g.nvec) {
             float x[VEC];
@@ -274,12 +302,12 @@ __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepPar
       return c;
     };
     int cnt = count(rt);
-    int total = __reduce_add_sync(0xffffffffu, (unsigned)cnt);
+    int total = (int)__reduce_add_sync(0xffffffffu, (unsigned)cnt);
     if (total > C && K <= 32) {
       // tighter bound: k-th largest of the 32 per-lane maxima (32 disjoint groups)
       rt = fmaxf(rt, warp_kth_of_lanes(mt, 32, K));
       cnt = count(rt);
-      total = __reduce_add_sync(0xffffffffu, (unsigned)cnt);
+      total = (int)__reduce_add_sync(0xffffffffu, (unsigned)cnt);
     }
     int incl = cnt;
 #pragma unroll
@@ -292,22 +320,24 @@ __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepPar
       CandSlot* slots = p.slots + (size_t)u * C;
 #pragma unroll
       for (int r = 0; r < VPL; ++r) {
-        const int jl = lane + 32 * r;
-        if (jl < g.nvec) {
-          float x[VEC];
-          values(r, x);
-          const int base_b = (g.j0 + jl) * 16 - g.lead;
+        if (vmax[r] >= rt) {
+          const int jl = lane + 32 * r;
+          if (jl < g.nvec) {
+            float x[VEC];
+            values(r, x);
+            const int base_b = (g.j0 + jl) * 16 - g.lead;
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) {
-            const int eb = base_b + e * ES;
-            if (x[e] >= rt && eb >= 0 && eb < row_bytes) {
-              if (pos < C) {
-                CandSlot cs;
-                cs.x = x[e];
-                cs.v = eb / ES;
-                slots[pos] = cs;
+            for (int e = 0; e < VEC; ++e) {
+              const int eb = base_b + e * ES;
+              if (x[e] >= rt && eb >= 0 && eb < row_bytes) {
+                if (pos < C) {
+                  CandSlot cs;
+                  cs.x = x[e];
+                  cs.v = eb / ES;
+                  slots[pos] = cs;
+                }
+                ++pos;
               }
-              ++pos;
             }
           }
         }
@@ -315,7 +345,7 @@ __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepPar
     }
     if (lane == 0) {
       reinterpret_cast<int*>(rec)[0] = total;
-      rec[1] = m;
+      rec[1] = M;
       rec[2] = ssum;
     }
   }

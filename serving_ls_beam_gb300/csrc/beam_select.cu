@@ -30,8 +30,12 @@ struct RowSel {
   int ncand;
 };
 
+constexpr int kPairTile = 1024;  // (beam, chunk) pairs whose slot counts are scanned at once
+
 struct __align__(16) SelSmem {
-  int nsel, big, ovf, nbest, nrl;
+  int nsel, big, ovf, nbest, nrl, ptotal;
+  int pc[kPairTile];   // slots to read per pair of the tile, then their exclusive prefix sums
+  int wsum[kSelWarps];
   int wc[kSelWarps];
   unsigned int hist[256];
   unsigned int prefix, pmask;
@@ -303,10 +307,22 @@ __global__ void __launch_bounds__(kSelThreads) beam_select_kernel(const StepPara
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
     ovf = __any_sync(0xffffffffu, ovf);
-    for (int g = lane; g < G; g += 32) {
+    // group maxima merged over the chunks: lanes split the (chunk, group) pairs
+    if (G <= 32) {
+      const int g = lane & (G - 1);
       float gm = -INFINITY;
-      for (int c = 0; c < nc; ++c) gm = fmaxf(gm, rec_ptr(p, u0 + c)[4 + g]);
-      sm.selg[warp][g] = gm;
+      for (int c = lane / G; c < nc; c += 32 / G) gm = fmaxf(gm, rec_ptr(p, u0 + c)[4 + g]);
+      for (int o = 16; o >= G; o >>= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, o));
+      if (lane < G) sm.selg[warp][lane] = gm;
+    } else {
+      float ga = -INFINITY, gb = -INFINITY;
+      for (int c = 0; c < nc; ++c) {
+        const float* r = rec_ptr(p, u0 + c);
+        ga = fmaxf(ga, r[4 + lane]);
+        gb = fmaxf(gb, r[4 + 32 + lane]);
+      }
+      sm.selg[warp][lane] = ga;
+      sm.selg[warp][32 + lane] = gb;
     }
     __syncwarp();
     const float rt = warp_kth_largest(sm.selg[warp], G, K);
@@ -334,20 +350,67 @@ __global__ void __launch_bounds__(kSelThreads) beam_select_kernel(const StepPara
   if (sm.ovf) path = 1;
   if (p.flags & kFlagForceExact) path = 2;
   if (path == 0) {
-    // 2. survivors of the row-level R-top-k, rescored: beam_score + x - lse
-    for (int pair = warp; pair < K * nc; pair += kSelWarps) {
-      const int j = pair / nc;
-      const RowSel& rs = sm.row[j];
-      if (rs.kind != ROW_LIVE) continue;
-      const long long u = (long long)(b * K + j) * nc + (pair - j * nc);
-      const int cnt = min(reinterpret_cast<const int*>(rec_ptr(p, u))[0], C);
-      const float rt = rs.rtopk;
-      const double cj = rs.c;
-      for (int q = lane; q < cnt; q += 32) {
-        const int2 raw = *reinterpret_cast<const int2*>(p.slots + (size_t)u * C + q);
+    // 2. survivors of the row-level R-top-k, rescored: beam_score + x - lse.  The slots of
+    // all (beam, chunk) pairs are flattened so that every load is independent.
+    const int P = K * nc;
+    for (int t0 = 0; t0 < P; t0 += kPairTile) {
+      const int nt = min(kPairTile, P - t0);
+      for (int i = tid; i < nt; i += kSelThreads) {
+        const int pair = t0 + i;
+        const int j = pair / nc;
+        int c = 0;
+        if (sm.row[j].kind == ROW_LIVE)
+          c = min(reinterpret_cast<const int*>(rec_ptr(p, (long long)b * K * nc + pair))[0], C);
+        sm.pc[i] = c;
+      }
+      __syncthreads();
+      // exclusive scan of pc[0..nt): 4 consecutive entries per thread
+      constexpr int kPer = kPairTile / kSelThreads;
+      int loc[kPer];
+      int run = 0;
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) {
+        const int i = tid * kPer + e;
+        loc[e] = run;
+        run += (i < nt) ? sm.pc[i] : 0;
+      }
+      int incl = run;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      if (lane == 31) sm.wsum[warp] = incl;
+      __syncthreads();
+      int wbase = 0, tot = 0;
+      for (int w = 0; w < kSelWarps; ++w) {
+        wbase += (w < warp) ? sm.wsum[w] : 0;
+        tot += sm.wsum[w];
+      }
+      const int tbase = wbase + incl - run;
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) {
+        const int i = tid * kPer + e;
+        if (i < nt) sm.pc[i] = tbase + loc[e];
+      }
+      __syncthreads();
+      for (int q = tid; q < tot; q += kSelThreads) {
+        int lo = 0, hi = nt - 1;  // last pair with prefix <= q
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (sm.pc[mid] <= q)
+            lo = mid;
+          else
+            hi = mid - 1;
+        }
+        const int pair = t0 + lo;
+        const int j = pair / nc;
+        const long long u = (long long)b * K * nc + pair;
+        const int2 raw = *reinterpret_cast<const int2*>(p.slots + (size_t)u * C + (q - sm.pc[lo]));
         const float x = __int_as_float(raw.x);
-        if (x >= rt) {
-          const Key key = make_key((float)(cj + (double)x), j, x, raw.y);
+        const RowSel& rs = sm.row[j];
+        if (x >= rs.rtopk) {
+          const Key key = make_key((float)(rs.c + (double)x), j, x, raw.y);
           const int pos = atomicAdd(&sm.nsel, 1);
           if (pos < kSelCap)
             sm.sel[pos] = key;
@@ -356,6 +419,7 @@ __global__ void __launch_bounds__(kSelThreads) beam_select_kernel(const StepPara
           atomicAdd(&sm.row[j].ncand, 1);
         }
       }
+      __syncthreads();
     }
     for (int idx = tid; idx < K * K; idx += kSelThreads) {
       const int j = idx / K, v = idx - (idx / K) * K;

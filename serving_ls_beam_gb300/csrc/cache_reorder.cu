@@ -39,13 +39,6 @@ struct Word<1> {
   using T = uint8_t;
 };
 
-// q = n / d for n < 2^31 with a precomputed multiplier (Granlund & Montgomery,
-// "Division by invariant integers using multiplication", 1994, round-up variant).
-__device__ __forceinline__ uint32_t fast_div(uint32_t n, uint32_t magic, int shift) {
-  const uint32_t hi = __umulhi(n, magic);
-  return (hi + n) >> shift;
-}
-
 template <int UNIT>
 __global__ void __launch_bounds__(kCopyThreads) cache_reorder_kernel(const ReorderParams p) {
   using W = typename Word<UNIT>::T;

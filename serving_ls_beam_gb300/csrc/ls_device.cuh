@@ -81,6 +81,39 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Packed fp32x2 arithmetic (sm_100 family): two lanes of float math per instruction.
+__device__ __forceinline__ unsigned long long pack2(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 unpack2(unsigned long long r) {
+  float2 f;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(r));
+  return f;
+}
+__device__ __forceinline__ unsigned long long sub2(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// q = n / d for n < 2^31 with a multiplier prepared on the host (Granlund & Montgomery,
+// "Division by invariant integers using multiplication", 1994, round-up variant).
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, uint32_t magic, int shift) {
+  return (__umulhi(n, magic) + n) >> shift;
+}
+
 // Order-preserving map of a float onto uint32 (ascending).  -0 is folded onto +0.
 __device__ __forceinline__ uint32_t float_ord(float f) {
   uint32_t u = __float_as_uint(f + 0.0f);

@@ -57,6 +57,16 @@ __host__ __device__ inline int pow2_ceil(int x) {
 }
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Granlund-Montgomery round-up multiplier for division by d (1 <= d < 2^31); the device
+// side is fast_div() in ls_device.cuh.  Exact for dividends below 2^31.
+inline void make_divisor(uint32_t d, uint32_t* magic, int* shift) {
+  int s = 0;
+  while ((1ull << s) < d) ++s;
+  const unsigned long long m = ((1ull << 32) * ((1ull << s) - d)) / d + 1;
+  *magic = (uint32_t)m;
+  *shift = s;
+}
+
 // Returns total == 0 for unsupported shapes.
 inline WsLayout ws_layout(int batch, int k, int vocab) {
   WsLayout w{};
@@ -104,6 +114,8 @@ struct StepParams {
   int batch, k, vocab, eos;
   int rows;
   int nc;         // chunks per row
+  uint32_t nc_magic;  // fast division by nc
+  int nc_shift;
   int groups;
   int slot_cap;
   int rec_stride;
