@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepPar
   const int n_mine = gw < units ? (units - gw + nwarps - 1) / nwarps : 0;
   const unsigned char* logits = static_cast<const unsigned char*>(p.logits);
   const int row_bytes = V * ES;
-  const unsigned long long kL2 = pack2(kLog2e, kLog2e);
+  const float2 kL2 = make_float2(kLog2e, kLog2e);
 
   if (lane == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(smem_addr(&bars[s]), 1);
@@ -250,20 +250,19 @@ __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepPar
     // x - M is exact for the terms that dominate the sum, so large logits keep precision
     float ssum = 0.0f;
     if (M != -INFINITY) {
-      const unsigned long long m2 = pack2(M, M);
-      unsigned long long acc = pack2(0.0f, 0.0f);
+      const float2 nm2 = make_float2(-M, -M);
+      float2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll
       for (int r = 0; r < VPL; ++r) {
         float x[VEC];
         values(r, x);
 #pragma unroll
         for (int e = 0; e < VEC; e += 2) {
-          const float2 t = unpack2(mul2(sub2(pack2(x[e], x[e + 1]), m2), kL2));
-          acc = add2(acc, pack2(fast_exp2(t.x), fast_exp2(t.y)));
+          const float2 t = __fmul2_rn(__fadd2_rn(make_float2(x[e], x[e + 1]), nm2), kL2);
+          acc = __fadd2_rn(acc, make_float2(fast_exp2(t.x), fast_exp2(t.y)));
         }
       }
-      const float2 a = unpack2(acc);
-      ssum = a.x + a.y;
+      ssum = acc.x + acc.y;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);

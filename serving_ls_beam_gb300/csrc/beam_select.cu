@@ -291,27 +291,62 @@ __global__ void __launch_bounds__(kSelThreads) beam_select_kernel(const StepPara
       continue;
     }
     const long long u0 = (long long)row * nc;
-    float M = -INFINITY;
-    for (int c = lane; c < nc; c += 32) M = fmaxf(M, rec_ptr(p, u0 + c)[1]);
-    M = warp_max(M);
-    float S = 0.0f;
+    // (max, sum of exp) merged over the chunks: online rescaling per lane, 4 chunks per
+    // round with their loads issued together, then a fixed shuffle tree (deterministic)
+    float M = -INFINITY, S = 0.0f;
     bool ovf = false;
-    for (int c = lane; c < nc; c += 32) {
-      const float* r = rec_ptr(p, u0 + c);
-      const float mc = r[1];
-      const float sc = r[2];
-      const int cnt = reinterpret_cast<const int*>(r)[0];
-      if (mc != -INFINITY) S += sc * exp2f((mc - M) * kLog2e);
-      ovf |= cnt > C;
+    for (int c0 = lane; c0 < nc; c0 += 4 * 32) {
+      float mc[4], sc[4];
+      int cn[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int c = c0 + 32 * t;
+        mc[t] = -INFINITY;
+        sc[t] = 0.0f;
+        cn[t] = 0;
+        if (c < nc) {
+          const float* r = rec_ptr(p, u0 + c);
+          cn[t] = reinterpret_cast<const int*>(r)[0];
+          mc[t] = r[1];
+          sc[t] = r[2];
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        ovf |= cn[t] > C;
+        const float Mn = fmaxf(M, mc[t]);
+        if (Mn != -INFINITY) {
+          S = S * exp2f((M - Mn) * kLog2e) + (mc[t] == -INFINITY ? 0.0f : sc[t] * exp2f((mc[t] - Mn) * kLog2e));
+          M = Mn;
+        }
+      }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+    for (int o = 16; o > 0; o >>= 1) {
+      const float Mo = __shfl_xor_sync(0xffffffffu, M, o);
+      const float So = __shfl_xor_sync(0xffffffffu, S, o);
+      const float Mn = fmaxf(M, Mo);
+      if (Mn != -INFINITY) {
+        S = (M == -INFINITY ? 0.0f : S * exp2f((M - Mn) * kLog2e)) +
+            (Mo == -INFINITY ? 0.0f : So * exp2f((Mo - Mn) * kLog2e));
+      }
+      M = Mn;
+    }
     ovf = __any_sync(0xffffffffu, ovf);
     // group maxima merged over the chunks: lanes split the (chunk, group) pairs
     if (G <= 32) {
       const int g = lane & (G - 1);
+      const int cs = 32 / G;
       float gm = -INFINITY;
-      for (int c = lane / G; c < nc; c += 32 / G) gm = fmaxf(gm, rec_ptr(p, u0 + c)[4 + g]);
+      for (int c0 = lane / G; c0 < nc; c0 += 4 * cs) {
+        float v[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int c = c0 + t * cs;
+          v[t] = c < nc ? rec_ptr(p, u0 + c)[4 + g] : -INFINITY;
+        }
+        gm = fmaxf(gm, fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])));
+      }
       for (int o = 16; o >= G; o >>= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, o));
       if (lane < G) sm.selg[warp][lane] = gm;
     } else {
@@ -394,29 +429,44 @@ __global__ void __launch_bounds__(kSelThreads) beam_select_kernel(const StepPara
         if (i < nt) sm.pc[i] = tbase + loc[e];
       }
       __syncthreads();
-      for (int q = tid; q < tot; q += kSelThreads) {
-        int lo = 0, hi = nt - 1;  // last pair with prefix <= q
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (sm.pc[mid] <= q)
-            lo = mid;
-          else
-            hi = mid - 1;
+      // 4 slots per thread per round, their loads issued together
+      for (int q0 = tid; q0 < tot; q0 += 4 * kSelThreads) {
+        int2 raw[4];
+        int jj[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int q = q0 + t * kSelThreads;
+          jj[t] = -1;
+          if (q < tot) {
+            int lo = 0, hi = nt - 1;  // last pair with prefix <= q
+            while (lo < hi) {
+              const int mid = (lo + hi + 1) >> 1;
+              if (sm.pc[mid] <= q)
+                lo = mid;
+              else
+                hi = mid - 1;
+            }
+            const int pair = t0 + lo;
+            jj[t] = pair / nc;
+            const long long u = (long long)b * K * nc + pair;
+            raw[t] = *reinterpret_cast<const int2*>(p.slots + (size_t)u * C + (q - sm.pc[lo]));
+          }
         }
-        const int pair = t0 + lo;
-        const int j = pair / nc;
-        const long long u = (long long)b * K * nc + pair;
-        const int2 raw = *reinterpret_cast<const int2*>(p.slots + (size_t)u * C + (q - sm.pc[lo]));
-        const float x = __int_as_float(raw.x);
-        const RowSel& rs = sm.row[j];
-        if (x >= rs.rtopk) {
-          const Key key = make_key((float)(rs.c + (double)x), j, x, raw.y);
-          const int pos = atomicAdd(&sm.nsel, 1);
-          if (pos < kSelCap)
-            sm.sel[pos] = key;
-          else
-            sm.big = 1;
-          atomicAdd(&sm.row[j].ncand, 1);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          if (jj[t] < 0) continue;
+          const int j = jj[t];
+          const float x = __int_as_float(raw[t].x);
+          const RowSel& rs = sm.row[j];
+          if (x >= rs.rtopk) {
+            const Key key = make_key((float)(rs.c + (double)x), j, x, raw[t].y);
+            const int pos = atomicAdd(&sm.nsel, 1);
+            if (pos < kSelCap)
+              sm.sel[pos] = key;
+            else
+              sm.big = 1;
+            atomicAdd(&sm.row[j].ncand, 1);
+          }
         }
       }
       __syncthreads();

@@ -27,14 +27,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+// Test the phase; the warp may be suspended for up to hint_ns while the phase is still
+// open (it resumes as soon as the phase completes), so a wait does not spin.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
       : "memory");
   return ok != 0;
 }
@@ -47,10 +49,11 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 
 // Wait for the barrier phase with the given parity; give up after limit_ns.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, long long limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+  const uint32_t hint = limit_ns < 100000 ? (uint32_t)limit_ns : 100000u;
+  if (mbar_try_wait(bar, parity, hint)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity, hint)) return true;
     if ((long long)(global_timer_ns() - t0) > limit_ns) return false;
   }
 }
@@ -80,33 +83,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 constexpr float kLog2e = 1.4426950408889634f;
-
-// Packed fp32x2 arithmetic (sm_100 family): two lanes of float math per instruction.
-__device__ __forceinline__ unsigned long long pack2(float a, float b) {
-  unsigned long long r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ float2 unpack2(unsigned long long r) {
-  float2 f;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(r));
-  return f;
-}
-__device__ __forceinline__ unsigned long long sub2(unsigned long long a, unsigned long long b) {
-  unsigned long long r;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ unsigned long long mul2(unsigned long long a, unsigned long long b) {
-  unsigned long long r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
-  unsigned long long r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
 
 // q = n / d for n < 2^31 with a multiplier prepared on the host (Granlund & Montgomery,
 // "Division by invariant integers using multiplication", 1994, round-up variant).
