@@ -88,6 +88,50 @@ __device__ __forceinline__ float vec_max(const uint4& d) {
   }
 }
 
+// Bit e set when element e of the vector is >= thr (values before any bias; thr is an
+// element value, hence exact in the element type).
+template <int DT>
+__device__ __forceinline__ uint32_t vec_ge_mask(const uint4& d, float thr) {
+  if constexpr (DT == DT_F32) {
+    return (__uint_as_float(d.x) >= thr ? 1u : 0u) | (__uint_as_float(d.y) >= thr ? 2u : 0u) |
+           (__uint_as_float(d.z) >= thr ? 4u : 0u) | (__uint_as_float(d.w) >= thr ? 8u : 0u);
+  } else {
+    const uint32_t w[4] = {d.x, d.y, d.z, d.w};
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t g;
+      if constexpr (DT == DT_F16) {
+        const __half2 t = __float2half2_rn(thr);
+        g = __hge2_mask(*reinterpret_cast<const __half2*>(&w[i]), t);
+      } else {
+        const __nv_bfloat162 t = __float2bfloat162_rn(thr);
+        g = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&w[i]), t);
+      }
+      m |= ((g & 1u) | ((g >> 15) & 2u)) << (2 * i);
+    }
+    return m;
+  }
+}
+
+// Element e (runtime index) of a 16-byte vector as float, without dynamic register indexing.
+template <int DT>
+__device__ __forceinline__ float vec_elem(const uint4& d, int e) {
+  if constexpr (DT == DT_F32) {
+    const uint32_t w = e == 0 ? d.x : e == 1 ? d.y : e == 2 ? d.z : d.w;
+    return __uint_as_float(w);
+  } else {
+    const int i = e >> 1;
+    const uint32_t w = i == 0 ? d.x : i == 1 ? d.y : i == 2 ? d.z : d.w;
+    const unsigned short h = (unsigned short)((e & 1) ? (w >> 16) : (w & 0xffffu));
+    if constexpr (DT == DT_F16) {
+      return __half2float(__ushort_as_half(h));
+    } else {
+      return __bfloat162float(__ushort_as_bfloat16(h));
+    }
+  }
+}
+
 template <int DT, bool BIAS, int VPL>
 __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepParams p) {
   constexpr int VEC = Traits<DT>::kVec;
@@ -106,7 +150,6 @@ __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepPar
   const int n_mine = gw < units ? (units - gw + nwarps - 1) / nwarps : 0;
   const unsigned char* logits = static_cast<const unsigned char*>(p.logits);
   const int row_bytes = V * ES;
-  const float2 kL2 = make_float2(kLog2e, kLog2e);
 
   if (lane == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(smem_addr(&bars[s]), 1);
@@ -194,9 +237,8 @@ __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepPar
     ++n_cons;
     if (lane == 0) fill(n_cons);  // the stage just read is free again
 
-    // x = logit (+ bias) of vector r
-    auto values = [&](int r, float (&x)[VEC]) {
-      unpack<DT>(d[r], x);
+    // x = logit + bias of vector r (bias only: the values without bias are d[r] itself)
+    auto add_bias = [&](int r, float (&x)[VEC]) {
       if constexpr (BIAS) {
         const int jl = lane + 32 * r;
         if (jl < g.nvec) {
@@ -222,17 +264,27 @@ __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepPar
         }
       }
     };
+    // with a bias the chunk is converted once to x = logit + bias, kept as floats
+    float xb[BIAS ? VPL * VEC : 1];
+    if constexpr (BIAS) {
+#pragma unroll
+      for (int r = 0; r < VPL; ++r) {
+        float x[VEC];
+        unpack<DT>(d[r], x);
+        add_bias(r, x);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) xb[r * VEC + e] = x[e];
+      }
+    }
 
-    // first traversal, part 1: per-vector maxima (packed 16-bit max when there is no bias)
+    // first traversal, part 1: per-vector maxima
     float vmax[VPL];
 #pragma unroll
     for (int r = 0; r < VPL; ++r) {
       if constexpr (BIAS) {
-        float x[VEC];
-        values(r, x);
-        float mr = x[0];
+        float mr = xb[r * VEC];
 #pragma unroll
-        for (int e = 1; e < VEC; ++e) mr = fmaxf(mr, x[e]);
+        for (int e = 1; e < VEC; ++e) mr = fmaxf(mr, xb[r * VEC + e]);
         vmax[r] = mr;
       } else {
         vmax[r] = vec_max<DT>(d[r]);
@@ -246,19 +298,30 @@ __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepPar
     }
     const float mt = fmaxf(m0, m1);
     const float M = warp_max(mt);
-    // first traversal, part 2: sum of exp(x - M) = 2^((x - M) log2 e), packed fp32x2;
-    // x - M is exact for the terms that dominate the sum, so large logits keep precision
+    // first traversal, part 2: sum of exp(x - M) = 2^((x - M) log2 e) with packed fp32x2.
+    // For |M| < 64, x log2e - M log2e in one fused multiply-add (the rounding of M log2e
+    // shifts every term alike, by at most 2^-18 in the exponent); otherwise the exact
+    // difference x - M first (exact for the terms that dominate the sum).
     float ssum = 0.0f;
     if (M != -INFINITY) {
-      const float2 nm2 = make_float2(-M, -M);
+      const float2 L2 = make_float2(kLog2e, kLog2e);
       float2 acc = make_float2(0.0f, 0.0f);
+      const bool fused = fabsf(M) < 64.0f;
+      const float2 nml = make_float2(-M * kLog2e, -M * kLog2e);
+      const float2 nm = make_float2(-M, -M);
 #pragma unroll
       for (int r = 0; r < VPL; ++r) {
         float x[VEC];
-        values(r, x);
+        if constexpr (BIAS) {
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) x[e] = xb[r * VEC + e];
+        } else {
+          unpack<DT>(d[r], x);
+        }
 #pragma unroll
         for (int e = 0; e < VEC; e += 2) {
-          const float2 t = __fmul2_rn(__fadd2_rn(make_float2(x[e], x[e + 1]), nm2), kL2);
+          const float2 xv = make_float2(x[e], x[e + 1]);
+          const float2 t = fused ? __ffma2_rn(xv, L2, nml) : __fmul2_rn(__fadd2_rn(xv, nm), L2);
           acc = __fadd2_rn(acc, make_float2(fast_exp2(t.x), fast_exp2(t.y)));
         }
       }
@@ -279,33 +342,43 @@ __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepPar
       rec[4 + 32 + lane] = m1;
       rt = warp_kth_of_64(m0, m1, K);
     }
-    // second traversal: survivors x >= rt; only vectors whose max reaches rt are opened
-    auto count = [&](float thr) -> int {
+    // second traversal: survivors x >= rt.  Only vectors whose max reaches rt are opened;
+    // their survivors are kept as bit masks (bit e of mask r = element e of vector r).
+    uint32_t mask[VPL];
+    auto build = [&](float thr) -> int {
       int c = 0;
 #pragma unroll
       for (int r = 0; r < VPL; ++r) {
-        if (vmax[r] >= thr) {
-          const int jl = lane + 32 * r;
-          if (jl < g.nvec) {
-            float x[VEC];
-            values(r, x);
-            const int base_b = (g.j0 + jl) * 16 - g.lead;
+        mask[r] = 0;
+        if (__any_sync(0xffffffffu, vmax[r] >= thr) && vmax[r] >= thr) {
+          uint32_t mr;
+          if constexpr (BIAS) {
+            mr = 0;
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) mr |= (xb[r * VEC + e] >= thr ? 1u : 0u) << e;
+          } else {
+            mr = vec_ge_mask<DT>(d[r], thr);
+          }
+          if (thr == -INFINITY) {  // every element passes: drop the ones outside the row
+            const int base_b = (g.j0 + lane + 32 * r) * 16 - g.lead;
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
               const int eb = base_b + e * ES;
-              c += (x[e] >= thr && eb >= 0 && eb < row_bytes) ? 1 : 0;
+              if (eb < 0 || eb >= row_bytes || lane + 32 * r >= g.nvec) mr &= ~(1u << e);
             }
           }
+          mask[r] = mr;
+          c += __popc(mr);
         }
       }
       return c;
     };
-    int cnt = count(rt);
+    int cnt = build(rt);
     int total = (int)__reduce_add_sync(0xffffffffu, (unsigned)cnt);
     if (total > C && K <= 32) {
       // tighter bound: k-th largest of the 32 per-lane maxima (32 disjoint groups)
       rt = fmaxf(rt, warp_kth_of_lanes(mt, 32, K));
-      cnt = count(rt);
+      cnt = build(rt);
       total = (int)__reduce_add_sync(0xffffffffu, (unsigned)cnt);
     }
     int incl = cnt;
@@ -319,26 +392,26 @@ __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepPar
       CandSlot* slots = p.slots + (size_t)u * C;
 #pragma unroll
       for (int r = 0; r < VPL; ++r) {
-        if (vmax[r] >= rt) {
-          const int jl = lane + 32 * r;
-          if (jl < g.nvec) {
-            float x[VEC];
-            values(r, x);
-            const int base_b = (g.j0 + jl) * 16 - g.lead;
+        uint32_t mr = mask[r];
+        const int base_e = ((g.j0 + lane + 32 * r) * 16 - g.lead) / ES;  // token id of element 0
+        while (mr) {
+          const int e = __ffs(mr) - 1;
+          mr &= mr - 1;
+          if (pos < C) {
+            CandSlot cs;
+            if constexpr (BIAS) {
+              float x = xb[r * VEC];
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-              const int eb = base_b + e * ES;
-              if (x[e] >= rt && eb >= 0 && eb < row_bytes) {
-                if (pos < C) {
-                  CandSlot cs;
-                  cs.x = x[e];
-                  cs.v = eb / ES;
-                  slots[pos] = cs;
-                }
-                ++pos;
-              }
+              for (int q = 1; q < VEC; ++q)
+                if (q == e) x = xb[r * VEC + q];
+              cs.x = x;
+            } else {
+              cs.x = vec_elem<DT>(d[r], e);
             }
+            cs.v = base_e + e;
+            slots[pos] = cs;
           }
+          ++pos;
         }
       }
     }

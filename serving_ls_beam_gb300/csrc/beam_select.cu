@@ -394,8 +394,11 @@ __global__ void __launch_bounds__(kSelThreads) beam_select_kernel(const StepPara
         const int pair = t0 + i;
         const int j = pair / nc;
         int c = 0;
-        if (sm.row[j].kind == ROW_LIVE)
-          c = min(reinterpret_cast<const int*>(rec_ptr(p, (long long)b * K * nc + pair))[0], C);
+        if (sm.row[j].kind == ROW_LIVE) {
+          // a chunk whose max is below the beam's R-top-k holds no survivor: skip its slots
+          const float* r = rec_ptr(p, (long long)b * K * nc + pair);
+          if (r[1] >= sm.row[j].rtopk) c = min(reinterpret_cast<const int*>(r)[0], C);
+        }
         sm.pc[i] = c;
       }
       __syncthreads();
