@@ -72,45 +72,57 @@ __device__ __forceinline__ float warp_kth_of_64(float a, float b, int k) {
   return __shfl_sync(0xffffffffu, mine, __ffs(hit) - 1);
 }
 
-// Max of the VEC values of a 16-byte vector (values before any bias).
+// Packed per-vector max: for 16-bit types a pair (max of even, max of odd elements) as
+// the type's 2-vector, kept as its 32-bit pattern; for fp32 the max itself.
 template <int DT>
-__device__ __forceinline__ float vec_max(const uint4& d) {
+__device__ __forceinline__ uint32_t vec_max_bits(const uint4& d) {
   if constexpr (DT == DT_F32) {
-    return fmaxf(fmaxf(__uint_as_float(d.x), __uint_as_float(d.y)), fmaxf(__uint_as_float(d.z), __uint_as_float(d.w)));
+    return __float_as_uint(
+        fmaxf(fmaxf(__uint_as_float(d.x), __uint_as_float(d.y)), fmaxf(__uint_as_float(d.z), __uint_as_float(d.w))));
   } else if constexpr (DT == DT_F16) {
     const __half2* h = reinterpret_cast<const __half2*>(&d);
     const __half2 m = __hmax2(__hmax2(h[0], h[1]), __hmax2(h[2], h[3]));
-    return fmaxf(__low2float(m), __high2float(m));
+    return *reinterpret_cast<const uint32_t*>(&m);
   } else {
     const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&d);
     const __nv_bfloat162 m = __hmax2(__hmax2(h[0], h[1]), __hmax2(h[2], h[3]));
-    return fmaxf(__low2float(m), __high2float(m));
+    return *reinterpret_cast<const uint32_t*>(&m);
   }
 }
-
-// Bit e set when element e of the vector is >= thr (values before any bias; thr is an
-// element value, hence exact in the element type).
 template <int DT>
-__device__ __forceinline__ uint32_t vec_ge_mask(const uint4& d, float thr) {
+__device__ __forceinline__ uint32_t max_bits(uint32_t a, uint32_t b) {
   if constexpr (DT == DT_F32) {
-    return (__uint_as_float(d.x) >= thr ? 1u : 0u) | (__uint_as_float(d.y) >= thr ? 2u : 0u) |
-           (__uint_as_float(d.z) >= thr ? 4u : 0u) | (__uint_as_float(d.w) >= thr ? 8u : 0u);
+    return __float_as_uint(fmaxf(__uint_as_float(a), __uint_as_float(b)));
+  } else if constexpr (DT == DT_F16) {
+    const __half2 m = __hmax2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+    return *reinterpret_cast<const uint32_t*>(&m);
   } else {
-    const uint32_t w[4] = {d.x, d.y, d.z, d.w};
-    uint32_t m = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint32_t g;
-      if constexpr (DT == DT_F16) {
-        const __half2 t = __float2half2_rn(thr);
-        g = __hge2_mask(*reinterpret_cast<const __half2*>(&w[i]), t);
-      } else {
-        const __nv_bfloat162 t = __float2bfloat162_rn(thr);
-        g = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&w[i]), t);
-      }
-      m |= ((g & 1u) | ((g >> 15) & 2u)) << (2 * i);
-    }
-    return m;
+    const __nv_bfloat162 m =
+        __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&a), *reinterpret_cast<const __nv_bfloat162*>(&b));
+    return *reinterpret_cast<const uint32_t*>(&m);
+  }
+}
+template <int DT>
+__device__ __forceinline__ float bits_max_float(uint32_t a) {
+  if constexpr (DT == DT_F32) {
+    return __uint_as_float(a);
+  } else if constexpr (DT == DT_F16) {
+    const __half2 h = *reinterpret_cast<const __half2*>(&a);
+    return fmaxf(__low2float(h), __high2float(h));
+  } else {
+    const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&a);
+    return fmaxf(__low2float(h), __high2float(h));
+  }
+}
+// true when the packed max reaches thr (thr is an element value, exact in the type)
+template <int DT>
+__device__ __forceinline__ bool bits_ge(uint32_t a, float thr) {
+  if constexpr (DT == DT_F32) {
+    return __uint_as_float(a) >= thr;
+  } else if constexpr (DT == DT_F16) {
+    return __hge2_mask(*reinterpret_cast<const __half2*>(&a), __float2half2_rn(thr)) != 0u;
+  } else {
+    return __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&a), __float2bfloat162_rn(thr)) != 0u;
   }
 }
 
@@ -233,19 +245,24 @@ __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepPar
         d[r] = make_uint4(w, w, w, w);
       }
     }
-    __syncwarp();
-    ++n_cons;
-    if (lane == 0) fill(n_cons);  // the stage just read is free again
 
-    // x = logit + bias of vector r (bias only: the values without bias are d[r] itself)
-    auto add_bias = [&](int r, float (&x)[VEC]) {
-      if constexpr (BIAS) {
+    // x = logit + bias of local vector jl's element e (bias only for tokens inside the row)
+    auto bias_of = [&](int jl, int e) -> float {
+      const int eb = (g.j0 + jl) * 16 - g.lead + e * ES;
+      return (eb >= 0 && eb < row_bytes) ? __ldg(p.bias + eb / ES) : 0.0f;
+    };
+    // with a bias the chunk is converted once to x = logit + bias, kept as floats
+    float xb[BIAS ? VPL * VEC : 1];
+    if constexpr (BIAS) {
+#pragma unroll
+      for (int r = 0; r < VPL; ++r) {
+        float x[VEC];
+        unpack<DT>(d[r], x);
         const int jl = lane + 32 * r;
+        const int base_b = (g.j0 + jl) * 16 - g.lead;
+        const int v0 = base_b / ES;  // token id of element 0 (negative before the row start)
         if (jl < g.nvec) {
-          const int base_b = (g.j0 + jl) * 16 - g.lead;
-          const int v0 = base_b / ES;  // token id of element 0 (negative before the row start)
-          const bool interior = base_b >= 0 && base_b + 16 <= row_bytes;
-          if (interior && ((reinterpret_cast<uintptr_t>(p.bias + v0) & 15) == 0)) {
+          if (base_b >= 0 && base_b + 16 <= row_bytes && ((reinterpret_cast<uintptr_t>(p.bias + v0) & 15) == 0)) {
 #pragma unroll
             for (int e = 0; e < VEC; e += 4) {
               const float4 bb = __ldg(reinterpret_cast<const float4*>(p.bias + v0 + e));
@@ -256,79 +273,38 @@ __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepPar
             }
           } else {
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-              const int v = v0 + e;
-              if (v >= 0 && v < V) x[e] += __ldg(p.bias + v);
-            }
+            for (int e = 0; e < VEC; ++e) x[e] += bias_of(jl, e);
           }
         }
-      }
-    };
-    // with a bias the chunk is converted once to x = logit + bias, kept as floats
-    float xb[BIAS ? VPL * VEC : 1];
-    if constexpr (BIAS) {
-#pragma unroll
-      for (int r = 0; r < VPL; ++r) {
-        float x[VEC];
-        unpack<DT>(d[r], x);
-        add_bias(r, x);
 #pragma unroll
         for (int e = 0; e < VEC; ++e) xb[r * VEC + e] = x[e];
       }
     }
 
-    // first traversal, part 1: per-vector maxima
-    float vmax[VPL];
+    // first traversal, part 1: per-vector maxima (packed), lane and chunk maxima
+    uint32_t vm[VPL];
 #pragma unroll
     for (int r = 0; r < VPL; ++r) {
       if constexpr (BIAS) {
         float mr = xb[r * VEC];
 #pragma unroll
         for (int e = 1; e < VEC; ++e) mr = fmaxf(mr, xb[r * VEC + e]);
-        vmax[r] = mr;
+        vm[r] = __float_as_uint(mr);
       } else {
-        vmax[r] = vec_max<DT>(d[r]);
+        vm[r] = vec_max_bits<DT>(d[r]);
       }
     }
-    float m0 = -INFINITY, m1 = -INFINITY;  // even / odd vectors (the two groups of a lane when G = 64)
+    constexpr int BT = BIAS ? DT_F32 : DT;  // type of the packed maxima
+    uint32_t b0 = vm[0], b1 = VPL > 1 ? vm[1] : vm[0];
 #pragma unroll
-    for (int r = 0; r < VPL; r += 2) {
-      m0 = fmaxf(m0, vmax[r]);
-      if (r + 1 < VPL) m1 = fmaxf(m1, vmax[r + 1]);
+    for (int r = 2; r < VPL; r += 2) {
+      b0 = max_bits<BT>(b0, vm[r]);
+      if (r + 1 < VPL) b1 = max_bits<BT>(b1, vm[r + 1]);
     }
+    const float m0 = bits_max_float<BT>(b0);  // even vectors (group lane when G = 64)
+    const float m1 = VPL > 1 ? bits_max_float<BT>(b1) : -INFINITY;  // odd vectors (group lane + 32)
     const float mt = fmaxf(m0, m1);
     const float M = warp_max(mt);
-    // first traversal, part 2: sum of exp(x - M) = 2^((x - M) log2 e) with packed fp32x2.
-    // For |M| < 64, x log2e - M log2e in one fused multiply-add (the rounding of M log2e
-    // shifts every term alike, by at most 2^-18 in the exponent); otherwise the exact
-    // difference x - M first (exact for the terms that dominate the sum).
-    float ssum = 0.0f;
-    if (M != -INFINITY) {
-      const float2 L2 = make_float2(kLog2e, kLog2e);
-      float2 acc = make_float2(0.0f, 0.0f);
-      const bool fused = fabsf(M) < 64.0f;
-      const float2 nml = make_float2(-M * kLog2e, -M * kLog2e);
-      const float2 nm = make_float2(-M, -M);
-#pragma unroll
-      for (int r = 0; r < VPL; ++r) {
-        float x[VEC];
-        if constexpr (BIAS) {
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) x[e] = xb[r * VEC + e];
-        } else {
-          unpack<DT>(d[r], x);
-        }
-#pragma unroll
-        for (int e = 0; e < VEC; e += 2) {
-          const float2 xv = make_float2(x[e], x[e + 1]);
-          const float2 t = fused ? __ffma2_rn(xv, L2, nml) : __fmul2_rn(__fadd2_rn(xv, nm), L2);
-          acc = __fadd2_rn(acc, make_float2(fast_exp2(t.x), fast_exp2(t.y)));
-        }
-      }
-      ssum = acc.x + acc.y;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
     // group maxima and the chunk's R-top-k
     float* rec = reinterpret_cast<float*>(p.rec + (size_t)u * p.rec_stride);
     float rt;
@@ -342,79 +318,170 @@ __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepPar
       rec[4 + 32 + lane] = m1;
       rt = warp_kth_of_64(m0, m1, K);
     }
-    // second traversal: survivors x >= rt.  Only vectors whose max reaches rt are opened;
-    // their survivors are kept as bit masks (bit e of mask r = element e of vector r).
-    uint32_t mask[VPL];
-    auto build = [&](float thr) -> int {
-      int c = 0;
+
+    // second traversal: survivors x >= rt.  The vectors whose max reaches rt are listed
+    // (one item per vector, items spread over the lanes) and re-read from shared memory.
+    auto list_items = [&](float thr, uint32_t (&qm)[VPL]) -> int {
+      int n = 0;
 #pragma unroll
       for (int r = 0; r < VPL; ++r) {
-        mask[r] = 0;
-        if (__any_sync(0xffffffffu, vmax[r] >= thr) && vmax[r] >= thr) {
-          uint32_t mr;
-          if constexpr (BIAS) {
-            mr = 0;
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) mr |= (xb[r * VEC + e] >= thr ? 1u : 0u) << e;
-          } else {
-            mr = vec_ge_mask<DT>(d[r], thr);
-          }
-          if (thr == -INFINITY) {  // every element passes: drop the ones outside the row
-            const int base_b = (g.j0 + lane + 32 * r) * 16 - g.lead;
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-              const int eb = base_b + e * ES;
-              if (eb < 0 || eb >= row_bytes || lane + 32 * r >= g.nvec) mr &= ~(1u << e);
-            }
-          }
-          mask[r] = mr;
-          c += __popc(mr);
-        }
+        bool hit;
+        if constexpr (BIAS)
+          hit = __uint_as_float(vm[r]) >= thr;
+        else
+          hit = bits_ge<DT>(vm[r], thr);
+        qm[r] = __ballot_sync(0xffffffffu, hit);
+        n += __popc(qm[r]);
       }
-      return c;
+      return n;
     };
-    int cnt = build(rt);
-    int total = (int)__reduce_add_sync(0xffffffffu, (unsigned)cnt);
+    // item t -> (vector row r, source lane)
+    auto item = [&](const uint32_t (&qm)[VPL], int t, int& r_out, int& l_out) {
+      int base = 0;
+      r_out = -1;
+#pragma unroll
+      for (int r = 0; r < VPL; ++r) {
+        const int c = __popc(qm[r]);
+        if (r_out < 0 && t < base + c) {
+          r_out = r;
+          l_out = (int)__fns(qm[r], 0, t - base + 1);
+        }
+        base += c;
+      }
+    };
+    // element mask of one item (bit e: element e survives)
+    auto item_mask = [&](int jl, float thr, const uint4& raw) -> uint32_t {
+      const int base_b = (g.j0 + jl) * 16 - g.lead;
+      float x[VEC];
+      unpack<DT>(raw, x);
+      uint32_t mr = 0;
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        const int eb = base_b + e * ES;
+        const bool in_row = jl < g.nvec && eb >= 0 && eb < row_bytes;
+        float xe = x[e];
+        if constexpr (BIAS) xe += in_row ? __ldg(p.bias + eb / ES) : 0.0f;
+        mr |= (in_row && xe >= thr ? 1u : 0u) << e;
+      }
+      return mr;
+    };
+    uint32_t qm[VPL];
+    int n_items = list_items(rt, qm);
+    int total = 0;
+    for (int t0 = 0; t0 < n_items; t0 += 32) {
+      int r, l;
+      item(qm, t0 + lane, r, l);
+      if (r >= 0) total += __popc(item_mask(l + 32 * r, rt, sv[l + 32 * r]));
+    }
+    total = (int)__reduce_add_sync(0xffffffffu, (unsigned)total);
     if (total > C && K <= 32) {
       // tighter bound: k-th largest of the 32 per-lane maxima (32 disjoint groups)
       rt = fmaxf(rt, warp_kth_of_lanes(mt, 32, K));
-      cnt = build(rt);
-      total = (int)__reduce_add_sync(0xffffffffu, (unsigned)cnt);
+      n_items = list_items(rt, qm);
+      total = 0;
+      for (int t0 = 0; t0 < n_items; t0 += 32) {
+        int r, l;
+        item(qm, t0 + lane, r, l);
+        if (r >= 0) total += __popc(item_mask(l + 32 * r, rt, sv[l + 32 * r]));
+      }
+      total = (int)__reduce_add_sync(0xffffffffu, (unsigned)total);
     }
-    int incl = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
-    }
-    if (cnt) {
-      int pos = incl - cnt;
+    {
       CandSlot* slots = p.slots + (size_t)u * C;
+      int written = 0;
+      for (int t0 = 0; t0 < n_items && written < C; t0 += 32) {
+        int r, l;
+        item(qm, t0 + lane, r, l);
+        uint32_t mr = 0;
+        uint4 raw = make_uint4(0, 0, 0, 0);
+        int jl = 0;
+        if (r >= 0) {
+          jl = l + 32 * r;
+          raw = sv[jl];
+          mr = item_mask(jl, rt, raw);
+        }
+        const int c = __popc(mr);
+        int incl = c;
 #pragma unroll
-      for (int r = 0; r < VPL; ++r) {
-        uint32_t mr = mask[r];
-        const int base_e = ((g.j0 + lane + 32 * r) * 16 - g.lead) / ES;  // token id of element 0
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += t;
+        }
+        int pos = written + incl - c;
+        const int base_b = (g.j0 + jl) * 16 - g.lead;
         while (mr) {
           const int e = __ffs(mr) - 1;
           mr &= mr - 1;
           if (pos < C) {
+            const int eb = base_b + e * ES;
             CandSlot cs;
-            if constexpr (BIAS) {
-              float x = xb[r * VEC];
-#pragma unroll
-              for (int q = 1; q < VEC; ++q)
-                if (q == e) x = xb[r * VEC + q];
-              cs.x = x;
-            } else {
-              cs.x = vec_elem<DT>(d[r], e);
-            }
-            cs.v = base_e + e;
+            float x = vec_elem<DT>(raw, e);
+            if constexpr (BIAS) x += __ldg(p.bias + eb / ES);
+            cs.x = x;
+            cs.v = eb / ES;
             slots[pos] = cs;
           }
           ++pos;
         }
+        written += __shfl_sync(0xffffffffu, incl, 31);
       }
     }
+    __syncwarp();
+    ++n_cons;
+    if (lane == 0) fill(n_cons);  // the stage is free again: the next copy lands during the sum
+
+    // first traversal, part 2: sum of exp(x - M) = 2^((x - M) log2 e) with packed fp32x2.
+    // For |M| < 64, x log2e - M log2e in one fused multiply-add (the rounding of M log2e
+    // shifts every term alike, by at most 2^-18 in the exponent); otherwise the exact
+    // difference x - M first (exact for the terms that dominate the sum).
+    float ssum = 0.0f;
+    if (M != -INFINITY) {
+      const float2 L2 = make_float2(kLog2e, kLog2e);
+      float2 acc0 = make_float2(0.0f, 0.0f), acc1 = make_float2(0.0f, 0.0f);
+      if (fabsf(M) < 64.0f) {
+        const float2 nml = make_float2(-M * kLog2e, -M * kLog2e);
+#pragma unroll
+        for (int r = 0; r < VPL; ++r) {
+          float x[VEC];
+          if constexpr (BIAS) {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) x[e] = xb[r * VEC + e];
+          } else {
+            unpack<DT>(d[r], x);
+          }
+#pragma unroll
+          for (int e = 0; e < VEC; e += 4) {
+            const float2 t0 = __ffma2_rn(make_float2(x[e], x[e + 1]), L2, nml);
+            const float2 t1 = __ffma2_rn(make_float2(x[e + 2], x[e + 3]), L2, nml);
+            acc0 = __fadd2_rn(acc0, make_float2(fast_exp2(t0.x), fast_exp2(t0.y)));
+            acc1 = __fadd2_rn(acc1, make_float2(fast_exp2(t1.x), fast_exp2(t1.y)));
+          }
+        }
+      } else {
+        const float2 nm = make_float2(-M, -M);
+#pragma unroll
+        for (int r = 0; r < VPL; ++r) {
+          float x[VEC];
+          if constexpr (BIAS) {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) x[e] = xb[r * VEC + e];
+          } else {
+            unpack<DT>(d[r], x);
+          }
+#pragma unroll
+          for (int e = 0; e < VEC; e += 4) {
+            const float2 t0 = __fmul2_rn(__fadd2_rn(make_float2(x[e], x[e + 1]), nm), L2);
+            const float2 t1 = __fmul2_rn(__fadd2_rn(make_float2(x[e + 2], x[e + 3]), nm), L2);
+            acc0 = __fadd2_rn(acc0, make_float2(fast_exp2(t0.x), fast_exp2(t0.y)));
+            acc1 = __fadd2_rn(acc1, make_float2(fast_exp2(t1.x), fast_exp2(t1.y)));
+          }
+        }
+      }
+      const float2 a = __fadd2_rn(acc0, acc1);
+      ssum = a.x + a.y;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
     if (lane == 0) {
       reinterpret_cast<int*>(rec)[0] = total;
       rec[1] = M;
