@@ -35,6 +35,10 @@ constexpr int kPairTile = 1024;  // (beam, chunk) pairs whose slot counts are sc
 struct __align__(16) SelSmem {
   int nsel, big, ovf, nbest, nrl, ptotal;
   int pc[kPairTile];   // slots to read per pair of the tile, then their exclusive prefix sums
+  float pm[kPairTile];  // chunk max of each (beam, chunk) pair (first tile only)
+  int pn[kPairTile];    // survivor count of each pair (first tile only)
+  float beam[kMaxK];
+  int fin[kMaxK];
   int wsum[kSelWarps];
   int wc[kSelWarps];
   unsigned int hist[256];
@@ -271,13 +275,18 @@ __global__ void __launch_bounds__(kSelThreads) beam_select_kernel(const StepPara
     sm.big = 0;
     sm.ovf = 0;
   }
+  // inputs that do not come from K1: read before waiting on it
+  for (int j = tid; j < K; j += kSelThreads) {
+    sm.beam[j] = p.beam[b * K + j];
+    sm.fin[j] = (p.finished && p.finished[b * K + j]) ? 1 : 0;
+  }
   grid_dependency_wait();  // K1's records and slots are complete and visible
   __syncthreads();
+  const bool keep_pairs = K * nc <= kPairTile;
   // 1. per beam: log_sum_exp, the row-level R-top-k and the score offset
   for (int j = warp; j < K; j += kSelWarps) {
-    const int row = b * K + j;
-    const bool fin = p.finished && p.finished[row];
-    const float beam = p.beam[row];
+    const bool fin = sm.fin[j] != 0;
+    const float beam = sm.beam[j];
     if (fin) {
       if (lane == 0) {
         RowSel rs;
@@ -290,36 +299,43 @@ __global__ void __launch_bounds__(kSelThreads) beam_select_kernel(const StepPara
       }
       continue;
     }
-    const long long u0 = (long long)row * nc;
-    // (max, sum of exp) merged over the chunks: online rescaling per lane, 4 chunks per
-    // round with their loads issued together, then a fixed shuffle tree (deterministic)
+    const long long u0 = (long long)(b * K + j) * nc;
+    // one pass over the chunk records: (max, sum of exp) with online rescaling, the group
+    // maxima (G <= 8 held per lane), then fixed shuffle trees (deterministic)
     float M = -INFINITY, S = 0.0f;
     bool ovf = false;
-    for (int c0 = lane; c0 < nc; c0 += 4 * 32) {
-      float mc[4], sc[4];
-      int cn[4];
+    float gl[8];
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int c = c0 + 32 * t;
-        mc[t] = -INFINITY;
-        sc[t] = 0.0f;
-        cn[t] = 0;
-        if (c < nc) {
-          const float* r = rec_ptr(p, u0 + c);
-          cn[t] = reinterpret_cast<const int*>(r)[0];
-          mc[t] = r[1];
-          sc[t] = r[2];
-        }
+    for (int g = 0; g < 8; ++g) gl[g] = -INFINITY;
+    for (int c = lane; c < nc; c += 32) {
+      const float4* r4 = reinterpret_cast<const float4*>(rec_ptr(p, u0 + c));
+      const float4 h = r4[0];
+      float4 ga = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY), gb = ga;
+      if (G <= 8) {
+        ga = r4[1];
+        if (G > 4) gb = r4[2];
       }
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        ovf |= cn[t] > C;
-        const float Mn = fmaxf(M, mc[t]);
-        if (Mn != -INFINITY) {
-          S = S * exp2f((M - Mn) * kLog2e) + (mc[t] == -INFINITY ? 0.0f : sc[t] * exp2f((mc[t] - Mn) * kLog2e));
-          M = Mn;
-        }
+      const int cnt = __float_as_int(h.x);
+      const float mc = h.y, sc = h.z;
+      if (keep_pairs) {
+        sm.pm[j * nc + c] = mc;
+        sm.pn[j * nc + c] = cnt;
       }
+      ovf |= cnt > C;
+      const float Mn = fmaxf(M, mc);
+      if (Mn != -INFINITY) {
+        S = (M == -INFINITY ? 0.0f : S * exp2f((M - Mn) * kLog2e)) +
+            (mc == -INFINITY ? 0.0f : sc * exp2f((mc - Mn) * kLog2e));
+        M = Mn;
+      }
+      gl[0] = fmaxf(gl[0], ga.x);
+      gl[1] = fmaxf(gl[1], ga.y);
+      gl[2] = fmaxf(gl[2], ga.z);
+      gl[3] = fmaxf(gl[3], ga.w);
+      gl[4] = fmaxf(gl[4], gb.x);
+      gl[5] = fmaxf(gl[5], gb.y);
+      gl[6] = fmaxf(gl[6], gb.z);
+      gl[7] = fmaxf(gl[7], gb.w);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -333,8 +349,14 @@ __global__ void __launch_bounds__(kSelThreads) beam_select_kernel(const StepPara
       M = Mn;
     }
     ovf = __any_sync(0xffffffffu, ovf);
-    // group maxima merged over the chunks: lanes split the (chunk, group) pairs
-    if (G <= 32) {
+    if (G <= 8) {
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        const float v = warp_max(gl[g]);
+        if (lane == 0 && g < G) sm.selg[warp][g] = v;
+      }
+    } else if (G <= 32) {
+      // group maxima merged over the chunks: lanes split the (chunk, group) pairs
       const int g = lane & (G - 1);
       const int cs = 32 / G;
       float gm = -INFINITY;
@@ -396,8 +418,17 @@ __global__ void __launch_bounds__(kSelThreads) beam_select_kernel(const StepPara
         int c = 0;
         if (sm.row[j].kind == ROW_LIVE) {
           // a chunk whose max is below the beam's R-top-k holds no survivor: skip its slots
-          const float* r = rec_ptr(p, (long long)b * K * nc + pair);
-          if (r[1] >= sm.row[j].rtopk) c = min(reinterpret_cast<const int*>(r)[0], C);
+          float mc;
+          int n;
+          if (keep_pairs) {
+            mc = sm.pm[pair];
+            n = sm.pn[pair];
+          } else {
+            const float* r = rec_ptr(p, (long long)b * K * nc + pair);
+            mc = r[1];
+            n = reinterpret_cast<const int*>(r)[0];
+          }
+          if (mc >= sm.row[j].rtopk) c = min(n, C);
         }
         sm.pc[i] = c;
       }
@@ -480,7 +511,7 @@ __global__ void __launch_bounds__(kSelThreads) beam_select_kernel(const StepPara
       if (kind == ROW_FIN && v == 0) {
         const int pos = atomicAdd(&sm.nsel, 1);
         if (pos < kSelCap)
-          sm.sel[pos] = make_key(p.beam[b * K + j], j, 0.0f, p.eos);
+          sm.sel[pos] = make_key(sm.beam[j], j, 0.0f, p.eos);
         else
           sm.big = 1;
       } else if (kind == ROW_DEAD) {
