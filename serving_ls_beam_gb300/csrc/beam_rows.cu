@@ -114,15 +114,54 @@ __device__ __forceinline__ float bits_max_float(uint32_t a) {
     return fmaxf(__low2float(h), __high2float(h));
   }
 }
-// true when the packed max reaches thr (thr is an element value, exact in the type)
-template <int DT>
-__device__ __forceinline__ bool bits_ge(uint32_t a, float thr) {
-  if constexpr (DT == DT_F32) {
-    return __uint_as_float(a) >= thr;
-  } else if constexpr (DT == DT_F16) {
-    return __hge2_mask(*reinterpret_cast<const __half2*>(&a), __float2half2_rn(thr)) != 0u;
+// thr in the packed layout of type T (both halves for 16-bit types; thr is an element
+// value, hence exact in the type)
+template <int T>
+__device__ __forceinline__ uint32_t thr_bits(float thr) {
+  if constexpr (T == DT_F32) {
+    return __float_as_uint(thr);
+  } else if constexpr (T == DT_F16) {
+    const __half2 t = __float2half2_rn(thr);
+    return *reinterpret_cast<const uint32_t*>(&t);
   } else {
-    return __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&a), __float2bfloat162_rn(thr)) != 0u;
+    const __nv_bfloat162 t = __float2bfloat162_rn(thr);
+    return *reinterpret_cast<const uint32_t*>(&t);
+  }
+}
+// true when either packed value reaches the packed threshold
+template <int T>
+__device__ __forceinline__ bool packed_ge(uint32_t a, uint32_t t) {
+  if constexpr (T == DT_F32) {
+    return __uint_as_float(a) >= __uint_as_float(t);
+  } else if constexpr (T == DT_F16) {
+    return __hge2_mask(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&t)) != 0u;
+  } else {
+    return __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&a), *reinterpret_cast<const __nv_bfloat162*>(&t)) != 0u;
+  }
+}
+
+// Bit e set when element e of the vector is >= thr (values before any bias; thr is an
+// element value, hence exact in the element type).
+template <int DT>
+__device__ __forceinline__ uint32_t vec_ge_mask(const uint4& d, float thr) {
+  if constexpr (DT == DT_F32) {
+    return (__uint_as_float(d.x) >= thr ? 1u : 0u) | (__uint_as_float(d.y) >= thr ? 2u : 0u) |
+           (__uint_as_float(d.z) >= thr ? 4u : 0u) | (__uint_as_float(d.w) >= thr ? 8u : 0u);
+  } else {
+    const uint32_t t = thr_bits<DT>(thr);
+    const uint32_t w[4] = {d.x, d.y, d.z, d.w};
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t g;
+      if constexpr (DT == DT_F16) {
+        g = __hge2_mask(*reinterpret_cast<const __half2*>(&w[i]), *reinterpret_cast<const __half2*>(&t));
+      } else {
+        g = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&w[i]), *reinterpret_cast<const __nv_bfloat162*>(&t));
+      }
+      m |= ((g & 1u) | ((g >> 15) & 2u)) << (2 * i);
+    }
+    return m;
   }
 }
 
@@ -319,87 +358,100 @@ __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepPar
       rt = warp_kth_of_64(m0, m1, K);
     }
 
-    // second traversal: survivors x >= rt.  The vectors whose max reaches rt are listed
-    // (one item per vector, items spread over the lanes) and re-read from shared memory.
-    auto list_items = [&](float thr, uint32_t (&qm)[VPL]) -> int {
+    // second traversal: survivors x >= rt.  The vectors whose max reaches rt are listed in
+    // the warp's shared list (one item per vector, up to 32 items a round, one item per
+    // lane) and re-read from the stage, which is still in shared memory.
+    int* wlist = reinterpret_cast<int*>(smem_raw + kRowListOff) + warp * 32;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    uint32_t qm[VPL];
+    auto list_items = [&](float thr) -> int {
+      const uint32_t t2 = thr_bits<BT>(thr);
       int n = 0;
 #pragma unroll
       for (int r = 0; r < VPL; ++r) {
-        bool hit;
-        if constexpr (BIAS)
-          hit = __uint_as_float(vm[r]) >= thr;
-        else
-          hit = bits_ge<DT>(vm[r], thr);
-        qm[r] = __ballot_sync(0xffffffffu, hit);
+        qm[r] = __ballot_sync(0xffffffffu, packed_ge<BT>(vm[r], t2));
         n += __popc(qm[r]);
       }
       return n;
     };
-    // item t -> (vector row r, source lane)
-    auto item = [&](const uint32_t (&qm)[VPL], int t, int& r_out, int& l_out) {
-      int base = 0;
-      r_out = -1;
+    // fill the list with items [base, base + 32); returns the item count of the round
+    auto fill_list = [&](int base, int n) -> int {
+      int pre = 0;
 #pragma unroll
       for (int r = 0; r < VPL; ++r) {
-        const int c = __popc(qm[r]);
-        if (r_out < 0 && t < base + c) {
-          r_out = r;
-          l_out = (int)__fns(qm[r], 0, t - base + 1);
+        if ((qm[r] >> lane) & 1u) {
+          const int pos = pre + __popc(qm[r] & lt_mask) - base;
+          if (pos >= 0 && pos < 32) wlist[pos] = (r << 5) | lane;
         }
-        base += c;
+        pre += __popc(qm[r]);
       }
+      __syncwarp();
+      return min(32, n - base);
     };
-    // element mask of one item (bit e: element e survives)
-    auto item_mask = [&](int jl, float thr, const uint4& raw) -> uint32_t {
+    // survivor mask of one listed vector (bit e: element e is in the row and >= thr)
+    auto item_mask = [&](int jl, const uint4& raw, float thr) -> uint32_t {
       const int base_b = (g.j0 + jl) * 16 - g.lead;
-      float x[VEC];
-      unpack<DT>(raw, x);
-      uint32_t mr = 0;
+      const bool interior = base_b >= 0 && base_b + 16 <= row_bytes;
+      uint32_t mr;
+      if constexpr (BIAS) {
+        float x[VEC];
+        unpack<DT>(raw, x);
+        mr = 0;
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        const int eb = base_b + e * ES;
-        const bool in_row = jl < g.nvec && eb >= 0 && eb < row_bytes;
-        float xe = x[e];
-        if constexpr (BIAS) xe += in_row ? __ldg(p.bias + eb / ES) : 0.0f;
-        mr |= (in_row && xe >= thr ? 1u : 0u) << e;
+        for (int e = 0; e < VEC; ++e) {
+          const int eb = base_b + e * ES;
+          const bool in_row = eb >= 0 && eb < row_bytes;
+          const float xe = x[e] + (in_row ? __ldg(p.bias + eb / ES) : 0.0f);
+          mr |= (in_row && xe >= thr ? 1u : 0u) << e;
+        }
+      } else {
+        mr = vec_ge_mask<DT>(raw, thr);
+        if (!interior) {
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) {
+            const int eb = base_b + e * ES;
+            if (eb < 0 || eb >= row_bytes) mr &= ~(1u << e);
+          }
+        }
       }
-      return mr;
+      return jl < g.nvec ? mr : 0u;
     };
-    uint32_t qm[VPL];
-    int n_items = list_items(rt, qm);
-    int total = 0;
-    for (int t0 = 0; t0 < n_items; t0 += 32) {
-      int r, l;
-      item(qm, t0 + lane, r, l);
-      if (r >= 0) total += __popc(item_mask(l + 32 * r, rt, sv[l + 32 * r]));
-    }
-    total = (int)__reduce_add_sync(0xffffffffu, (unsigned)total);
+    auto count_survivors = [&](float thr, int n) -> int {
+      int c = 0;
+      for (int base = 0; base < n; base += 32) {
+        const int m = fill_list(base, n);
+        if (lane < m) {
+          const int it = wlist[lane];
+          const int jl = (it & 31) + 32 * (it >> 5);
+          c += __popc(item_mask(jl, sv[jl], thr));
+        }
+        __syncwarp();
+      }
+      return (int)__reduce_add_sync(0xffffffffu, (unsigned)c);
+    };
+    int n_items = list_items(rt);
+    int total = count_survivors(rt, n_items);
     if (total > C && K <= 32) {
       // tighter bound: k-th largest of the 32 per-lane maxima (32 disjoint groups)
       rt = fmaxf(rt, warp_kth_of_lanes(mt, 32, K));
-      n_items = list_items(rt, qm);
-      total = 0;
-      for (int t0 = 0; t0 < n_items; t0 += 32) {
-        int r, l;
-        item(qm, t0 + lane, r, l);
-        if (r >= 0) total += __popc(item_mask(l + 32 * r, rt, sv[l + 32 * r]));
-      }
-      total = (int)__reduce_add_sync(0xffffffffu, (unsigned)total);
+      n_items = list_items(rt);
+      total = count_survivors(rt, n_items);
     }
     {
       CandSlot* slots = p.slots + (size_t)u * C;
       int written = 0;
-      for (int t0 = 0; t0 < n_items && written < C; t0 += 32) {
-        int r, l;
-        item(qm, t0 + lane, r, l);
+      for (int base = 0; base < n_items && written < C; base += 32) {
+        const int m = fill_list(base, n_items);
         uint32_t mr = 0;
         uint4 raw = make_uint4(0, 0, 0, 0);
         int jl = 0;
-        if (r >= 0) {
-          jl = l + 32 * r;
+        if (lane < m) {
+          const int it = wlist[lane];
+          jl = (it & 31) + 32 * (it >> 5);
           raw = sv[jl];
-          mr = item_mask(jl, rt, raw);
+          mr = item_mask(jl, raw, rt);
         }
+        __syncwarp();
         const int c = __popc(mr);
         int incl = c;
 #pragma unroll

@@ -13,7 +13,8 @@ namespace lsb {
 // 32 x VPL 16-byte vectors at a time, streamed through its own 2-stage shared ring.
 constexpr int kRowThreads = 256;
 constexpr int kRowWarps = kRowThreads / 32;
-constexpr int kRowBarBytes = 128;  // per-warp mbarriers at the start of shared memory
+constexpr int kRowListOff = 128;   // per-warp mbarriers in [0, 128), then per-warp item lists
+constexpr int kRowBarBytes = kRowListOff + kRowWarps * 32 * 4;  // start of the stage buffers
 constexpr int kVplMin = 4;         // smallest vectors-per-lane variant built
 // K2 (beam_select.cu): one CTA per batch.
 constexpr int kSelThreads = 256;
