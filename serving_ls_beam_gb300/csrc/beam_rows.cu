@@ -266,10 +266,14 @@ __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepPar
     // the chunk into registers; bytes outside the row become -inf
     const uint4* sv = reinterpret_cast<const uint4*>(stages + (size_t)s * kStageBytes);
     uint4 d[VPL];
+    // a chunk of CV whole vectors that starts and ends inside the row needs no masking
+    const bool interior_chunk = g.nvec == CV && g.j0 * 16 - g.lead >= 0 && (g.j0 + CV) * 16 - g.lead <= row_bytes;
 #pragma unroll
     for (int r = 0; r < VPL; ++r) {
       const int jl = lane + 32 * r;
-      if (jl < g.nvec) {
+      if (interior_chunk) {
+        d[r] = sv[jl];
+      } else if (jl < g.nvec) {
         d[r] = sv[jl];
         const int base_b = (g.j0 + jl) * 16 - g.lead;  // row byte offset of element 0
         if (base_b < 0 || base_b + 16 > row_bytes) {
@@ -416,32 +420,14 @@ __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepPar
       }
       return jl < g.nvec ? mr : 0u;
     };
-    auto count_survivors = [&](float thr, int n) -> int {
-      int c = 0;
+    // survivors, one round of up to 32 listed vectors at a time; masks are computed once
+    // per round and written at once unless the chunk overflows its slots, in which case
+    // the bound is tightened (k <= 32) and the chunk filtered again
+    CandSlot* slots = p.slots + (size_t)u * C;
+    auto filter = [&](float thr, int n, bool write) -> int {
+      int written = 0;
       for (int base = 0; base < n; base += 32) {
         const int m = fill_list(base, n);
-        if (lane < m) {
-          const int it = wlist[lane];
-          const int jl = (it & 31) + 32 * (it >> 5);
-          c += __popc(item_mask(jl, sv[jl], thr));
-        }
-        __syncwarp();
-      }
-      return (int)__reduce_add_sync(0xffffffffu, (unsigned)c);
-    };
-    int n_items = list_items(rt);
-    int total = count_survivors(rt, n_items);
-    if (total > C && K <= 32) {
-      // tighter bound: k-th largest of the 32 per-lane maxima (32 disjoint groups)
-      rt = fmaxf(rt, warp_kth_of_lanes(mt, 32, K));
-      n_items = list_items(rt);
-      total = count_survivors(rt, n_items);
-    }
-    {
-      CandSlot* slots = p.slots + (size_t)u * C;
-      int written = 0;
-      for (int base = 0; base < n_items && written < C; base += 32) {
-        const int m = fill_list(base, n_items);
         uint32_t mr = 0;
         uint4 raw = make_uint4(0, 0, 0, 0);
         int jl = 0;
@@ -449,7 +435,7 @@ __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepPar
           const int it = wlist[lane];
           jl = (it & 31) + 32 * (it >> 5);
           raw = sv[jl];
-          mr = item_mask(jl, raw, rt);
+          mr = item_mask(jl, raw, thr);
         }
         __syncwarp();
         const int c = __popc(mr);
@@ -459,24 +445,40 @@ __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepPar
           const int t = __shfl_up_sync(0xffffffffu, incl, o);
           if (lane >= o) incl += t;
         }
-        int pos = written + incl - c;
-        const int base_b = (g.j0 + jl) * 16 - g.lead;
-        while (mr) {
-          const int e = __ffs(mr) - 1;
-          mr &= mr - 1;
-          if (pos < C) {
-            const int eb = base_b + e * ES;
-            CandSlot cs;
-            float x = vec_elem<DT>(raw, e);
-            if constexpr (BIAS) x += __ldg(p.bias + eb / ES);
-            cs.x = x;
-            cs.v = eb / ES;
-            slots[pos] = cs;
+        if (write) {
+          int pos = written + incl - c;
+          const int base_b = (g.j0 + jl) * 16 - g.lead;
+          while (mr) {
+            const int e = __ffs(mr) - 1;
+            mr &= mr - 1;
+            if (pos < C) {
+              const int eb = base_b + e * ES;
+              CandSlot cs;
+              float x = vec_elem<DT>(raw, e);
+              if constexpr (BIAS) x += __ldg(p.bias + eb / ES);
+              cs.x = x;
+              cs.v = eb / ES;
+              slots[pos] = cs;
+            }
+            ++pos;
           }
-          ++pos;
         }
         written += __shfl_sync(0xffffffffu, incl, 31);
       }
+      return written;
+    };
+    int n_items = list_items(rt);
+    // common case: everything fits, count and write in one pass (every listed vector
+    // holds at least one survivor, so more than C vectors means more than C survivors)
+    int total = (n_items <= C) ? filter(rt, n_items, true) : C + 1;
+    if (total > C) {
+      if (K <= 32) {
+        // tighter bound: k-th largest of the 32 per-lane maxima (32 disjoint groups)
+        rt = fmaxf(rt, warp_kth_of_lanes(mt, 32, K));
+        n_items = list_items(rt);
+      }
+      total = filter(rt, n_items, false);
+      if (total <= C) filter(rt, n_items, true);
     }
     __syncwarp();
     ++n_cons;
