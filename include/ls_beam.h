@@ -141,6 +141,27 @@ LS_API const char* ls_status_string(ls_status status);
 LS_API ls_status ls_read_row_stats(const void* workspace, int batch, int k, int vocab, float* lse,
                             float* rtopk, int32_t* ncand, int32_t* path, void* stream);
 
+/*
+ * The beam step for callers that cannot allocate device memory (no counterpart in the
+ * article; it exists for callers such as plugins of a host framework that owns all
+ * device memory, or serving loops with a fixed memory budget, where cudaMalloc is not
+ * available at request time).  Same arguments and results as ls_beam_step, without the
+ * workspace: the scratch lives in a fixed 64 MiB array in this library's device memory,
+ * held by every GPU that loads the library until the process exits.  The library
+ * allocates nothing here either.
+ *  - Shapes whose ls_beam_step_workspace_size exceeds 64 MiB return LS_ERR_UNSUPPORTED.
+ *  - The first call on a device looks up that device's address of the array (the
+ *    device must be current); make that first call before any stream capture.
+ *  - All calls share the one array, which keeps the last call's contents; its status
+ *    word is cleared at the start of each call and is not reported.  Calls whose work
+ *    overlaps on the GPU (different streams, or threads without ordering) race on it.
+ */
+LS_API ls_status ls_beam_step_noalloc(const void* logits, ls_dtype logit_dtype, const float* bias,
+                                      const float* beam_scores, const uint8_t* finished, int batch,
+                                      int k, int vocab, int eos_id, int32_t* out_token,
+                                      int32_t* out_parent, float* out_score, uint8_t* out_finished,
+                                      void* stream);
+
 #ifdef __cplusplus
 }
 #endif

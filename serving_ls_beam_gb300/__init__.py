@@ -18,7 +18,7 @@ __all__ = [
     "LS_OK", "LS_ERR_INVALID_ARG", "LS_ERR_UNSUPPORTED", "LS_ERR_CUDA", "LS_ERR_TIMEOUT", "LS_ERR_INTERNAL",
     "LS_DTYPE_F32", "LS_DTYPE_F16", "LS_DTYPE_BF16", "LS_MAX_K", "LsBeamError", "library_path", "load_library",
     "check", "ls_beam_step_workspace_size", "ls_workspace_init", "ls_beam_step", "ls_cache_reorder",
-    "ls_read_status", "ls_status_string", "ls_read_row_stats",
+    "ls_read_status", "ls_status_string", "ls_read_row_stats", "ls_beam_step_noalloc",
 ]
 
 LS_OK, LS_ERR_INVALID_ARG, LS_ERR_UNSUPPORTED, LS_ERR_CUDA, LS_ERR_TIMEOUT, LS_ERR_INTERNAL = range(6)
@@ -63,6 +63,8 @@ def load_library():
         lib.ls_status_string.restype = ctypes.c_char_p
         lib.ls_read_row_stats.argtypes = [vp, ip, ip, ip, vp, vp, vp, vp, vp]
         lib.ls_read_row_stats.restype = ip
+        lib.ls_beam_step_noalloc.argtypes = [vp, ip, vp, vp, vp, ip, ip, ip, ip, vp, vp, vp, vp, vp]
+        lib.ls_beam_step_noalloc.restype = ip
         _lib = lib
         return lib
 
@@ -122,6 +124,16 @@ def ls_beam_step(logits, bias, beam_scores, finished, eos_id: int, out_token, ou
         _ptr(logits), _dtype_code(logits), _ptr(bias), _ptr(beam_scores), _ptr(finished), batch, k, vocab,
         int(eos_id), _ptr(out_token), _ptr(out_parent), _ptr(out_score), _ptr(out_finished), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream))
+
+
+def ls_beam_step_noalloc(logits, bias, beam_scores, finished, eos_id: int, out_token, out_parent, out_score,
+                         out_finished, stream=None) -> int:
+    """ls_beam_step for callers that cannot allocate: no workspace argument, the library's
+    fixed device scratch is used instead (shapes needing more than 64 MiB are rejected)."""
+    batch, k, vocab = logits.shape
+    return load_library().ls_beam_step_noalloc(
+        _ptr(logits), _dtype_code(logits), _ptr(bias), _ptr(beam_scores), _ptr(finished), batch, k, vocab,
+        int(eos_id), _ptr(out_token), _ptr(out_parent), _ptr(out_score), _ptr(out_finished), _stream(stream))
 
 
 def ls_cache_reorder(src, dst, parent, length: int, workspace=None, stream=None) -> int:
