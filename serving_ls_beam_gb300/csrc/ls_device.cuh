@@ -47,8 +47,24 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-// Wait for the barrier phase with the given parity; give up after limit_ns.
+// Non-blocking test of the phase.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the barrier phase with the given parity; give up after limit_ns (a limit of 0
+// gives up at once unless the phase is already complete).
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, long long limit_ns) {
+  if (mbar_test_wait(bar, parity)) return true;
+  if (limit_ns <= 0) return false;
   const uint32_t hint = limit_ns < 100000 ? (uint32_t)limit_ns : 100000u;
   if (mbar_try_wait(bar, parity, hint)) return true;
   const uint64_t t0 = global_timer_ns();
