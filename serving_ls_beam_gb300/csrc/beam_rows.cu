@@ -35,6 +35,9 @@ namespace {
 
 constexpr int kStages = 2;
 constexpr long long kDrainLimitNs = 2000000000LL;  // 2 s for copies already in flight
+// shared-memory layout: [mbarriers | per-warp item lists | stage buffers]
+static_assert(kRowWarps * kStages * 8 <= kRowListOff, "mbarriers overlap the item lists");
+static_assert(kRowBarBytes % 16 == 0, "stage buffers must be 16-byte aligned for bulk copies");
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
