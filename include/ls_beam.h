@@ -153,8 +153,9 @@ LS_API ls_status ls_read_row_stats(const void* workspace, int batch, int k, int 
  *  - The first call on a device looks up that device's address of the array (the
  *    device must be current); make that first call before any stream capture.
  *  - All calls share the one array, which keeps the last call's contents; its status
- *    word is cleared at the start of each call and is not reported.  Calls whose work
- *    overlaps on the GPU (different streams, or threads without ordering) race on it.
+ *    word and arrival counters are cleared at the start of each call, and the status is
+ *    not reported.  Calls whose work overlaps on the GPU (different streams, or threads
+ *    without ordering) race on it.
  */
 LS_API ls_status ls_beam_step_noalloc(const void* logits, ls_dtype logit_dtype, const float* bias,
                                       const float* beam_scores, const uint8_t* finished, int batch,

@@ -185,7 +185,10 @@ ls_status ls_beam_step(const void* logits, ls_dtype logit_dtype, const float* bi
   p.out_score = out_score;
   p.out_finished = out_finished;
   p.status = reinterpret_cast<uint32_t*>(ws + wl.status_off);
-  p.done = reinterpret_cast<uint32_t*>(ws + wl.done_off);
+  p.row_cnt = reinterpret_cast<uint32_t*>(ws + wl.rowcnt_off);
+  p.batch_cnt = reinterpret_cast<uint32_t*>(ws + wl.batchcnt_off);
+  p.row_cand = reinterpret_cast<unsigned long long*>(ws + wl.rowcand_off);
+  p.row_ncand = reinterpret_cast<int32_t*>(ws + wl.rowncand_off);
   p.rec = ws + wl.rec_off;
   p.slots = reinterpret_cast<CandSlot*>(ws + wl.slot_off);
   p.rowstat = reinterpret_cast<RowStat*>(ws + wl.rowstat_off);

@@ -44,7 +44,8 @@ struct CandSlot {
 };
 
 struct WsLayout {
-  size_t status_off, done_off, rec_off, slot_off, rowstat_off, bstat_off, total;
+  size_t status_off, rowcnt_off, batchcnt_off, rec_off, slot_off, rowcand_off, rowncand_off, rowstat_off, bstat_off,
+      total;
   int nc_max;      // most chunks per row any plan may use
   int groups;      // G: number of R-top-k groups (power of two >= k)
   int slot_cap;    // C: candidate slots per chunk
@@ -82,12 +83,18 @@ inline WsLayout ws_layout(int batch, int k, int vocab) {
   size_t off = 0;
   w.status_off = off;
   off += 256;
-  w.done_off = off;
+  w.rowcnt_off = off;
+  off = align_up(off + rows * 4, 256);
+  w.batchcnt_off = off;
   off = align_up(off + (size_t)batch * 4, 256);
   w.rec_off = off;
   off = align_up(off + rows * w.nc_max * w.rec_stride, 256);
   w.slot_off = off;
   off = align_up(off + rows * w.nc_max * w.slot_cap * sizeof(CandSlot), 256);
+  w.rowcand_off = off;
+  off = align_up(off + rows * w.slot_cap * 16, 256);
+  w.rowncand_off = off;
+  off = align_up(off + rows * 4, 256);
   w.rowstat_off = off;
   off = align_up(off + rows * sizeof(RowStat), 256);
   w.bstat_off = off;
@@ -107,9 +114,12 @@ struct StepParams {
   float* out_score;
   uint8_t* out_finished;
   uint32_t* status;
-  uint32_t* done;
+  uint32_t* row_cnt;     // chunks of each beam done in this call (reset by the beam's last warp)
+  uint32_t* batch_cnt;   // beams of each batch done in this call (reset by the batch's last warp)
   unsigned char* rec;
   CandSlot* slots;
+  unsigned long long* row_cand;  // per beam: up to slot_cap keys (hi, lo) of its final survivors
+  int32_t* row_ncand;
   RowStat* rowstat;
   int32_t* bstat;
   int batch, k, vocab, eos;
