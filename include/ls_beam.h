@@ -128,7 +128,8 @@ LS_API ls_status ls_read_status(void* workspace, void* stream);
 LS_API const char* ls_status_string(ls_status status);
 
 /*
- * Diagnostic readback of the last ls_beam_step on `workspace` (synchronises `stream`).
+ * Diagnostic readback of the last ls_beam_step on `workspace` of `workspace_bytes` (the
+ * size given to that call; synchronises `stream`).
  * All outputs are HOST arrays, each may be NULL:
  *   lse      [batch*k] f32 log_sum_exp of each live beam (NaN for finished beams)
  *   rtopk    [batch*k] f32 the beam's R-top-k threshold (the k-th largest of its
@@ -138,8 +139,9 @@ LS_API const char* ls_status_string(ls_status status);
  *   path     [batch]   int32 0 = candidate queue, 1 = exact fallback (queue overflow),
  *            2 = exact fallback (forced for testing), 3 = exact fallback (large queue)
  */
-LS_API ls_status ls_read_row_stats(const void* workspace, int batch, int k, int vocab, float* lse,
-                            float* rtopk, int32_t* ncand, int32_t* path, void* stream);
+LS_API ls_status ls_read_row_stats(const void* workspace, size_t workspace_bytes, int batch, int k,
+                                   int vocab, float* lse, float* rtopk, int32_t* ncand, int32_t* path,
+                                   void* stream);
 
 /*
  * The beam step for callers that cannot allocate device memory (no counterpart in the

@@ -64,7 +64,9 @@ extern "C" ls_status ls_beam_step_noalloc(const void* logits, ls_dtype logit_dty
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // the status word and the arrival counters must start at zero; everything else the
   // step reads it writes first
-  const size_t zero_bytes = lsb::ws_layout(batch, k, vocab).rec_off;
+  const lsb::WsLayout wl = lsb::ws_layout(batch, k, vocab, kNoAllocScratchBytes);
+  if (wl.total == 0) return LS_ERR_UNSUPPORTED;
+  const size_t zero_bytes = wl.batchcnt_off + (size_t)batch * 4;
   if (cudaMemsetAsync(scratch, 0, zero_bytes, st) != cudaSuccess) {
     cudaGetLastError();
     return LS_ERR_CUDA;
