@@ -51,6 +51,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--decode-steps", type=int, default=0,
+                    help="run only the first N decode steps of the workload (for small profiling runs)")
     return ap.parse_args()
 
 
@@ -247,7 +249,7 @@ def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
     _build.build()
     lsb.load_library()
     wr = shard_workload(w, rank)
-    T = wr.steps
+    T = min(wr.steps, args.decode_steps) if args.decode_steps > 0 else wr.steps
     B, K, V = wr.batch, wr.k, wr.vocab
     es = 2 if wr.dtype in ("f16", "bf16") else 4
     tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[wr.dtype]
@@ -256,7 +258,7 @@ def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
     t0 = time.time()
     host_logits = np.empty((T, B, K, V), np.float16 if wr.dtype == "f16" else np.float32)
     for t in range(T):
-        host_logits[t] = synth.logits(wr, t + 1 if T > 1 else 0)
+        host_logits[t] = synth.logits(wr, t + 1 if wr.steps > 1 else 0)
     d_logits = torch.from_numpy(host_logits).to(dev)
     bias_np = synth.bias(wr)
     d_bias = None if bias_np is None else torch.from_numpy(bias_np).to(dev)
@@ -272,7 +274,7 @@ def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
     setup_s = time.time() - t0
 
     def lens(t):  # cache positions refreshed at decode step t (1-based)
-        return t if T > 1 else (wr.kv_shape[2] if wr.kv_shape else 0)
+        return t if wr.steps > 1 else (wr.kv_shape[2] if wr.kv_shape else 0)
 
     stream = torch.cuda.Stream(device=dev)
     try:  # events inside a captured graph must be "external" record nodes to be timed

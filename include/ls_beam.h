@@ -128,8 +128,7 @@ LS_API ls_status ls_read_status(void* workspace, void* stream);
 LS_API const char* ls_status_string(ls_status status);
 
 /*
- * Diagnostic readback of the last ls_beam_step on `workspace` of `workspace_bytes` (the
- * size given to that call; synchronises `stream`).
+ * Diagnostic readback of the last ls_beam_step on `workspace` (synchronises `stream`).
  * All outputs are HOST arrays, each may be NULL:
  *   lse      [batch*k] f32 log_sum_exp of each live beam (NaN for finished beams)
  *   rtopk    [batch*k] f32 the beam's R-top-k threshold (the k-th largest of its
@@ -139,9 +138,8 @@ LS_API const char* ls_status_string(ls_status status);
  *   path     [batch]   int32 0 = candidate queue, 1 = exact fallback (queue overflow),
  *            2 = exact fallback (forced for testing), 3 = exact fallback (large queue)
  */
-LS_API ls_status ls_read_row_stats(const void* workspace, size_t workspace_bytes, int batch, int k,
-                                   int vocab, float* lse, float* rtopk, int32_t* ncand, int32_t* path,
-                                   void* stream);
+LS_API ls_status ls_read_row_stats(const void* workspace, int batch, int k, int vocab, float* lse,
+                            float* rtopk, int32_t* ncand, int32_t* path, void* stream);
 
 /*
  * The beam step for callers that cannot allocate device memory (no counterpart in the
@@ -155,9 +153,8 @@ LS_API ls_status ls_read_row_stats(const void* workspace, size_t workspace_bytes
  *  - The first call on a device looks up that device's address of the array (the
  *    device must be current); make that first call before any stream capture.
  *  - All calls share the one array, which keeps the last call's contents; its status
- *    word and arrival counters are cleared at the start of each call, and the status is
- *    not reported.  Calls whose work overlaps on the GPU (different streams, or threads
- *    without ordering) race on it.
+ *    word is cleared at the start of each call and is not reported.  Calls whose work
+ *    overlaps on the GPU (different streams, or threads without ordering) race on it.
  */
 LS_API ls_status ls_beam_step_noalloc(const void* logits, ls_dtype logit_dtype, const float* bias,
                                       const float* beam_scores, const uint8_t* finished, int batch,

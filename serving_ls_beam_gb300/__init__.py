@@ -61,7 +61,7 @@ def load_library():
         lib.ls_read_status.restype = ip
         lib.ls_status_string.argtypes = [ip]
         lib.ls_status_string.restype = ctypes.c_char_p
-        lib.ls_read_row_stats.argtypes = [vp, sz, ip, ip, ip, vp, vp, vp, vp, vp]
+        lib.ls_read_row_stats.argtypes = [vp, ip, ip, ip, vp, vp, vp, vp, vp]
         lib.ls_read_row_stats.restype = ip
         lib.ls_beam_step_noalloc.argtypes = [vp, ip, vp, vp, vp, ip, ip, ip, ip, vp, vp, vp, vp, vp]
         lib.ls_beam_step_noalloc.restype = ip
@@ -159,8 +159,7 @@ def ls_read_row_stats(workspace, batch: int, k: int, vocab: int, stream=None):
     rt = np.empty(batch * k, np.float32)
     nc = np.empty(batch * k, np.int32)
     path = np.empty(batch, np.int32)
-    st = load_library().ls_read_row_stats(_ptr(workspace), workspace.numel() * workspace.element_size(), batch, k,
-                                          vocab, lse.ctypes.data, rt.ctypes.data, nc.ctypes.data, path.ctypes.data,
-                                          _stream(stream))
+    st = load_library().ls_read_row_stats(_ptr(workspace), batch, k, vocab, lse.ctypes.data, rt.ctypes.data,
+                                          nc.ctypes.data, path.ctypes.data, _stream(stream))
     check(st, "ls_read_row_stats")
     return lse.reshape(batch, k), rt.reshape(batch, k), nc.reshape(batch, k), path

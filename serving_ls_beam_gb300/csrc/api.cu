@@ -121,8 +121,8 @@ extern "C" {
 size_t ls_beam_step_workspace_size(int batch, int k, int vocab) {
   if (batch < 0 || k < 1 || k > LS_MAX_K || vocab < k) return 0;
   if ((long long)k * vocab >= (1ll << 31) || vocab > (1 << 28)) return 0;
-  if ((long long)batch * k * ws_layout_with_area(batch, k, vocab, 0).nc_max >= (1ll << 31)) return 0;
-  return ws_required_bytes(batch, k, vocab);
+  if ((long long)batch * k * ws_layout(batch, k, vocab).nc_max >= (1ll << 31)) return 0;
+  return ws_layout(batch, k, vocab).total;
 }
 
 ls_status ls_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
@@ -141,8 +141,8 @@ ls_status ls_beam_step(const void* logits, ls_dtype logit_dtype, const float* bi
   if (!dtype_ok(logit_dtype)) return LS_ERR_INVALID_ARG;
   if (batch == 0) return LS_OK;
   if (!logits || !beam_scores || !out_token || !out_parent || !out_score || !workspace) return LS_ERR_INVALID_ARG;
-  const WsLayout wl = ws_layout(batch, k, vocab, workspace_bytes);
-  if (wl.total == 0) return LS_ERR_INVALID_ARG;  // workspace too small for this shape
+  const WsLayout wl = ws_layout(batch, k, vocab);
+  if (wl.total == 0 || workspace_bytes < wl.total) return LS_ERR_INVALID_ARG;
   const int es = dtype_bytes(logit_dtype);
   if (!aligned(logits, es) || (bias && !aligned(bias, 4)) || !aligned(beam_scores, 4) || !aligned(out_token, 4) ||
       !aligned(out_parent, 4) || !aligned(out_score, 4) || !aligned(workspace, 256))
@@ -185,10 +185,7 @@ ls_status ls_beam_step(const void* logits, ls_dtype logit_dtype, const float* bi
   p.out_score = out_score;
   p.out_finished = out_finished;
   p.status = reinterpret_cast<uint32_t*>(ws + wl.status_off);
-  p.row_cnt = reinterpret_cast<uint32_t*>(ws + wl.rowcnt_off);
-  p.batch_cnt = reinterpret_cast<uint32_t*>(ws + wl.batchcnt_off);
-  p.row_cand = reinterpret_cast<unsigned long long*>(ws + wl.rowcand_off);
-  p.row_ncand = reinterpret_cast<int32_t*>(ws + wl.rowncand_off);
+  p.done = reinterpret_cast<uint32_t*>(ws + wl.done_off);
   p.rec = ws + wl.rec_off;
   p.slots = reinterpret_cast<CandSlot*>(ws + wl.slot_off);
   p.rowstat = reinterpret_cast<RowStat*>(ws + wl.rowstat_off);
@@ -292,12 +289,11 @@ const char* ls_status_string(ls_status status) {
   }
 }
 
-ls_status ls_read_row_stats(const void* workspace, size_t workspace_bytes, int batch, int k, int vocab, float* lse,
-                            float* rtopk, int32_t* ncand, int32_t* path, void* stream) {
+ls_status ls_read_row_stats(const void* workspace, int batch, int k, int vocab, float* lse, float* rtopk,
+                            int32_t* ncand, int32_t* path, void* stream) {
   if (!workspace || batch < 0 || k < 1 || k > LS_MAX_K || vocab < k) return LS_ERR_INVALID_ARG;
   if (batch == 0) return LS_OK;
-  const WsLayout wl = ws_layout(batch, k, vocab, workspace_bytes);
-  if (wl.total == 0) return LS_ERR_INVALID_ARG;
+  const WsLayout wl = ws_layout(batch, k, vocab);
   const size_t rows = (size_t)batch * k;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const unsigned char* ws = static_cast<const unsigned char*>(workspace);

@@ -186,307 +186,6 @@ __device__ __forceinline__ float vec_elem(const uint4& d, int e) {
   }
 }
 
-// ---------------------------------------------------------------- fine rank inside K1
-// The warp that completes a beam (its last chunk to arrive) merges the beam's chunk
-// records and keeps the survivors of the beam-level R-top-k; the warp that completes a
-// batch ranks those survivors and writes the step's outputs.  Arrivals use the
-// fence-then-atomic pattern; the finishing warp fences and reads through L2.
-
-__device__ __forceinline__ const float* rec_at(const StepParams& p, long long u) {
-  return reinterpret_cast<const float*>(p.rec + (size_t)u * p.rec_stride);
-}
-
-// Beam `row`: log_sum_exp, row-level R-top-k (k-th largest of the G group maxima merged
-// over all chunks: the article's k-group bound for the whole beam) and its survivors,
-// rescored as beam_score + x - lse and stored as rank keys.  row_ncand = -1 asks for the
-// exact fallback (a chunk overflowed, or too many survivors).
-__device__ __noinline__ void row_finalize(const StepParams& p, int row) {
-  const int lane = threadIdx.x & 31;
-  const int K = p.k, nc = p.nc, G = p.groups, C = p.slot_cap;
-  const int j = row % K;
-  const long long u0 = (long long)row * nc;
-  const float beam = __ldg(p.beam + row);
-  float M = -INFINITY, S = 0.0f;
-  bool ovf = false;
-  float gl[8];
-#pragma unroll
-  for (int g = 0; g < 8; ++g) gl[g] = -INFINITY;
-  for (int c = lane; c < nc; c += 32) {
-    const float4* r4 = reinterpret_cast<const float4*>(rec_at(p, u0 + c));
-    const float4 h = __ldcg(r4);
-    float4 ga = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY), gb = ga;
-    if (G <= 8) {
-      ga = __ldcg(r4 + 1);
-      if (G > 4) gb = __ldcg(r4 + 2);
-    }
-    ovf |= __float_as_int(h.x) > C;
-    const float mc = h.y, sc = h.z;
-    const float Mn = fmaxf(M, mc);
-    if (Mn != -INFINITY) {
-      S = (M == -INFINITY ? 0.0f : S * fast_exp2((M - Mn) * kLog2e)) +
-          (mc == -INFINITY ? 0.0f : sc * fast_exp2((mc - Mn) * kLog2e));
-      M = Mn;
-    }
-    gl[0] = fmaxf(gl[0], ga.x);
-    gl[1] = fmaxf(gl[1], ga.y);
-    gl[2] = fmaxf(gl[2], ga.z);
-    gl[3] = fmaxf(gl[3], ga.w);
-    gl[4] = fmaxf(gl[4], gb.x);
-    gl[5] = fmaxf(gl[5], gb.y);
-    gl[6] = fmaxf(gl[6], gb.z);
-    gl[7] = fmaxf(gl[7], gb.w);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float Mo = __shfl_xor_sync(0xffffffffu, M, o);
-    const float So = __shfl_xor_sync(0xffffffffu, S, o);
-    const float Mn = fmaxf(M, Mo);
-    if (Mn != -INFINITY)
-      S = (M == -INFINITY ? 0.0f : S * fast_exp2((M - Mn) * kLog2e)) +
-          (Mo == -INFINITY ? 0.0f : So * fast_exp2((Mo - Mn) * kLog2e));
-    M = Mn;
-  }
-  ovf = __any_sync(0xffffffffu, ovf);
-  float R;
-  if (G <= 8) {
-#pragma unroll
-    for (int g = 0; g < 8; ++g) gl[g] = warp_max(gl[g]);
-    R = -INFINITY;
-#pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      if (g < G) {
-        int rank = 0;
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          if (q < G) rank += (gl[q] > gl[g]) || (gl[q] == gl[g] && q < g);
-        if (rank == K - 1) R = gl[g];
-      }
-    }
-  } else if (G <= 32) {
-    const int g = lane & (G - 1);
-    float gm = -INFINITY;
-    for (int c = lane / G; c < nc; c += 32 / G) gm = fmaxf(gm, __ldcg(rec_at(p, u0 + c) + 4 + g));
-    for (int o = 16; o >= G; o >>= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, o));
-    R = warp_kth_of_lanes(gm, G, K);
-  } else {
-    float ga = -INFINITY, gb = -INFINITY;
-    for (int c = 0; c < nc; ++c) {
-      ga = fmaxf(ga, __ldcg(rec_at(p, u0 + c) + 4 + lane));
-      gb = fmaxf(gb, __ldcg(rec_at(p, u0 + c) + 4 + 32 + lane));
-    }
-    R = warp_kth_of_64(ga, gb, K);
-  }
-  const float log_s = logf(S);
-  const float lse = M == -INFINITY ? -INFINITY : M + log_s;
-  const bool dead = (M == -INFINITY) || (beam == -INFINITY);
-  ulonglong2* out = reinterpret_cast<ulonglong2*>(p.row_cand) + (size_t)row * C;
-  int n = 0;
-  if (dead) {
-    for (int v = lane; v < K; v += 32) {
-      const Key key = make_key(-INFINITY, j, 0.0f, v);
-      out[v] = make_ulonglong2(key.hi, key.lo);
-    }
-    n = K;
-  } else if (!ovf) {
-    const double cj = (double)beam - (double)M - (double)log_s;  // beam_score - lse
-    const unsigned lt = (1u << lane) - 1u;
-    for (int c0 = 0; c0 < nc && n <= C; c0 += 32) {
-      // this lane's chunk: its survivors count if its max reaches R
-      const int c = c0 + lane;
-      int cnt = 0;
-      if (c < nc) {
-        const float4 h = __ldcg(reinterpret_cast<const float4*>(rec_at(p, u0 + c)));
-        if (h.y >= R) cnt = min(__float_as_int(h.x), C);
-      }
-      int pre = cnt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, pre, o);
-        if (lane >= o) pre += t;
-      }
-      const int tot = __shfl_sync(0xffffffffu, pre, 31);
-      pre -= cnt;  // exclusive prefix of this lane's chunk
-      // the round's slots, flattened over the lanes
-      for (int i0 = 0; i0 < tot; i0 += 32) {
-        const int i = i0 + lane;
-        int owner = 0;
-#pragma unroll
-        for (int st = 16; st > 0; st >>= 1) {  // last lane whose prefix <= i
-          const int cand = owner + st;
-          const int pc = __shfl_sync(0xffffffffu, pre, cand);
-          if (pc <= i) owner = cand;
-        }
-        const int po = __shfl_sync(0xffffffffu, pre, owner);
-        bool surv = false;
-        float x = 0.0f;
-        int v = 0;
-        if (i < tot) {
-          const int2 raw = __ldcg(reinterpret_cast<const int2*>(p.slots + (size_t)(u0 + c0 + owner) * C + (i - po)));
-          x = __int_as_float(raw.x);
-          v = raw.y;
-          surv = x >= R;
-        }
-        const unsigned bal = __ballot_sync(0xffffffffu, surv);
-        if (surv) {
-          const int pos = n + __popc(bal & lt);
-          if (pos < C) {
-            const Key key = make_key((float)(cj + (double)x), j, x, v);
-            out[pos] = make_ulonglong2(key.hi, key.lo);
-          }
-        }
-        n += __popc(bal);
-      }
-    }
-  }
-  const bool exact = ovf || n > C;
-  if (lane == 0) {
-    RowStat st;
-    st.lse = lse;
-    st.rtopk = R;
-    st.ncand = exact ? -1 : n;
-    st.pad = 0;
-    p.rowstat[row] = st;
-    p.row_ncand[row] = exact ? -1 : n;
-    p.row_cnt[row] = 0u;  // every chunk of the beam has arrived
-  }
-}
-
-// Batch `b`: rank the survivors of its beams (finished beams offer (eos_id, beam score))
-// and write the k best.  Batches that need the exact fallback are left to K2 (path > 0).
-__device__ __noinline__ void batch_finalize(const StepParams& p, int b) {
-  const int lane = threadIdx.x & 31;
-  const int K = p.k;
-  constexpr int kPer = 8;  // keys per lane: up to 256 survivors per batch ranked here
-  int total = 0;
-  bool exact = (p.flags & kFlagForceExact) != 0;
-  int path = exact ? 2 : 0;
-  for (int j0 = 0; j0 < K; j0 += 32) {
-    const int j = j0 + lane;
-    int nj = 0;
-    if (j < K) {
-      const int row = b * K + j;
-      const bool fin = p.finished && p.finished[row];
-      nj = fin ? 1 : __ldcg(p.row_ncand + row);
-      if (!fin && nj < 0) {
-        exact = true;
-        if (path == 0) path = 1;
-      }
-    }
-    total += (int)__reduce_add_sync(0xffffffffu, (unsigned)max(nj, 0));
-  }
-  exact = __any_sync(0xffffffffu, exact);
-  path = __reduce_max_sync(0xffffffffu, (unsigned)path);
-  if (!exact && total > 32 * kPer) {
-    exact = true;
-    path = 3;
-  }
-  if (exact) {
-    if (lane == 0) {
-      p.bstat[b] = path;
-      p.batch_cnt[b] = 0u;
-    }
-    return;
-  }
-  // key i (0 <= i < total) lives in lane i % 32, slot i / 32; beams in order, then survivors
-  Key mine[kPer];
-#pragma unroll
-  for (int m = 0; m < kPer; ++m) {
-    mine[m].hi = ~0ull;
-    mine[m].lo = ~0ull;
-  }
-  int base = 0;
-  for (int j = 0; j < K; ++j) {
-    const int row = b * K + j;
-    const bool fin = p.finished && p.finished[row];
-    const int nj = fin ? 1 : __ldcg(p.row_ncand + row);
-#pragma unroll
-    for (int m = 0; m < kPer; ++m) {
-      const int i = lane + 32 * m;
-      if (i >= base && i < base + nj) {
-        if (fin) {
-          mine[m] = make_key(__ldg(p.beam + row), j, 0.0f, p.eos);
-        } else {
-          const ulonglong2 kk = __ldcg(reinterpret_cast<const ulonglong2*>(p.row_cand) + (size_t)row * p.slot_cap + (i - base));
-          mine[m].hi = kk.x;
-          mine[m].lo = kk.y;
-        }
-      }
-    }
-    base += nj;
-  }
-  int rank[kPer];
-#pragma unroll
-  for (int m = 0; m < kPer; ++m) rank[m] = 0;
-  for (int i = 0; i < total; ++i) {
-    const int src = i & 31, slot = i >> 5;
-    unsigned long long hi = 0, lo = 0;
-#pragma unroll
-    for (int m = 0; m < kPer; ++m)
-      if (m == slot) {
-        hi = mine[m].hi;
-        lo = mine[m].lo;
-      }
-    Key other;
-    other.hi = __shfl_sync(0xffffffffu, hi, src);
-    other.lo = __shfl_sync(0xffffffffu, lo, src);
-#pragma unroll
-    for (int m = 0; m < kPer; ++m) rank[m] += key_less(other, mine[m]) ? 1 : 0;
-  }
-#pragma unroll
-  for (int m = 0; m < kPer; ++m) {
-    const int i = lane + 32 * m;
-    if (i < total && rank[m] < K) {
-      const Key key = mine[m];
-      const int o = b * K + rank[m];
-      const int parent = key_parent(key);
-      const int token = key_token(key);
-      p.out_token[o] = token;
-      p.out_parent[o] = parent;
-      p.out_score[o] = key_score(key);
-      if (p.out_finished) {
-        const bool fin = p.finished && p.finished[b * K + parent];
-        p.out_finished[o] = (fin || token == p.eos) ? 1 : 0;
-      }
-    }
-  }
-  if (lane == 0) {
-    p.bstat[b] = 0;
-    p.batch_cnt[b] = 0u;
-  }
-}
-
-// A warp is done with its part of beam `row` (a chunk, or the whole beam when it is
-// finished and has no chunk to process): count the arrival, and finish the beam / batch
-// when this was the last part.
-__device__ __forceinline__ void arrive(const StepParams& p, int row, bool is_chunk) {
-  const int lane = threadIdx.x & 31;
-  __threadfence();  // this warp's records and survivors are visible before its arrival
-  __syncwarp();
-  bool last_row = !is_chunk;
-  if (is_chunk) {
-    unsigned old = 0;
-    if (lane == 0) old = atomicAdd(p.row_cnt + row, 1u);
-    old = __shfl_sync(0xffffffffu, old, 0);
-    last_row = old == (unsigned)(p.nc - 1);
-    if (last_row) {
-      __threadfence();
-      row_finalize(p, row);
-      __threadfence();
-      __syncwarp();
-    }
-  }
-  if (last_row) {
-    const int b = row / p.k;
-    unsigned old = 0;
-    if (lane == 0) old = atomicAdd(p.batch_cnt + b, 1u);
-    old = __shfl_sync(0xffffffffu, old, 0);
-    if (old == (unsigned)(p.k - 1)) {
-      __threadfence();
-      batch_finalize(p, b);
-    }
-  }
-}
-
 template <int DT, bool BIAS, int VPL>
 __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepParams p) {
   constexpr int VEC = Traits<DT>::kVec;
@@ -559,12 +258,7 @@ __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepPar
   bool aborted = false;
   for (int i = 0; i < n_mine; ++i) {
     const int u = gw + i * nwarps;
-    if (!live(u)) {
-      // a finished beam has no chunk to process: the owner of its chunk 0 arrives for it
-      const int row = row_of(u);
-      if (u == row * nc) arrive(p, row, false);
-      continue;
-    }
+    if (!live(u)) continue;
     const Geo g = geometry(u);
     const int s = n_cons % kStages;
     const bool ok = mbar_wait_bounded(smem_addr(&bars[s]), (uint32_t)((n_cons / kStages) & 1), p.spin_limit_ns);
@@ -850,7 +544,6 @@ __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepPar
       rec[1] = M;
       rec[2] = ssum;
     }
-    arrive(p, row_of(u), true);
   }
 
   if (aborted && lane == 0) {

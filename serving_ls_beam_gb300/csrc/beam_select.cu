@@ -1,17 +1,18 @@
-// Beam-step kernel K2: the exact fallback of the fine rank.  The fine rank itself runs
-// inside K1 (the warp that completes a batch ranks its beams' survivors).  K1 marks a
-// batch for this kernel when a chunk overflowed its survivor slots, a beam kept more
-// survivors than its list holds, the batch has more survivors than one warp ranks, or the
-// exact path is forced for testing.  One CTA per batch: CTAs of unmarked batches return
-// at once.
+// Beam-step kernel K2: the fine rank.  One CTA per batch merges the chunk records of
+// that batch's beams, re-applies each beam's row-level R-top-k, rescores the surviving
+// candidates and ranks them; the k best are the step's output.
 //
 // Method: LightSeq inference article (31duo.com, itemid-283120), hierarchical decoding
-// section — the step's result is the exact top-k of every sequence.  Without a usable
-// candidate queue the exact top-k is found directly: a radix select of each beam's top-k
-// logits (larger x first, then the smaller token id), merged across beams.
+// section: candidates above R-top-k are rescored as beam_score + logit - log_sum_exp
+// and one sort of that short queue per batch gives the exact top-k of every sequence.
 //
 // GB300 design: launched with programmatic dependent launch behind K1, so its launch
-// and prologue overlap K1's last wave; `griddepcontrol.wait` orders it after K1's writes.
+// and prologue overlap K1's last wave; `griddepcontrol.wait` orders it after K1's
+// writes.  The queue is short (about a dozen survivors per beam for k = 4), so instead
+// of a sort each survivor's rank is counted against all the others in shared memory,
+// O(n^2 / threads), and the k with rank < k are written.  A batch whose chunk slots
+// overflowed, or with more than kSelCap survivors, takes an exact path that needs no
+// queue: a per-beam radix select of the top-k logits, merged across beams.
 #include "ls_device.cuh"
 #include "ls_dtype.cuh"
 #include "ls_internal.h"
@@ -29,16 +30,23 @@ struct RowSel {
   int ncand;
 };
 
+constexpr int kPairTile = 1024;  // (beam, chunk) pairs whose slot counts are scanned at once
+
 struct __align__(16) SelSmem {
-  int nbest, nrl;
+  int nsel, big, ovf, nbest, nrl, ptotal;
+  int pc[kPairTile];   // slots to read per pair of the tile, then their exclusive prefix sums
+  float pm[kPairTile];  // chunk max of each (beam, chunk) pair (first tile only)
+  int pn[kPairTile];    // survivor count of each pair (first tile only)
   float beam[kMaxK];
   int fin[kMaxK];
+  int wsum[kSelWarps];
   int wc[kSelWarps];
   unsigned int hist[256];
   unsigned int prefix, pmask;
   int need;
   RowSel row[kMaxK];
   float selg[kSelWarps][64];
+  Key sel[kSelCap];
   Key mg[2 * kMaxK];
   Key best[kMaxK];
   Key rl[kMaxK];
@@ -262,15 +270,19 @@ __global__ void __launch_bounds__(kSelThreads) beam_select_kernel(const StepPara
   const int K = p.k, nc = p.nc, G = p.groups, C = p.slot_cap;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = blockIdx.x;
+  if (tid == 0) {
+    sm.nsel = 0;
+    sm.big = 0;
+    sm.ovf = 0;
+  }
   // inputs that do not come from K1: read before waiting on it
   for (int j = tid; j < K; j += kSelThreads) {
     sm.beam[j] = p.beam[b * K + j];
     sm.fin[j] = (p.finished && p.finished[b * K + j]) ? 1 : 0;
   }
-  grid_dependency_wait();  // K1's records, survivors and batch marks are complete and visible
-  const int path = p.bstat[b];
-  if (path == 0) return;  // K1 ranked this batch
+  grid_dependency_wait();  // K1's records and slots are complete and visible
   __syncthreads();
+  const bool keep_pairs = K * nc <= kPairTile;
   // 1. per beam: log_sum_exp, the row-level R-top-k and the score offset
   for (int j = warp; j < K; j += kSelWarps) {
     const bool fin = sm.fin[j] != 0;
@@ -291,6 +303,7 @@ __global__ void __launch_bounds__(kSelThreads) beam_select_kernel(const StepPara
     // one pass over the chunk records: (max, sum of exp) with online rescaling, the group
     // maxima (G <= 8 held per lane), then fixed shuffle trees (deterministic)
     float M = -INFINITY, S = 0.0f;
+    bool ovf = false;
     float gl[8];
 #pragma unroll
     for (int g = 0; g < 8; ++g) gl[g] = -INFINITY;
@@ -302,7 +315,13 @@ __global__ void __launch_bounds__(kSelThreads) beam_select_kernel(const StepPara
         ga = r4[1];
         if (G > 4) gb = r4[2];
       }
+      const int cnt = __float_as_int(h.x);
       const float mc = h.y, sc = h.z;
+      if (keep_pairs) {
+        sm.pm[j * nc + c] = mc;
+        sm.pn[j * nc + c] = cnt;
+      }
+      ovf |= cnt > C;
       const float Mn = fmaxf(M, mc);
       if (Mn != -INFINITY) {
         S = (M == -INFINITY ? 0.0f : S * exp2f((M - Mn) * kLog2e)) +
@@ -329,6 +348,7 @@ __global__ void __launch_bounds__(kSelThreads) beam_select_kernel(const StepPara
       }
       M = Mn;
     }
+    ovf = __any_sync(0xffffffffu, ovf);
     if (G <= 8) {
 #pragma unroll
       for (int g = 0; g < 8; ++g) {
@@ -378,11 +398,148 @@ __global__ void __launch_bounds__(kSelThreads) beam_select_kernel(const StepPara
         rs.lse = (float)((double)M + (double)log_s);
       }
       sm.row[j] = rs;
+      if (ovf) sm.ovf = 1;
     }
     __syncwarp();
   }
   __syncthreads();
-  exact_select<DT, BIAS>(p, sm, b, path);
+  int path = 0;
+  if (sm.ovf) path = 1;
+  if (p.flags & kFlagForceExact) path = 2;
+  if (path == 0) {
+    // 2. survivors of the row-level R-top-k, rescored: beam_score + x - lse.  The slots of
+    // all (beam, chunk) pairs are flattened so that every load is independent.
+    const int P = K * nc;
+    for (int t0 = 0; t0 < P; t0 += kPairTile) {
+      const int nt = min(kPairTile, P - t0);
+      for (int i = tid; i < nt; i += kSelThreads) {
+        const int pair = t0 + i;
+        const int j = pair / nc;
+        int c = 0;
+        if (sm.row[j].kind == ROW_LIVE) {
+          // a chunk whose max is below the beam's R-top-k holds no survivor: skip its slots
+          float mc;
+          int n;
+          if (keep_pairs) {
+            mc = sm.pm[pair];
+            n = sm.pn[pair];
+          } else {
+            const float* r = rec_ptr(p, (long long)b * K * nc + pair);
+            mc = r[1];
+            n = reinterpret_cast<const int*>(r)[0];
+          }
+          if (mc >= sm.row[j].rtopk) c = min(n, C);
+        }
+        sm.pc[i] = c;
+      }
+      __syncthreads();
+      // exclusive scan of pc[0..nt): 4 consecutive entries per thread
+      constexpr int kPer = kPairTile / kSelThreads;
+      int loc[kPer];
+      int run = 0;
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) {
+        const int i = tid * kPer + e;
+        loc[e] = run;
+        run += (i < nt) ? sm.pc[i] : 0;
+      }
+      int incl = run;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      if (lane == 31) sm.wsum[warp] = incl;
+      __syncthreads();
+      int wbase = 0, tot = 0;
+      for (int w = 0; w < kSelWarps; ++w) {
+        wbase += (w < warp) ? sm.wsum[w] : 0;
+        tot += sm.wsum[w];
+      }
+      const int tbase = wbase + incl - run;
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) {
+        const int i = tid * kPer + e;
+        if (i < nt) sm.pc[i] = tbase + loc[e];
+      }
+      __syncthreads();
+      // 4 slots per thread per round, their loads issued together
+      for (int q0 = tid; q0 < tot; q0 += 4 * kSelThreads) {
+        int2 raw[4];
+        int jj[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int q = q0 + t * kSelThreads;
+          jj[t] = -1;
+          if (q < tot) {
+            int lo = 0, hi = nt - 1;  // last pair with prefix <= q
+            while (lo < hi) {
+              const int mid = (lo + hi + 1) >> 1;
+              if (sm.pc[mid] <= q)
+                lo = mid;
+              else
+                hi = mid - 1;
+            }
+            const int pair = t0 + lo;
+            jj[t] = pair / nc;
+            const long long u = (long long)b * K * nc + pair;
+            raw[t] = *reinterpret_cast<const int2*>(p.slots + (size_t)u * C + (q - sm.pc[lo]));
+          }
+        }
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          if (jj[t] < 0) continue;
+          const int j = jj[t];
+          const float x = __int_as_float(raw[t].x);
+          const RowSel& rs = sm.row[j];
+          if (x >= rs.rtopk) {
+            const Key key = make_key((float)(rs.c + (double)x), j, x, raw[t].y);
+            const int pos = atomicAdd(&sm.nsel, 1);
+            if (pos < kSelCap)
+              sm.sel[pos] = key;
+            else
+              sm.big = 1;
+            atomicAdd(&sm.row[j].ncand, 1);
+          }
+        }
+      }
+      __syncthreads();
+    }
+    for (int idx = tid; idx < K * K; idx += kSelThreads) {
+      const int j = idx / K, v = idx - (idx / K) * K;
+      const int kind = sm.row[j].kind;
+      if (kind == ROW_FIN && v == 0) {
+        const int pos = atomicAdd(&sm.nsel, 1);
+        if (pos < kSelCap)
+          sm.sel[pos] = make_key(sm.beam[j], j, 0.0f, p.eos);
+        else
+          sm.big = 1;
+      } else if (kind == ROW_DEAD) {
+        const int pos = atomicAdd(&sm.nsel, 1);
+        if (pos < kSelCap)
+          sm.sel[pos] = make_key(-INFINITY, j, 0.0f, v);
+        else
+          sm.big = 1;
+        if (v == 0) sm.row[j].ncand = K;
+      }
+    }
+    __syncthreads();
+    if (sm.big) path = 3;
+  }
+  if (path != 0) {
+    exact_select<DT, BIAS>(p, sm, b, path);
+    return;
+  }
+  // 3. rank of every survivor among the survivors; ranks 0..K-1 are the output
+  const int n = sm.nsel;
+  for (int i = tid; i < n; i += kSelThreads) {
+    const Key ki = sm.sel[i];
+    int rank = 0;
+    for (int q = 0; q < n; ++q) rank += key_less(sm.sel[q], ki);
+    if (rank < K) write_output(p, b, rank, ki);
+  }
+  write_row_stats(p, sm, b, false);
+  if (tid == 0) p.bstat[b] = 0;
 }
 
 template <int DT, bool BIAS>

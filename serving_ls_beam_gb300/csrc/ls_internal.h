@@ -44,8 +44,7 @@ struct CandSlot {
 };
 
 struct WsLayout {
-  size_t status_off, rowcnt_off, batchcnt_off, rec_off, slot_off, rowcand_off, rowncand_off, rowstat_off, bstat_off,
-      total;
+  size_t status_off, done_off, rec_off, slot_off, rowstat_off, bstat_off, total;
   int nc_max;      // most chunks per row any plan may use
   int groups;      // G: number of R-top-k groups (power of two >= k)
   int slot_cap;    // C: candidate slots per chunk
@@ -69,14 +68,8 @@ inline void make_divisor(uint32_t d, uint32_t* magic, int* shift) {
   *shift = s;
 }
 
-// Arrival counters live in a fixed area right after the status word, sized from the
-// workspace's byte count alone, so every shape served by one workspace uses the same
-// (zeroed) counter area and no shape's data ever overlaps it.
-inline size_t counter_area_bytes(size_t workspace_bytes) { return align_up(workspace_bytes / 64, 256); }
-
-// Layout for one call.  total == 0 for unsupported shapes.  `data_total` is the end of the
-// data regions when the counter area is `area` bytes.
-inline WsLayout ws_layout_with_area(int batch, int k, int vocab, size_t area) {
+// Returns total == 0 for unsupported shapes.
+inline WsLayout ws_layout(int batch, int k, int vocab) {
   WsLayout w{};
   if (batch < 0 || k < 1 || k > kMaxK || vocab < k) return w;
   const size_t rows = (size_t)batch * (size_t)k;
@@ -86,44 +79,20 @@ inline WsLayout ws_layout_with_area(int batch, int k, int vocab, size_t area) {
   // chunks of 32 x kVplMin vectors over a row of up to 4-byte elements (+ 15 bytes of lead)
   const long long nv_max = (15 + 4ll * vocab + 15) / 16;
   w.nc_max = (int)((nv_max + 32 * kVplMin - 1) / (32 * kVplMin));
-  w.status_off = 0;
-  w.rowcnt_off = 256;
-  w.batchcnt_off = 256 + rows * 4;
-  size_t off = 256 + area;
+  size_t off = 0;
+  w.status_off = off;
+  off += 256;
+  w.done_off = off;
+  off = align_up(off + (size_t)batch * 4, 256);
   w.rec_off = off;
   off = align_up(off + rows * w.nc_max * w.rec_stride, 256);
   w.slot_off = off;
   off = align_up(off + rows * w.nc_max * w.slot_cap * sizeof(CandSlot), 256);
-  w.rowcand_off = off;
-  off = align_up(off + rows * w.slot_cap * 16, 256);
-  w.rowncand_off = off;
-  off = align_up(off + rows * 4, 256);
   w.rowstat_off = off;
   off = align_up(off + rows * sizeof(RowStat), 256);
   w.bstat_off = off;
   off = align_up(off + (size_t)batch * 4, 256);
   w.total = off;
-  return w;
-}
-
-// Smallest workspace for the shape: its counter area (workspace / 64) must hold the
-// shape's counters and the data must fit after it.
-inline size_t ws_required_bytes(int batch, int k, int vocab) {
-  const size_t need_cnt = ((size_t)batch * k + (size_t)batch) * 4;
-  const WsLayout w0 = ws_layout_with_area(batch, k, vocab, 0);
-  if (w0.total == 0) return 0;
-  size_t ws = align_up(w0.total + w0.total / 63 + 512, 256);
-  while (counter_area_bytes(ws) < need_cnt || ws_layout_with_area(batch, k, vocab, counter_area_bytes(ws)).total > ws)
-    ws = align_up(ws + ws / 64 + 256, 256);
-  return ws;
-}
-
-// Layout of a call on a workspace of `workspace_bytes`; total == 0 when it does not fit.
-inline WsLayout ws_layout(int batch, int k, int vocab, size_t workspace_bytes) {
-  const size_t area = counter_area_bytes(workspace_bytes);
-  WsLayout w = ws_layout_with_area(batch, k, vocab, area);
-  const size_t need_cnt = ((size_t)batch * k + (size_t)batch) * 4;
-  if (w.total == 0 || w.total > workspace_bytes || area < need_cnt) w.total = 0;
   return w;
 }
 
@@ -138,12 +107,9 @@ struct StepParams {
   float* out_score;
   uint8_t* out_finished;
   uint32_t* status;
-  uint32_t* row_cnt;     // chunks of each beam done in this call (reset by the beam's last warp)
-  uint32_t* batch_cnt;   // beams of each batch done in this call (reset by the batch's last warp)
+  uint32_t* done;
   unsigned char* rec;
   CandSlot* slots;
-  unsigned long long* row_cand;  // per beam: up to slot_cap keys (hi, lo) of its final survivors
-  int32_t* row_ncand;
   RowStat* rowstat;
   int32_t* bstat;
   int batch, k, vocab, eos;

@@ -10,9 +10,9 @@
 //
 // Limits and sharing: shapes whose scratch (ls_beam_step_workspace_size) exceeds
 // kNoAllocScratchBytes are rejected.  Every call uses the same array and leaves its
-// contents behind; the status word and the arrival counters are cleared at the start of
-// each call.  Calls whose work overlaps on the GPU (different streams, or different host
-// threads without ordering) race on the array and must not be issued.
+// contents behind; the status word is cleared at the start of each call.  Calls whose
+// work overlaps on the GPU (different streams, or different host threads without
+// ordering) race on the array and must not be issued.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -62,12 +62,8 @@ extern "C" ls_status ls_beam_step_noalloc(const void* logits, ls_dtype logit_dty
   void* scratch = scratch_address();
   if (!scratch) return LS_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // the status word and the arrival counters must start at zero; everything else the
-  // step reads it writes first
-  const lsb::WsLayout wl = lsb::ws_layout(batch, k, vocab, kNoAllocScratchBytes);
-  if (wl.total == 0) return LS_ERR_UNSUPPORTED;
-  const size_t zero_bytes = wl.batchcnt_off + (size_t)batch * 4;
-  if (cudaMemsetAsync(scratch, 0, zero_bytes, st) != cudaSuccess) {
+  // the status word must start at zero; everything else the step reads it writes first
+  if (cudaMemsetAsync(scratch, 0, 256, st) != cudaSuccess) {
     cudaGetLastError();
     return LS_ERR_CUDA;
   }
