@@ -19,7 +19,7 @@
  *   - "update the cache" after selection: oracle_cache_reorder() is the
  *     plain gather of the cache rows by parent beam.
  *
- * Readings where the article is silent (each also listed in the design doc):
+ * Readings where the article is silent:
  *   - x = logit + bias[v] (bias optional) is the value used everywhere.
  *   - candidate score s = beam_score + x - lse, lse = log sum_v exp(x_v).
  *   - a finished beam contributes exactly one candidate (eos_id, its score
