@@ -21,6 +21,7 @@ constexpr long long kDefaultSpinNs = 2000000000LL;  // 2 s per bounded wait
 struct DeviceInfo {
   bool ready = false;
   int sms = 0;
+  bool select_ready = false;  // K2's dynamic shared-memory limit raised
   // K1 occupancy per [dtype][bias][vpl index]; 0 = not configured yet
   int step_occ[3][2][2] = {};
   int copy_occ[5] = {};
@@ -86,6 +87,15 @@ int step_occupancy(DeviceInfo* di, int dtype, bool bias, int vpl) {
     occ = o;
   }
   return occ;
+}
+
+bool select_configured(DeviceInfo* di) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!di->select_ready) {
+    if (beam_select_config() != cudaSuccess) return false;
+    di->select_ready = true;
+  }
+  return true;
 }
 
 int copy_occupancy(DeviceInfo* di, int unit) {
@@ -201,6 +211,10 @@ ls_status ls_beam_step(const void* logits, ls_dtype logit_dtype, const float* bi
   p.slot_cap = wl.slot_cap;
   p.rec_stride = wl.rec_stride;
   p.flags = dbg.flags;
+  // K2 copies a batch's slots to shared memory in one bulk copy when they fit (k <= 8)
+  const long long stage = (long long)k * nc * wl.slot_cap * (long long)sizeof(CandSlot);
+  p.sel_stage_bytes = (k <= 8 && nc <= 128 && (long long)k * nc <= 1024 && stage <= kSelStageMax) ? (int)stage : 0;
+  if (!select_configured(di)) return cuda_fail(cudaErrorUnknown);
   p.units = units;
   p.spin_limit_ns = dbg.spin_ns;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -51,7 +51,7 @@ __device__ __forceinline__ float warp_kth_of_lanes(float v, int n, int k) {
   int rank = 0;
   for (int q = 0; q < n; ++q) {
     const float w = __shfl_sync(0xffffffffu, v, q);
-    rank += (w > v) || (w == v && q < lane);
+    rank += (w > v) | ((w == v) & (q < lane));
   }
   const unsigned hit = __ballot_sync(0xffffffffu, lane < n && rank == k - 1);
   return __shfl_sync(0xffffffffu, v, __ffs(hit) - 1);
@@ -64,10 +64,10 @@ __device__ __forceinline__ float warp_kth_of_64(float a, float b, int k) {
   for (int q = 0; q < 32; ++q) {
     const float wa = __shfl_sync(0xffffffffu, a, q);
     const float wb = __shfl_sync(0xffffffffu, b, q);
-    ra += (wa > a) || (wa == a && q < lane);
+    ra += (wa > a) | ((wa == a) & (q < lane));
     ra += (wb > a);
     rb += (wa >= b);
-    rb += (wb > b) || (wb == b && q < lane);
+    rb += (wb > b) | ((wb == b) & (q < lane));
   }
   const bool ha = ra == k - 1, hb = rb == k - 1;
   const unsigned hit = __ballot_sync(0xffffffffu, ha || hb);
@@ -210,6 +210,9 @@ __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepPar
     fence_barrier_init();
   }
   __syncwarp();
+  // the fine-rank kernel may be scheduled from now on: its CTAs take the SM space this
+  // grid's CTAs free as they finish, and wait for the whole grid before reading its output
+  grid_launch_dependents();
 
   auto row_of = [&](int u) -> int { return (int)fast_div((uint32_t)u, p.nc_magic, p.nc_shift); };
   auto live = [&](int u) -> bool { return !(p.finished && p.finished[row_of(u)]); };

@@ -33,6 +33,7 @@ struct RowSel {
 constexpr int kPairTile = 1024;  // (beam, chunk) pairs whose slot counts are scanned at once
 
 struct __align__(16) SelSmem {
+  unsigned long long sbar;  // completion of the slot staging copy
   int nsel, big, ovf, nbest, nrl, ptotal;
   int pc[kPairTile];   // slots to read per pair of the tile, then their exclusive prefix sums
   float pm[kPairTile];  // chunk max of each (beam, chunk) pair (first tile only)
@@ -67,7 +68,7 @@ __device__ __forceinline__ float warp_kth_largest(const float* vals, int n, int 
     int rank = 0;
     for (int q = 0; q < n; ++q) {
       const float w = vals[q];
-      rank += (w > v) || (w == v && q < g);
+      rank += (w > v) | ((w == v) & (q < g));
     }
     if (rank == k - 1) res = v;
   }
@@ -78,17 +79,14 @@ __device__ __forceinline__ const float* rec_ptr(const StepParams& p, long long u
   return reinterpret_cast<const float*>(p.rec + (size_t)u * p.rec_stride);
 }
 
-__device__ __forceinline__ void write_output(const StepParams& p, int b, int r, const Key& key) {
+__device__ __forceinline__ void write_output(const StepParams& p, const SelSmem& sm, int b, int r, const Key& key) {
   const int o = b * p.k + r;
   const int parent = key_parent(key);
   const int token = key_token(key);
   p.out_token[o] = token;
   p.out_parent[o] = parent;
   p.out_score[o] = key_score(key);
-  if (p.out_finished) {
-    const bool fin = p.finished && p.finished[b * p.k + parent];
-    p.out_finished[o] = (fin || token == p.eos) ? 1 : 0;
-  }
+  if (p.out_finished) p.out_finished[o] = (sm.fin[parent] || token == p.eos) ? 1 : 0;
 }
 
 __device__ __forceinline__ void write_row_stats(const StepParams& p, const SelSmem& sm, int b, bool exact) {
@@ -259,14 +257,277 @@ __device__ void exact_select(const StepParams& p, SelSmem& sm, int b, int path) 
     __syncthreads();
     merge_into_best(sm, K);
   }
-  for (int r = tid; r < K && r < sm.nbest; r += kSelThreads) write_output(p, b, r, sm.best[r]);
+  for (int r = tid; r < K && r < sm.nbest; r += kSelThreads) write_output(p, sm, b, r, sm.best[r]);
   write_row_stats(p, sm, b, true);
   if (tid == 0) p.bstat[b] = path;
 }
 
+// Fine rank of batch b for k <= 8 (G <= 8 group maxima per beam) with at most 128 chunks per
+// beam and kPairTile (beam, chunk) pairs per batch: the common case, kept short because the
+// code runs once per CTA right after K1 (every instruction line is fetched cold).
+//   AB. warp j merges beam j's chunk records (loads issued together): the row max M, then
+//       S = sum of the chunk sums rescaled to M, the G group maxima and the row-level
+//       R-top-k (k-th largest of them); lse = M + log S.
+//   C.  each warp flattens the slots of its own run of pairs (a warp scan, no CTA barrier),
+//       keeps the slots with x >= R of their beam and rescores them into rank keys.
+//   D.  each key's rank is counted against the others; ranks < k are the outputs.
+// Returns the path: 0 when the outputs are written, otherwise the reason for the exact path.
+//
+// With dry = true the same code runs without any global store and with its loops capped,
+// on whatever the workspace holds: a CTA that becomes resident while K1 is still running
+// makes this pass before waiting on K1, so that the instructions of the real pass are
+// already in the SM's instruction cache (fetching them cold costs microseconds per phase,
+// more than the work itself).  Every count and address stays clamped, so stale or
+// half-written records are harmless; nothing the dry pass computes is kept.
 template <int DT, bool BIAS>
-__global__ void __launch_bounds__(kSelThreads) beam_select_kernel(const StepParams p) {
+__device__ __forceinline__ int queue_select(const StepParams& p, SelSmem& sm, unsigned char* stage, int b, bool dry) {
+  const int K = p.k, nc = p.nc, G = p.groups, C = p.slot_cap;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const long long ub = (long long)b * K * nc;
+  // the batch's slots (contiguous) land in shared memory while AB runs
+  const bool staged = !dry && p.sel_stage_bytes > 0;
+  if (staged && tid == 0) {
+    const uint32_t bar = smem_addr(&sm.sbar);
+    mbar_init(bar, 1);
+    fence_barrier_init();
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    mbar_arrive_expect_tx(bar, (uint32_t)p.sel_stage_bytes);
+    bulk_load_plain(smem_addr(stage), p.slots + (size_t)ub * C, (uint32_t)p.sel_stage_bytes, bar);
+  }
+  // AB
+  if (warp < K) {
+    const int j = warp;
+    if (sm.fin[j]) {
+      if (lane == 0) {
+        RowSel rs;
+        rs.c = 0.0;
+        rs.rtopk = __int_as_float(0x7fc00000);
+        rs.lse = __int_as_float(0x7fc00000);
+        rs.kind = ROW_FIN;
+        rs.ncand = 1;
+        sm.row[j] = rs;
+      }
+    } else {
+      const long long u0 = ((long long)b * K + j) * nc;
+      float m[4], sc[4];
+      float4 ga[4], gb[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int c = lane + 32 * i;
+        m[i] = -INFINITY;
+        sc[i] = 0.0f;
+        ga[i] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        gb[i] = ga[i];
+        if (c < nc) {
+          const float4* r4 = reinterpret_cast<const float4*>(rec_ptr(p, u0 + c));
+          const float4 h = __ldcg(r4);
+          ga[i] = __ldcg(r4 + 1);
+          if (G > 4) gb[i] = __ldcg(r4 + 2);
+          m[i] = h.y;
+          sc[i] = h.z;
+          sm.pn[j * nc + c] = dry ? 0 : __float_as_int(h.x);
+        }
+      }
+      const float M = warp_max(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])));
+      float ls = 0.0f;
+      bool ovf = false;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int c = lane + 32 * i;
+        if (c < nc) {
+          if (m[i] != -INFINITY) ls += sc[i] * exp2f((m[i] - M) * kLog2e);
+          sm.pm[j * nc + c] = m[i];
+          ovf |= sm.pn[j * nc + c] > C;
+        }
+      }
+      float S = ls;
+#pragma unroll 1
+      for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+      // group maxima: lane-local over its chunks, then over the warp
+      float g8[8] = {ga[0].x, ga[0].y, ga[0].z, ga[0].w, gb[0].x, gb[0].y, gb[0].z, gb[0].w};
+#pragma unroll
+      for (int i = 1; i < 4; ++i) {
+        g8[0] = fmaxf(g8[0], ga[i].x);
+        g8[1] = fmaxf(g8[1], ga[i].y);
+        g8[2] = fmaxf(g8[2], ga[i].z);
+        g8[3] = fmaxf(g8[3], ga[i].w);
+        g8[4] = fmaxf(g8[4], gb[i].x);
+        g8[5] = fmaxf(g8[5], gb[i].y);
+        g8[6] = fmaxf(g8[6], gb[i].z);
+        g8[7] = fmaxf(g8[7], gb[i].w);
+      }
+#pragma unroll 1
+      for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+        for (int g = 0; g < 8; ++g) g8[g] = fmaxf(g8[g], __shfl_xor_sync(0xffffffffu, g8[g], o));
+      }
+      // lane g < G holds group max g; R = the k-th largest (ties by group index)
+      float v = g8[0];
+#pragma unroll
+      for (int g = 1; g < 8; ++g) v = lane == g ? g8[g] : v;
+      int rank = 0;
+#pragma unroll 1
+      for (int q = 0; q < G; ++q) {
+        const float w = __shfl_sync(0xffffffffu, v, q);
+        rank += (w > v) | ((w == v) & (q < lane));
+      }
+      const unsigned hit = __ballot_sync(0xffffffffu, lane < G && rank == K - 1);
+      const float R = __shfl_sync(0xffffffffu, v, __ffs(hit) - 1);
+      ovf = __any_sync(0xffffffffu, ovf);
+      if (lane == 0) {
+        const float beam = sm.beam[j];
+        RowSel rs;
+        rs.rtopk = R;
+        rs.ncand = 0;
+        if (M == -INFINITY || beam == -INFINITY) {
+          rs.kind = ROW_DEAD;
+          rs.c = -(double)INFINITY;
+          rs.lse = M == -INFINITY ? -INFINITY : M + logf(S);
+        } else {
+          const float log_s = logf(S);
+          rs.kind = ROW_LIVE;
+          rs.c = (double)beam - (double)M - (double)log_s;  // beam - lse, lse = M + log S
+          rs.lse = (float)((double)M + (double)log_s);
+        }
+        sm.row[j] = rs;
+        if (ovf) sm.ovf = 1;
+      }
+    }
+  }
+  __syncthreads();
+  if (!dry) {
+    if (sm.ovf) return 1;
+    if (p.flags & kFlagForceExact) return 2;
+  }
+
+  // C: warp w takes pairs [qb, qe); pair q = j * nc + c
+  const int P = K * nc;
+  const int T = (P + kSelWarps - 1) / kSelWarps;
+  const int qb = warp * T, qe = min(P, qb + T);
+  int run = 0;
+#pragma unroll 1
+  for (int q0 = qb; q0 < qe; q0 += 32) {
+    const int q = q0 + lane;
+    int cnt = 0;
+    if (q < qe) {
+      const RowSel& rs = sm.row[q / nc];
+      if (dry)
+        cnt = 1;  // one slot per pair: every load below stays inside the pair's slots
+      else if (rs.kind == ROW_LIVE && sm.pm[q] >= rs.rtopk)
+        cnt = min(sm.pn[q], C);
+    }
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (q < qe) sm.pc[q] = run + incl - cnt;
+    run += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  __syncwarp();
+  if (staged && !mbar_wait_bounded(smem_addr(&sm.sbar), 0, p.spin_limit_ns)) {
+    // the copy did not complete in time: record it, let it land, write nothing
+    if (tid == 0) {
+      atomicOr(p.status, kDevTimeout);
+      mbar_wait_bounded(smem_addr(&sm.sbar), 0, 2000000000LL);
+    }
+    __syncthreads();
+    return -1;
+  }
+  if (dry) run = min(run, 32);
+  const CandSlot* sslots = reinterpret_cast<const CandSlot*>(stage);
+  const unsigned lt_mask = (1u << lane) - 1u;
+  // 4 slots per lane per round, loads issued together; no data-dependent branch (a
+  // divergent branch costs more than the work it guards here)
+  // binary-search depth: the largest power of two below the warp's pair count
+  int top = 1;
+  while (top * 2 < qe - qb) top *= 2;
+#pragma unroll 1
+  for (int i0 = 0; i0 < run; i0 += 4 * 32) {
+    int2 raw[4];
+    int jj[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int i = i0 + t * 32 + lane;
+      jj[t] = -1;
+      raw[t] = make_int2((int)0xff800000u, 0);
+      if (i0 + t * 32 < run) {  // warp-uniform
+        // last pair of [qb, qe) whose prefix is <= i
+        int lo = qb;
+#pragma unroll 1
+        for (int st = top; st > 0; st >>= 1) {
+          const int cand = min(lo + st, qe - 1);
+          lo = (sm.pc[cand] <= i) ? cand : lo;
+        }
+        if (i < run) {
+          jj[t] = (int)fast_div((uint32_t)lo, p.nc_magic, p.nc_shift);
+          const size_t si = (size_t)lo * C + (i - sm.pc[lo]);
+          raw[t] = staged ? *reinterpret_cast<const int2*>(sslots + si)
+                          : __ldcg(reinterpret_cast<const int2*>(p.slots + (size_t)ub * C + si));
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int jr = max(jj[t], 0);
+      const float x = __int_as_float(raw[t].x);
+      const RowSel& rs = sm.row[jr];
+      const bool surv = (jj[t] >= 0) & (x >= rs.rtopk);
+      const unsigned m = __ballot_sync(0xffffffffu, surv);
+      if (m != 0u) {  // warp-uniform
+        int base = 0;
+        if (lane == 0) base = atomicAdd(&sm.nsel, __popc(m));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        const int pos = base + __popc(m & lt_mask);
+        if (surv & (pos < kSelCap)) sm.sel[pos] = make_key((float)(rs.c + (double)x), jr, x, raw[t].y);
+        // survivors per beam: the first lane of each beam's group adds the group's count
+        const unsigned same = __match_any_sync(0xffffffffu, surv ? jr : -1);
+        if (surv & ((same & lt_mask) == 0u)) atomicAdd(&sm.row[jr].ncand, __popc(same));
+      }
+    }
+  }
+  // finished beams offer (eos_id, beam score); beams with no finite score offer k tokens
+  if (tid < K * K) {
+    const int jr = tid / K, v = tid - jr * K;
+    const int kind = sm.row[jr].kind;
+    if ((kind == ROW_FIN && v == 0) || kind == ROW_DEAD) {
+      const int pos = atomicAdd(&sm.nsel, 1);
+      if (pos < kSelCap)
+        sm.sel[pos] = kind == ROW_FIN ? make_key(sm.beam[jr], jr, 0.0f, p.eos) : make_key(-INFINITY, jr, 0.0f, v);
+      else
+        sm.big = 1;
+      if (kind == ROW_DEAD && v == 0) sm.row[jr].ncand = K;
+    }
+  }
+  __syncthreads();
+  if ((sm.big || sm.nsel > kSelCap) && !dry) return 3;
+  // D
+  const int n = dry ? min(sm.nsel, 32) : sm.nsel;
+#pragma unroll 1
+  for (int i = tid; i < n; i += kSelThreads) {
+    const Key ki = sm.sel[i];
+    int r0 = 0, r1 = 0;
+    int q = 0;
+#pragma unroll 1
+    for (; q + 1 < n; q += 2) {
+      r0 += key_less(sm.sel[q], ki);
+      r1 += key_less(sm.sel[q + 1], ki);
+    }
+    if (q < n) r0 += key_less(sm.sel[q], ki);
+    if (r0 + r1 < K && !dry) write_output(p, sm, b, r0 + r1, ki);
+  }
+  if (!dry) {
+    write_row_stats(p, sm, b, false);
+    if (tid == 0) p.bstat[b] = 0;
+  }
+  return 0;
+}
+
+template <int DT, bool BIAS>
+__global__ void __launch_bounds__(kSelThreads, 1) beam_select_kernel(const StepParams p) {
   __shared__ SelSmem sm;
+  extern __shared__ __align__(128) unsigned char sel_stage[];
   const int K = p.k, nc = p.nc, G = p.groups, C = p.slot_cap;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = blockIdx.x;
@@ -280,8 +541,24 @@ __global__ void __launch_bounds__(kSelThreads) beam_select_kernel(const StepPara
     sm.beam[j] = p.beam[b * K + j];
     sm.fin[j] = (p.finished && p.finished[b * K + j]) ? 1 : 0;
   }
+  __syncthreads();
+  const bool queue_path = K <= 8 && nc <= 128 && K * nc <= kPairTile;
+  if (queue_path) {
+    queue_select<DT, BIAS>(p, sm, sel_stage, b, true);  // warms the instruction cache (no stores)
+    __syncthreads();
+    if (tid == 0) {
+      sm.nsel = 0;
+      sm.big = 0;
+      sm.ovf = 0;
+    }
+  }
   grid_dependency_wait();  // K1's records and slots are complete and visible
   __syncthreads();
+  if (queue_path) {
+    const int path = queue_select<DT, BIAS>(p, sm, sel_stage, b, false);
+    if (path > 0) exact_select<DT, BIAS>(p, sm, b, path);
+    return;
+  }
   const bool keep_pairs = K * nc <= kPairTile;
   // 1. per beam: log_sum_exp, the row-level R-top-k and the score offset
   for (int j = warp; j < K; j += kSelWarps) {
@@ -536,7 +813,7 @@ __global__ void __launch_bounds__(kSelThreads) beam_select_kernel(const StepPara
     const Key ki = sm.sel[i];
     int rank = 0;
     for (int q = 0; q < n; ++q) rank += key_less(sm.sel[q], ki);
-    if (rank < K) write_output(p, b, rank, ki);
+    if (rank < K) write_output(p, sm, b, rank, ki);
   }
   write_row_stats(p, sm, b, false);
   if (tid == 0) p.bstat[b] = 0;
@@ -547,7 +824,7 @@ cudaError_t launch_t(const StepParams& p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.batch);
   cfg.blockDim = dim3(kSelThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = (size_t)p.sel_stage_bytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -557,7 +834,22 @@ cudaError_t launch_t(const StepParams& p, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, beam_select_kernel<DT, BIAS>, p);
 }
 
+template <int DT, bool BIAS>
+cudaError_t config_t() {
+  return cudaFuncSetAttribute(beam_select_kernel<DT, BIAS>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelStageMax);
+}
+
 }  // namespace
+
+cudaError_t beam_select_config() {
+  cudaError_t e = config_t<DT_F32, false>();
+  if (e == cudaSuccess) e = config_t<DT_F32, true>();
+  if (e == cudaSuccess) e = config_t<DT_F16, false>();
+  if (e == cudaSuccess) e = config_t<DT_F16, true>();
+  if (e == cudaSuccess) e = config_t<DT_BF16, false>();
+  if (e == cudaSuccess) e = config_t<DT_BF16, true>();
+  return e;
+}
 
 cudaError_t launch_beam_select(const StepParams& p, int dtype, cudaStream_t stream) {
   const bool bias = p.bias != nullptr;

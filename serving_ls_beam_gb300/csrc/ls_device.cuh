@@ -92,6 +92,13 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+// 1-D bulk copy global -> shared without an L2 hint (same alignment rules as bulk_load).
+__device__ __forceinline__ void bulk_load_plain(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -133,8 +140,10 @@ __device__ __forceinline__ Key make_key(float s, int parent, float x, int token)
   k.lo = ((unsigned long long)xo << 32) | (uint32_t)token;
   return k;
 }
+// Written without short-circuit operators: a branch per comparison costs several times
+// the comparison itself in the fine rank's loops.
 __device__ __forceinline__ bool key_less(const Key& a, const Key& b) {
-  return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo);
+  return (a.hi < b.hi) | ((a.hi == b.hi) & (a.lo < b.lo));
 }
 __device__ __forceinline__ float key_score(const Key& k) { return ord_float(~(uint32_t)(k.hi >> 32)); }
 __device__ __forceinline__ int key_parent(const Key& k) { return (int)(uint32_t)(k.hi & 0xffffffffu); }

@@ -21,6 +21,7 @@ constexpr int kSelThreads = 256;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kMaxK = 64;
 constexpr int kSelCap = 512;  // survivors the fine rank holds in shared memory
+constexpr int kSelStageMax = 96 * 1024;  // a batch's candidate slots staged in shared memory (bytes)
 
 // Device status bits (workspace word 0).
 constexpr uint32_t kDevTimeout = 1u << 0;
@@ -121,6 +122,7 @@ struct StepParams {
   int slot_cap;
   int rec_stride;
   int flags;
+  int sel_stage_bytes;  // K2: bytes of a batch's slots copied to shared memory, 0 = read in place
   long long units;  // rows * nc
   long long spin_limit_ns;
 };
@@ -145,6 +147,7 @@ size_t beam_rows_smem_bytes(int vpl);
 cudaError_t beam_rows_config(int dtype, bool bias, int vpl, int* occupancy);
 cudaError_t launch_beam_rows(const StepParams& p, int dtype, int vpl, int grid, cudaStream_t stream);
 cudaError_t launch_beam_select(const StepParams& p, int dtype, cudaStream_t stream);
+cudaError_t beam_select_config();  // once per device: allow kSelStageMax of dynamic shared memory
 cudaError_t launch_cache_reorder(const ReorderParams& p, int unit, int grid, cudaStream_t stream);
 cudaError_t cache_reorder_occupancy(int unit, int* occupancy);
 
