@@ -56,6 +56,8 @@ def _load():
             lib.oracle_rtopk_stats.restype = ip
             lib.oracle_cache_reorder.argtypes = [vp, vp, ip, vp, ip, ip, ip, ip, ip, ip, ip]
             lib.oracle_cache_reorder.restype = ip
+            lib.oracle_backtrack.argtypes = [vp, vp, ip, ip, ip, ip, vp, vp]
+            lib.oracle_backtrack.restype = ip
             _lib = lib
     return _lib
 
@@ -128,3 +130,18 @@ def cache_reorder(src, parent, length, dst=None):
     if rc != 0:
         raise ValueError(f"oracle_cache_reorder failed ({rc})")
     return out
+
+
+def backtrack(token_hist, parent_hist, eos_id):
+    """Token sequences [batch, k, steps] and lengths [batch, k] of the final beams, read back through
+    the parent pointers of the per-step history [steps, batch, k]."""
+    lib = _load()
+    tok = np.ascontiguousarray(token_hist, dtype=np.int32)
+    par = np.ascontiguousarray(parent_hist, dtype=np.int32)
+    steps, batch, k = tok.shape
+    seq = np.empty((batch, k, steps), np.int32)
+    ln = np.empty((batch, k), np.int32)
+    rc = lib.oracle_backtrack(_ptr(tok), _ptr(par), steps, batch, k, int(eos_id), _ptr(seq), _ptr(ln))
+    if rc != 0:
+        raise ValueError(f"oracle_backtrack failed ({rc})")
+    return seq, ln

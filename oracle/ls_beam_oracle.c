@@ -262,3 +262,40 @@ int oracle_cache_reorder(const void* src, void* dst, int elem_bytes, const int32
       }
   return 0;
 }
+
+/*
+ * End of a search: the token sequence of every final beam, read back through the
+ * per-step parent pointers (the step after the decode loop; the article's decoding
+ * keeps a beam's history by parent beam, which the cache refresh also follows).
+ *
+ * token_hist, parent_hist [steps, batch, k]: the outputs of decode steps 1..steps
+ * (step t's beam j continued beam parent_hist[t, b, j] of step t-1 and appended
+ * token_hist[t, b, j]).  For final beam j of batch b:
+ *   c_{steps-1} = j,  seq[b, j, t] = token_hist[t, b, c_t],  c_{t-1} = parent_hist[t, b, c_t].
+ * len[b, j] = 1 + the first t with seq[b, j, t] == eos_id, or steps when there is none.
+ * Returns -1 on bad arguments (including a parent outside [0, k) on a walked path).
+ */
+int oracle_backtrack(const int32_t* token_hist, const int32_t* parent_hist, int steps, int batch, int k,
+                     int eos_id, int32_t* out_seq, int32_t* out_len) {
+  if (steps < 0 || batch < 0 || k < 1) return -1;
+  if (steps == 0 || batch == 0) return 0;
+  if (!token_hist || !parent_hist || !out_seq || !out_len) return -1;
+  for (int b = 0; b < batch; ++b)
+    for (int j = 0; j < k; ++j) {
+      int c = j;
+      for (int t = steps - 1; t >= 0; --t) {
+        if (c < 0 || c >= k) return -1;
+        size_t h = ((size_t)t * batch + b) * k + c;
+        out_seq[((size_t)b * k + j) * steps + t] = token_hist[h];
+        c = parent_hist[h];
+      }
+      int len = steps;
+      for (int t = 0; t < steps; ++t)
+        if (out_seq[((size_t)b * k + j) * steps + t] == eos_id) {
+          len = t + 1;
+          break;
+        }
+      out_len[(size_t)b * k + j] = len;
+    }
+  return 0;
+}
