@@ -270,7 +270,7 @@ def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
         layers, heads, max_len, head_dim = wr.kv_shape
         shape = (layers, wr.rows, heads, max_len, head_dim)
         caches = [torch.from_numpy(synth.kv_cache(shape, wr.seed, which=i)).to(dev) for i in range(2)]
-    loop = BeamSearchLoop(B, K, V, wr.eos_id, kv_shape=wr.kv_shape, device=dev, caches=caches)
+    loop = BeamSearchLoop(B, K, V, wr.eos_id, kv_shape=wr.kv_shape, device=dev, caches=caches, max_steps=T)
     setup_s = time.time() - t0
 
     def lens(t):  # cache positions refreshed at decode step t (1-based)
@@ -278,10 +278,10 @@ def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
 
     stream = torch.cuda.Stream(device=dev)
     try:  # events inside a captured graph must be "external" record nodes to be timed
-        ev_k = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)] for _ in range(T)]
+        ev_k = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)] for _ in range(T + 1)]
         graph_events = True
     except TypeError:
-        ev_k = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(T)]
+        ev_k = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(T + 1)]
         graph_events = False
 
     def run_all(instrument: bool):
@@ -290,17 +290,22 @@ def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
             if instrument:
                 ev_k[t][0].record()
             s, n = loop.cur, 1 - loop.cur
+            tok, par = loop.token_out(t + 1), loop.parent_out(t + 1)
             lsb.check(lsb.ls_beam_step(d_logits[t], d_bias, loop.scores[s], loop.finished[s], wr.eos_id,
-                                       loop.token[n], loop.parent[n], loop.scores[n], loop.finished[n],
-                                       loop.workspace), "ls_beam_step")
+                                       tok, par, loop.scores[n], loop.finished[n], loop.workspace), "ls_beam_step")
             if instrument:
                 ev_k[t][1].record()
             if loop.cache is not None:
-                lsb.check(lsb.ls_cache_reorder(loop.cache[s], loop.cache[n], loop.parent[n], lens(t + 1)),
-                          "ls_cache_reorder")
+                lsb.check(lsb.ls_cache_reorder(loop.cache[s], loop.cache[n], par, lens(t + 1)), "ls_cache_reorder")
             if instrument:
                 ev_k[t][2].record()
             loop.cur = n
+        # end of the search: every final beam's token sequence from the parent history
+        if instrument:
+            ev_k[T][0].record()
+        loop.finalize(T)
+        if instrument:
+            ev_k[T][1].record()
 
     # warm the library's per-device setup outside capture, then capture both graphs
     with torch.cuda.stream(stream):
@@ -316,7 +321,7 @@ def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
             run_all(True)
     torch.cuda.synchronize()
 
-    launches_per_step = T * (2 if loop.cache is not None else 1)
+    launches_per_step = T * (3 if loop.cache is not None else 2) + 1  # K1, K2, K4 per decode step + backtrack
     for _ in range(args.warmup):
         g_plain.replay()
     torch.cuda.synchronize()
@@ -334,7 +339,7 @@ def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
         barrier(world)
         ms_plain = e0.elapsed_time(e1)
         # per-kernel durations: the same graph with an event around each kernel
-        k1_ms, k4_ms = 0.0, 0.0
+        k1_ms, k4_ms, bt_ms = 0.0, 0.0, 0.0
         reps = max(1, min(args.steps, 3))
         with torch.cuda.stream(stream):
             for _ in range(reps):
@@ -347,9 +352,11 @@ def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
                     k1_ms += ev_k[t][0].elapsed_time(ev_k[t][1])
                     if loop.cache is not None:
                         k4_ms += ev_k[t][1].elapsed_time(ev_k[t][2])
+                bt_ms += ev_k[T][0].elapsed_time(ev_k[T][1])
     lsb.check(lsb.ls_read_status(loop.workspace, stream), "device status")
     k1_ms /= reps
     k4_ms /= reps
+    bt_ms /= reps
     ms_total = max_over_ranks(ms_plain, world, dev)
     ms_per_step = ms_total / args.steps
     decode_steps = T * args.steps * world
@@ -375,7 +382,12 @@ def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
         kern["cache_reorder"] = {"bound": "hbm", "achieved": k4_gbs, "peak": peak, "unit": "GB/s",
                                  "frac": k4_gbs / peak, "traffic": recorded_traffic("cache_reorder", wr.name),
                                  "us_per_launch": k4_ms * 1e3 / T, "algorithmic_bytes_per_launch": k4_bytes / T}
-    dominant = max(kern, key=lambda n: kern[n]["us_per_launch"])
+    bt_bytes = 2 * T * B * K * 4 + B * K * (T + 1) * 4  # history read, sequences and lengths written
+    bt_gbs = bt_bytes / (bt_ms / 1e3) / 1e9 if bt_ms > 0 else 0.0
+    kern["backtrack"] = {"bound": "latency", "achieved": bt_gbs, "peak": peak, "unit": "GB/s", "frac": bt_gbs / peak,
+                         "traffic": None, "us_per_launch": bt_ms * 1e3, "algorithmic_bytes_per_launch": bt_bytes,
+                         "launches_per_step": 1}
+    dominant = max((n for n in kern if n != "backtrack"), key=lambda n: kern[n]["us_per_launch"])
     roof = {key: kern[dominant][key] for key in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
     roof["kernel"] = dominant
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback"
@@ -423,6 +435,8 @@ def bench_e2e(args, wr, loop, host_logits, bias_np, beam0, fin0, lens, dev, worl
     h2d_done = [torch.cuda.Event() for _ in range(2)]
     buf_free = [torch.cuda.Event() for _ in range(2)]
     d2h_done = [torch.cuda.Event() for _ in range(T)]
+    seq_host = torch.empty(wr.batch * wr.k * T, dtype=torch.int32).pin_memory()
+    len_host = torch.empty((wr.batch, wr.k), dtype=torch.int32).pin_memory()
 
     def one_run():
         loop.reset(beam0, fin0)
@@ -446,6 +460,10 @@ def bench_e2e(args, wr, loop, host_logits, bias_np, beam0, fin0, lens, dev, worl
                 if bool(out_host["finished"][t - 1].all()):
                     stop = t
                     break
+        # the search's result: every final beam's token sequence, read back to the host
+        seq, ln = loop.finalize(stop)
+        seq_host[: seq.numel()].copy_(seq.reshape(-1), non_blocking=True)
+        len_host.copy_(ln, non_blocking=True)
         torch.cuda.synchronize()
         return stop
 
@@ -463,9 +481,11 @@ def bench_e2e(args, wr, loop, host_logits, bias_np, beam0, fin0, lens, dev, worl
     lsb.check(lsb.ls_read_status(loop.workspace), "device status")
     h2d = int(pinned[0].numel() * pinned.element_size())
     d2h = int(sum(v[0].numel() * v.element_size() for v in out_host.values()))
-    return {"value": steps_done * world / dt, "unit": UNIT, "h2d_bytes_per_step": h2d * T, "d2h_bytes_per_step": d2h * T,
-            "decode_steps_run": steps_done, "note": "per benchmark step (all decode steps): logits H2D from pinned "
-            "memory every decode step, outputs D2H every decode step, wall clock"}
+    d2h_final = (wr.batch * wr.k * T + wr.batch * wr.k) * 4
+    return {"value": steps_done * world / dt, "unit": UNIT, "h2d_bytes_per_step": h2d * T,
+            "d2h_bytes_per_step": d2h * T + d2h_final, "decode_steps_run": steps_done,
+            "note": "per benchmark step (all decode steps): logits H2D from pinned memory every decode step, "
+                    "outputs D2H every decode step, final token sequences D2H at the end, wall clock"}
 
 
 def bench_reference(args, w: synth.Workload):

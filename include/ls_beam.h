@@ -119,6 +119,27 @@ LS_API ls_status ls_cache_reorder(const void* src, void* dst, ls_dtype dtype, co
                            int head_dim, void* workspace, void* stream);
 
 /*
+ * End of a search: the token sequence of every final beam, read back through the
+ * per-step parent pointers (article: decoding keeps, for every new beam, the beam it
+ * continued — the same parent index the cache refresh follows).
+ *
+ *  token_hist, parent_hist  [steps, batch, k] int32, device: the out_token / out_parent of
+ *              decode steps 1..steps (step t's beam j appended token_hist[t, b, j] to beam
+ *              parent_hist[t, b, j] of step t-1).
+ *  out_seq     [batch, k, steps] int32, device: out_seq[b, j, t] = the token final beam j
+ *              of batch b took at step t (final beams in the order of the last step, i.e.
+ *              best first).
+ *  out_len     [batch, k] int32, device: 1 + the first t whose token is eos_id, or steps.
+ *  workspace   NULL, or a workspace initialised by ls_workspace_init: a parent outside
+ *              [0, k) on a walked path then sets LS_ERR_INTERNAL in its status word (the
+ *              walk stays in bounds; that beam's output is unspecified).
+ *  steps == 0 or batch == 0 is a no-op.  Buffers are caller-owned; nothing is allocated.
+ */
+LS_API ls_status ls_backtrack(const int32_t* token_hist, const int32_t* parent_hist, int steps, int batch,
+                              int k, int eos_id, int32_t* out_seq, int32_t* out_len, void* workspace,
+                              void* stream);
+
+/*
  * Synchronise `stream`, return the status the device recorded in `workspace` since
  * the last read, and clear it.  LS_OK when nothing was recorded.
  */

@@ -18,7 +18,7 @@ __all__ = [
     "LS_OK", "LS_ERR_INVALID_ARG", "LS_ERR_UNSUPPORTED", "LS_ERR_CUDA", "LS_ERR_TIMEOUT", "LS_ERR_INTERNAL",
     "LS_DTYPE_F32", "LS_DTYPE_F16", "LS_DTYPE_BF16", "LS_MAX_K", "LsBeamError", "library_path", "load_library",
     "check", "ls_beam_step_workspace_size", "ls_workspace_init", "ls_beam_step", "ls_cache_reorder",
-    "ls_read_status", "ls_status_string", "ls_read_row_stats", "ls_beam_step_noalloc",
+    "ls_read_status", "ls_status_string", "ls_read_row_stats", "ls_beam_step_noalloc", "ls_backtrack",
 ]
 
 LS_OK, LS_ERR_INVALID_ARG, LS_ERR_UNSUPPORTED, LS_ERR_CUDA, LS_ERR_TIMEOUT, LS_ERR_INTERNAL = range(6)
@@ -65,6 +65,8 @@ def load_library():
         lib.ls_read_row_stats.restype = ip
         lib.ls_beam_step_noalloc.argtypes = [vp, ip, vp, vp, vp, ip, ip, ip, ip, vp, vp, vp, vp, vp]
         lib.ls_beam_step_noalloc.restype = ip
+        lib.ls_backtrack.argtypes = [vp, vp, ip, ip, ip, ip, vp, vp, vp, vp]
+        lib.ls_backtrack.restype = ip
         _lib = lib
         return lib
 
@@ -145,6 +147,13 @@ def ls_cache_reorder(src, dst, parent, length: int, workspace=None, stream=None)
     return load_library().ls_cache_reorder(
         _ptr(src), _ptr(dst), _dtype_code(src), _ptr(parent), layers, batch, k, heads, max_len, int(length),
         head_dim, _ptr(workspace), _stream(stream))
+
+
+def ls_backtrack(token_hist, parent_hist, eos_id: int, out_seq, out_len, workspace=None, stream=None) -> int:
+    """token_hist, parent_hist [steps, batch, k] int32; out_seq [batch, k, steps] int32; out_len [batch, k] int32."""
+    steps, batch, k = token_hist.shape
+    return load_library().ls_backtrack(_ptr(token_hist), _ptr(parent_hist), steps, batch, k, int(eos_id),
+                                       _ptr(out_seq), _ptr(out_len), _ptr(workspace), _stream(stream))
 
 
 def ls_read_status(workspace, stream=None) -> int:

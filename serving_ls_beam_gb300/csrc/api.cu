@@ -277,6 +277,36 @@ ls_status ls_cache_reorder(const void* src, void* dst, ls_dtype dtype, const int
   return e == cudaSuccess ? LS_OK : cuda_fail(e);
 }
 
+ls_status ls_backtrack(const int32_t* token_hist, const int32_t* parent_hist, int steps, int batch, int k,
+                       int eos_id, int32_t* out_seq, int32_t* out_len, void* workspace, void* stream) {
+  if (steps < 0 || batch < 0 || k < 1 || k > LS_MAX_K) return LS_ERR_INVALID_ARG;
+  if (steps == 0 || batch == 0) return LS_OK;
+  if (!token_hist || !parent_hist || !out_seq || !out_len) return LS_ERR_INVALID_ARG;
+  if ((long long)steps * batch * k >= (1ll << 31)) return LS_ERR_UNSUPPORTED;
+  if (!aligned(token_hist, 4) || !aligned(parent_hist, 4) || !aligned(out_seq, 4) || !aligned(out_len, 4))
+    return LS_ERR_INVALID_ARG;
+  if (workspace && !aligned(workspace, 256)) return LS_ERR_INVALID_ARG;
+  const Debug dbg = read_debug();
+  if (dbg.check_ptrs) {
+    const void* ptrs[] = {token_hist, parent_hist, out_seq, out_len, workspace};
+    for (const void* q : ptrs)
+      if (q && !device_reachable(q)) return LS_ERR_INVALID_ARG;
+  }
+  BacktrackParams p;
+  p.tok = token_hist;
+  p.par = parent_hist;
+  p.seq = out_seq;
+  p.len = out_len;
+  p.status = workspace ? reinterpret_cast<uint32_t*>(workspace) : nullptr;
+  p.steps = steps;
+  p.batch = batch;
+  p.k = k;
+  p.eos = eos_id;
+  p.tile = backtrack_tile(k, steps);
+  const cudaError_t e = launch_backtrack(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? LS_OK : cuda_fail(e);
+}
+
 ls_status ls_read_status(void* workspace, void* stream) {
   if (!workspace) return LS_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

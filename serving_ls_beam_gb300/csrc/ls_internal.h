@@ -23,6 +23,11 @@ constexpr int kMaxK = 64;
 constexpr int kSelCap = 512;  // survivors the fine rank holds in shared memory
 constexpr int kSelStageMax = 96 * 1024;  // a batch's candidate slots staged in shared memory (bytes)
 
+// Backtrack (backtrack.cu): one CTA per batch, the history staged kBtTileElems entries of
+// (token, parent) at a time: 3 x 4 x kBtTileElems = 48 KB of shared memory at most.
+constexpr int kBtThreads = 128;
+constexpr int kBtTileElems = 4096;
+
 // Device status bits (workspace word 0).
 constexpr uint32_t kDevTimeout = 1u << 0;
 constexpr uint32_t kDevBadParent = 1u << 1;
@@ -142,6 +147,16 @@ struct ReorderParams {
   long long pairs;  // layers * rows
 };
 
+struct BacktrackParams {
+  const int32_t* tok;  // [steps, batch, k]
+  const int32_t* par;  // [steps, batch, k]
+  int32_t* seq;        // [batch, k, steps]
+  int32_t* len;        // [batch, k]
+  uint32_t* status;    // may be null
+  int steps, batch, k, eos;
+  int tile;            // steps staged per round
+};
+
 // Launchers (defined next to their kernels).
 size_t beam_rows_smem_bytes(int vpl);
 cudaError_t beam_rows_config(int dtype, bool bias, int vpl, int* occupancy);
@@ -150,5 +165,8 @@ cudaError_t launch_beam_select(const StepParams& p, int dtype, cudaStream_t stre
 cudaError_t beam_select_config();  // once per device: allow kSelStageMax of dynamic shared memory
 cudaError_t launch_cache_reorder(const ReorderParams& p, int unit, int grid, cudaStream_t stream);
 cudaError_t cache_reorder_occupancy(int unit, int* occupancy);
+int backtrack_tile(int k, int steps);
+size_t backtrack_smem_bytes(int k, int tile);
+cudaError_t launch_backtrack(const BacktrackParams& p, cudaStream_t stream);
 
 }  // namespace lsb

@@ -7,6 +7,11 @@ finished flags becoming the next step's beam state.  Everything stays on the
 GPU: the beam state and the two cache buffers alternate between two sets
 (ping-pong), so a run of steps can be captured in one CUDA graph.
 
+With ``max_steps`` > 0 every step writes its tokens and parents straight into a
+[max_steps, batch, k] history, and ``finalize`` turns the history into the token
+sequence and length of every final beam (``ls_backtrack``): the n-best list of each
+batch, best first, for a search stopped at the length limit or when every beam finished.
+
 Follows the LightSeq inference article (31duo.com, itemid-283120): decoding =
 vocab softmax + beam selection + cache refresh per step, with every buffer
 allocated once at its static maximum (memory-reuse section).
@@ -15,14 +20,15 @@ from __future__ import annotations
 
 import torch
 
-from . import check, ls_beam_step, ls_beam_step_workspace_size, ls_cache_reorder, ls_workspace_init
+from . import check, ls_backtrack, ls_beam_step, ls_beam_step_workspace_size, ls_cache_reorder, ls_workspace_init
 
 
 class BeamSearchLoop:
     def __init__(self, batch: int, k: int, vocab: int, eos_id: int, kv_shape=None, kv_dtype=torch.float16,
-                 device="cuda", caches=None):
+                 device="cuda", caches=None, max_steps: int = 0):
         """kv_shape = (layers, heads, max_len, head_dim) or None for no cache refresh.
-        caches: optional pair of preallocated [layers, batch*k, heads, max_len, head_dim] tensors."""
+        caches: optional pair of preallocated [layers, batch*k, heads, max_len, head_dim] tensors.
+        max_steps: length limit of a search; > 0 keeps the token / parent history for finalize()."""
         self.batch, self.k, self.vocab, self.eos_id = batch, k, vocab, eos_id
         self.device = torch.device(device)
         dev = self.device
@@ -43,6 +49,20 @@ class BeamSearchLoop:
         else:
             self.cache = None
         self.cur = 0
+        self.max_steps = max_steps
+        if max_steps > 0:
+            self.token_hist = torch.zeros(max_steps, batch, k, dtype=torch.int32, device=dev)
+            self.parent_hist = torch.zeros(max_steps, batch, k, dtype=torch.int32, device=dev)
+            self.seq_buf = torch.empty(batch * k * max_steps, dtype=torch.int32, device=dev)
+            self.seq_len = torch.empty(batch, k, dtype=torch.int32, device=dev)
+        self._last = (self.token[0], self.parent[0])
+
+    def token_out(self, t: int) -> torch.Tensor:
+        """Where decode step t (1-based) writes its tokens: the history slice, or the next state set."""
+        return self.token_hist[t - 1] if self.max_steps > 0 else self.token[1 - self.cur]
+
+    def parent_out(self, t: int) -> torch.Tensor:
+        return self.parent_hist[t - 1] if self.max_steps > 0 else self.parent[1 - self.cur]
 
     def reset(self, beam_scores=None, finished=None):
         """Start a new search: beam state set 0 from the given tensors (default: scores 0, none finished)."""
@@ -59,15 +79,32 @@ class BeamSearchLoop:
     def step(self, logits: torch.Tensor, t: int, bias=None, stream=None) -> int:
         """Decode step t (1-based): beam step on `logits` [batch, k, vocab], then the cache refresh of
         positions [0, t).  Returns the index of the state set holding this step's outputs."""
+        if self.max_steps > 0 and not 1 <= t <= self.max_steps:
+            raise ValueError(f"decode step {t} outside 1..{self.max_steps}")
         s, n = self.cur, 1 - self.cur
-        check(ls_beam_step(logits, bias, self.scores[s], self.finished[s], self.eos_id, self.token[n], self.parent[n],
+        tok, par = self.token_out(t), self.parent_out(t)
+        check(ls_beam_step(logits, bias, self.scores[s], self.finished[s], self.eos_id, tok, par,
                            self.scores[n], self.finished[n], self.workspace, stream), "ls_beam_step")
         if self.cache is not None:
-            check(ls_cache_reorder(self.cache[s], self.cache[n], self.parent[n], t, stream=stream), "ls_cache_reorder")
+            check(ls_cache_reorder(self.cache[s], self.cache[n], par, t, stream=stream), "ls_cache_reorder")
         self.cur = n
+        self._last = (tok, par)
         return n
 
     def outputs(self, idx: int | None = None):
+        """The last step's tokens and parents with the beam state of set idx (default: the current one)."""
         i = self.cur if idx is None else idx
-        return {"token": self.token[i], "parent": self.parent[i], "score": self.scores[i],
+        return {"token": self._last[0], "parent": self._last[1], "score": self.scores[i],
                 "finished": self.finished[i]}
+
+    def finalize(self, steps: int, stream=None):
+        """Token sequences [batch, k, steps] and lengths [batch, k] of the final beams after `steps` decode
+        steps (best beam first), read back through the parent history on the device."""
+        if self.max_steps <= 0:
+            raise ValueError("the loop keeps no history (max_steps = 0)")
+        if not 1 <= steps <= self.max_steps:
+            raise ValueError(f"steps {steps} outside 1..{self.max_steps}")
+        seq = self.seq_buf[: self.batch * self.k * steps].view(self.batch, self.k, steps)
+        check(ls_backtrack(self.token_hist[:steps], self.parent_hist[:steps], self.eos_id, seq, self.seq_len,
+                           self.workspace, stream), "ls_backtrack")
+        return seq, self.seq_len

@@ -77,6 +77,11 @@ def test_host_argument_checks(lib):
     assert lib.ls_cache_reorder(p, p, 1, p, 1, 1, 0, 1, 4, 2, 8, None, None) == E  # k = 0
     assert lib.ls_cache_reorder(p, p, 1, p, 1, 1, 2, 1, 4, 2, 8, None, None) == E  # src == dst
     assert lib.ls_cache_reorder(None, None, 1, None, 1, 1, 2, 1, 4, 0, 8, None, None) == 0  # len 0 no-op
+    assert lib.ls_backtrack(p, p, -1, 2, 3, 0, p, p, None, None) == E  # steps < 0
+    assert lib.ls_backtrack(p, p, 4, 2, 0, 0, p, p, None, None) == E  # k = 0
+    assert lib.ls_backtrack(p, p, 4, 2, 65, 0, p, p, None, None) == E  # k > 64
+    assert lib.ls_backtrack(None, p, 4, 2, 3, 0, p, p, None, None) == E  # no history
+    assert lib.ls_backtrack(None, None, 0, 2, 3, 0, None, None, None, None) == 0  # no steps: no-op
     assert lib.ls_read_status(None, None) == E
     assert lib.ls_workspace_init(None, 0, None) == E
 

@@ -1,5 +1,6 @@
 """64-step autoregressive workload c5 (batch 256, beam 4, vocab 40000, fp16, cache
-[6, 1024, 16, 64, 64]) on the GPU against the oracle's own trajectory.
+[6, 1024, 16, 64, 64]) on the GPU against the oracle's own trajectory, then the end-of-search token sequences read
+back through the parent history on the device against the oracle's backtrack.
 
 The GPU runs every batch; the oracle runs a sample of batches, each step feeding
 its own outputs (beam scores, finished flags, parents) into the next one, so no
@@ -7,7 +8,8 @@ oracle input ever comes from the GPU.  Batches are independent, so a sampled
 batch is compared at every step until the oracle shows a near-tie (two scores
 within 1e-4 among its first k+1 candidates), after which the two trajectories may
 legitimately part; that batch is then dropped from the comparison.  At the end
-the cache rows of every batch still in the comparison must match bitwise.
+the cache rows and the final token sequences of every batch still in the comparison must
+match bitwise.
 """
 import numpy as np
 import pytest
@@ -37,7 +39,8 @@ def test_c5_trajectory_sampled(dev, oracle_mod):
     steps = w.steps
     sample = [0, 37, 101, 128, 200, 255]
     caches = [torch.from_numpy(synth.kv_cache(shape, w.seed, which=i)).to(dev) for i in range(2)]
-    loop = BeamSearchLoop(w.batch, w.k, w.vocab, w.eos_id, kv_shape=w.kv_shape, device=dev, caches=caches)
+    loop = BeamSearchLoop(w.batch, w.k, w.vocab, w.eos_id, kv_shape=w.kv_shape, device=dev, caches=caches,
+                          max_steps=steps)
     loop.reset(torch.from_numpy(synth.beam_scores(w, 0)).to(dev))
     # oracle state for the sampled batches
     rows = [b * w.k + j for b in sample for j in range(w.k)]
@@ -47,6 +50,7 @@ def test_c5_trajectory_sampled(dev, oracle_mod):
     alive = set(range(len(sample)))
     cur = 0
     compared = 0
+    o_tok, o_par = [], []
     for t in range(1, steps + 1):
         lg = synth.logits(w, t)
         idx = loop.step(torch.from_numpy(lg).to(dev), t)
@@ -62,6 +66,8 @@ def test_c5_trajectory_sampled(dev, oracle_mod):
                 assert (gpu_s["token"][i] == ora["token"][i, : w.k]).all()
                 assert (gpu_s["parent"][i] == ora["parent"][i, : w.k]).all()
                 compared += 1
+        o_tok.append(ora["token"][:, : w.k].astype(np.int32))
+        o_par.append(ora["parent"][:, : w.k].astype(np.int32))
         # the oracle's next state comes from its own outputs
         n = 1 - cur
         o_cache[n] = oracle_mod.cache_reorder(o_cache[cur], ora["parent"][:, : w.k], t, dst=o_cache[n])
@@ -73,3 +79,9 @@ def test_c5_trajectory_sampled(dev, oracle_mod):
     for i in sorted(alive):
         sl = slice(i * w.k, (i + 1) * w.k)
         assert np.array_equal(final[:, sl].view(np.int16), o_cache[cur][:, sl].view(np.int16))
+    seq, ln = loop.finalize(steps)
+    seq, ln = seq.cpu().numpy()[sample], ln.cpu().numpy()[sample]
+    o_seq, o_len = oracle_mod.backtrack(np.stack(o_tok), np.stack(o_par), w.eos_id)
+    for i in sorted(alive):
+        np.testing.assert_array_equal(seq[i], o_seq[i])
+        np.testing.assert_array_equal(ln[i], o_len[i])
