@@ -58,6 +58,8 @@ def _load():
             lib.oracle_cache_reorder.restype = ip
             lib.oracle_backtrack.argtypes = [vp, vp, ip, ip, ip, ip, vp, vp]
             lib.oracle_backtrack.restype = ip
+            lib.oracle_sample.argtypes = [vp, ip, vp, ip, ip, ip, ctypes.c_double, vp, vp, vp, vp]
+            lib.oracle_sample.restype = ip
             _lib = lib
     return _lib
 
@@ -145,3 +147,23 @@ def backtrack(token_hist, parent_hist, eos_id):
     if rc != 0:
         raise ValueError(f"oracle_backtrack failed ({rc})")
     return seq, ln
+
+
+def sample(logits, u, top_k, top_p=1.0, *, bias=None, dtype=None):
+    """Sampling decoding of rows of logits [..., vocab]: top_k / top_p restriction, inverse CDF at u.
+    Returns token (int32), logprob (float64, under the full softmax) and margin (distance of u from
+    the nearest cumulative boundary of the kept candidates)."""
+    lib = _load()
+    lg, code = _logit_code(np.asarray(logits), dtype)
+    vocab = lg.shape[-1]
+    rows = lg.size // vocab
+    bi = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32).reshape(vocab)
+    uu = np.ascontiguousarray(u, dtype=np.float64).reshape(rows)
+    tok = np.empty(rows, np.int32)
+    lp = np.empty(rows, np.float64)
+    mg = np.empty(rows, np.float64)
+    rc = lib.oracle_sample(_ptr(lg), code, _ptr(bi), rows, vocab, int(top_k), float(top_p), _ptr(uu), _ptr(tok),
+                           _ptr(lp), _ptr(mg))
+    if rc != 0:
+        raise ValueError(f"oracle_sample failed ({rc})")
+    return {"token": tok, "logprob": lp, "margin": mg}

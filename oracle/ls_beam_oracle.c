@@ -299,3 +299,75 @@ int oracle_backtrack(const int32_t* token_hist, const int32_t* parent_hist, int 
     }
   return 0;
 }
+
+/*
+ * Sampling decoding (the article's other decoding mode next to beam search): one row of
+ * logits per sequence, x = logit + bias.  The top_k tokens by x (ties: smaller token id
+ * first) carry probabilities proportional to exp(x), renormalised over those top_k; with
+ * top_p < 1 only the shortest prefix of them (in that order) whose cumulative probability
+ * reaches top_p is kept and renormalised again.  The token drawn for uniform u in [0, 1)
+ * is the first candidate whose cumulative probability exceeds u (inverse CDF).
+ * out_logprob = x(token) - log sum_v exp(x_v) over the whole row.
+ * out_margin (may be NULL) = distance of u from the nearest cumulative boundary of the
+ * kept set (a draw this close to a boundary may legitimately round either way).
+ * Returns -1 on bad arguments.
+ */
+int oracle_sample(const void* logits, int dtype, const float* bias, int rows, int vocab, int top_k,
+                  double top_p, const double* u, int32_t* out_token, double* out_logprob,
+                  double* out_margin) {
+  if (!logits || !u || !out_token || !out_logprob) return -1;
+  if (rows < 0 || vocab < 1 || top_k < 1 || top_k > vocab || !(top_p > 0.0) || top_p > 1.0) return -1;
+  double* x = (double*)malloc(sizeof(double) * (size_t)vocab);
+  orc_cand* c = (orc_cand*)malloc(sizeof(orc_cand) * (size_t)vocab);
+  double* cum = (double*)malloc(sizeof(double) * (size_t)top_k);
+  if (!x || !c || !cum) {
+    free(x);
+    free(c);
+    free(cum);
+    return -1;
+  }
+  for (int r = 0; r < rows; ++r) {
+    orc_row_values(logits, dtype, bias, (size_t)r, vocab, x);
+    const double lse = orc_log_sum_exp(x, vocab);
+    for (int v = 0; v < vocab; ++v) {
+      c[v].s = x[v];
+      c[v].flat = v;
+    }
+    qsort(c, (size_t)vocab, sizeof(orc_cand), orc_cmp_cand);  /* x descending, token ascending */
+    const double x0 = c[0].s;
+    double acc = 0.0;
+    for (int i = 0; i < top_k; ++i) {
+      acc += exp(c[i].s - x0);
+      cum[i] = acc;
+    }
+    int m = top_k;  /* kept prefix */
+    if (top_p < 1.0) {
+      for (int i = 0; i < top_k; ++i)
+        if (cum[i] >= top_p * cum[top_k - 1]) {
+          m = i + 1;
+          break;
+        }
+    }
+    const double target = u[r] * cum[m - 1];
+    int pick = m - 1;
+    for (int i = 0; i < m; ++i)
+      if (cum[i] > target) {
+        pick = i;
+        break;
+      }
+    out_token[r] = c[pick].flat;
+    out_logprob[r] = c[pick].s - lse;
+    if (out_margin) {
+      double mg = 1.0;
+      for (int i = 0; i < m - 1; ++i) {
+        const double d = fabs(cum[i] / cum[m - 1] - u[r]);
+        if (d < mg) mg = d;
+      }
+      out_margin[r] = mg;
+    }
+  }
+  free(x);
+  free(c);
+  free(cum);
+  return 0;
+}
