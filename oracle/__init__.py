@@ -152,7 +152,7 @@ def backtrack(token_hist, parent_hist, eos_id):
 def sample(logits, u, top_k, top_p=1.0, *, bias=None, dtype=None):
     """Sampling decoding of rows of logits [..., vocab]: top_k / top_p restriction, inverse CDF at u.
     Returns token (int32), logprob (float64, under the full softmax) and margin (distance of u from
-    the nearest cumulative boundary of the kept candidates)."""
+    the nearest cumulative boundary of the kept candidates, or of top_p from one of the top_k's)."""
     lib = _load()
     lg, code = _logit_code(np.asarray(logits), dtype)
     vocab = lg.shape[-1]

@@ -308,8 +308,10 @@ int oracle_backtrack(const int32_t* token_hist, const int32_t* parent_hist, int 
  * reaches top_p is kept and renormalised again.  The token drawn for uniform u in [0, 1)
  * is the first candidate whose cumulative probability exceeds u (inverse CDF).
  * out_logprob = x(token) - log sum_v exp(x_v) over the whole row.
- * out_margin (may be NULL) = distance of u from the nearest cumulative boundary of the
- * kept set (a draw this close to a boundary may legitimately round either way).
+ * out_margin (may be NULL) = the smaller of the distance of u from the nearest cumulative
+ * boundary of the kept set and, with top_p < 1, the distance of top_p from the nearest
+ * cumulative boundary of the top_k (a draw or a cut this close to a boundary may
+ * legitimately round either way).
  * Returns -1 on bad arguments.
  */
 int oracle_sample(const void* logits, int dtype, const float* bias, int rows, int vocab, int top_k,
@@ -363,6 +365,11 @@ int oracle_sample(const void* logits, int dtype, const float* bias, int rows, in
         const double d = fabs(cum[i] / cum[m - 1] - u[r]);
         if (d < mg) mg = d;
       }
+      if (top_p < 1.0)
+        for (int i = 0; i < top_k; ++i) {
+          const double d = fabs(cum[i] / cum[top_k - 1] - top_p);
+          if (d < mg) mg = d;
+        }
       out_margin[r] = mg;
     }
   }
