@@ -50,6 +50,7 @@ def parse_args():
     ap.add_argument("--workload", default="c5", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sampling", action="store_true", help="skip the sampling-decoding measurement")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--decode-steps", type=int, default=0,
                     help="run only the first N decode steps of the workload (for small profiling runs)")
@@ -398,6 +399,10 @@ def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
     if not args.no_e2e:
         e2e = bench_e2e(args, wr, loop, host_logits, bias_np, beam0, fin0, lens, dev, world)
 
+    sampling = None
+    if not args.no_sampling:
+        sampling = bench_sampling(dev, peak)
+
     clocks = clk.summary()
     cfg = {"workload": f"{wr.name}: batch {B}, beam {K}, vocab {V}, {wr.dtype} logits, "
                        f"{T} decode step(s)" + (f", KV cache {[wr.kv_shape[0], wr.rows, *wr.kv_shape[1:]]} fp16 "
@@ -411,9 +416,58 @@ def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
         "dtype": wr.dtype, "data": "synthetic (seeded generators, workload recipe in synth/)", "config": cfg,
         "logit_gbs": k1_gbs, "step_gbs": step_gbs, "step_roofline_frac": step_gbs / peak,
         "roofline": roof, "roofline_kernels": kern, "gpu_launches": launches_per_step * args.steps,
-        "clocks": clocks, "e2e": e2e, "setup_s": round(setup_s, 1),
+        "clocks": clocks, "e2e": e2e, "sampling": sampling, "setup_s": round(setup_s, 1),
     }
     return line
+
+
+def bench_sampling(dev, peak, calls: int = 16):
+    """Sampling decoding (ls_sample: K1 then K5) on workload s1: one CUDA graph of `calls` calls over as
+    many distinct logit sets (1.3 GB in all, larger than L2), timed with CUDA events."""
+    import torch
+
+    import serving_ls_beam_gb300 as lsb
+
+    w = synth.SAMPLE_WORKLOADS["s1"]
+    ins = [synth.sample_inputs(w, step=i) for i in range(calls)]
+    rows, vocab, top_k, top_p = w.batch, w.vocab, ins[0]["top_k"], ins[0]["top_p"]
+    lg = [torch.from_numpy(d["logits"]).to(dev) for d in ins]
+    u = [torch.from_numpy(d["u"]).to(dev) for d in ins]
+    tok = torch.empty((calls, rows), dtype=torch.int32, device=dev)
+    lp = torch.empty((calls, rows), dtype=torch.float32, device=dev)
+    ws = torch.empty(lsb.ls_sample_workspace_size(rows, top_k, vocab), dtype=torch.uint8, device=dev)
+    lsb.check(lsb.ls_workspace_init(ws))
+    stream = torch.cuda.Stream(device=dev)
+
+    def run():
+        for i in range(calls):
+            lsb.check(lsb.ls_sample(lg[i], None, u[i], top_k, top_p, tok[i], lp[i], ws), "ls_sample")
+
+    with torch.cuda.stream(stream):
+        run()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        run()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 5
+    with torch.cuda.stream(stream):
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+    torch.cuda.synchronize()
+    lsb.check(lsb.ls_read_status(ws), "device status")
+    us = e0.elapsed_time(e1) * 1e3 / (reps * calls)
+    nbytes = rows * vocab * 2 + rows * 12  # logits once; uniform in, token and log-probability out
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"workload": f"s1: {rows} rows, vocab {vocab}, f16 logits N(0,2), top_k {top_k}, top_p {top_p}",
+            "us_per_call": us, "rows_per_s": rows / (us * 1e-6), "achieved": gbs, "peak": peak, "unit": "GB/s",
+            "frac": gbs / peak, "algorithmic_bytes_per_call": nbytes, "launches_per_call": 2,
+            "l2": f"{calls} distinct logit sets per graph ({calls * rows * vocab * 2 / 1e9:.2f} GB)"}
 
 
 def bench_e2e(args, wr, loop, host_logits, bias_np, beam0, fin0, lens, dev, world):

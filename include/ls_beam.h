@@ -119,6 +119,37 @@ LS_API ls_status ls_cache_reorder(const void* src, void* dst, ls_dtype dtype, co
                            int head_dim, void* workspace, void* stream);
 
 /*
+ * Workspace bytes for ls_sample on `rows` rows of `vocab` logits keeping top_k candidates
+ * (0 for unsupported shapes: top_k outside [1, LS_MAX_K] or above vocab).
+ */
+LS_API size_t ls_sample_workspace_size(int rows, int top_k, int vocab);
+
+/*
+ * Sampling decoding (article: decoding by sampling, next to beam search): one token per
+ * sequence from the top_k candidates of its logits, optionally cut to the top-p prefix,
+ * drawn by inverse CDF at the caller's uniform.  The first traversal is the beam step's:
+ * log_sum_exp and the R-top-k bound in one pass over the logits, then only the logits at
+ * or above the bound are ranked.
+ *
+ *  logits      [rows, vocab] row-major, logit_dtype, device; bias [vocab] f32 or NULL,
+ *              added first (x = logit + bias).
+ *  u           [rows] f32 uniforms in [0, 1), device (the random numbers are the caller's).
+ *  top_k       1..LS_MAX_K, <= vocab: the top_k tokens by x (ties: smaller token id first)
+ *              with probabilities proportional to exp(x), renormalised over them.
+ *  top_p       in (0, 1]: below 1, only the shortest prefix of those (best first) whose
+ *              cumulative probability reaches top_p is kept and renormalised.
+ *  out_token   [rows] int32: the first kept candidate whose cumulative probability
+ *              exceeds u.
+ *  out_logprob [rows] f32 or NULL: x(token) - log sum_v exp(x_v) over the whole row.
+ *  workspace   device, >= ls_sample_workspace_size(rows, top_k, vocab) bytes, zero-filled
+ *              once by ls_workspace_init; calls sharing it must be ordered.
+ *  rows == 0 is a no-op.  NaN or +inf logits are not supported.
+ */
+LS_API ls_status ls_sample(const void* logits, ls_dtype logit_dtype, const float* bias, const float* u,
+                           int rows, int vocab, int top_k, float top_p, int32_t* out_token,
+                           float* out_logprob, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * End of a search: the token sequence of every final beam, read back through the
  * per-step parent pointers (article: decoding keeps, for every new beam, the beam it
  * continued — the same parent index the cache refresh follows).

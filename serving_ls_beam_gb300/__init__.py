@@ -19,6 +19,7 @@ __all__ = [
     "LS_DTYPE_F32", "LS_DTYPE_F16", "LS_DTYPE_BF16", "LS_MAX_K", "LsBeamError", "library_path", "load_library",
     "check", "ls_beam_step_workspace_size", "ls_workspace_init", "ls_beam_step", "ls_cache_reorder",
     "ls_read_status", "ls_status_string", "ls_read_row_stats", "ls_beam_step_noalloc", "ls_backtrack",
+    "ls_sample_workspace_size", "ls_sample",
 ]
 
 LS_OK, LS_ERR_INVALID_ARG, LS_ERR_UNSUPPORTED, LS_ERR_CUDA, LS_ERR_TIMEOUT, LS_ERR_INTERNAL = range(6)
@@ -67,6 +68,10 @@ def load_library():
         lib.ls_beam_step_noalloc.restype = ip
         lib.ls_backtrack.argtypes = [vp, vp, ip, ip, ip, ip, vp, vp, vp, vp]
         lib.ls_backtrack.restype = ip
+        lib.ls_sample_workspace_size.argtypes = [ip, ip, ip]
+        lib.ls_sample_workspace_size.restype = sz
+        lib.ls_sample.argtypes = [vp, ip, vp, vp, ip, ip, ip, ctypes.c_float, vp, vp, vp, sz, vp]
+        lib.ls_sample.restype = ip
         _lib = lib
         return lib
 
@@ -154,6 +159,19 @@ def ls_backtrack(token_hist, parent_hist, eos_id: int, out_seq, out_len, workspa
     steps, batch, k = token_hist.shape
     return load_library().ls_backtrack(_ptr(token_hist), _ptr(parent_hist), steps, batch, k, int(eos_id),
                                        _ptr(out_seq), _ptr(out_len), _ptr(workspace), _stream(stream))
+
+
+def ls_sample_workspace_size(rows: int, top_k: int, vocab: int) -> int:
+    return int(load_library().ls_sample_workspace_size(rows, top_k, vocab))
+
+
+def ls_sample(logits, bias, u, top_k: int, top_p: float, out_token, out_logprob, workspace, stream=None) -> int:
+    """logits [rows, vocab] (f32/f16/bf16), bias [vocab] f32 or None, u [rows] f32, out_token [rows] int32,
+    out_logprob [rows] f32 or None, workspace a uint8 device tensor of ls_sample_workspace_size() bytes."""
+    rows, vocab = logits.shape
+    return load_library().ls_sample(_ptr(logits), _dtype_code(logits), _ptr(bias), _ptr(u), rows, vocab, int(top_k),
+                                    float(top_p), _ptr(out_token), _ptr(out_logprob), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _stream(stream))
 
 
 def ls_read_status(workspace, stream=None) -> int:

@@ -89,6 +89,32 @@ int step_occupancy(DeviceInfo* di, int dtype, bool bias, int vpl) {
   return occ;
 }
 
+// K1's launch plan for `rows` rows of `vocab` logits of `es` bytes.
+struct RowPlan {
+  int vpl, nc;
+  long long units, grid;
+};
+
+ls_status plan_rows(DeviceInfo* di, const Debug& dbg, int dtype, int es, bool bias, int vocab, long long rows,
+                    const WsLayout& wl, RowPlan* out) {
+  // 8 vectors per lane (4 KB chunks) unless 16-bit logits with a bias (register pressure)
+  const int vpl = dbg.vpl ? dbg.vpl : ((es == 2 && bias) ? 4 : 8);
+  const int occ = step_occupancy(di, dtype, bias, vpl);
+  if (occ < 1) return cuda_fail(cudaErrorUnknown);
+  // a row spans at most ceil((15 + vocab * es) / 16) aligned 16-byte vectors
+  const long long nv_max = (15 + (long long)vocab * es + 15) / 16;
+  const int cv = 32 * vpl;
+  const int nc = (int)((nv_max + cv - 1) / cv);
+  if (nc > wl.nc_max) return LS_ERR_INTERNAL;
+  out->vpl = vpl;
+  out->nc = nc;
+  out->units = rows * nc;
+  const long long grid_full = (long long)di->sms * occ;
+  const long long grid_need = (out->units + kRowWarps - 1) / kRowWarps;
+  out->grid = grid_need < grid_full ? grid_need : grid_full;
+  return LS_OK;
+}
+
 bool select_configured(DeviceInfo* di) {
   std::lock_guard<std::mutex> lk(g_mu);
   if (!di->select_ready) {
@@ -169,20 +195,12 @@ ls_status ls_beam_step(const void* logits, ls_dtype logit_dtype, const float* bi
   if (!di) return cuda_fail(cudaErrorUnknown);
 
   const int dtype = (int)logit_dtype;
-  // 8 vectors per lane (4 KB chunks) unless 16-bit logits with a bias (register pressure)
-  const int vpl = dbg.vpl ? dbg.vpl : ((es == 2 && bias) ? 4 : 8);
-  const int occ = step_occupancy(di, dtype, bias != nullptr, vpl);
-  if (occ < 1) return cuda_fail(cudaErrorUnknown);
   const long long rows = (long long)batch * k;
-  // a row spans at most ceil((15 + vocab * es) / 16) aligned 16-byte vectors
-  const long long nv_max = (15 + (long long)vocab * es + 15) / 16;
-  const int cv = 32 * vpl;
-  const int nc = (int)((nv_max + cv - 1) / cv);
-  if (nc > wl.nc_max) return LS_ERR_INTERNAL;
-  const long long units = rows * nc;
-  const long long grid_full = (long long)di->sms * occ;
-  const long long grid_need = (units + kRowWarps - 1) / kRowWarps;
-  const long long grid = grid_need < grid_full ? grid_need : grid_full;
+  RowPlan plan;
+  const ls_status ps = plan_rows(di, dbg, dtype, es, bias != nullptr, vocab, rows, wl, &plan);
+  if (ps != LS_OK) return ps;
+  const int vpl = plan.vpl, nc = plan.nc;
+  const long long units = plan.units, grid = plan.grid;
 
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   StepParams p;
@@ -274,6 +292,88 @@ ls_status ls_cache_reorder(const void* src, void* dst, ls_dtype dtype, const int
   const long long grid_full = (long long)di->sms * occ;
   const long long grid = p.pairs < grid_full ? p.pairs : grid_full;
   cudaError_t e = launch_cache_reorder(p, unit, (int)grid, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? LS_OK : cuda_fail(e);
+}
+
+size_t ls_sample_workspace_size(int rows, int top_k, int vocab) {
+  if (rows < 0 || top_k < 1 || top_k > LS_MAX_K || vocab < top_k) return 0;
+  if (vocab > (1 << 28) || (long long)rows * ws_layout_sample(rows, top_k, vocab).nc_max >= (1ll << 31)) return 0;
+  return ws_layout_sample(rows, top_k, vocab).total;
+}
+
+ls_status ls_sample(const void* logits, ls_dtype logit_dtype, const float* bias, const float* u, int rows, int vocab,
+                    int top_k, float top_p, int32_t* out_token, float* out_logprob, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  if (rows < 0 || top_k < 1 || top_k > LS_MAX_K || vocab < top_k || vocab > (1 << 28)) return LS_ERR_INVALID_ARG;
+  if (!(top_p > 0.0f) || !(top_p <= 1.0f)) return LS_ERR_INVALID_ARG;
+  if (!dtype_ok(logit_dtype)) return LS_ERR_INVALID_ARG;
+  if (rows == 0) return LS_OK;
+  if (!logits || !u || !out_token || !workspace) return LS_ERR_INVALID_ARG;
+  const WsLayout wl = ws_layout_sample(rows, top_k, vocab);
+  if (wl.total == 0 || workspace_bytes < wl.total) return LS_ERR_INVALID_ARG;
+  if ((long long)rows * wl.nc_max >= (1ll << 31)) return LS_ERR_UNSUPPORTED;
+  const int es = dtype_bytes(logit_dtype);
+  if (!aligned(logits, es) || (bias && !aligned(bias, 4)) || !aligned(u, 4) || !aligned(out_token, 4) ||
+      (out_logprob && !aligned(out_logprob, 4)) || !aligned(workspace, 256))
+    return LS_ERR_INVALID_ARG;
+  const Debug dbg = read_debug();
+  if (dbg.check_ptrs) {
+    const void* ptrs[] = {logits, bias, u, out_token, out_logprob, workspace};
+    for (const void* q : ptrs)
+      if (q && !device_reachable(q)) return LS_ERR_INVALID_ARG;
+  }
+  int dev = 0;
+  DeviceInfo* di = device_info(&dev);
+  if (!di) return cuda_fail(cudaErrorUnknown);
+  const int dtype = (int)logit_dtype;
+  RowPlan plan;
+  const ls_status ps = plan_rows(di, dbg, dtype, es, bias != nullptr, vocab, rows, wl, &plan);
+  if (ps != LS_OK) return ps;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  // K1 over the rows: one row per sequence, top_k elements kept per row, none finished
+  StepParams p = {};
+  p.logits = logits;
+  p.bias = bias;
+  p.status = reinterpret_cast<uint32_t*>(ws + wl.status_off);
+  p.done = reinterpret_cast<uint32_t*>(ws + wl.done_off);
+  p.rec = ws + wl.rec_off;
+  p.slots = reinterpret_cast<CandSlot*>(ws + wl.slot_off);
+  p.rowstat = reinterpret_cast<RowStat*>(ws + wl.rowstat_off);
+  p.bstat = reinterpret_cast<int32_t*>(ws + wl.bstat_off);
+  p.batch = rows;
+  p.k = top_k;
+  p.vocab = vocab;
+  p.rows = rows;
+  p.nc = plan.nc;
+  make_divisor((uint32_t)plan.nc, &p.nc_magic, &p.nc_shift);
+  p.groups = wl.groups;
+  p.slot_cap = wl.slot_cap;
+  p.rec_stride = wl.rec_stride;
+  p.flags = dbg.flags;
+  p.units = plan.units;
+  p.spin_limit_ns = dbg.spin_ns;
+  SampleParams q;
+  q.rec = p.rec;
+  q.slots = p.slots;
+  q.logits = logits;
+  q.bias = bias;
+  q.u = u;
+  q.out_token = out_token;
+  q.out_logprob = out_logprob;
+  q.rowstat = p.rowstat;
+  q.bstat = p.bstat;
+  q.rows = rows;
+  q.vocab = vocab;
+  q.k = top_k;
+  q.nc = plan.nc;
+  q.groups = wl.groups;
+  q.slot_cap = wl.slot_cap;
+  q.rec_stride = wl.rec_stride;
+  q.flags = dbg.flags;
+  q.top_p = top_p;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_beam_rows(p, dtype, plan.vpl, (int)plan.grid, st);
+  if (e == cudaSuccess) e = launch_sample_select(q, dtype, st);
   return e == cudaSuccess ? LS_OK : cuda_fail(e);
 }
 

@@ -74,11 +74,10 @@ inline void make_divisor(uint32_t d, uint32_t* magic, int* shift) {
   *shift = s;
 }
 
-// Returns total == 0 for unsupported shapes.
-inline WsLayout ws_layout(int batch, int k, int vocab) {
+// Layout for `rows` rows of logits, `nb` per-batch entries and k (the number of top
+// elements a row's bound must keep).
+inline WsLayout ws_layout_rows(size_t rows, size_t nb, int k, int vocab) {
   WsLayout w{};
-  if (batch < 0 || k < 1 || k > kMaxK || vocab < k) return w;
-  const size_t rows = (size_t)batch * (size_t)k;
   w.groups = pow2_ceil(k);
   w.slot_cap = (int)align_up((size_t)(4 * k + 32), 8);
   w.rec_stride = (int)align_up((size_t)(16 + 4 * w.groups), 16);
@@ -89,7 +88,7 @@ inline WsLayout ws_layout(int batch, int k, int vocab) {
   w.status_off = off;
   off += 256;
   w.done_off = off;
-  off = align_up(off + (size_t)batch * 4, 256);
+  off = align_up(off + nb * 4, 256);
   w.rec_off = off;
   off = align_up(off + rows * w.nc_max * w.rec_stride, 256);
   w.slot_off = off;
@@ -97,9 +96,21 @@ inline WsLayout ws_layout(int batch, int k, int vocab) {
   w.rowstat_off = off;
   off = align_up(off + rows * sizeof(RowStat), 256);
   w.bstat_off = off;
-  off = align_up(off + (size_t)batch * 4, 256);
+  off = align_up(off + nb * 4, 256);
   w.total = off;
   return w;
+}
+
+// Beam step: batch * k rows, one entry per batch.  Returns total == 0 for unsupported shapes.
+inline WsLayout ws_layout(int batch, int k, int vocab) {
+  if (batch < 0 || k < 1 || k > kMaxK || vocab < k) return WsLayout{};
+  return ws_layout_rows((size_t)batch * (size_t)k, (size_t)batch, k, vocab);
+}
+
+// Sampling: one row per sequence, top_k kept per row.
+inline WsLayout ws_layout_sample(int rows, int top_k, int vocab) {
+  if (rows < 0 || top_k < 1 || top_k > kMaxK || vocab < top_k) return WsLayout{};
+  return ws_layout_rows((size_t)rows, (size_t)rows, top_k, vocab);
 }
 
 // ---------------------------------------------------------------- kernel parameters
@@ -157,6 +168,20 @@ struct BacktrackParams {
   int tile;            // steps staged per round
 };
 
+struct SampleParams {
+  const unsigned char* rec;  // K1's chunk records and slots of the rows
+  const CandSlot* slots;
+  const void* logits;        // [rows, vocab] (exact fallback)
+  const float* bias;
+  const float* u;            // [rows] uniforms in [0, 1)
+  int32_t* out_token;
+  float* out_logprob;        // may be null
+  RowStat* rowstat;
+  int32_t* bstat;
+  int rows, vocab, k, nc, groups, slot_cap, rec_stride, flags;
+  float top_p;
+};
+
 // Launchers (defined next to their kernels).
 size_t beam_rows_smem_bytes(int vpl);
 cudaError_t beam_rows_config(int dtype, bool bias, int vpl, int* occupancy);
@@ -168,5 +193,6 @@ cudaError_t cache_reorder_occupancy(int unit, int* occupancy);
 int backtrack_tile(int k, int steps);
 size_t backtrack_smem_bytes(int k, int tile);
 cudaError_t launch_backtrack(const BacktrackParams& p, cudaStream_t stream);
+cudaError_t launch_sample_select(const SampleParams& p, int dtype, cudaStream_t stream);
 
 }  // namespace lsb

@@ -32,7 +32,7 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-TAG_LOGITS, TAG_BIAS, TAG_BEAM, TAG_FINISHED, TAG_TIED, TAG_OFFSET, TAG_KV, TAG_PARENT = range(1, 9)
+TAG_LOGITS, TAG_BIAS, TAG_BEAM, TAG_FINISHED, TAG_TIED, TAG_OFFSET, TAG_KV, TAG_PARENT, TAG_UNIFORM = range(1, 10)
 
 _THREADS = max(1, min(16, os.cpu_count() or 1))
 
@@ -228,3 +228,19 @@ def normal(shape, seed: int, *key: int, dtype=np.float32, scale: float = 1.0) ->
 
 def uniform(shape, lo: float, hi: float, seed: int, *key: int) -> np.ndarray:
     return rng(seed, *key).uniform(lo, hi, shape).astype(np.float32)
+
+
+# Sampling decoding: one row of logits per sequence (a Workload with k = 1), the kept
+# candidates (top_k, top_p) and one uniform per row, all seeded.
+#   s1  1024 rows, vocab 40000, fp16 N(0,2), top_k 8, top_p 0.9, u ~ U(0,1), seed 5
+SAMPLE_WORKLOADS = {
+    "s1": Workload("s1", 1024, 1, 40000, "f16", 5, logit_var=2.0, extra={"top_k": 8, "top_p": 0.9}),
+}
+
+
+def sample_inputs(w: Workload, step: int = 0) -> dict:
+    """Logits [rows, vocab], bias, uniforms [rows] (f32 in [0, 1)), top_k and top_p of a sampling workload."""
+    lg = logits(w, step).reshape(w.batch, w.vocab)
+    u = rng(w.seed, TAG_UNIFORM, step).random(w.batch).astype(np.float32)
+    u = np.minimum(u, np.float32(1.0) - np.float32(2.0 ** -24))
+    return {"logits": lg, "bias": bias(w), "u": u, "top_k": int(w.extra["top_k"]), "top_p": float(w.extra["top_p"])}
