@@ -8,12 +8,14 @@
 // survivors above that bound, takes the exact top-k among them, and draws by inverse CDF
 // at the caller's uniform u.
 //
-// GB300 design: one CTA per row, launched with programmatic dependent launch behind K1.
-// The row's records are merged by all threads (group maxima through shared-memory atomics
-// on order-preserving bits), the candidates are ranked in shared memory with branch-free
-// comparisons, and the final draw (k <= 64 terms in double) is one thread's loop.  A row
-// whose chunk slots overflowed, or with more candidates than fit, takes an exact radix
-// select of its top-k over the logits instead.
+// GB300 design: one warp per row, eight rows per CTA, launched with programmatic
+// dependent launch behind K1.  A warp merges its row's chunk records (group maxima through
+// shared-memory atomics on order-preserving bits), gathers the survivors of the row's
+// bound from the chunk slots, ranks them in shared memory with branch-free comparisons,
+// and draws in fp32 across its lanes (a prefix sum of the k probabilities, then ballots for
+// the top-p cut and the inverse CDF): no CTA barrier on the way.  A row whose chunk slots
+// overflowed, or with more survivors than a warp holds, is flagged and its exact top-k
+// taken afterwards by the whole CTA (a radix select over its logits).
 #include "ls_device.cuh"
 #include "ls_dtype.cuh"
 #include "ls_internal.h"
@@ -22,21 +24,29 @@ namespace lsb {
 namespace {
 
 constexpr int kSampThreads = 256;
-constexpr int kSampWarps = kSampThreads / 32;
-constexpr int kSampCap = 1024;  // candidates held in shared memory
+constexpr int kSampWarps = kSampThreads / 32;  // rows per CTA
+constexpr int kSampWarpCap = 128;              // survivors a warp holds for its row
+constexpr int kSampHdr = 128;                  // chunk headers a warp keeps in shared memory
 
 struct __align__(16) SampSmem {
-  unsigned int gmax[64];  // group maxima as order-preserving bits
-  float wm[kSampWarps], ws[kSampWarps];
-  float M, S, R, lse;
-  int ovf, n;
-  float cx[kSampCap];  // candidates (x, token)
-  int cv[kSampCap];
-  float tx[kMaxK];  // the top-k, best first
-  int tv[kMaxK];
+  unsigned int gmax[kSampWarps][64];  // group maxima as order-preserving bits
+  float cm[kSampWarps][kSampHdr];     // chunk max and survivor count of the first chunks
+  int cn[kSampWarps][kSampHdr];
+  float cx[kSampWarps][kSampWarpCap];  // survivors (x, token)
+  int cv[kSampWarps][kSampWarpCap];
+  float tx[kSampWarps][kMaxK];  // the top-k, best first
+  int tv[kSampWarps][kMaxK];
+  int n[kSampWarps];
+  int path[kSampWarps];
+  float lse[kSampWarps];
+  float R[kSampWarps];
+  // exact path (whole CTA, one row at a time)
+  float ex[kMaxK];
+  int ev[kMaxK];
+  int xn;
   unsigned int hist[256];
   unsigned int prefix, pmask;
-  int need, nsel;
+  int need;
   int wc[kSampWarps];
 };
 
@@ -47,35 +57,54 @@ __device__ __forceinline__ void merge_ms(float& M, float& S, float mo, float so)
   M = Mn;
 }
 
-// x ranks before y: larger value first, then smaller token
+// a ranks before b: larger value first, then smaller token
 __device__ __forceinline__ bool before(float xa, int va, float xb, int vb) {
   return (xa > xb) | ((xa == xb) & (va < vb));
 }
 
-// Rank the sm.n candidates; rank < k goes to position rank of the top-k.
-__device__ void rank_candidates(SampSmem& sm, int K) {
-  const int n = sm.n;
-  for (int i = threadIdx.x; i < n; i += kSampThreads) {
-    const float xi = sm.cx[i];
-    const int vi = sm.cv[i];
-    int r0 = 0, r1 = 0, q = 0;
-#pragma unroll 1
-    for (; q + 1 < n; q += 2) {
-      r0 += before(sm.cx[q], sm.cv[q], xi, vi);
-      r1 += before(sm.cx[q + 1], sm.cv[q + 1], xi, vi);
-    }
-    if (q < n) r0 += before(sm.cx[q], sm.cv[q], xi, vi);
-    const int r = r0 + r1;
-    if (r < K) {
-      sm.tx[r] = xi;
-      sm.tv[r] = vi;
-    }
+__device__ __forceinline__ float warp_incl_scan(float v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float t = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += t;
+  }
+  return v;
+}
+
+// The draw of one row by one warp from its top-k (tx/tv, best first): probabilities
+// exp(x - x_0) renormalised over the k, the top-p prefix, the inverse CDF at u.
+__device__ __forceinline__ void draw(const SampleParams& p, const float* tx, const int* tv, float lse, float u,
+                                     int r) {
+  const int lane = threadIdx.x & 31, K = p.k;
+  const float x0 = tx[0];
+  const float e0 = lane < K ? expf(tx[lane] - x0) : 0.0f;
+  const float e1 = lane + 32 < K ? expf(tx[lane + 32] - x0) : 0.0f;
+  const float c0 = warp_incl_scan(e0);
+  const float t0 = __shfl_sync(0xffffffffu, c0, 31);
+  const float c1 = warp_incl_scan(e1) + t0;
+  const float tot = __shfl_sync(0xffffffffu, c1, 31);
+  int mk = K;  // kept prefix
+  if (p.top_p < 1.0f) {
+    const float lim = p.top_p * tot;
+    const unsigned b0 = __ballot_sync(0xffffffffu, (lane < K) & (c0 >= lim));
+    const unsigned b1 = __ballot_sync(0xffffffffu, (lane + 32 < K) & (c1 >= lim));
+    mk = b0 ? __ffs(b0) : (b1 ? 32 + __ffs(b1) : K);
+  }
+  const float totm = mk <= 32 ? __shfl_sync(0xffffffffu, c0, mk - 1) : __shfl_sync(0xffffffffu, c1, (mk - 33) & 31);
+  const float target = u * totm;
+  const unsigned h0 = __ballot_sync(0xffffffffu, (lane < mk) & (c0 > target));
+  const unsigned h1 = __ballot_sync(0xffffffffu, (lane + 32 < mk) & (c1 > target));
+  const int pick = h0 ? __ffs(h0) - 1 : (h1 ? 31 + __ffs(h1) : mk - 1);
+  if (lane == 0) {
+    p.out_token[r] = tv[pick];
+    if (p.out_logprob) p.out_logprob[r] = tx[pick] - lse;
   }
 }
 
-// Exact top-k of the row without the candidate slots: radix select of the k-th largest
-// value (8 bits at a time from the top), then every element above it and the first
-// equal ones in token order.  Leaves exactly k candidates in sm.cx / sm.cv.
+// Exact top-k of row r without the candidate slots, by the whole CTA: radix select of the
+// k-th largest value (8 bits at a time from the top), then every element above it and the
+// first equal ones in token order.  Leaves exactly k candidates in sm.ex / sm.ev.
 template <int DT, bool BIAS>
 __device__ void exact_candidates(const SampleParams& p, SampSmem& sm, int r) {
   constexpr int ES = Traits<DT>::kBytes;
@@ -90,7 +119,7 @@ __device__ void exact_candidates(const SampleParams& p, SampSmem& sm, int r) {
     sm.prefix = 0;
     sm.pmask = 0;
     sm.need = K;
-    sm.n = 0;
+    sm.xn = 0;
   }
   __syncthreads();
   for (int shift = 24; shift >= 0; shift -= 8) {
@@ -121,10 +150,10 @@ __device__ void exact_candidates(const SampleParams& p, SampSmem& sm, int r) {
   for (int v = tid; v < V; v += kSampThreads) {
     const float x = load_x(v);
     if (float_ord(x) > tkey) {
-      const int pos = atomicAdd(&sm.n, 1);
-      if (pos < kSampCap) {
-        sm.cx[pos] = x;
-        sm.cv[pos] = v;
+      const int pos = atomicAdd(&sm.xn, 1);
+      if (pos < kMaxK) {
+        sm.ex[pos] = x;
+        sm.ev[pos] = v;
       }
     }
   }
@@ -148,172 +177,176 @@ __device__ void exact_candidates(const SampleParams& p, SampSmem& sm, int r) {
     }
     const int off = taken + before_w + __popc(ballot & ((1u << lane) - 1u));
     if (eq && off < need_eq) {
-      const int pos = atomicAdd(&sm.n, 1);
-      if (pos < kSampCap) {
-        sm.cx[pos] = x;
-        sm.cv[pos] = v;
+      const int pos = atomicAdd(&sm.xn, 1);
+      if (pos < kMaxK) {
+        sm.ex[pos] = x;
+        sm.ev[pos] = v;
       }
     }
     taken += total;
     __syncthreads();
   }
-  if (tid == 0 && sm.n > K) sm.n = K;  // greater + equal taken == k
-  __syncthreads();
 }
 
 template <int DT, bool BIAS>
 __global__ void __launch_bounds__(kSampThreads, 1) sample_select_kernel(const SampleParams p) {
   __shared__ SampSmem sm;
   const int K = p.k, nc = p.nc, G = p.groups, C = p.slot_cap;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int r = blockIdx.x;
-  const float u = p.u[r];  // not written by K1: read before waiting on it
-  if (tid < 64) sm.gmax[tid] = float_ord(-INFINITY);
-  if (tid == 0) {
-    sm.ovf = 0;
-    sm.n = 0;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int r = blockIdx.x * kSampWarps + w;
+  const bool row_ok = r < p.rows;
+  const float u = row_ok ? p.u[r] : 0.0f;  // not written by K1: read before waiting on it
+  sm.gmax[w][lane] = float_ord(-INFINITY);
+  sm.gmax[w][lane + 32] = float_ord(-INFINITY);
+  if (lane == 0) {
+    sm.n[w] = 0;
+    sm.path[w] = 0;
   }
   grid_dependency_wait();  // K1's records and slots are complete and visible
-  __syncthreads();
-  const long long u0 = (long long)r * nc;
-  auto rec = [&](long long uu) { return reinterpret_cast<const float*>(p.rec + (size_t)uu * p.rec_stride); };
-  // 1. (max, sum of exp) over the chunks, the group maxima merged over the chunks
-  float m = -INFINITY, s = 0.0f;
-  bool ovf = false;
-  for (int c = tid; c < nc; c += kSampThreads) {
-    const float4 h = __ldcg(reinterpret_cast<const float4*>(rec(u0 + c)));
-    ovf |= __float_as_int(h.x) > C;
-    merge_ms(m, s, h.y, h.z);
-  }
-  for (int i = tid; i < nc * G; i += kSampThreads) {
-    const int c = i / G, g = i - c * G;
-    atomicMax(&sm.gmax[g], float_ord(__ldcg(rec(u0 + c) + 4 + g)));
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float mo = __shfl_xor_sync(0xffffffffu, m, o);
-    const float so = __shfl_xor_sync(0xffffffffu, s, o);
-    merge_ms(m, s, mo, so);
-  }
-  ovf = __any_sync(0xffffffffu, ovf);
-  if (lane == 0) {
-    sm.wm[warp] = m;
-    sm.ws[warp] = s;
-    if (ovf) sm.ovf = 1;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    float M = lane < kSampWarps ? sm.wm[lane] : -INFINITY, S = lane < kSampWarps ? sm.ws[lane] : 0.0f;
+  __syncwarp();
+  int path = 0;
+  if (row_ok) {
+    const long long u0 = (long long)r * nc;
+    auto rec = [&](int c) { return reinterpret_cast<const float*>(p.rec + (size_t)(u0 + c) * p.rec_stride); };
+    // 1. (max, sum of exp) and the group maxima over the row's chunks
+    float m = -INFINITY, s = 0.0f;
+    bool ovf = false;
+    for (int c = lane; c < nc; c += 32) {
+      const float4 h = __ldcg(reinterpret_cast<const float4*>(rec(c)));
+      const int cnt = __float_as_int(h.x);
+      ovf |= cnt > C;
+      merge_ms(m, s, h.y, h.z);
+      if (c < kSampHdr) {
+        sm.cm[w][c] = h.y;
+        sm.cn[w][c] = cnt;
+      }
+      for (int g = 0; g < G; ++g) atomicMax(&sm.gmax[w][g], float_ord(__ldcg(rec(c) + 4 + g)));
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      const float mo = __shfl_xor_sync(0xffffffffu, M, o);
-      const float so = __shfl_xor_sync(0xffffffffu, S, o);
-      merge_ms(M, S, mo, so);
+      const float mo = __shfl_xor_sync(0xffffffffu, m, o);
+      const float so = __shfl_xor_sync(0xffffffffu, s, o);
+      merge_ms(m, s, mo, so);
     }
+    ovf = __any_sync(0xffffffffu, ovf);
+    __syncwarp();
     // R-top-k: the k-th largest of the G group maxima (ties by group index)
-    const float a = lane < G ? ord_float(sm.gmax[lane]) : -INFINITY;
-    const float b = lane + 32 < G ? ord_float(sm.gmax[lane + 32]) : -INFINITY;
+    const float a = lane < G ? ord_float(sm.gmax[w][lane]) : -INFINITY;
+    const float b = lane + 32 < G ? ord_float(sm.gmax[w][lane + 32]) : -INFINITY;
     int ra = 0, rb = 0;
 #pragma unroll 1
-    for (int q = 0; q < 32; ++q) {
+    for (int q = 0; q < min(G, 32); ++q) {
       const float wa = __shfl_sync(0xffffffffu, a, q);
       const float wb = __shfl_sync(0xffffffffu, b, q);
-      const bool qa = q < G, qb = q + 32 < G;  // only the G real groups are ranked
-      ra += (qa & ((wa > a) | ((wa == a) & (q < lane)))) + (qb & (wb > a));
-      rb += (qa & (wa >= b)) + (qb & ((wb > b) | ((wb == b) & (q < lane))));
+      const bool qb = q + 32 < G;  // only the G real groups are ranked
+      ra += ((wa > a) | ((wa == a) & (q < lane))) + (qb & (wb > a));
+      rb += (wa >= b) + (qb & ((wb > b) | ((wb == b) & (q < lane))));
     }
     const unsigned hit = __ballot_sync(0xffffffffu, ((lane < G) & (ra == K - 1)) | ((lane + 32 < G) & (rb == K - 1)));
     const int hl = __ffs(hit) - 1;
-    const float va = __shfl_sync(0xffffffffu, a, hl), vb = __shfl_sync(0xffffffffu, b, hl);
-    const int rah = __shfl_sync(0xffffffffu, ra, hl);
-    if (lane == 0) {
-      sm.M = M;
-      sm.S = S;
-      sm.R = (hl < G && rah == K - 1) ? va : vb;
-      sm.lse = M == -INFINITY ? -INFINITY : M + logf(S);
-    }
-  }
-  __syncthreads();
-  const float R = sm.R;
-  int path = sm.ovf ? 1 : 0;
-  if (p.flags & kFlagForceExact) path = 2;
-  if (path == 0) {
-    // 2. survivors of the row's R-top-k from the chunks that can hold one
-    for (int c = tid; c < nc; c += kSampThreads) {
-      const float4 h = __ldcg(reinterpret_cast<const float4*>(rec(u0 + c)));
-      const int n = h.y >= R ? min(__float_as_int(h.x), C) : 0;
-      const CandSlot* sl = p.slots + (size_t)(u0 + c) * C;
-      for (int s0 = 0; s0 < n; s0 += 4) {
-        int2 raw[4];
+    const float va = __shfl_sync(0xffffffffu, a, hl & 31), vb = __shfl_sync(0xffffffffu, b, hl & 31);
+    const int rah = __shfl_sync(0xffffffffu, ra, hl & 31);
+    const float R = rah == K - 1 ? va : vb;
+    const float lse = m == -INFINITY ? -INFINITY : m + logf(s);
+    path = ovf ? 1 : 0;
+    if (p.flags & kFlagForceExact) path = 2;
+    if (path == 0) {
+      // 2. survivors of the row's bound from the chunks whose max reaches it
+      for (int c = lane; c < nc; c += 32) {
+        float mc;
+        int cnt;
+        if (c < kSampHdr) {
+          mc = sm.cm[w][c];
+          cnt = sm.cn[w][c];
+        } else {
+          const float4 h = __ldcg(reinterpret_cast<const float4*>(rec(c)));
+          mc = h.y;
+          cnt = __float_as_int(h.x);
+        }
+        const int n = mc >= R ? min(cnt, C) : 0;
+        const CandSlot* sl = p.slots + (size_t)(u0 + c) * C;
+        for (int s0 = 0; s0 < n; s0 += 4) {
+          int2 raw[4];
 #pragma unroll
-        for (int t = 0; t < 4; ++t) raw[t] = s0 + t < n ? __ldcg(reinterpret_cast<const int2*>(sl + s0 + t)) : make_int2((int)0xff800000u, 0);
+          for (int t = 0; t < 4; ++t)
+            raw[t] = s0 + t < n ? __ldcg(reinterpret_cast<const int2*>(sl + s0 + t)) : make_int2((int)0xff800000u, 0);
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const float x = __int_as_float(raw[t].x);
-          if ((s0 + t < n) & (x >= R)) {
-            const int pos = atomicAdd(&sm.n, 1);
-            if (pos < kSampCap) {
-              sm.cx[pos] = x;
-              sm.cv[pos] = raw[t].y;
+          for (int t = 0; t < 4; ++t) {
+            const float x = __int_as_float(raw[t].x);
+            if ((s0 + t < n) & (x >= R)) {
+              const int pos = atomicAdd(&sm.n[w], 1);
+              if (pos < kSampWarpCap) {
+                sm.cx[w][pos] = x;
+                sm.cv[w][pos] = raw[t].y;
+              }
             }
           }
         }
       }
+      __syncwarp();
+      const int n = sm.n[w];
+      if (n > kSampWarpCap || n < K) path = 3;
+      if (path == 0) {
+        // 3. the exact top-k among the survivors, best first
+        for (int i = lane; i < n; i += 32) {
+          const float xi = sm.cx[w][i];
+          const int vi = sm.cv[w][i];
+          int r0 = 0, r1 = 0, q = 0;
+#pragma unroll 1
+          for (; q + 1 < n; q += 2) {
+            r0 += before(sm.cx[w][q], sm.cv[w][q], xi, vi);
+            r1 += before(sm.cx[w][q + 1], sm.cv[w][q + 1], xi, vi);
+          }
+          if (q < n) r0 += before(sm.cx[w][q], sm.cv[w][q], xi, vi);
+          if (r0 + r1 < K) {
+            sm.tx[w][r0 + r1] = xi;
+            sm.tv[w][r0 + r1] = vi;
+          }
+        }
+        __syncwarp();
+        // 4. the draw
+        draw(p, sm.tx[w], sm.tv[w], lse, u, r);
+      }
+    }
+    if (lane == 0) {
+      RowStat st;
+      st.lse = lse;
+      st.rtopk = R;
+      st.ncand = path == 0 ? sm.n[w] : -1;
+      st.pad = 0;
+      p.rowstat[r] = st;
+      p.bstat[r] = path;
+      sm.path[w] = path;
+      sm.lse[w] = lse;
+    }
+  }
+  // rows that need the exact top-k: the whole CTA, one row at a time
+  __syncthreads();
+  for (int w2 = 0; w2 < kSampWarps; ++w2) {
+    if (sm.path[w2] == 0) continue;  // CTA-uniform
+    const int r2 = blockIdx.x * kSampWarps + w2;
+    exact_candidates<DT, BIAS>(p, sm, r2);
+    if (w == 0) {
+      // rank the k candidates (lanes hold entries lane and lane + 32)
+      for (int i = lane; i < K; i += 32) {
+        const float xi = sm.ex[i];
+        const int vi = sm.ev[i];
+        int rk = 0;
+        for (int q = 0; q < K; ++q) rk += before(sm.ex[q], sm.ev[q], xi, vi);
+        sm.tx[w2][rk] = xi;
+        sm.tv[w2][rk] = vi;
+      }
+      __syncwarp();
+      draw(p, sm.tx[w2], sm.tv[w2], sm.lse[w2], p.u[r2], r2);
     }
     __syncthreads();
-    if (sm.n > kSampCap || sm.n < K) path = 3;
-  }
-  const int ncand = sm.n;
-  __syncthreads();
-  if (path != 0) exact_candidates<DT, BIAS>(p, sm, r);
-  // 3. the exact top-k, best first
-  rank_candidates(sm, K);
-  __syncthreads();
-  // 4. the draw: cumulative probabilities over the top-k (renormalised), the top-p prefix,
-  // then the first candidate whose cumulative probability exceeds u
-  if (tid == 0) {
-    const double x0 = sm.tx[0];
-    double tot = 0.0;
-    for (int i = 0; i < K; ++i) tot += exp((double)sm.tx[i] - x0);
-    int mk = K;
-    double totm = tot;
-    if (p.top_p < 1.0f) {
-      double acc = 0.0;
-      for (int i = 0; i < K; ++i) {
-        acc += exp((double)sm.tx[i] - x0);
-        if (acc >= (double)p.top_p * tot) {
-          mk = i + 1;
-          totm = acc;
-          break;
-        }
-      }
-    }
-    const double target = (double)u * totm;
-    double acc = 0.0;
-    int pick = mk - 1;
-    for (int i = 0; i < mk; ++i) {
-      acc += exp((double)sm.tx[i] - x0);
-      if (acc > target) {
-        pick = i;
-        break;
-      }
-    }
-    p.out_token[r] = sm.tv[pick];
-    if (p.out_logprob) p.out_logprob[r] = sm.tx[pick] - sm.lse;
-    RowStat st;
-    st.lse = sm.lse;
-    st.rtopk = R;
-    st.ncand = path == 0 ? ncand : -1;
-    st.pad = 0;
-    p.rowstat[r] = st;
-    p.bstat[r] = path;
   }
 }
 
 template <int DT, bool BIAS>
 cudaError_t launch_t(const SampleParams& p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)p.rows);
+  cfg.gridDim = dim3((unsigned)((p.rows + kSampWarps - 1) / kSampWarps));
   cfg.blockDim = dim3(kSampThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
