@@ -60,6 +60,8 @@ def _load():
             lib.oracle_backtrack.restype = ip
             lib.oracle_sample.argtypes = [vp, ip, vp, ip, ip, ip, ctypes.c_double, vp, vp, vp, vp]
             lib.oracle_sample.restype = ip
+            lib.oracle_cache_refresh_inplace.argtypes = [vp, ip, vp, ip, ip, ip, ip, ip, ip, ip]
+            lib.oracle_cache_refresh_inplace.restype = ip
             _lib = lib
     return _lib
 
@@ -167,3 +169,20 @@ def sample(logits, u, top_k, top_p=1.0, *, bias=None, dtype=None):
     if rc != 0:
         raise ValueError(f"oracle_sample failed ({rc})")
     return {"token": tok, "logprob": lp, "margin": mg}
+
+
+def cache_refresh_inplace(cache, parent, length):
+    """In-place refresh of the [layers, batch*k, heads, max_len, head_dim] cache by parent beam
+    (positions < length; every row reads the state before the step).  Returns the new cache."""
+    lib = _load()
+    out = np.ascontiguousarray(cache).copy()
+    layers, rows, heads, max_len, head_dim = out.shape
+    par = np.ascontiguousarray(parent, dtype=np.int32)
+    batch, k = par.shape
+    if batch * k != rows:
+        raise ValueError("parent shape does not match cache rows")
+    rc = lib.oracle_cache_refresh_inplace(_ptr(out), out.dtype.itemsize, _ptr(par), layers, batch, k, heads, max_len,
+                                          int(length), head_dim)
+    if rc != 0:
+        raise ValueError(f"oracle_cache_refresh_inplace failed ({rc})")
+    return out

@@ -378,3 +378,24 @@ int oracle_sample(const void* logits, int dtype, const float* bias, int rows, in
   free(cum);
   return 0;
 }
+
+/*
+ * Beam-cache refresh in place: cache[l, b*k+j, h, p, :] becomes the old
+ * cache[l, b*k+parent[b,j], h, p, :] for p < len (every row reads the state before the
+ * step, whatever order rows are written in); positions p >= len keep their own content.
+ * Written as the definition: a full copy of the old cache, then the gather from it.
+ * Returns -1 on bad arguments (including a parent outside [0, k)), -2 on allocation failure.
+ */
+int oracle_cache_refresh_inplace(void* cache, int elem_bytes, const int32_t* parent, int layers, int batch, int k,
+                                 int heads, int max_len, int len, int head_dim) {
+  if (!cache || !parent || elem_bytes < 1) return -1;
+  if (layers < 0 || batch < 0 || k < 1 || heads < 0 || max_len < 0 || len < 0 || len > max_len || head_dim < 0)
+    return -1;
+  const size_t total = (size_t)layers * batch * k * heads * max_len * head_dim * (size_t)elem_bytes;
+  void* old = malloc(total ? total : 1);
+  if (!old) return -2;
+  memcpy(old, cache, total);
+  const int rc = oracle_cache_reorder(old, cache, elem_bytes, parent, layers, batch, k, heads, max_len, len, head_dim);
+  free(old);
+  return rc;
+}
