@@ -271,7 +271,13 @@ def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
         layers, heads, max_len, head_dim = wr.kv_shape
         shape = (layers, wr.rows, heads, max_len, head_dim)
         caches = [torch.from_numpy(synth.kv_cache(shape, wr.seed, which=i)).to(dev) for i in range(2)]
-    loop = BeamSearchLoop(B, K, V, wr.eos_id, kv_shape=wr.kv_shape, device=dev, caches=caches, max_steps=T)
+    # the headline loop refreshes the cache in place (copy on change); the out-of-place
+    # (ping-pong) refresh of the same search is timed too and reported beside it
+    loop = BeamSearchLoop(B, K, V, wr.eos_id, kv_shape=wr.kv_shape, device=dev, caches=caches, max_steps=T,
+                          inplace=True)
+    loop_oop = None
+    if caches is not None:
+        loop_oop = BeamSearchLoop(B, K, V, wr.eos_id, kv_shape=wr.kv_shape, device=dev, caches=caches, max_steps=T)
     setup_s = time.time() - t0
 
     def lens(t):  # cache positions refreshed at decode step t (1-based)
@@ -285,79 +291,94 @@ def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
         ev_k = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(T + 1)]
         graph_events = False
 
-    def run_all(instrument: bool):
-        loop.reset(beam0, fin0)
+    def run_all(lp, instrument: bool):
+        lp.reset(beam0, fin0)
         for t in range(T):
             if instrument:
                 ev_k[t][0].record()
-            s, n = loop.cur, 1 - loop.cur
-            tok, par = loop.token_out(t + 1), loop.parent_out(t + 1)
-            lsb.check(lsb.ls_beam_step(d_logits[t], d_bias, loop.scores[s], loop.finished[s], wr.eos_id,
-                                       tok, par, loop.scores[n], loop.finished[n], loop.workspace), "ls_beam_step")
+            s, n = lp.cur, 1 - lp.cur
+            tok, par = lp.token_out(t + 1), lp.parent_out(t + 1)
+            lsb.check(lsb.ls_beam_step(d_logits[t], d_bias, lp.scores[s], lp.finished[s], wr.eos_id,
+                                       tok, par, lp.scores[n], lp.finished[n], lp.workspace), "ls_beam_step")
             if instrument:
                 ev_k[t][1].record()
-            if loop.cache is not None:
-                lsb.check(lsb.ls_cache_reorder(loop.cache[s], loop.cache[n], par, lens(t + 1)), "ls_cache_reorder")
+            if lp.cache is not None:
+                if lp.inplace:
+                    lsb.check(lsb.ls_cache_refresh_inplace(lp.cache[0], par, lens(t + 1), lp.workspace),
+                              "ls_cache_refresh_inplace")
+                else:
+                    lsb.check(lsb.ls_cache_reorder(lp.cache[s], lp.cache[n], par, lens(t + 1)), "ls_cache_reorder")
             if instrument:
                 ev_k[t][2].record()
-            loop.cur = n
+            lp.cur = n
         # end of the search: every final beam's token sequence from the parent history
         if instrument:
             ev_k[T][0].record()
-        loop.finalize(T)
+        lp.finalize(T)
         if instrument:
             ev_k[T][1].record()
 
-    # warm the library's per-device setup outside capture, then capture both graphs
-    with torch.cuda.stream(stream):
-        run_all(False)
-    torch.cuda.synchronize()
-    lsb.check(lsb.ls_read_status(loop.workspace, stream), "device status")
-    g_plain, g_inst = torch.cuda.CUDAGraph(), None
-    with torch.cuda.graph(g_plain, stream=stream):
-        run_all(False)
-    if graph_events:
-        g_inst = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_inst, stream=stream):
-            run_all(True)
-    torch.cuda.synchronize()
+    def capture(lp):
+        # warm the library's per-device setup outside capture, then capture both graphs
+        with torch.cuda.stream(stream):
+            run_all(lp, False)
+        torch.cuda.synchronize()
+        lsb.check(lsb.ls_read_status(lp.workspace, stream), "device status")
+        gp, gi = torch.cuda.CUDAGraph(), None
+        with torch.cuda.graph(gp, stream=stream):
+            run_all(lp, False)
+        if graph_events:
+            gi = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gi, stream=stream):
+                run_all(lp, True)
+        torch.cuda.synchronize()
+        return gp, gi
 
-    launches_per_step = T * (3 if loop.cache is not None else 2) + 1  # K1, K2, K4 per decode step + backtrack
-    for _ in range(args.warmup):
-        g_plain.replay()
-    torch.cuda.synchronize()
-    barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
+    def time_graphs(lp, gp, gi):
+        """ms for args.steps replays of gp, then per-kernel ms per search from gi (K1+K2, K4, backtrack)."""
+        for _ in range(args.warmup):
+            gp.replay()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(world)
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             e0.record()
             for _ in range(args.steps):
-                g_plain.replay()
+                gp.replay()
             e1.record()
         torch.cuda.synchronize()
         barrier(world)
-        ms_plain = e0.elapsed_time(e1)
-        # per-kernel durations: the same graph with an event around each kernel
-        k1_ms, k4_ms, bt_ms = 0.0, 0.0, 0.0
+        ms = e0.elapsed_time(e1)
+        k1, k4, bt = 0.0, 0.0, 0.0
         reps = max(1, min(args.steps, 3))
         with torch.cuda.stream(stream):
             for _ in range(reps):
-                if g_inst is not None:
-                    g_inst.replay()
+                if gi is not None:
+                    gi.replay()
                 else:
-                    run_all(True)
+                    run_all(lp, True)
                 torch.cuda.synchronize()
                 for t in range(T):
-                    k1_ms += ev_k[t][0].elapsed_time(ev_k[t][1])
-                    if loop.cache is not None:
-                        k4_ms += ev_k[t][1].elapsed_time(ev_k[t][2])
-                bt_ms += ev_k[T][0].elapsed_time(ev_k[T][1])
-    lsb.check(lsb.ls_read_status(loop.workspace, stream), "device status")
-    k1_ms /= reps
-    k4_ms /= reps
-    bt_ms /= reps
+                    k1 += ev_k[t][0].elapsed_time(ev_k[t][1])
+                    if lp.cache is not None:
+                        k4 += ev_k[t][1].elapsed_time(ev_k[t][2])
+                bt += ev_k[T][0].elapsed_time(ev_k[T][1])
+        lsb.check(lsb.ls_read_status(lp.workspace, stream), "device status")
+        return ms, k1 / reps, k4 / reps, bt / reps
+
+    launches_per_step = T * (3 if loop.cache is not None else 2) + 1  # K1, K2, K4 per decode step + backtrack
+    g_plain, g_inst = capture(loop)
+    with ClockSampler(local) as clk:
+        ms_plain, k1_ms, k4_ms, bt_ms = time_graphs(loop, g_plain, g_inst)
+        parents_run = loop.parent_hist.cpu().numpy() if loop.cache is not None else None
+        oop = None
+        if loop_oop is not None:
+            del g_plain, g_inst
+            go_plain, go_inst = capture(loop_oop)
+            oop = time_graphs(loop_oop, go_plain, go_inst)
+            del go_plain, go_inst
     ms_total = max_over_ranks(ms_plain, world, dev)
     ms_per_step = ms_total / args.steps
     decode_steps = T * args.steps * world
@@ -367,22 +388,48 @@ def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
     fin_rows = 0 if fin_np is None else int(fin_np.sum())
     logit_bytes_launch = (wr.rows - fin_rows) * V * es + (V * 4 if bias_np is not None else 0) + wr.rows * 13
     k1_bytes = logit_bytes_launch * T
-    k4_bytes = 0
+    k4_bytes, k4_dense_bytes = 0, 0
     if loop.cache is not None:
         layers, heads, max_len, head_dim = wr.kv_shape
+        # in place: each batch reads the slabs of the parents its changed beams need and writes
+        # the changed beams (exact, from the run's parents); out of place: every row both ways
+        par = parents_run.reshape(T, B, K)
+        changed = par != np.arange(K)[None, None, :]
+        needed = np.zeros((T, B, K), bool)
+        for j in range(K):
+            needed[np.arange(T)[:, None], np.arange(B)[None, :], par[:, :, j]] |= changed[:, :, j]
+        moved_rows = changed.sum(axis=(1, 2)) + needed.sum(axis=(1, 2))
         for t in range(1, T + 1):
-            k4_bytes += 2 * layers * wr.rows * heads * lens(t) * head_dim * 2
+            slab = layers * heads * lens(t) * head_dim * 2
+            k4_bytes += int(moved_rows[t - 1]) * slab
+            k4_dense_bytes += 2 * wr.rows * slab
     peak, peak_src = hbm_peak()
     k1_gbs = k1_bytes / (k1_ms / 1e3) / 1e9
     kern = {"beam_step": {"bound": "hbm", "achieved": k1_gbs, "peak": peak, "unit": "GB/s", "frac": k1_gbs / peak,
                           "traffic": recorded_traffic("beam_step", wr.name),
                           "us_per_launch": k1_ms * 1e3 / T,
                           "algorithmic_bytes_per_launch": k1_bytes / T}}
+    oop_line = None
     if loop.cache is not None:
         k4_gbs = k4_bytes / (k4_ms / 1e3) / 1e9
-        kern["cache_reorder"] = {"bound": "hbm", "achieved": k4_gbs, "peak": peak, "unit": "GB/s",
-                                 "frac": k4_gbs / peak, "traffic": recorded_traffic("cache_reorder", wr.name),
-                                 "us_per_launch": k4_ms * 1e3 / T, "algorithmic_bytes_per_launch": k4_bytes / T}
+        kern["cache_refresh_inplace"] = {
+            "bound": "hbm", "achieved": k4_gbs, "peak": peak, "unit": "GB/s", "frac": k4_gbs / peak,
+            "traffic": recorded_traffic("cache_refresh_inplace", wr.name), "us_per_launch": k4_ms * 1e3 / T,
+            "algorithmic_bytes_per_launch": k4_bytes / T,
+            "note": "copy on change: bytes of the parents read and the beams written, from the run's parents; "
+                    f"{k4_dense_bytes / T:.0f} B per launch if every row were moved"}
+        if oop is not None:
+            o_ms, o_k1, o_k4, o_bt = oop
+            o_ms = max_over_ranks(o_ms, world, dev)
+            o_gbs = k4_dense_bytes / (o_k4 / 1e3) / 1e9
+            oop_line = {"value": T * args.steps * world / (o_ms / 1e3), "unit": UNIT, "ms_per_step": o_ms / args.steps,
+                        "cache_reorder": {"bound": "hbm", "achieved": o_gbs, "peak": peak, "unit": "GB/s",
+                                          "frac": o_gbs / peak,
+                                          "traffic": recorded_traffic("cache_reorder", wr.name),
+                                          "us_per_launch": o_k4 * 1e3 / T,
+                                          "algorithmic_bytes_per_launch": k4_dense_bytes / T},
+                        "beam_step_us_per_launch": o_k1 * 1e3 / T,
+                        "note": "the same search with the out-of-place (ping-pong) cache refresh"}
     bt_bytes = 2 * T * B * K * 4 + B * K * (T + 1) * 4  # history read, sequences and lengths written
     bt_gbs = bt_bytes / (bt_ms / 1e3) / 1e9 if bt_ms > 0 else 0.0
     kern["backtrack"] = {"bound": "latency", "achieved": bt_gbs, "peak": peak, "unit": "GB/s", "frac": bt_gbs / peak,
@@ -406,17 +453,20 @@ def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
     clocks = clk.summary()
     cfg = {"workload": f"{wr.name}: batch {B}, beam {K}, vocab {V}, {wr.dtype} logits, "
                        f"{T} decode step(s)" + (f", KV cache {[wr.kv_shape[0], wr.rows, *wr.kv_shape[1:]]} fp16 "
-                                                f"refreshed by parent (len = step)" if wr.kv_shape else ""),
+                                                f"refreshed by parent (len = step), in place" if wr.kv_shape else ""),
            "batch": B, "beam": K, "vocab": V, "logit_dtype": wr.dtype, "decode_steps_per_step": T,
            "l2": f"inputs larger than L2: {host_logits.nbytes / 1e9:.2f} GB of logits per benchmark step",
-           "graph": f"one CUDA graph of the {T}-step loop", "parallelism": f"replicas x{world} (independent batches)"}
+           "graph": f"one CUDA graph of the {T}-step loop and the end-of-search backtrack",
+           "cache_refresh": "in place, copy on change (out-of-place figures under cache_refresh_out_of_place)",
+           "parallelism": f"replicas x{world} (independent batches)"}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": wr.dtype, "data": "synthetic (seeded generators, workload recipe in synth/)", "config": cfg,
         "logit_gbs": k1_gbs, "step_gbs": step_gbs, "step_roofline_frac": step_gbs / peak,
         "roofline": roof, "roofline_kernels": kern, "gpu_launches": launches_per_step * args.steps,
-        "clocks": clocks, "e2e": e2e, "sampling": sampling, "setup_s": round(setup_s, 1),
+        "clocks": clocks, "e2e": e2e, "sampling": sampling, "cache_refresh_out_of_place": oop_line,
+        "setup_s": round(setup_s, 1),
     }
     return line
 

@@ -119,6 +119,23 @@ LS_API ls_status ls_cache_reorder(const void* src, void* dst, ls_dtype dtype, co
                            int head_dim, void* workspace, void* stream);
 
 /*
+ * Beam-cache refresh in place, copy on change (article: "update the cache" after the
+ * selection): for every row j whose parent is not j itself,
+ *   cache[l, b*k+j, h, p, :] = (state before the call) cache[l, b*k + parent[b*k+j], h, p, :]
+ * for p < len; rows with parent[b*k+j] == j and positions p >= len are not touched.  The
+ * result on [0, len) equals ls_cache_reorder from a copy of the cache.
+ *
+ * cache [layers, batch*k, heads, max_len, head_dim] of dtype, device; parent [batch, k]
+ * int32 in [0, k), device; k <= LS_MAX_K.  An out-of-range parent leaves that row as it is
+ * and, when `workspace` is not NULL, sets LS_ERR_INTERNAL in its status word.  workspace:
+ * NULL or a workspace initialised by ls_workspace_init (only its status word is used).
+ * len == 0 or an empty shape is a no-op.  Nothing is allocated.
+ */
+LS_API ls_status ls_cache_refresh_inplace(void* cache, ls_dtype dtype, const int32_t* parent, int layers,
+                                          int batch, int k, int heads, int max_len, int len, int head_dim,
+                                          void* workspace, void* stream);
+
+/*
  * Workspace bytes for ls_sample on `rows` rows of `vocab` logits keeping top_k candidates
  * (0 for unsupported shapes: top_k outside [1, LS_MAX_K] or above vocab).
  */

@@ -19,7 +19,7 @@ __all__ = [
     "LS_DTYPE_F32", "LS_DTYPE_F16", "LS_DTYPE_BF16", "LS_MAX_K", "LsBeamError", "library_path", "load_library",
     "check", "ls_beam_step_workspace_size", "ls_workspace_init", "ls_beam_step", "ls_cache_reorder",
     "ls_read_status", "ls_status_string", "ls_read_row_stats", "ls_beam_step_noalloc", "ls_backtrack",
-    "ls_sample_workspace_size", "ls_sample",
+    "ls_sample_workspace_size", "ls_sample", "ls_cache_refresh_inplace",
 ]
 
 LS_OK, LS_ERR_INVALID_ARG, LS_ERR_UNSUPPORTED, LS_ERR_CUDA, LS_ERR_TIMEOUT, LS_ERR_INTERNAL = range(6)
@@ -72,6 +72,8 @@ def load_library():
         lib.ls_sample_workspace_size.restype = sz
         lib.ls_sample.argtypes = [vp, ip, vp, vp, ip, ip, ip, ctypes.c_float, vp, vp, vp, sz, vp]
         lib.ls_sample.restype = ip
+        lib.ls_cache_refresh_inplace.argtypes = [vp, ip, vp, ip, ip, ip, ip, ip, ip, ip, vp, vp]
+        lib.ls_cache_refresh_inplace.restype = ip
         _lib = lib
         return lib
 
@@ -172,6 +174,17 @@ def ls_sample(logits, bias, u, top_k: int, top_p: float, out_token, out_logprob,
     return load_library().ls_sample(_ptr(logits), _dtype_code(logits), _ptr(bias), _ptr(u), rows, vocab, int(top_k),
                                     float(top_p), _ptr(out_token), _ptr(out_logprob), _ptr(workspace),
                                     workspace.numel() * workspace.element_size(), _stream(stream))
+
+
+def ls_cache_refresh_inplace(cache, parent, length: int, workspace=None, stream=None) -> int:
+    """cache [layers, batch*k, heads, max_len, head_dim] (refreshed in place); parent [batch, k] int32."""
+    layers, rows, heads, max_len, head_dim = cache.shape
+    batch, k = parent.shape
+    if batch * k != rows:
+        raise ValueError("parent shape does not match cache rows")
+    return load_library().ls_cache_refresh_inplace(
+        _ptr(cache), _dtype_code(cache), _ptr(parent), layers, batch, k, heads, max_len, int(length), head_dim,
+        _ptr(workspace), _stream(stream))
 
 
 def ls_read_status(workspace, stream=None) -> int:

@@ -25,6 +25,9 @@ struct DeviceInfo {
   // K1 occupancy per [dtype][bias][vpl index]; 0 = not configured yet
   int step_occ[3][2][2] = {};
   int copy_occ[5] = {};
+  int inplace_occ[5] = {};
+  int inplace_tma_occ = 0;
+  size_t inplace_tma_smem = 0;
 };
 
 std::mutex g_mu;
@@ -40,7 +43,7 @@ struct Debug {
   bool check_ptrs = true;
 };
 
-// LS_BEAM_DEBUG: comma-separated "exact", "spin=<ns>", "vpl=<4|8>", "nocheck".
+// LS_BEAM_DEBUG: comma-separated "exact", "ipplain", "spin=<ns>", "vpl=<4|8>", "nocheck".
 Debug read_debug() {
   Debug d;
   const char* env = std::getenv("LS_BEAM_DEBUG");
@@ -50,6 +53,7 @@ Debug read_debug() {
   buf[sizeof buf - 1] = 0;
   for (char* tok = std::strtok(buf, ","); tok; tok = std::strtok(nullptr, ",")) {
     if (!std::strcmp(tok, "exact")) d.flags |= kFlagForceExact;
+    else if (!std::strcmp(tok, "ipplain")) d.flags |= kFlagPlainInplace;
     else if (!std::strncmp(tok, "spin=", 5)) d.spin_ns = std::atoll(tok + 5);
     else if (!std::strncmp(tok, "vpl=", 4)) d.vpl = std::atoi(tok + 4);
     else if (!std::strcmp(tok, "nocheck")) d.check_ptrs = false;
@@ -113,6 +117,29 @@ ls_status plan_rows(DeviceInfo* di, const Debug& dbg, int dtype, int es, bool bi
   const long long grid_need = (out->units + kRowWarps - 1) / kRowWarps;
   out->grid = grid_need < grid_full ? grid_need : grid_full;
   return LS_OK;
+}
+
+int inplace_occupancy(DeviceInfo* di, int unit) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int& occ = di->inplace_occ[unit_index(unit)];
+  if (occ == 0) {
+    int o = 0;
+    if (cache_inplace_occupancy(unit, &o) != cudaSuccess || o < 1) return 0;
+    occ = o;
+  }
+  return occ;
+}
+
+int inplace_tma_occupancy(DeviceInfo* di, int batch, int k) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  const size_t smem = cache_inplace_tma_smem(batch, k);
+  if (di->inplace_tma_occ == 0 || di->inplace_tma_smem != smem) {
+    int o = 0;
+    if (cache_inplace_tma_occupancy(batch, k, &o) != cudaSuccess || o < 1) return 0;
+    di->inplace_tma_occ = o;
+    di->inplace_tma_smem = smem;
+  }
+  return di->inplace_tma_occ;
 }
 
 bool select_configured(DeviceInfo* di) {
@@ -292,6 +319,62 @@ ls_status ls_cache_reorder(const void* src, void* dst, ls_dtype dtype, const int
   const long long grid_full = (long long)di->sms * occ;
   const long long grid = p.pairs < grid_full ? p.pairs : grid_full;
   cudaError_t e = launch_cache_reorder(p, unit, (int)grid, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? LS_OK : cuda_fail(e);
+}
+
+ls_status ls_cache_refresh_inplace(void* cache, ls_dtype dtype, const int32_t* parent, int layers, int batch, int k,
+                                   int heads, int max_len, int len, int head_dim, void* workspace, void* stream) {
+  if (layers < 0 || batch < 0 || k < 1 || k > LS_MAX_K || heads < 0 || max_len < 0 || len < 0 || len > max_len ||
+      head_dim < 0)
+    return LS_ERR_INVALID_ARG;
+  if (!dtype_ok(dtype)) return LS_ERR_INVALID_ARG;
+  if (layers == 0 || batch == 0 || heads == 0 || len == 0 || head_dim == 0) return LS_OK;
+  if (!cache || !parent) return LS_ERR_INVALID_ARG;
+  if (!aligned(parent, 4) || (workspace && !aligned(workspace, 256))) return LS_ERR_INVALID_ARG;
+  const Debug dbg = read_debug();
+  if (dbg.check_ptrs) {
+    if (!device_reachable(cache) || !device_reachable(parent)) return LS_ERR_INVALID_ARG;
+    if (workspace && !device_reachable(workspace)) return LS_ERR_INVALID_ARG;
+  }
+  const long long es = dtype_bytes(dtype);
+  const long long slab_stride = (long long)max_len * head_dim * es;
+  const long long row_stride = slab_stride * heads;
+  const long long layer_stride = row_stride * batch * k;
+  const long long slab_bytes = (long long)len * head_dim * es;
+  const uintptr_t c0 = reinterpret_cast<uintptr_t>(cache);
+  int unit = 16;
+  while (unit > 1 && ((c0 % unit) || (slab_bytes % unit) || (slab_stride % unit))) unit >>= 1;
+  const long long units = (long long)layers * batch * heads;
+  if (units >= (1ll << 40) || (long long)batch * k >= (1ll << 31)) return LS_ERR_UNSUPPORTED;
+  int dev = 0;
+  DeviceInfo* di = device_info(&dev);
+  if (!di) return cuda_fail(cudaErrorUnknown);
+  InplaceParams p;
+  p.cache = static_cast<unsigned char*>(cache);
+  p.parent = parent;
+  p.status = workspace ? reinterpret_cast<uint32_t*>(workspace) : nullptr;
+  p.spin_limit_ns = dbg.spin_ns;
+  p.layer_stride = layer_stride;
+  p.row_stride = row_stride;
+  p.slab_stride = slab_stride;
+  p.slab_bytes = slab_bytes;
+  p.batch = batch;
+  p.k = k;
+  p.heads = heads;
+  p.layers = layers;
+  p.units = units;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // bulk copies when every slab and tile is 16-byte aligned and the parents fit in shared memory
+  const bool tma = unit == 16 && (long long)batch * k <= kIpTmaMaxParents && !(dbg.flags & kFlagPlainInplace);
+  const int occ = tma ? inplace_tma_occupancy(di, batch, k) : inplace_occupancy(di, unit);
+  if (occ < 1) return cuda_fail(cudaErrorUnknown);
+  const long long stage = tma ? kIpTmaStage : kIpStageBytes;
+  const long long tile = (stage / k) / unit * unit;  // every row's tile fits one staging buffer
+  p.tile_bytes = (int)(tile < slab_bytes ? tile : slab_bytes);
+  const long long items = tma ? units * ((slab_bytes + p.tile_bytes - 1) / p.tile_bytes) : units;
+  const long long grid_full = (long long)di->sms * occ;
+  const long long grid = items < grid_full ? items : grid_full;
+  const cudaError_t e = tma ? launch_cache_inplace_tma(p, (int)grid, st) : launch_cache_inplace(p, unit, (int)grid, st);
   return e == cudaSuccess ? LS_OK : cuda_fail(e);
 }
 

@@ -35,6 +35,7 @@ constexpr uint32_t kDevInternal = 1u << 2;
 
 // Debug flags (LS_BEAM_DEBUG).
 constexpr int kFlagForceExact = 1;
+constexpr int kFlagPlainInplace = 2;  // the in-place refresh without bulk copies
 
 // ---------------------------------------------------------------- workspace layout
 struct alignas(16) RowStat {
@@ -182,6 +183,24 @@ struct SampleParams {
   float top_p;
 };
 
+// In-place cache refresh (cache_inplace.cu): staging space per CTA of the plain kernel, per
+// stage of the bulk-copy kernel (two stages), and the parents the bulk-copy kernel stages.
+constexpr int kIpStageBytes = 48 * 1024;
+constexpr int kIpTmaStage = 32 * 1024;
+constexpr int kIpTmaMaxParents = 8192;
+
+struct InplaceParams {
+  unsigned char* cache;
+  const int32_t* parent;  // [batch, k]
+  uint32_t* status;       // may be null
+  long long spin_limit_ns;  // bounded waits of the bulk-copy kernel
+  long long layer_stride, row_stride, slab_stride;  // bytes
+  long long slab_bytes;   // len * head_dim * es
+  int tile_bytes;         // positions staged at a time, in bytes (<= kIpStageBytes / k)
+  int batch, k, heads, layers;
+  long long units;        // layers * batch * heads
+};
+
 // Launchers (defined next to their kernels).
 size_t beam_rows_smem_bytes(int vpl);
 cudaError_t beam_rows_config(int dtype, bool bias, int vpl, int* occupancy);
@@ -194,5 +213,10 @@ int backtrack_tile(int k, int steps);
 size_t backtrack_smem_bytes(int k, int tile);
 cudaError_t launch_backtrack(const BacktrackParams& p, cudaStream_t stream);
 cudaError_t launch_sample_select(const SampleParams& p, int dtype, cudaStream_t stream);
+cudaError_t launch_cache_inplace(const InplaceParams& p, int unit, int grid, cudaStream_t stream);
+cudaError_t cache_inplace_occupancy(int unit, int* occupancy);
+size_t cache_inplace_tma_smem(int batch, int k);
+cudaError_t launch_cache_inplace_tma(const InplaceParams& p, int grid, cudaStream_t stream);
+cudaError_t cache_inplace_tma_occupancy(int batch, int k, int* occupancy);
 
 }  // namespace lsb

@@ -7,6 +7,9 @@ finished flags becoming the next step's beam state.  Everything stays on the
 GPU: the beam state and the two cache buffers alternate between two sets
 (ping-pong), so a run of steps can be captured in one CUDA graph.
 
+With ``inplace=True`` the cache is one buffer refreshed in place, copy on change
+(``ls_cache_refresh_inplace``): rows that continue themselves are not moved.
+
 With ``max_steps`` > 0 every step writes its tokens and parents straight into a
 [max_steps, batch, k] history, and ``finalize`` turns the history into the token
 sequence and length of every final beam (``ls_backtrack``): the n-best list of each
@@ -20,15 +23,17 @@ from __future__ import annotations
 
 import torch
 
-from . import check, ls_backtrack, ls_beam_step, ls_beam_step_workspace_size, ls_cache_reorder, ls_workspace_init
+from . import (check, ls_backtrack, ls_beam_step, ls_beam_step_workspace_size, ls_cache_refresh_inplace,
+               ls_cache_reorder, ls_workspace_init)
 
 
 class BeamSearchLoop:
     def __init__(self, batch: int, k: int, vocab: int, eos_id: int, kv_shape=None, kv_dtype=torch.float16,
-                 device="cuda", caches=None, max_steps: int = 0):
+                 device="cuda", caches=None, max_steps: int = 0, inplace: bool = False):
         """kv_shape = (layers, heads, max_len, head_dim) or None for no cache refresh.
         caches: optional pair of preallocated [layers, batch*k, heads, max_len, head_dim] tensors.
-        max_steps: length limit of a search; > 0 keeps the token / parent history for finalize()."""
+        max_steps: length limit of a search; > 0 keeps the token / parent history for finalize().
+        inplace: refresh one cache buffer in place (caches[0] when given) instead of ping-pong."""
         self.batch, self.k, self.vocab, self.eos_id = batch, k, vocab, eos_id
         self.device = torch.device(device)
         dev = self.device
@@ -44,11 +49,12 @@ class BeamSearchLoop:
             layers, heads, max_len, head_dim = kv_shape
             shape = (layers, batch * k, heads, max_len, head_dim)
             if caches is None:
-                caches = [torch.zeros(shape, dtype=kv_dtype, device=dev) for _ in range(2)]
-            self.cache = list(caches)
+                caches = [torch.zeros(shape, dtype=kv_dtype, device=dev) for _ in range(1 if inplace else 2)]
+            self.cache = list(caches)[:1] if inplace else list(caches)
         else:
             self.cache = None
         self.cur = 0
+        self.inplace = inplace
         self.max_steps = max_steps
         if max_steps > 0:
             self.token_hist = torch.zeros(max_steps, batch, k, dtype=torch.int32, device=dev)
@@ -86,10 +92,18 @@ class BeamSearchLoop:
         check(ls_beam_step(logits, bias, self.scores[s], self.finished[s], self.eos_id, tok, par,
                            self.scores[n], self.finished[n], self.workspace, stream), "ls_beam_step")
         if self.cache is not None:
-            check(ls_cache_reorder(self.cache[s], self.cache[n], par, t, stream=stream), "ls_cache_reorder")
+            if self.inplace:
+                check(ls_cache_refresh_inplace(self.cache[0], par, t, self.workspace, stream),
+                      "ls_cache_refresh_inplace")
+            else:
+                check(ls_cache_reorder(self.cache[s], self.cache[n], par, t, stream=stream), "ls_cache_reorder")
         self.cur = n
         self._last = (tok, par)
         return n
+
+    def current_cache(self):
+        """The cache buffer holding the latest step's refresh."""
+        return self.cache[0] if self.inplace else self.cache[self.cur]
 
     def outputs(self, idx: int | None = None):
         """The last step's tokens and parents with the beam state of set idx (default: the current one)."""
