@@ -371,7 +371,13 @@ ls_status ls_cache_refresh_inplace(void* cache, ls_dtype dtype, const int32_t* p
   const long long stage = tma ? kIpTmaStage : kIpStageBytes;
   const long long tile = (stage / k) / unit * unit;  // every row's tile fits one staging buffer
   p.tile_bytes = (int)(tile < slab_bytes ? tile : slab_bytes);
-  const long long items = tma ? units * ((slab_bytes + p.tile_bytes - 1) / p.tile_bytes) : units;
+  // short slabs: the bulk-copy kernel moves as many heads of a (layer, batch) as fit at once
+  long long hg = slab_bytes <= tile ? stage / ((long long)k * slab_bytes) : 1;
+  hg = hg < 1 ? 1 : (hg > heads ? heads : hg);
+  p.heads_per_item = (int)hg;
+  const long long items = tma ? (long long)layers * batch * ((heads + hg - 1) / hg) *
+                                    ((slab_bytes + p.tile_bytes - 1) / p.tile_bytes)
+                              : units;
   const long long grid_full = (long long)di->sms * occ;
   const long long grid = items < grid_full ? items : grid_full;
   const cudaError_t e = tma ? launch_cache_inplace_tma(p, (int)grid, st) : launch_cache_inplace(p, unit, (int)grid, st);

@@ -151,7 +151,10 @@ __global__ void __launch_bounds__(32) cache_inplace_tma_kernel(const InplacePara
   __syncwarp();
   if (lane != 0) return;  // lane 0 drives every copy from here on
 
-  const long long bh = (long long)p.batch * p.heads;
+  // an item: heads [h0, h0 + hg) of one (layer, batch), or one tile of one head's slabs
+  const int HG = p.heads_per_item;
+  const long long groups = (p.heads + HG - 1) / HG;
+  const long long bg = (long long)p.batch * groups;
   const long long ntiles = (p.slab_bytes + p.tile_bytes - 1) / p.tile_bytes;
   uint32_t uses[2] = {0u, 0u};
   int cur = 0;
@@ -160,7 +163,7 @@ __global__ void __launch_bounds__(32) cache_inplace_tma_kernel(const InplacePara
   bool have_prev = false;
   unsigned char* pv_base = nullptr;
   unsigned long long pv_changed = 0, pv_needed = 0;
-  int pv_b = 0, pv_tb = 0, pv_buf = 0;
+  int pv_b = 0, pv_tb = 0, pv_buf = 0, pv_hg = 0;
   uint32_t pv_parity = 0;
 
   auto finish_prev = [&]() {
@@ -174,18 +177,21 @@ __global__ void __launch_bounds__(32) cache_inplace_tma_kernel(const InplacePara
       if (!((pv_changed >> j) & 1ull)) continue;
       const int q = par_s[pv_b * K + j];
       const int slot = __popcll(pv_needed & ((1ull << q) - 1ull));
-      bulk_store(pv_base + (size_t)j * p.row_stride, smem_addr(src + (size_t)slot * pv_tb), (uint32_t)pv_tb);
+      for (int hh = 0; hh < pv_hg; ++hh)
+        bulk_store(pv_base + (size_t)j * p.row_stride + (size_t)hh * p.slab_stride,
+                   smem_addr(src + ((size_t)slot * pv_hg + hh) * pv_tb), (uint32_t)pv_tb);
     }
     bulk_commit();
   };
 
-  for (long long it = blockIdx.x; it < p.units * ntiles && !aborted; it += gridDim.x) {
+  for (long long it = blockIdx.x; it < (long long)p.layers * bg * ntiles && !aborted; it += gridDim.x) {
     const long long unit = it / ntiles;
     const long long tile = it - unit * ntiles;
-    const int l = (int)(unit / bh);
-    const long long rem = unit - (long long)l * bh;
-    const int b = (int)(rem / p.heads);
-    const int h = (int)(rem - (long long)b * p.heads);
+    const int l = (int)(unit / bg);
+    const long long rem = unit - (long long)l * bg;
+    const int b = (int)(rem / groups);
+    const int h0 = (int)(rem - (long long)b * groups) * HG;
+    const int hg = min(HG, p.heads - h0);
     unsigned long long changed = 0, needed = 0;
     for (int j = 0; j < K; ++j) {
       const int q = par_s[b * K + j];
@@ -200,16 +206,18 @@ __global__ void __launch_bounds__(32) cache_inplace_tma_kernel(const InplacePara
     const long long t0 = tile * p.tile_bytes;
     const int tb = (int)min((long long)p.tile_bytes, p.slab_bytes - t0);
     unsigned char* base = p.cache + (size_t)l * p.layer_stride + (size_t)b * K * p.row_stride +
-                          (size_t)h * p.slab_stride + t0;
+                          (size_t)h0 * p.slab_stride + t0;
     // buffer `cur` was last read by the stores of the item before the previous one
     bulk_wait_read<0>();
     const uint32_t b_addr = smem_addr(&bar[cur]);
-    mbar_arrive_expect_tx(b_addr, (uint32_t)(__popcll(needed) * tb));
+    mbar_arrive_expect_tx(b_addr, (uint32_t)(__popcll(needed) * hg * tb));
     unsigned char* dst = tsm + (size_t)cur * kIpTmaStage;
     int slot = 0;
     for (int q = 0; q < K; ++q) {
       if (!((needed >> q) & 1ull)) continue;
-      bulk_load_plain(smem_addr(dst + (size_t)slot * tb), base + (size_t)q * p.row_stride, (uint32_t)tb, b_addr);
+      for (int hh = 0; hh < hg; ++hh)
+        bulk_load_plain(smem_addr(dst + ((size_t)slot * hg + hh) * tb),
+                        base + (size_t)q * p.row_stride + (size_t)hh * p.slab_stride, (uint32_t)tb, b_addr);
       ++slot;
     }
     if (have_prev) finish_prev();
@@ -219,6 +227,7 @@ __global__ void __launch_bounds__(32) cache_inplace_tma_kernel(const InplacePara
     pv_needed = needed;
     pv_b = b;
     pv_tb = tb;
+    pv_hg = hg;
     pv_buf = cur;
     pv_parity = uses[cur] & 1u;
     ++uses[cur];

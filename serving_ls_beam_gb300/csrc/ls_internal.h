@@ -196,7 +196,8 @@ struct InplaceParams {
   long long spin_limit_ns;  // bounded waits of the bulk-copy kernel
   long long layer_stride, row_stride, slab_stride;  // bytes
   long long slab_bytes;   // len * head_dim * es
-  int tile_bytes;         // positions staged at a time, in bytes (<= kIpStageBytes / k)
+  int tile_bytes;         // positions staged at a time, in bytes (<= stage / k)
+  int heads_per_item;     // bulk-copy kernel: heads of one (layer, batch) moved together
   int batch, k, heads, layers;
   long long units;        // layers * batch * heads
 };

@@ -59,6 +59,8 @@ CASES = [  # (dtype, layers, batch, k, heads, max_len, len, head_dim)
     ("bf16", 2, 5, 3, 4, 8, 8, 7),
     ("f16", 1, 4, 64, 2, 64, 64, 64),  # 64 rows of 8 KB slabs: staged in tiles
     ("f32", 2, 3, 5, 1, 10, 1, 16),
+    ("f16", 1, 3, 4, 16, 64, 20, 64),  # short slabs: 3 heads per item, a last group of 1
+    ("f16", 2, 5, 4, 7, 64, 3, 64),    # all 7 heads in one item
 ]
 
 
