@@ -236,6 +236,19 @@ def cpu_baseline(w: synth.Workload, target_s: float = 12.0):
 
 
 # ------------------------------------------------------------------ GPU arm
+def workload_config(w: synth.Workload, T: int, world: int) -> dict:
+    """The `config` object of the JSON line (the same for both arms)."""
+    return {"workload": f"{w.name}: batch {w.batch}, beam {w.k}, vocab {w.vocab}, {w.dtype} logits, "
+                        f"{T} decode step(s)" + (f", KV cache {[w.kv_shape[0], w.rows, *w.kv_shape[1:]]} fp16 "
+                                                 f"refreshed by parent (len = step), in place" if w.kv_shape else ""),
+            "batch": w.batch, "beam": w.k, "vocab": w.vocab, "logit_dtype": w.dtype, "decode_steps_per_step": T,
+            "l2": f"inputs larger than L2: {T * w.rows * w.vocab * (2 if w.dtype != 'f32' else 4) / 1e9:.2f} GB of "
+                  f"logits per benchmark step",
+            "graph": f"one CUDA graph of the {T}-step loop and the end-of-search backtrack",
+            "cache_refresh": "in place, copy on change (out-of-place figures under cache_refresh_out_of_place)",
+            "parallelism": f"replicas x{world} (independent batches)"}
+
+
 def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
     import torch
 
@@ -451,14 +464,7 @@ def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
         sampling = bench_sampling(dev, peak)
 
     clocks = clk.summary()
-    cfg = {"workload": f"{wr.name}: batch {B}, beam {K}, vocab {V}, {wr.dtype} logits, "
-                       f"{T} decode step(s)" + (f", KV cache {[wr.kv_shape[0], wr.rows, *wr.kv_shape[1:]]} fp16 "
-                                                f"refreshed by parent (len = step), in place" if wr.kv_shape else ""),
-           "batch": B, "beam": K, "vocab": V, "logit_dtype": wr.dtype, "decode_steps_per_step": T,
-           "l2": f"inputs larger than L2: {host_logits.nbytes / 1e9:.2f} GB of logits per benchmark step",
-           "graph": f"one CUDA graph of the {T}-step loop and the end-of-search backtrack",
-           "cache_refresh": "in place, copy on change (out-of-place figures under cache_refresh_out_of_place)",
-           "parallelism": f"replicas x{world} (independent batches)"}
+    cfg = workload_config(wr, T, world)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -521,23 +527,25 @@ def bench_sampling(dev, peak, calls: int = 16):
 
 
 def bench_e2e(args, wr, loop, host_logits, bias_np, beam0, fin0, lens, dev, world):
-    """Logits copied from pinned host memory each decode step (copy stream, double-buffered),
-    outputs read back each step; the all-finished stop is checked one step behind."""
+    """Logits copied from pinned host memory each decode step (copy stream, NBUF device buffers),
+    outputs read back each step; the all-finished stop is checked LAG steps behind, so the copy of
+    a step's logits overlaps the compute of the steps before it."""
     import torch
 
     import serving_ls_beam_gb300 as lsb
 
     T = host_logits.shape[0]
     pinned = torch.from_numpy(host_logits).pin_memory()
-    bufs = [torch.empty(pinned.shape[1:], dtype=pinned.dtype, device=dev) for _ in range(2)]
+    NBUF, LAG = 3, 2
+    bufs = [torch.empty(pinned.shape[1:], dtype=pinned.dtype, device=dev) for _ in range(NBUF)]
     d_bias = None if bias_np is None else torch.from_numpy(bias_np).to(dev)
     out_host = {key: torch.empty((T,) + tuple(loop.token[0].shape), dtype=dt).pin_memory()
                 for key, dt in (("token", torch.int32), ("parent", torch.int32), ("score", torch.float32),
                                 ("finished", torch.uint8))}
     comp = torch.cuda.current_stream(dev)
     copy = torch.cuda.Stream(device=dev)
-    h2d_done = [torch.cuda.Event() for _ in range(2)]
-    buf_free = [torch.cuda.Event() for _ in range(2)]
+    h2d_done = [torch.cuda.Event() for _ in range(NBUF)]
+    buf_free = [torch.cuda.Event() for _ in range(NBUF)]
     d2h_done = [torch.cuda.Event() for _ in range(T)]
     seq_host = torch.empty(wr.batch * wr.k * T, dtype=torch.int32).pin_memory()
     len_host = torch.empty((wr.batch, wr.k), dtype=torch.int32).pin_memory()
@@ -546,9 +554,9 @@ def bench_e2e(args, wr, loop, host_logits, bias_np, beam0, fin0, lens, dev, worl
         loop.reset(beam0, fin0)
         stop = T
         for t in range(T):
-            i = t % 2
+            i = t % NBUF
             with torch.cuda.stream(copy):
-                if t >= 2:
+                if t >= NBUF:
                     copy.wait_event(buf_free[i])
                 bufs[i].copy_(pinned[t], non_blocking=True)
                 h2d_done[i].record(copy)
@@ -559,10 +567,10 @@ def bench_e2e(args, wr, loop, host_logits, bias_np, beam0, fin0, lens, dev, worl
             for key in out_host:
                 out_host[key][t].copy_(o[key], non_blocking=True)
             d2h_done[t].record(comp)
-            if t >= 1:
-                d2h_done[t - 1].synchronize()
-                if bool(out_host["finished"][t - 1].all()):
-                    stop = t
+            if t >= LAG:
+                d2h_done[t - LAG].synchronize()
+                if bool(out_host["finished"][t - LAG].all()):
+                    stop = t + 1  # the steps already enqueued have run
                     break
         # the search's result: every final beam's token sequence, read back to the host
         seq, ln = loop.finalize(stop)
@@ -588,8 +596,9 @@ def bench_e2e(args, wr, loop, host_logits, bias_np, beam0, fin0, lens, dev, worl
     d2h_final = (wr.batch * wr.k * T + wr.batch * wr.k) * 4
     return {"value": steps_done * world / dt, "unit": UNIT, "h2d_bytes_per_step": h2d * T,
             "d2h_bytes_per_step": d2h * T + d2h_final, "decode_steps_run": steps_done,
-            "note": "per benchmark step (all decode steps): logits H2D from pinned memory every decode step, "
-                    "outputs D2H every decode step, final token sequences D2H at the end, wall clock"}
+            "note": "per benchmark step (all decode steps): logits H2D from pinned memory every decode step "
+                    "(3 device buffers, copy stream), outputs D2H every decode step, the all-finished stop checked "
+                    "2 steps behind, final token sequences D2H at the end, wall clock"}
 
 
 def bench_reference(args, w: synth.Workload):
@@ -612,7 +621,7 @@ def bench_reference(args, w: synth.Workload):
     return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": per * w.batch * T * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic (seeded generators)", "impl": "reference",
-            "config": {"workload": w.name, "batch": w.batch, "beam": w.k, "vocab": w.vocab},
+            "config": workload_config(w, T, 1),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
