@@ -213,6 +213,9 @@ __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepPar
   // the fine-rank kernel may be scheduled from now on: its CTAs take the SM space this
   // grid's CTAs free as they finish, and wait for the whole grid before reading its output
   grid_launch_dependents();
+  // this grid may itself start while the previous kernel of the stream finishes (the cache
+  // refresh of the previous decode step): wait for it before reading any input
+  grid_dependency_wait();
 
   auto row_of = [&](int u) -> int { return (int)fast_div((uint32_t)u, p.nc_magic, p.nc_shift); };
   auto live = [&](int u) -> bool { return !(p.finished && p.finished[row_of(u)]); };
@@ -561,8 +564,8 @@ __global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepPar
 template <int DT, bool BIAS, int VPL>
 cudaError_t launch_t(const StepParams& p, int grid, cudaStream_t stream) {
   const size_t smem = beam_rows_smem_bytes(VPL);
-  beam_rows_kernel<DT, BIAS, VPL><<<grid, kRowThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  PdlLaunch l(dim3((unsigned)grid), dim3(kRowThreads), smem, stream);
+  return cudaLaunchKernelEx(&l.cfg, beam_rows_kernel<DT, BIAS, VPL>, p);
 }
 
 template <int DT, bool BIAS, int VPL>

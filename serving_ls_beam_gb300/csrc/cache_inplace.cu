@@ -12,6 +12,7 @@
 // rows that are both read and overwritten (swaps, cycles) need no ordering and no global
 // temporary.  Slabs longer than the staging space are done a tile of positions at a time.
 #include "ls_device.cuh"
+#include "ls_dtype.cuh"
 #include "ls_internal.h"
 
 namespace lsb {
@@ -58,6 +59,8 @@ __global__ void __launch_bounds__(kIpThreads) cache_inplace_kernel(const Inplace
   __shared__ IpShared sh;
   const int K = p.k, tid = threadIdx.x;
   const long long bh = (long long)p.batch * p.heads;
+  grid_launch_dependents();
+  grid_dependency_wait();  // the parents come from the beam step just before
   for (long long unit = blockIdx.x; unit < p.units; unit += gridDim.x) {
     const int l = (int)(unit / bh);
     const long long rem = unit - (long long)l * bh;
@@ -142,6 +145,8 @@ __global__ void __launch_bounds__(32) cache_inplace_tma_kernel(const InplacePara
   __shared__ __align__(8) unsigned long long bar[2];
   const int K = p.k, lane = threadIdx.x;
   int* par_s = reinterpret_cast<int*>(tsm + 2 * (size_t)kIpTmaStage);
+  grid_launch_dependents();
+  grid_dependency_wait();  // the parents come from the beam step just before
   for (int i = lane; i < p.batch * K; i += 32) par_s[i] = __ldg(p.parent + i);
   if (lane == 0) {
     mbar_init(smem_addr(&bar[0]), 1);
@@ -246,8 +251,8 @@ __global__ void __launch_bounds__(32) cache_inplace_tma_kernel(const InplacePara
 
 template <int UNIT>
 cudaError_t launch_u(const InplaceParams& p, int grid, size_t smem, cudaStream_t stream) {
-  cache_inplace_kernel<UNIT><<<grid, kIpThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  PdlLaunch l(dim3((unsigned)grid), dim3(kIpThreads), smem, stream);
+  return cudaLaunchKernelEx(&l.cfg, cache_inplace_kernel<UNIT>, p);
 }
 
 template <int UNIT>
@@ -265,8 +270,8 @@ size_t cache_inplace_tma_smem(int batch, int k) {
 }
 
 cudaError_t launch_cache_inplace_tma(const InplaceParams& p, int grid, cudaStream_t stream) {
-  cache_inplace_tma_kernel<<<grid, 32, cache_inplace_tma_smem(p.batch, p.k), stream>>>(p);
-  return cudaGetLastError();
+  PdlLaunch l(dim3((unsigned)grid), dim3(32), cache_inplace_tma_smem(p.batch, p.k), stream);
+  return cudaLaunchKernelEx(&l.cfg, cache_inplace_tma_kernel, p);
 }
 
 cudaError_t cache_inplace_tma_occupancy(int batch, int k, int* occ) {

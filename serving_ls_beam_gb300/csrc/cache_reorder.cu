@@ -8,6 +8,7 @@
 // slabs of len*head_dim elements at a fixed stride, copied as UNIT-byte words with
 // several independent loads in flight per thread before the stores.
 #include "ls_device.cuh"
+#include "ls_dtype.cuh"
 #include "ls_internal.h"
 
 namespace lsb {
@@ -43,6 +44,8 @@ template <int UNIT>
 __global__ void __launch_bounds__(kCopyThreads) cache_reorder_kernel(const ReorderParams p) {
   using W = typename Word<UNIT>::T;
   const uint32_t per_pair = (uint32_t)p.slab_units * (uint32_t)p.heads;
+  grid_launch_dependents();
+  grid_dependency_wait();  // the parents come from the beam step just before
   for (long long pair = blockIdx.x; pair < p.pairs; pair += gridDim.x) {
     const int l = (int)(pair / p.rows);
     const int r = (int)(pair - (long long)l * p.rows);
@@ -76,8 +79,8 @@ __global__ void __launch_bounds__(kCopyThreads) cache_reorder_kernel(const Reord
 
 template <int UNIT>
 cudaError_t launch_u(const ReorderParams& p, int grid, cudaStream_t stream) {
-  cache_reorder_kernel<UNIT><<<grid, kCopyThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  PdlLaunch l(dim3((unsigned)grid), dim3(kCopyThreads), 0, stream);
+  return cudaLaunchKernelEx(&l.cfg, cache_reorder_kernel<UNIT>, p);
 }
 
 template <int UNIT>

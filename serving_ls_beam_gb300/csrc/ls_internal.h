@@ -202,6 +202,24 @@ struct InplaceParams {
   long long units;        // layers * batch * heads
 };
 
+// Launch configuration with programmatic dependent launch: the kernel may be scheduled
+// while the previous kernel of the stream finishes; it must call griddepcontrol.wait
+// before touching anything that kernel (or any earlier work) writes.
+struct PdlLaunch {
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  PdlLaunch(dim3 grid, dim3 block, size_t smem, cudaStream_t stream) : cfg{}, attr{} {
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+};
+
 // Launchers (defined next to their kernels).
 size_t beam_rows_smem_bytes(int vpl);
 cudaError_t beam_rows_config(int dtype, bool bias, int vpl, int* occupancy);
