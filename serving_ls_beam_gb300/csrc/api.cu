@@ -23,7 +23,7 @@ struct DeviceInfo {
   int sms = 0;
   bool select_ready = false;  // K2's dynamic shared-memory limit raised
   // K1 occupancy per [dtype][bias][vpl index]; 0 = not configured yet
-  int step_occ[3][2][2] = {};
+  int step_occ[3][2][3] = {};
   int copy_occ[5] = {};
   int inplace_occ[5] = {};
   int inplace_tma_occ = 0;
@@ -33,7 +33,7 @@ struct DeviceInfo {
 std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
 
-int vpl_index(int vpl) { return vpl == 4 ? 0 : (vpl == 8 ? 1 : -1); }
+int vpl_index(int vpl) { return vpl == 4 ? 0 : (vpl == 8 ? 1 : (vpl == 16 ? 2 : -1)); }
 int unit_index(int unit) { return unit == 16 ? 0 : unit == 8 ? 1 : unit == 4 ? 2 : unit == 2 ? 3 : 4; }
 
 struct Debug {
@@ -43,7 +43,7 @@ struct Debug {
   bool check_ptrs = true;
 };
 
-// LS_BEAM_DEBUG: comma-separated "exact", "ipplain", "spin=<ns>", "vpl=<4|8>", "nocheck".
+// LS_BEAM_DEBUG: comma-separated "exact", "ipplain", "spin=<ns>", "vpl=<4|8|16>", "nocheck".
 Debug read_debug() {
   Debug d;
   const char* env = std::getenv("LS_BEAM_DEBUG");

@@ -33,10 +33,13 @@
 namespace lsb {
 namespace {
 
-constexpr int kStages = 2;
+// stages of a warp's ring: two for chunks up to 4 KB, one for 8 KB chunks (the other warps
+// of the SM hide the load latency; the shared memory per warp stays 8 KB)
+__host__ __device__ constexpr int stages_for(int vpl) { return vpl >= 16 ? 1 : 2; }
+constexpr int kStagesMax = 2;
 constexpr long long kDrainLimitNs = 2000000000LL;  // 2 s for copies already in flight
 // shared-memory layout: [mbarriers | per-warp item lists | stage buffers]
-static_assert(kRowWarps * kStages * 8 <= kRowListOff, "mbarriers overlap the item lists");
+static_assert(kRowWarps * kStagesMax * 8 <= kRowListOff, "mbarriers overlap the item lists");
 static_assert(kRowBarBytes % 16 == 0, "stage buffers must be 16-byte aligned for bulk copies");
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -187,7 +190,8 @@ __device__ __forceinline__ float vec_elem(const uint4& d, int e) {
 }
 
 template <int DT, bool BIAS, int VPL>
-__global__ void __launch_bounds__(kRowThreads, 3) beam_rows_kernel(const StepParams p) {
+__global__ void __launch_bounds__(kRowThreads, VPL >= 16 ? 2 : 3) beam_rows_kernel(const StepParams p) {
+  constexpr int kStages = stages_for(VPL);
   constexpr int VEC = Traits<DT>::kVec;
   constexpr int ES = Traits<DT>::kBytes;
   constexpr int CV = 32 * VPL;  // vectors per chunk
@@ -582,6 +586,7 @@ cudaError_t dispatch_vpl(bool launch, const StepParams* p, int vpl, int grid, cu
   switch (vpl) {
     case 4: return launch ? launch_t<DT, BIAS, 4>(*p, grid, stream) : config_t<DT, BIAS, 4>(occ);
     case 8: return launch ? launch_t<DT, BIAS, 8>(*p, grid, stream) : config_t<DT, BIAS, 8>(occ);
+    case 16: return launch ? launch_t<DT, BIAS, 16>(*p, grid, stream) : config_t<DT, BIAS, 16>(occ);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -604,7 +609,9 @@ cudaError_t dispatch(bool launch, const StepParams* p, int dtype, bool bias, int
 
 }  // namespace
 
-size_t beam_rows_smem_bytes(int vpl) { return kRowBarBytes + (size_t)kRowWarps * kStages * 32 * vpl * 16; }
+size_t beam_rows_smem_bytes(int vpl) {
+  return kRowBarBytes + (size_t)kRowWarps * stages_for(vpl) * 32 * vpl * 16;
+}
 
 cudaError_t beam_rows_config(int dtype, bool bias, int vpl, int* occupancy) {
   return dispatch(false, nullptr, dtype, bias, vpl, 0, nullptr, occupancy);
