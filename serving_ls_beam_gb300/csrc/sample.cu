@@ -211,8 +211,14 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_select_kernel(const Sa
     // 1. (max, sum of exp) and the group maxima over the row's chunks
     float m = -INFINITY, s = 0.0f;
     bool ovf = false;
+    // G <= 8: the group maxima in registers (two vector loads per chunk, then a shuffle
+    // tree); more groups go through shared-memory atomics
+    float g8[8];
+#pragma unroll
+    for (int g = 0; g < 8; ++g) g8[g] = -INFINITY;
     for (int c = lane; c < nc; c += 32) {
-      const float4 h = __ldcg(reinterpret_cast<const float4*>(rec(c)));
+      const float4* r4 = reinterpret_cast<const float4*>(rec(c));
+      const float4 h = __ldcg(r4);
       const int cnt = __float_as_int(h.x);
       ovf |= cnt > C;
       merge_ms(m, s, h.y, h.z);
@@ -220,7 +226,20 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_select_kernel(const Sa
         sm.cm[w][c] = h.y;
         sm.cn[w][c] = cnt;
       }
-      for (int g = 0; g < G; ++g) atomicMax(&sm.gmax[w][g], float_ord(__ldcg(rec(c) + 4 + g)));
+      if (G <= 8) {
+        const float4 ga = __ldcg(r4 + 1);
+        const float4 gb = G > 4 ? __ldcg(r4 + 2) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        g8[0] = fmaxf(g8[0], ga.x);
+        g8[1] = fmaxf(g8[1], ga.y);
+        g8[2] = fmaxf(g8[2], ga.z);
+        g8[3] = fmaxf(g8[3], ga.w);
+        g8[4] = fmaxf(g8[4], gb.x);
+        g8[5] = fmaxf(g8[5], gb.y);
+        g8[6] = fmaxf(g8[6], gb.z);
+        g8[7] = fmaxf(g8[7], gb.w);
+      } else {
+        for (int g = 0; g < G; ++g) atomicMax(&sm.gmax[w][g], float_ord(__ldcg(rec(c) + 4 + g)));
+      }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -229,10 +248,24 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_select_kernel(const Sa
       merge_ms(m, s, mo, so);
     }
     ovf = __any_sync(0xffffffffu, ovf);
-    __syncwarp();
+    float a, b;
+    if (G <= 8) {
+#pragma unroll 1
+      for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+        for (int g = 0; g < 8; ++g) g8[g] = fmaxf(g8[g], __shfl_xor_sync(0xffffffffu, g8[g], o));
+      }
+      float v = g8[0];
+#pragma unroll
+      for (int g = 1; g < 8; ++g) v = lane == g ? g8[g] : v;
+      a = lane < G ? v : -INFINITY;
+      b = -INFINITY;
+    } else {
+      __syncwarp();
+      a = lane < G ? ord_float(sm.gmax[w][lane]) : -INFINITY;
+      b = lane + 32 < G ? ord_float(sm.gmax[w][lane + 32]) : -INFINITY;
+    }
     // R-top-k: the k-th largest of the G group maxima (ties by group index)
-    const float a = lane < G ? ord_float(sm.gmax[w][lane]) : -INFINITY;
-    const float b = lane + 32 < G ? ord_float(sm.gmax[w][lane + 32]) : -INFINITY;
     int ra = 0, rb = 0;
 #pragma unroll 1
     for (int q = 0; q < min(G, 32); ++q) {
