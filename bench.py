@@ -454,6 +454,14 @@ def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback"
     step_gbs = (k1_bytes + k4_bytes) / (ms_plain / args.steps / 1e3) / 1e9
 
+    # ---- candidate statistics of the last decode step of the timed search (read after timing)
+    _, _, ncand, path = lsb.ls_read_row_stats(loop.workspace, B, K, V)
+    live = ncand >= 0
+    cand = {"per_beam_mean": float(ncand[live].mean()) if live.any() else None,
+            "per_batch_mean": float(np.where(live, ncand, 0).sum(axis=1).mean()),
+            "exact_path_batches": int((path != 0).sum()), "batches": int(B),
+            "note": "survivors of each beam's R-top-k at the last decode step (the queue the fine rank sorts)"}
+
     # ---- end to end through the C ABI with host buffers
     e2e = None
     if not args.no_e2e:
@@ -472,6 +480,7 @@ def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
         "logit_gbs": k1_gbs, "step_gbs": step_gbs, "step_roofline_frac": step_gbs / peak,
         "roofline": roof, "roofline_kernels": kern, "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks, "e2e": e2e, "sampling": sampling, "cache_refresh_out_of_place": oop_line,
+        "candidates": cand,
         "setup_s": round(setup_s, 1),
     }
     return line
