@@ -28,7 +28,7 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2}
+DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2, "f64": 3}
 
 
 def build(force: bool = False) -> str:
@@ -62,6 +62,8 @@ def _load():
             lib.oracle_sample.restype = ip
             lib.oracle_cache_refresh_inplace.argtypes = [vp, ip, vp, ip, ip, ip, ip, ip, ip, ip]
             lib.oracle_cache_refresh_inplace.restype = ip
+            lib.oracle_logits.argtypes = [vp, vp, ip, ip, ip, ip, vp]
+            lib.oracle_logits.restype = ip
             _lib = lib
     return _lib
 
@@ -71,6 +73,8 @@ def _ptr(a):
 
 
 def _logit_code(logits: np.ndarray, dtype: str | None) -> tuple[np.ndarray, int]:
+    if logits.dtype == np.float64:
+        return np.ascontiguousarray(logits), DTYPE_CODES["f64"]
     if logits.dtype == np.float32:
         return np.ascontiguousarray(logits), DTYPE_CODES["f32"]
     if logits.dtype == np.float16:
@@ -186,3 +190,33 @@ def cache_refresh_inplace(cache, parent, length):
     if rc != 0:
         raise ValueError(f"oracle_cache_refresh_inplace failed ({rc})")
     return out
+
+
+def logits(hidden, weight, dtype=None):
+    """Output projection in double: x[r, v] = sum_d hidden[r, d] * weight[v, d].
+    hidden [rows, dim], weight [vocab, dim]: float32, float16, or uint16 bits with dtype 'f16' / 'bf16'.
+    Returns float64 [rows, vocab]."""
+    lib = _load()
+    h, code = _logit_code(np.asarray(hidden), dtype)
+    w, wcode = _logit_code(np.asarray(weight), dtype)
+    if code != wcode or code == DTYPE_CODES["f64"]:
+        raise TypeError("hidden and weight need one element type (f32, f16 or bf16)")
+    rows, dim = h.shape
+    vocab, dim_w = w.shape
+    if dim_w != dim:
+        raise ValueError(f"hidden dim {dim} != weight dim {dim_w}")
+    out = np.empty((rows, vocab), np.float64)
+    rc = lib.oracle_logits(_ptr(h), _ptr(w), code, rows, vocab, dim, _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle_logits failed ({rc})")
+    return out
+
+
+def logits_beam_step(hidden, weight, beam_scores, *, dtype=None, bias=None, finished=None, eos_id=0, m_out=None):
+    """Beam step on the projection's logits: hidden [batch, k, dim], weight [vocab, dim].
+    The logits are those of logits() (double); the step is beam_step() on them."""
+    hd = np.asarray(hidden)
+    batch, k, dim = hd.shape
+    x = logits(hd.reshape(batch * k, dim), weight, dtype)
+    return beam_step(x.reshape(batch, k, -1), beam_scores, bias=bias, finished=finished, eos_id=eos_id,
+                     m_out=m_out)

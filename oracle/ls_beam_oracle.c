@@ -40,6 +40,7 @@
 #define ORC_F32 0
 #define ORC_F16 1
 #define ORC_BF16 2
+#define ORC_F64 3 /* logits already in double (the output projection below) */
 
 /* IEEE 754 binary16: sign, 5-bit biased exponent, 10-bit fraction. */
 static double orc_half_to_double(uint16_t h) {
@@ -68,6 +69,7 @@ static double orc_logit(const void* logits, int dtype, size_t idx) {
   switch (dtype) {
     case ORC_F32: return (double)((const float*)logits)[idx];
     case ORC_F16: return orc_half_to_double(((const uint16_t*)logits)[idx]);
+    case ORC_F64: return ((const double*)logits)[idx];
     default: return orc_bf16_to_double(((const uint16_t*)logits)[idx]);
   }
 }
@@ -124,7 +126,7 @@ int oracle_beam_step(const void* logits, int dtype, const float* bias, const flo
   if (!logits || !beam_scores || !out_token || !out_parent || !out_score || !out_finished)
     return -1;
   if (batch < 0 || k < 1 || vocab < 1 || m_out < 1 || eos_id < 0 || eos_id >= vocab) return -1;
-  if (dtype != ORC_F32 && dtype != ORC_F16 && dtype != ORC_BF16) return -1;
+  if (dtype != ORC_F32 && dtype != ORC_F16 && dtype != ORC_BF16 && dtype != ORC_F64) return -1;
   size_t ncap = (size_t)k * (size_t)vocab;
   orc_cand* cand = (orc_cand*)malloc(ncap * sizeof(orc_cand));
   double* x = (double*)malloc((size_t)vocab * sizeof(double));
@@ -176,6 +178,34 @@ int oracle_beam_step(const void* logits, int dtype, const float* bias, const flo
   }
   free(cand);
   free(x);
+  return 0;
+}
+
+/*
+ * The step before the beam step: the decoder's output projection, whose result is
+ * the logit tensor the article's first traversal reads.  logits = hidden . weight^T:
+ *   x[r, v] = sum_d hidden[r, d] * weight[v, d]
+ * hidden [rows, dim] and weight [vocab, dim] (the projection matrix, one row per token)
+ * hold dtype 0 f32, 1 f16 bits or 2 bf16 bits; out [rows, vocab] is double.  The
+ * inputs decode exactly to double, their products are exact in double (at most 48
+ * significant bits), and the dim products are summed in order d = 0, 1, ...
+ * Returns 0, or -1 on bad arguments.
+ */
+int oracle_logits(const void* hidden, const void* weight, int dtype, int rows, int vocab, int dim,
+                  double* out) {
+  if (!hidden || !weight || !out || rows < 0 || vocab < 0 || dim < 0) return -1;
+  if (dtype != ORC_F32 && dtype != ORC_F16 && dtype != ORC_BF16) return -1;
+  double* h = (double*)malloc(((size_t)dim + 1) * sizeof(double));
+  if (!h) return -2;
+  for (int r = 0; r < rows; ++r) {
+    for (int d = 0; d < dim; ++d) h[d] = orc_logit(hidden, dtype, (size_t)r * dim + d);
+    for (int v = 0; v < vocab; ++v) {
+      double acc = 0.0;
+      for (int d = 0; d < dim; ++d) acc += h[d] * orc_logit(weight, dtype, (size_t)v * dim + d);
+      out[(size_t)r * vocab + v] = acc;
+    }
+  }
+  free(h);
   return 0;
 }
 
