@@ -164,13 +164,22 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def source_hash() -> str:
+# the sources each recorded kernel's traffic depends on: its own kernels plus the shared
+# launch code and headers (a change to any of them makes the recorded counters stale)
+KERNEL_SOURCES = {
+    "beam_step": ("beam_rows.cu", "beam_select.cu"),
+    "cache_refresh_inplace": ("cache_inplace.cu",),
+    "cache_reorder": ("cache_reorder.cu",),
+}
+SHARED_SOURCES = ("api.cu", "ls_internal.h", "ls_device.cuh", "ls_dtype.cuh")
+
+
+def source_hash(kernel: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "serving_ls_beam_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, fn), "rb") as f:
-                h.update(f.read())
+    for fn in SHARED_SOURCES + KERNEL_SOURCES[kernel]:
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
@@ -184,7 +193,7 @@ def recorded_traffic(kernel: str, workload: str):
                     continue
                 parts = ln.split()
                 if len(parts) >= 4 and parts[0] == kernel and parts[1] == workload:
-                    return float(parts[2]) if parts[3] == source_hash() else None
+                    return float(parts[2]) if parts[3] == source_hash(kernel) else None
     except OSError:
         return None
     return None

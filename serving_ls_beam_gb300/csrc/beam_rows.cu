@@ -360,16 +360,24 @@ __global__ void __launch_bounds__(kRowThreads, VPL >= 16 ? 2 : 3) beam_rows_kern
     const float m0 = bits_max_float<BT>(b0);  // even vectors (group lane when G = 64)
     const float m1 = VPL > 1 ? bits_max_float<BT>(b1) : -INFINITY;  // odd vectors (group lane + 32)
     const float mt = fmaxf(m0, m1);
-    const float M = warp_max(mt);
-    // group maxima and the chunk's R-top-k
+    // group maxima, the chunk max M and the chunk's R-top-k
     float* rec = reinterpret_cast<float*>(p.rec + (size_t)u * p.rec_stride);
-    float rt;
+    float M, rt;
     if (G <= 32) {
       float gmv = mt;
       for (int o = 16; o >= G; o >>= 1) gmv = fmaxf(gmv, __shfl_xor_sync(0xffffffffu, gmv, o));
       if (lane < G) rec[4 + lane] = gmv;
-      rt = warp_kth_of_lanes(gmv, G, K);
+      // the remaining levels of the same tree give the chunk max and the least group max,
+      // which is the k-th largest of the G group maxima when G = k
+      float mx = gmv, mn = gmv;
+      for (int o = G >> 1; o > 0; o >>= 1) {
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      }
+      M = mx;
+      rt = (G == K) ? mn : warp_kth_of_lanes(gmv, G, K);
     } else {
+      M = warp_max(mt);
       rec[4 + lane] = m0;
       rec[4 + 32 + lane] = m1;
       rt = warp_kth_of_64(m0, m1, K);

@@ -361,18 +361,26 @@ __device__ __forceinline__ int queue_select(const StepParams& p, SelSmem& sm, un
 #pragma unroll
         for (int g = 0; g < 8; ++g) g8[g] = fmaxf(g8[g], __shfl_xor_sync(0xffffffffu, g8[g], o));
       }
-      // lane g < G holds group max g; R = the k-th largest (ties by group index)
-      float v = g8[0];
+      // every lane holds the G group maxima; R = the k-th largest of them
+      float R = g8[0];
+      if (G == K) {
+        // k group maxima: the k-th largest is the least one
 #pragma unroll
-      for (int g = 1; g < 8; ++g) v = lane == g ? g8[g] : v;
-      int rank = 0;
+        for (int g = 1; g < 8; ++g) R = g < G ? fminf(R, g8[g]) : R;
+      } else {
+        // lane g < G takes group max g and counts the larger ones (ties by group index)
+        float v = g8[0];
+#pragma unroll
+        for (int g = 1; g < 8; ++g) v = lane == g ? g8[g] : v;
+        int rank = 0;
 #pragma unroll 1
-      for (int q = 0; q < G; ++q) {
-        const float w = __shfl_sync(0xffffffffu, v, q);
-        rank += (w > v) | ((w == v) & (q < lane));
+        for (int q = 0; q < G; ++q) {
+          const float w = __shfl_sync(0xffffffffu, v, q);
+          rank += (w > v) | ((w == v) & (q < lane));
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, lane < G && rank == K - 1);
+        R = __shfl_sync(0xffffffffu, v, __ffs(hit) - 1);
       }
-      const unsigned hit = __ballot_sync(0xffffffffu, lane < G && rank == K - 1);
-      const float R = __shfl_sync(0xffffffffu, v, __ffs(hit) - 1);
       ovf = __any_sync(0xffffffffu, ovf);
       if (lane == 0) {
         const float beam = sm.beam[j];

@@ -248,13 +248,15 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_select_kernel(const Sa
       merge_ms(m, s, mo, so);
     }
     ovf = __any_sync(0xffffffffu, ovf);
-    float a, b;
+    float a, b, gmin = INFINITY;
     if (G <= 8) {
 #pragma unroll 1
       for (int o = 16; o > 0; o >>= 1) {
 #pragma unroll
         for (int g = 0; g < 8; ++g) g8[g] = fmaxf(g8[g], __shfl_xor_sync(0xffffffffu, g8[g], o));
       }
+#pragma unroll
+      for (int g = 0; g < 8; ++g) gmin = g < G ? fminf(gmin, g8[g]) : gmin;
       float v = g8[0];
 #pragma unroll
       for (int g = 1; g < 8; ++g) v = lane == g ? g8[g] : v;
@@ -265,21 +267,25 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_select_kernel(const Sa
       a = lane < G ? ord_float(sm.gmax[w][lane]) : -INFINITY;
       b = lane + 32 < G ? ord_float(sm.gmax[w][lane + 32]) : -INFINITY;
     }
-    // R-top-k: the k-th largest of the G group maxima (ties by group index)
-    int ra = 0, rb = 0;
+    // R-top-k: the k-th largest of the G group maxima (ties by group index); with k group
+    // maxima in registers it is the least of them
+    float R = gmin;
+    if (!(G <= 8 && G == K)) {
+      int ra = 0, rb = 0;
 #pragma unroll 1
-    for (int q = 0; q < min(G, 32); ++q) {
-      const float wa = __shfl_sync(0xffffffffu, a, q);
-      const float wb = __shfl_sync(0xffffffffu, b, q);
-      const bool qb = q + 32 < G;  // only the G real groups are ranked
-      ra += ((wa > a) | ((wa == a) & (q < lane))) + (qb & (wb > a));
-      rb += (wa >= b) + (qb & ((wb > b) | ((wb == b) & (q < lane))));
+      for (int q = 0; q < min(G, 32); ++q) {
+        const float wa = __shfl_sync(0xffffffffu, a, q);
+        const float wb = __shfl_sync(0xffffffffu, b, q);
+        const bool qb = q + 32 < G;  // only the G real groups are ranked
+        ra += ((wa > a) | ((wa == a) & (q < lane))) + (qb & (wb > a));
+        rb += (wa >= b) + (qb & ((wb > b) | ((wb == b) & (q < lane))));
+      }
+      const unsigned hit = __ballot_sync(0xffffffffu, ((lane < G) & (ra == K - 1)) | ((lane + 32 < G) & (rb == K - 1)));
+      const int hl = __ffs(hit) - 1;
+      const float va = __shfl_sync(0xffffffffu, a, hl & 31), vb = __shfl_sync(0xffffffffu, b, hl & 31);
+      const int rah = __shfl_sync(0xffffffffu, ra, hl & 31);
+      R = rah == K - 1 ? va : vb;
     }
-    const unsigned hit = __ballot_sync(0xffffffffu, ((lane < G) & (ra == K - 1)) | ((lane + 32 < G) & (rb == K - 1)));
-    const int hl = __ffs(hit) - 1;
-    const float va = __shfl_sync(0xffffffffu, a, hl & 31), vb = __shfl_sync(0xffffffffu, b, hl & 31);
-    const int rah = __shfl_sync(0xffffffffu, ra, hl & 31);
-    const float R = rah == K - 1 ? va : vb;
     const float lse = m == -INFINITY ? -INFINITY : m + logf(s);
     path = ovf ? 1 : 0;
     if (p.flags & kFlagForceExact) path = 2;
