@@ -104,6 +104,38 @@ LS_API ls_status ls_beam_step(const void* logits, ls_dtype logit_dtype, const fl
                        size_t workspace_bytes, void* stream);
 
 /*
+ * The beam step fused into the output projection that produces its logits (the step
+ * before the article's first traversal, which reads the [batch, k, vocab] logits the
+ * projection wrote).  logits = hidden . weight^T are accumulated on the tensor cores a
+ * tile at a time and never stored: each tile's epilogue runs the first traversal on it
+ * (per beam and 512-token chunk the max, the sum of exp and the group maxima, and the
+ * candidates at or above the chunk's R-top-k bound), then the fine rank of ls_beam_step
+ * runs on those candidates.
+ *
+ *  hidden      [batch, k, dim] row-major, dtype, device, 16-byte aligned: each beam's last
+ *              decoder state.
+ *  weight      [vocab, dim] row-major, dtype, device, 16-byte aligned: the projection,
+ *              one row per token (x[v] = hidden . weight[v] + bias[v]).
+ *  dtype       LS_DTYPE_F16 or LS_DTYPE_BF16, both operands.  The products are exact and
+ *              are summed in f32 on the tensor cores in an unspecified order, so a logit
+ *              differs from the exact dot product by a few f32 roundings of partial sums of
+ *              at most sum_d |hidden[d] * weight[v, d]|.
+ *  dim         hidden size: a multiple of 8, at least 8.
+ *  k           1 <= k <= 32 (k up to LS_MAX_K returns LS_ERR_UNSUPPORTED).
+ *  All other arguments, the results (outputs, order, ties, finished beams, -inf) and the
+ *  workspace (ls_beam_step_workspace_size(batch, k, vocab) bytes, shared with ls_beam_step)
+ *  are those of ls_beam_step with x = logit + bias.  The rows of finished beams are
+ *  multiplied but not used.  Argument errors return LS_ERR_INVALID_ARG with nothing
+ *  enqueued; a device wait that runs out is reported by ls_read_status.
+ */
+LS_API ls_status ls_logits_beam_step(const void* hidden, const void* weight, ls_dtype dtype, int dim,
+                                     const float* bias, const float* beam_scores,
+                                     const uint8_t* finished, int batch, int k, int vocab, int eos_id,
+                                     int32_t* out_token, int32_t* out_parent, float* out_score,
+                                     uint8_t* out_finished, void* workspace, size_t workspace_bytes,
+                                     void* stream);
+
+/*
  * Beam-cache refresh by parent beam (article: "update the cache" after selection):
  *   dst[l, b*k+j, h, p, :] = src[l, b*k + parent[b*k+j], h, p, :]   for p < len.
  * Layout [layers, batch*k, heads, max_len, head_dim], element size from dtype

@@ -19,7 +19,7 @@ __all__ = [
     "LS_DTYPE_F32", "LS_DTYPE_F16", "LS_DTYPE_BF16", "LS_MAX_K", "LsBeamError", "library_path", "load_library",
     "check", "ls_beam_step_workspace_size", "ls_workspace_init", "ls_beam_step", "ls_cache_reorder",
     "ls_read_status", "ls_status_string", "ls_read_row_stats", "ls_beam_step_noalloc", "ls_backtrack",
-    "ls_sample_workspace_size", "ls_sample", "ls_cache_refresh_inplace",
+    "ls_sample_workspace_size", "ls_sample", "ls_cache_refresh_inplace", "ls_logits_beam_step",
 ]
 
 LS_OK, LS_ERR_INVALID_ARG, LS_ERR_UNSUPPORTED, LS_ERR_CUDA, LS_ERR_TIMEOUT, LS_ERR_INTERNAL = range(6)
@@ -74,6 +74,8 @@ def load_library():
         lib.ls_sample.restype = ip
         lib.ls_cache_refresh_inplace.argtypes = [vp, ip, vp, ip, ip, ip, ip, ip, ip, ip, vp, vp]
         lib.ls_cache_refresh_inplace.restype = ip
+        lib.ls_logits_beam_step.argtypes = [vp, vp, ip, ip, vp, vp, vp, ip, ip, ip, ip, vp, vp, vp, vp, vp, sz, vp]
+        lib.ls_logits_beam_step.restype = ip
         _lib = lib
         return lib
 
@@ -132,6 +134,21 @@ def ls_beam_step(logits, bias, beam_scores, finished, eos_id: int, out_token, ou
     return load_library().ls_beam_step(
         _ptr(logits), _dtype_code(logits), _ptr(bias), _ptr(beam_scores), _ptr(finished), batch, k, vocab,
         int(eos_id), _ptr(out_token), _ptr(out_parent), _ptr(out_score), _ptr(out_finished), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+
+
+def ls_logits_beam_step(hidden, weight, bias, beam_scores, finished, eos_id: int, out_token, out_parent, out_score,
+                        out_finished, workspace, stream=None) -> int:
+    """The beam step fused into the output projection: hidden [batch, k, dim] and weight [vocab, dim]
+    (both f16 or both bf16, logits = hidden . weight^T, never stored); everything else as ls_beam_step.
+    The workspace is the one of ls_beam_step_workspace_size(batch, k, vocab)."""
+    batch, k, dim = hidden.shape
+    vocab, dim_w = weight.shape
+    if dim_w != dim or weight.dtype != hidden.dtype:
+        raise ValueError("weight must be [vocab, dim] of the hidden states' dtype")
+    return load_library().ls_logits_beam_step(
+        _ptr(hidden), _ptr(weight), _dtype_code(hidden), dim, _ptr(bias), _ptr(beam_scores), _ptr(finished), batch, k,
+        vocab, int(eos_id), _ptr(out_token), _ptr(out_parent), _ptr(out_score), _ptr(out_finished), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream))
 
 

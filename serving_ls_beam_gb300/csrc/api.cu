@@ -22,6 +22,7 @@ struct DeviceInfo {
   bool ready = false;
   int sms = 0;
   bool select_ready = false;  // K2's dynamic shared-memory limit raised
+  bool logits_ready = false;  // K0's dynamic shared-memory limit raised
   // K1 occupancy per [dtype][bias][vpl index]; 0 = not configured yet
   int step_occ[3][2][3] = {};
   int copy_occ[5] = {};
@@ -151,6 +152,59 @@ bool select_configured(DeviceInfo* di) {
   return true;
 }
 
+bool logits_configured(DeviceInfo* di) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!di->logits_ready) {
+    if (logits_rows_config() != cudaSuccess) return false;
+    di->logits_ready = true;
+  }
+  return true;
+}
+
+// cuTensorMapEncodeTiled, looked up in the driver once (the library does not link libcuda).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// Tensor map of a row-major [outer, inner] f16 / bf16 matrix read in boxes of kLgBK inner
+// elements (128 bytes, one 128-byte swizzle row) by box_outer rows; reads outside the
+// matrix return zeros.
+bool encode_kmajor(CUtensorMap* m, const void* base, ls_dtype dt, long long inner, long long outer, int box_outer) {
+  const EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  const cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kLgBK, (cuuint32_t)box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt == LS_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16 for K0's tile: f32 accumulators, A and
+// B of the same 16-bit type, both K-major, M = kLgM, N = kLgN.
+uint32_t umma_idesc(bool bf16) {
+  const uint32_t ab = bf16 ? 1u : 0u;
+  return (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(kLgN >> 3) << 17) | ((uint32_t)(kLgM >> 4) << 24);
+}
+
 int copy_occupancy(DeviceInfo* di, int unit) {
   std::lock_guard<std::mutex> lk(g_mu);
   int& occ = di->copy_occ[unit_index(unit)];
@@ -265,6 +319,94 @@ ls_status ls_beam_step(const void* logits, ls_dtype logit_dtype, const float* bi
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_beam_rows(p, dtype, vpl, (int)grid, st);
   if (e == cudaSuccess) e = launch_beam_select(p, dtype, st);
+  return e == cudaSuccess ? LS_OK : cuda_fail(e);
+}
+
+ls_status ls_logits_beam_step(const void* hidden, const void* weight, ls_dtype dtype, int dim, const float* bias,
+                              const float* beam_scores, const uint8_t* finished, int batch, int k, int vocab,
+                              int eos_id, int32_t* out_token, int32_t* out_parent, float* out_score,
+                              uint8_t* out_finished, void* workspace, size_t workspace_bytes, void* stream) {
+  if (batch < 0 || k < 1 || k > LS_MAX_K || vocab < k) return LS_ERR_INVALID_ARG;
+  if ((long long)k * vocab >= (1ll << 31) || vocab > (1 << 28)) return LS_ERR_INVALID_ARG;
+  if (eos_id < 0 || eos_id >= vocab) return LS_ERR_INVALID_ARG;
+  if (dtype != LS_DTYPE_F16 && dtype != LS_DTYPE_BF16) return LS_ERR_INVALID_ARG;
+  if (dim < 8 || dim % 8 != 0) return LS_ERR_INVALID_ARG;
+  if (k > kLgMaxK) return LS_ERR_UNSUPPORTED;
+  if (batch == 0) return LS_OK;
+  if (!hidden || !weight || !beam_scores || !out_token || !out_parent || !out_score || !workspace)
+    return LS_ERR_INVALID_ARG;
+  const WsLayout wl = ws_layout(batch, k, vocab);
+  if (wl.total == 0 || workspace_bytes < wl.total) return LS_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(weight, 16) || (bias && !aligned(bias, 4)) || !aligned(beam_scores, 4) ||
+      !aligned(out_token, 4) || !aligned(out_parent, 4) || !aligned(out_score, 4) || !aligned(workspace, 256))
+    return LS_ERR_INVALID_ARG;
+  const long long rows = (long long)batch * k;
+  if (rows >= (1ll << 31) || rows * dim >= (1ll << 40)) return LS_ERR_UNSUPPORTED;
+  const Debug dbg = read_debug();
+  if (dbg.check_ptrs) {
+    const void* ptrs[] = {hidden, weight, bias, beam_scores, finished, out_token, out_parent, out_score, out_finished,
+                          workspace};
+    for (const void* q : ptrs)
+      if (q && !device_reachable(q)) return LS_ERR_INVALID_ARG;
+  }
+  int dev = 0;
+  DeviceInfo* di = device_info(&dev);
+  if (!di) return cuda_fail(cudaErrorUnknown);
+  if (!logits_configured(di) || !select_configured(di)) return cuda_fail(cudaErrorUnknown);
+  const int nc = (vocab + kLgChunk - 1) / kLgChunk;
+  if (nc > wl.nc_max) return LS_ERR_INTERNAL;
+
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  LogitsParams lp;
+  StepParams& p = lp.s;
+  p = StepParams{};
+  p.logits = nullptr;  // the logits are never stored
+  p.bias = bias;
+  p.beam = beam_scores;
+  p.finished = finished;
+  p.out_token = out_token;
+  p.out_parent = out_parent;
+  p.out_score = out_score;
+  p.out_finished = out_finished;
+  p.status = reinterpret_cast<uint32_t*>(ws + wl.status_off);
+  p.done = reinterpret_cast<uint32_t*>(ws + wl.done_off);
+  p.rec = ws + wl.rec_off;
+  p.slots = reinterpret_cast<CandSlot*>(ws + wl.slot_off);
+  p.rowstat = reinterpret_cast<RowStat*>(ws + wl.rowstat_off);
+  p.bstat = reinterpret_cast<int32_t*>(ws + wl.bstat_off);
+  p.batch = batch;
+  p.k = k;
+  p.vocab = vocab;
+  p.eos = eos_id;
+  p.rows = (int)rows;
+  p.nc = nc;
+  make_divisor((uint32_t)nc, &p.nc_magic, &p.nc_shift);
+  p.groups = wl.groups;
+  p.slot_cap = wl.slot_cap;
+  p.rec_stride = wl.rec_stride;
+  p.flags = dbg.flags;
+  const long long stage = (long long)k * nc * wl.slot_cap * (long long)sizeof(CandSlot);
+  p.sel_stage_bytes = (k <= 8 && nc <= 128 && (long long)k * nc <= 1024 && stage <= kSelStageMax) ? (int)stage : 0;
+  p.units = rows * nc;
+  p.spin_limit_ns = dbg.spin_ns;
+  lp.idesc = umma_idesc(dtype == LS_DTYPE_BF16);
+  lp.dim = dim;
+  lp.n_m = (int)((rows + kLgM - 1) / kLgM);
+  const long long n_tiles = (long long)lp.n_m * nc;
+  if (n_tiles >= (1ll << 31)) return LS_ERR_UNSUPPORTED;
+  lp.n_tiles = (int)n_tiles;
+  const int grid = (int)(n_tiles < di->sms ? n_tiles : di->sms);
+
+  CUtensorMap mh, mw;
+  if (!encode_kmajor(&mh, hidden, dtype, dim, rows, kLgM) || !encode_kmajor(&mw, weight, dtype, dim, vocab, kLgN))
+    return cuda_fail(cudaErrorUnknown);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_logits_rows(mh, mw, lp, grid, st);
+  if (e == cudaSuccess) {
+    StepParams ps = p;
+    ps.bias = nullptr;  // the slots hold x = logit + bias already
+    e = launch_beam_select(ps, (int)LS_DTYPE_F32, st);
+  }
   return e == cudaSuccess ? LS_OK : cuda_fail(e);
 }
 

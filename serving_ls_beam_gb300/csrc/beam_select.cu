@@ -153,10 +153,14 @@ __device__ void merge_into_best(SelSmem& sm, int K) {
 
 // Exact fine rank of batch b without the candidate queue: per live beam, a radix select
 // of its top-K logits (order: larger x first, then smaller token id), merged across beams.
+// Without logits (p.logits null: the chunk records and slots came from the projection's
+// epilogue, whose chunks keep every candidate at or above their bound, or else their own
+// top-K, in token order) the select runs over the beam's slots instead of its row.
 template <int DT, bool BIAS>
 __device__ void exact_select(const StepParams& p, SelSmem& sm, int b, int path) {
   constexpr int ES = Traits<DT>::kBytes;
-  const int K = p.k, V = p.vocab;
+  const int K = p.k, V = p.vocab, C = p.slot_cap, nc = p.nc;
+  const bool from_slots = p.logits == nullptr;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
     sm.nbest = 0;
@@ -182,11 +186,24 @@ __device__ void exact_select(const StepParams& p, SelSmem& sm, int b, int path) 
       merge_into_best(sm, K);
       continue;
     }
-    const unsigned char* rowp = static_cast<const unsigned char*>(p.logits) + (size_t)row * V * ES;
-    auto load_x = [&](int v) -> float {
-      float x = load_elem<DT>(rowp + (size_t)v * ES);
-      if constexpr (BIAS) x += __ldg(p.bias + v);
-      return x;
+    const unsigned char* rowp =
+        from_slots ? nullptr : static_cast<const unsigned char*>(p.logits) + (size_t)row * V * ES;
+    const long long u0 = (long long)row * nc;
+    const int n_src = from_slots ? nc * C : V;
+    // element i of the beam's source, in token order: (x, token), or false when i is empty
+    auto src = [&](int i, float& x, int& v) -> bool {
+      if (from_slots) {
+        const int c = i / C, sl = i - c * C;
+        if (sl >= __float_as_int(rec_ptr(p, u0 + c)[0])) return false;
+        const CandSlot cs = p.slots[(u0 + c) * C + sl];
+        x = cs.x;
+        v = cs.v;
+        return true;
+      }
+      x = load_elem<DT>(rowp + (size_t)i * ES);
+      if constexpr (BIAS) x += __ldg(p.bias + i);
+      v = i;
+      return true;
     };
     // radix select of the K-th largest order key, 8 bits at a time from the top
     if (tid == 0) {
@@ -199,8 +216,11 @@ __device__ void exact_select(const StepParams& p, SelSmem& sm, int b, int path) 
       for (int i = tid; i < 256; i += kSelThreads) sm.hist[i] = 0;
       __syncthreads();
       const uint32_t prefix = sm.prefix, pmask = sm.pmask;
-      for (int v = tid; v < V; v += kSelThreads) {
-        const uint32_t o = float_ord(load_x(v));
+      for (int i = tid; i < n_src; i += kSelThreads) {
+        float x;
+        int v;
+        if (!src(i, x, v)) continue;
+        const uint32_t o = float_ord(x);
         if ((o & pmask) == prefix) atomicAdd(&sm.hist[(o >> shift) & 255u], 1u);
       }
       __syncthreads();
@@ -220,8 +240,10 @@ __device__ void exact_select(const StepParams& p, SelSmem& sm, int b, int path) 
     }
     const uint32_t tkey = sm.prefix;
     const int need_eq = sm.need;  // elements equal to the threshold to take, in token order
-    for (int v = tid; v < V; v += kSelThreads) {
-      const float x = load_x(v);
+    for (int i = tid; i < n_src; i += kSelThreads) {
+      float x;
+      int v;
+      if (!src(i, x, v)) continue;
       if (float_ord(x) > tkey) {
         const int pos = atomicAdd(&sm.nrl, 1);
         if (pos < kMaxK) sm.rl[pos] = make_key((float)(rs.c + (double)x), j, x, v);
@@ -229,14 +251,12 @@ __device__ void exact_select(const StepParams& p, SelSmem& sm, int b, int path) 
     }
     __syncthreads();
     int taken = 0;
-    for (int base = 0; base < V && taken < need_eq; base += kSelThreads) {
-      const int v = base + tid;
+    for (int base = 0; base < n_src && taken < need_eq; base += kSelThreads) {
+      const int i = base + tid;
       float x = 0.0f;
+      int v = 0;
       bool eq = false;
-      if (v < V) {
-        x = load_x(v);
-        eq = float_ord(x) == tkey;
-      }
+      if (i < n_src && src(i, x, v)) eq = float_ord(x) == tkey;
       const unsigned ballot = __ballot_sync(0xffffffffu, eq);
       if (lane == 0) sm.wc[warp] = __popc(ballot);
       __syncthreads();

@@ -2,6 +2,7 @@
 // Nothing here is part of the public interface (include/ls_beam.h).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -22,6 +23,16 @@ constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kMaxK = 64;
 constexpr int kSelCap = 512;  // survivors the fine rank holds in shared memory
 constexpr int kSelStageMax = 96 * 1024;  // a batch's candidate slots staged in shared memory (bytes)
+
+// K0 (logits_rows.cu): the output projection fused with the first traversal; tiles of
+// kLgM rows x kLgChunk columns (one chunk record per row), computed as two sub-tiles of
+// kLgN columns, kLgBK of the hidden size per pipeline stage.
+constexpr int kLgM = 128;
+constexpr int kLgN = 256;
+constexpr int kLgChunk = 2 * kLgN;
+constexpr int kLgBK = 64;
+constexpr int kLgThreads = 192;
+constexpr int kLgMaxK = 32;
 
 // Backtrack (backtrack.cu): one CTA per batch, the history staged kBtTileElems entries of
 // (token, parent) at a time: 3 x 4 x kBtTileElems = 48 KB of shared memory at most.
@@ -144,6 +155,14 @@ struct StepParams {
   long long spin_limit_ns;
 };
 
+struct LogitsParams {
+  StepParams s;    // workspace, shapes and flags shared with the fine rank (logits unused)
+  uint32_t idesc;  // tcgen05 instruction descriptor (operand type, tile shape)
+  int dim;         // hidden size
+  int n_m;         // kLgM-row blocks
+  int n_tiles;     // n_m * nc
+};
+
 struct ReorderParams {
   const unsigned char* src;
   unsigned char* dst;
@@ -225,6 +244,10 @@ size_t beam_rows_smem_bytes(int vpl);
 cudaError_t beam_rows_config(int dtype, bool bias, int vpl, int* occupancy);
 cudaError_t launch_beam_rows(const StepParams& p, int dtype, int vpl, int grid, cudaStream_t stream);
 cudaError_t launch_beam_select(const StepParams& p, int dtype, cudaStream_t stream);
+size_t logits_rows_smem_bytes();
+cudaError_t logits_rows_config();  // once per device: the kernels' dynamic shared memory
+cudaError_t launch_logits_rows(const CUtensorMap& mh, const CUtensorMap& mw, const LogitsParams& lp, int grid,
+                               cudaStream_t stream);
 cudaError_t beam_select_config();  // once per device: allow kSelStageMax of dynamic shared memory
 cudaError_t launch_cache_reorder(const ReorderParams& p, int unit, int grid, cudaStream_t stream);
 cudaError_t cache_reorder_occupancy(int unit, int* occupancy);

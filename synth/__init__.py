@@ -22,6 +22,9 @@ c4     batch 8, beam 8, vocab 120000, fp32 logits 2*t(3); round(5%) of rows get 
 c5     batch 256, beam 4, vocab 40000, fp16 logits N(0,2) + per-step scalar offset
        U(-5,5) (added before fp16 rounding), 64 steps, step-1 beam scores 0, eos 2,
        cache [6, 1024, 16, 64, 64] fp16 N(0,1), seed 4
+p5     the c5 decode step with its logits made by the output projection: batch 256, beam 4,
+       vocab 40000, hidden size 1024; decoder states N(0,1) and projection N(0, 2/1024)
+       (so the logits are ~N(0,2) as in c5), both bf16; beam scores U(-5,0), eos 2, seed 6
 =====  ==============================================================================
 """
 from __future__ import annotations
@@ -33,6 +36,7 @@ from dataclasses import dataclass, field
 import numpy as np
 
 TAG_LOGITS, TAG_BIAS, TAG_BEAM, TAG_FINISHED, TAG_TIED, TAG_OFFSET, TAG_KV, TAG_PARENT, TAG_UNIFORM = range(1, 10)
+TAG_HIDDEN, TAG_WEIGHT = 10, 11
 
 _THREADS = max(1, min(16, os.cpu_count() or 1))
 
@@ -244,3 +248,45 @@ def sample_inputs(w: Workload, step: int = 0) -> dict:
     u = rng(w.seed, TAG_UNIFORM, step).random(w.batch).astype(np.float32)
     u = np.minimum(u, np.float32(1.0) - np.float32(2.0 ** -24))
     return {"logits": lg, "bias": bias(w), "u": u, "top_k": int(w.extra["top_k"]), "top_p": float(w.extra["top_p"])}
+
+
+# Projection-fused step (the logits are hidden . weight^T, computed by the step itself).
+PROJ_WORKLOADS = {
+    "p5": Workload("p5", 256, 4, 40000, "bf16", 6, logit_var=2.0, beam_range=(-5.0, 0.0), extra={"dim": 1024}),
+}
+
+
+def hidden_states(w: Workload, dim: int, step: int = 0, batches=None) -> np.ndarray:
+    """Decoder states [batch, k, dim] N(0,1) in w.dtype (bf16 as uint16 bits); one stream per batch."""
+    idx = range(w.batch) if batches is None else list(batches)
+    out = [_round_to(rng(w.seed, TAG_HIDDEN, step, b).standard_normal((w.k, dim), dtype=np.float32), w.dtype)
+           for b in idx]
+    return np.stack(out)
+
+
+def projection(w: Workload, dim: int) -> np.ndarray:
+    """Output projection [vocab, dim] N(0, logit_var / dim) in w.dtype (bf16 as uint16 bits)."""
+    a = rng(w.seed, TAG_WEIGHT).standard_normal((w.vocab, dim), dtype=np.float32)
+    a *= np.float32(np.sqrt(w.logit_var / dim))
+    return _round_to(a, w.dtype)
+
+
+def projection_inputs(w: Workload, dim: int | None = None, step: int = 0, batches=None) -> dict:
+    """All inputs of one projection-fused step (host arrays)."""
+    dim = int(dim or w.extra["dim"])
+    fin = finished(w)
+    bs = beam_scores(w, step)
+    if batches is not None:
+        idx = np.asarray(list(batches))
+        bs = bs[idx]
+        fin = None if fin is None else fin[idx]
+    return {
+        "hidden": hidden_states(w, dim, step, batches),
+        "weight": projection(w, dim),
+        "bias": bias(w),
+        "beam_scores": bs,
+        "finished": fin,
+        "eos_id": w.eos_id,
+        "dtype": w.dtype,
+        "dim": dim,
+    }

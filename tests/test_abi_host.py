@@ -78,6 +78,20 @@ def test_host_argument_checks(lib):
     assert lib.ls_cache_reorder(p, p, 1, p, 1, 1, 2, 1, 4, 2, 8, None, None) == E  # src == dst
     assert lib.ls_cache_reorder(None, None, 1, None, 1, 1, 2, 1, 4, 0, 8, None, None) == 0  # len 0 no-op
     assert lib.ls_backtrack(p, p, -1, 2, 3, 0, p, p, None, None) == E  # steps < 0
+    # the projection-fused step: f16 / bf16 operands, dim a multiple of 8, 16-byte aligned operands
+    F = lib.ls_logits_beam_step
+    F.argtypes = [ctypes.c_void_p] * 2 + [ctypes.c_int] * 2 + [ctypes.c_void_p] * 3 + [ctypes.c_int] * 4 + \
+        [ctypes.c_void_p] * 5 + [ctypes.c_size_t, ctypes.c_void_p]
+    q = ctypes.c_void_p(24)  # 8-byte aligned only
+    assert F(p, p, 0, 64, None, p, None, 2, 4, 100, 0, p, p, p, None, p, 1 << 20, None) == E  # f32 operands
+    assert F(p, p, 2, 60, None, p, None, 2, 4, 100, 0, p, p, p, None, p, 1 << 20, None) == E  # dim % 8
+    assert F(p, p, 2, 0, None, p, None, 2, 4, 100, 0, p, p, p, None, p, 1 << 20, None) == E  # dim 0
+    assert F(q, p, 2, 64, None, p, None, 2, 4, 100, 0, p, p, p, None, p, 1 << 20, None) == E  # misaligned hidden
+    assert F(p, q, 2, 64, None, p, None, 2, 4, 100, 0, p, p, p, None, p, 1 << 20, None) == E  # misaligned weight
+    assert F(p, p, 2, 64, None, p, None, 2, 4, 100, 100, p, p, p, None, p, 1 << 20, None) == E  # eos
+    assert F(p, p, 2, 64, None, p, None, 2, 4, 100, 0, p, p, p, None, p, 10, None) == E  # tiny workspace
+    assert F(p, p, 2, 64, None, p, None, 2, 33, 100, 0, p, p, p, None, p, 1 << 30, None) == 2  # k > 32
+    assert F(None, None, 2, 64, None, None, None, 0, 4, 100, 0, None, None, None, None, None, 0, None) == 0
     assert lib.ls_backtrack(p, p, 4, 2, 0, 0, p, p, None, None) == E  # k = 0
     assert lib.ls_backtrack(p, p, 4, 2, 65, 0, p, p, None, None) == E  # k > 64
     assert lib.ls_backtrack(None, p, 4, 2, 3, 0, p, p, None, None) == E  # no history
