@@ -39,6 +39,7 @@ import synth  # noqa: E402
 METRIC = "beam-search decode steps/s and logit GB/s vs GB300 HBM roofline (1 GPU)"
 UNIT = "decode steps/s"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0  # one earlier cuBLAS bf16 measurement on a GB300 (burst)
 
 
 def parse_args():
@@ -51,6 +52,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sampling", action="store_true", help="skip the sampling-decoding measurement")
+    ap.add_argument("--no-projection", action="store_true",
+                    help="skip the measurement of the beam step fused into the output projection")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--decode-steps", type=int, default=0,
                     help="run only the first N decode steps of the workload (for small profiling runs)")
@@ -105,6 +108,17 @@ def hbm_peak():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def tensor_peak():
+    """Dense bf16 tensor throughput (burst: kernels timed in short graphs), TFLOP/s."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 class ClockSampler:
@@ -480,6 +494,10 @@ def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
     if not args.no_sampling:
         sampling = bench_sampling(dev, peak)
 
+    projection = None
+    if not args.no_projection:
+        projection = bench_projection(dev)
+
     clocks = clk.summary()
     cfg = workload_config(wr, T, world)
     line = {
@@ -488,7 +506,8 @@ def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
         "dtype": wr.dtype, "data": "synthetic (seeded generators, workload recipe in synth/)", "config": cfg,
         "logit_gbs": k1_gbs, "step_gbs": step_gbs, "step_roofline_frac": step_gbs / peak,
         "roofline": roof, "roofline_kernels": kern, "gpu_launches": launches_per_step * args.steps,
-        "clocks": clocks, "e2e": e2e, "sampling": sampling, "cache_refresh_out_of_place": oop_line,
+        "clocks": clocks, "e2e": e2e, "sampling": sampling, "projection_step": projection,
+        "cache_refresh_out_of_place": oop_line,
         "candidates": cand,
         "setup_s": round(setup_s, 1),
     }
@@ -542,6 +561,86 @@ def bench_sampling(dev, peak, calls: int = 16):
             "us_per_call": us, "rows_per_s": rows / (us * 1e-6), "achieved": gbs, "peak": peak, "unit": "GB/s",
             "frac": gbs / peak, "algorithmic_bytes_per_call": nbytes, "launches_per_call": 2,
             "l2": f"{calls} distinct logit sets per graph ({calls * rows * vocab * 2 / 1e9:.2f} GB)"}
+
+
+def bench_projection(dev, calls: int = 12, copies: int = 3):
+    """The beam step fused into the output projection (ls_logits_beam_step: K0 then K2) on workload p5:
+    one CUDA graph of `calls` calls over `copies` copies of the projection (82 MB each, 246 MB in all,
+    larger than L2) and `calls` sets of decoder states, timed with CUDA events.  For comparison the same
+    step unfused: a cuBLAS bf16 GEMM (torch.mm) that writes bf16 logits, then ls_beam_step on them."""
+    import torch
+
+    import serving_ls_beam_gb300 as lsb
+
+    w = synth.PROJ_WORKLOADS["p5"]
+    dim = int(w.extra["dim"])
+    B, K, V, rows = w.batch, w.k, w.vocab, w.rows
+    tpeak, tsrc = tensor_peak()
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).view(torch.int16).view(torch.bfloat16).to(dev)
+
+    w0 = bf16(synth.projection(w, dim))
+    wts = [w0] + [w0.clone() for _ in range(copies - 1)]
+    hs = [bf16(synth.hidden_states(w, dim, step=i)) for i in range(calls)]
+    beam = torch.from_numpy(synth.beam_scores(w)).to(dev)
+    tok = torch.empty((calls, B, K), dtype=torch.int32, device=dev)
+    par = torch.empty_like(tok)
+    sc = torch.empty((calls, B, K), dtype=torch.float32, device=dev)
+    of = torch.empty((calls, B, K), dtype=torch.uint8, device=dev)
+    ws = torch.empty(lsb.ls_beam_step_workspace_size(B, K, V), dtype=torch.uint8, device=dev)
+    lsb.check(lsb.ls_workspace_init(ws))
+    logits = torch.empty((rows, V), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def fused():
+        for i in range(calls):
+            lsb.check(lsb.ls_logits_beam_step(hs[i], wts[i % copies], None, beam, None, w.eos_id, tok[i], par[i],
+                                              sc[i], of[i], ws), "ls_logits_beam_step")
+
+    def unfused():
+        for i in range(calls):
+            torch.mm(hs[i].view(rows, dim), wts[i % copies].t(), out=logits)
+            lsb.check(lsb.ls_beam_step(logits.view(B, K, V), None, beam, None, w.eos_id, tok[i], par[i], sc[i], of[i],
+                                       ws), "ls_beam_step")
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 5
+        with torch.cuda.stream(stream):
+            e0.record()
+            for _ in range(reps):
+                g.replay()
+            e1.record()
+        torch.cuda.synchronize()
+        lsb.check(lsb.ls_read_status(ws), "device status")
+        return e0.elapsed_time(e1) * 1e3 / (reps * calls)
+
+    us = timed(fused)
+    fused_tok = tok.clone()
+    us_unfused = timed(unfused)
+    flops = 2.0 * rows * V * dim
+    tf = flops / (us * 1e-6) / 1e12
+    # the two paths select from logits that differ only by rounding (f32 accumulators vs bf16 logits)
+    agree = float((fused_tok == tok).float().mean().item())
+    return {"workload": f"p5: batch {B}, beam {K}, vocab {V}, hidden {dim}, bf16 decoder states and projection",
+            "bound": "tensor", "us_per_call": us, "achieved": tf, "peak": tpeak, "unit": "TFLOP/s",
+            "frac": tf / tpeak, "peak_source": f"{tsrc} (MEASURED_PEAKS.json bf16_tflops)" if tsrc == "measured"
+            else "fallback", "flops_per_call": flops, "launches_per_call": 2,
+            "decode_steps_per_s": 1e6 / us, "unfused_us_per_call": us_unfused,
+            "unfused": "cuBLAS bf16 GEMM writing bf16 logits (torch.mm) + ls_beam_step on them",
+            "token_agreement_with_unfused": agree,
+            "l2": f"{copies} projection copies ({copies * V * dim * 2 / 1e6:.0f} MB) and {calls} decoder-state sets "
+                  "per graph"}
 
 
 def bench_e2e(args, wr, loop, host_logits, bias_np, beam0, fin0, lens, dev, world):

@@ -23,6 +23,7 @@ struct DeviceInfo {
   int sms = 0;
   bool select_ready = false;  // K2's dynamic shared-memory limit raised
   bool logits_ready = false;  // K0's dynamic shared-memory limit raised
+  int logits_clusters = 0;    // co-resident clusters of two K0 CTAs
   // K1 occupancy per [dtype][bias][vpl index]; 0 = not configured yet
   int step_occ[3][2][3] = {};
   int copy_occ[5] = {};
@@ -156,9 +157,15 @@ bool logits_configured(DeviceInfo* di) {
   std::lock_guard<std::mutex> lk(g_mu);
   if (!di->logits_ready) {
     if (logits_rows_config() != cudaSuccess) return false;
+    di->logits_clusters = logits_rows_max_clusters();
     di->logits_ready = true;
   }
   return true;
+}
+
+int logits_clusters(DeviceInfo* di) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  return di->logits_clusters;
 }
 
 // cuTensorMapEncodeTiled, looked up in the driver once (the library does not link libcuda).
@@ -183,7 +190,7 @@ EncodeTiledFn encode_tiled_fn() {
 }
 
 // Tensor map of a row-major [outer, inner] f16 / bf16 matrix read in boxes of kLgBK inner
-// elements (128 bytes, one 128-byte swizzle row) by box_outer rows; reads outside the
+// elements (kLgSwizzleBytes, one swizzle row) by box_outer rows; reads outside the
 // matrix return zeros.
 bool encode_kmajor(CUtensorMap* m, const void* base, ls_dtype dt, long long inner, long long outer, int box_outer) {
   const EncodeTiledFn fn = encode_tiled_fn();
@@ -194,7 +201,8 @@ bool encode_kmajor(CUtensorMap* m, const void* base, ls_dtype dt, long long inne
   const cuuint32_t estr[2] = {1, 1};
   return fn(m, dt == LS_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            kLgSwizzleBytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -353,8 +361,27 @@ ls_status ls_logits_beam_step(const void* hidden, const void* weight, ls_dtype d
   DeviceInfo* di = device_info(&dev);
   if (!di) return cuda_fail(cudaErrorUnknown);
   if (!logits_configured(di) || !select_configured(di)) return cuda_fail(cudaErrorUnknown);
-  const int nc = (vocab + kLgChunk - 1) / kLgChunk;
-  if (nc > wl.nc_max) return LS_ERR_INTERNAL;
+  // chunk width: 1 to kLgMaxSubPerChunk sub-tiles, the one whose tiles spread best over the
+  // clusters (fewest sub-tiles for the busiest cluster), within the workspace's chunks per
+  // row and leaving every sub-tile of a chunk room for k candidates
+  const long long n_m = (rows + kLgM - 1) / kLgM;
+  const int n_mp = (int)((n_m + 1) / 2);
+  const int sub_per_row = (vocab + kLgN - 1) / kLgN;
+  const int clusters = logits_clusters(di);
+  if (clusters < 1) return cuda_fail(cudaErrorUnknown);
+  int spc = 0;
+  long long best = 0;
+  for (int s = 1; s <= kLgMaxSubPerChunk; ++s) {
+    const long long ncs = (sub_per_row + s - 1) / s;
+    if (ncs > wl.nc_max || wl.slot_cap - k * (s - 1) < 2 * k) continue;
+    const long long rounds = ((long long)n_mp * ncs + clusters - 1) / clusters;
+    if (spc == 0 || rounds * s < best) {
+      spc = s;
+      best = rounds * s;
+    }
+  }
+  if (spc == 0) return LS_ERR_INTERNAL;
+  const int nc = (sub_per_row + spc - 1) / spc;
 
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   LogitsParams lp;
@@ -391,14 +418,17 @@ ls_status ls_logits_beam_step(const void* hidden, const void* weight, ls_dtype d
   p.spin_limit_ns = dbg.spin_ns;
   lp.idesc = umma_idesc(dtype == LS_DTYPE_BF16);
   lp.dim = dim;
-  lp.n_m = (int)((rows + kLgM - 1) / kLgM);
-  const long long n_tiles = (long long)lp.n_m * nc;
+  lp.n_mp = n_mp;
+  lp.sub_per_chunk = spc;
+  lp.sub_per_row = sub_per_row;
+  const long long n_tiles = (long long)lp.n_mp * nc;
   if (n_tiles >= (1ll << 31)) return LS_ERR_UNSUPPORTED;
   lp.n_tiles = (int)n_tiles;
-  const int grid = (int)(n_tiles < di->sms ? n_tiles : di->sms);
+  const int grid = 2 * (int)(n_tiles < clusters ? n_tiles : clusters);
 
   CUtensorMap mh, mw;
-  if (!encode_kmajor(&mh, hidden, dtype, dim, rows, kLgM) || !encode_kmajor(&mw, weight, dtype, dim, vocab, kLgN))
+  if (!encode_kmajor(&mh, hidden, dtype, dim, rows, kLgM) ||
+      !encode_kmajor(&mw, weight, dtype, dim, vocab, kLgN / 2))  // each CTA of a pair loads half
     return cuda_fail(cudaErrorUnknown);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_logits_rows(mh, mw, lp, grid, st);

@@ -74,6 +74,21 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// Wait for the phase like mbar_wait_bounded, sleeping sleep_ns between polls: for waits
+// that can last microseconds (a pipeline stage, a whole tile), so that a waiting thread does
+// not take issue slots from the warps of its SM doing the work.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, long long limit_ns,
+                                                uint32_t sleep_ns) {
+  if (mbar_test_wait(bar, parity)) return true;
+  if (limit_ns <= 0) return false;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t n = 1;; ++n) {
+    __nanosleep(sleep_ns);
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((n & 15u) == 0 && (long long)(global_timer_ns() - t0) > limit_ns) return false;
+  }
+}
+
 // L2 policy: the logits are read exactly once, so let them leave L2 first.
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t pol;

@@ -25,12 +25,13 @@ constexpr int kSelCap = 512;  // survivors the fine rank holds in shared memory
 constexpr int kSelStageMax = 96 * 1024;  // a batch's candidate slots staged in shared memory (bytes)
 
 // K0 (logits_rows.cu): the output projection fused with the first traversal; tiles of
-// kLgM rows x kLgChunk columns (one chunk record per row), computed as two sub-tiles of
+// kLgM rows x one chunk (one chunk record per row) of 1 to kLgMaxSubPerChunk sub-tiles of
 // kLgN columns, kLgBK of the hidden size per pipeline stage.
 constexpr int kLgM = 128;
 constexpr int kLgN = 256;
-constexpr int kLgChunk = 2 * kLgN;
+constexpr int kLgMaxSubPerChunk = 4;
 constexpr int kLgBK = 64;
+constexpr int kLgSwizzleBytes = kLgBK * 2;  // a stage row of kLgBK 16-bit elements is one swizzle row
 constexpr int kLgThreads = 192;
 constexpr int kLgMaxK = 32;
 
@@ -159,8 +160,10 @@ struct LogitsParams {
   StepParams s;    // workspace, shapes and flags shared with the fine rank (logits unused)
   uint32_t idesc;  // tcgen05 instruction descriptor (operand type, tile shape)
   int dim;         // hidden size
-  int n_m;         // kLgM-row blocks
-  int n_tiles;     // n_m * nc
+  int n_mp;        // pairs of kLgM-row blocks (one pair per cluster of two CTAs)
+  int sub_per_chunk;  // kLgN-column sub-tiles per chunk
+  int sub_per_row;    // ceil(vocab / kLgN)
+  int n_tiles;     // n_mp * nc
 };
 
 struct ReorderParams {
@@ -245,6 +248,7 @@ cudaError_t beam_rows_config(int dtype, bool bias, int vpl, int* occupancy);
 cudaError_t launch_beam_rows(const StepParams& p, int dtype, int vpl, int grid, cudaStream_t stream);
 cudaError_t launch_beam_select(const StepParams& p, int dtype, cudaStream_t stream);
 size_t logits_rows_smem_bytes();
+int logits_rows_max_clusters();  // co-resident clusters of two K0 CTAs (0 on error)
 cudaError_t logits_rows_config();  // once per device: the kernels' dynamic shared memory
 cudaError_t launch_logits_rows(const CUtensorMap& mh, const CUtensorMap& mw, const LogitsParams& lp, int grid,
                                cudaStream_t stream);

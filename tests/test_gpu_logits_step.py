@@ -166,19 +166,22 @@ def test_repeat_is_deterministic(dev):
             np.testing.assert_array_equal(o[key], gpu["all"][0][key])
 
 
-def test_ties_overflow_chunk_slots(dev, oracle_mod):
-    # weight rows repeat every 7 tokens: each row of logits holds 7 distinct values, the
-    # largest about 37 times per 256-token half chunk -- the second half of every chunk
-    # overflows the slots left to it, so it keeps its own top k; ties go to the smaller
-    # token id.  2 chunks x 41 slots x 4 beams stay within the fine rank's queue.
-    inp = make(6, 4, 1000, 64, "bf16", seed=23)
-    inp["weight"] = np.ascontiguousarray(inp["weight"][np.arange(1000) % 7])
+@pytest.mark.parametrize("k,period", [(4, 7), (16, 3)])
+def test_ties_overflow_chunk_slots(dev, oracle_mod, k, period):
+    # weight rows repeat every `period` tokens: each row of logits holds `period` distinct
+    # values, the largest 256 / period times per 256-token sub-tile -- a later sub-tile of
+    # every chunk overflows the slots left to it, so it keeps its own top k (one register
+    # pass for k <= 8, k passes above); ties go to the smaller token id.  For k = 4, 2 chunks
+    # x 41 slots x 4 beams stay within the fine rank's queue.
+    inp = make(6, k, 1000, 64, "bf16", seed=23)
+    inp["weight"] = np.ascontiguousarray(inp["weight"][np.arange(1000) % period])
     gpu = run_gpu(inp, dev)
     ora = check(oracle_mod, inp, gpu)
-    assert np.all(gpu["path"] == 0)
+    if k == 4:
+        assert np.all(gpu["path"] == 0)
     # identical weight rows give identical logits, so the tie order is exact
-    np.testing.assert_array_equal(gpu["token"], ora["token"][:, :4])
-    np.testing.assert_array_equal(gpu["parent"], ora["parent"][:, :4])
+    np.testing.assert_array_equal(gpu["token"], ora["token"][:, :k])
+    np.testing.assert_array_equal(gpu["parent"], ora["parent"][:, :k])
 
 
 def test_ties_overflow_batch_queue(dev, oracle_mod):
