@@ -108,9 +108,9 @@ LS_API ls_status ls_beam_step(const void* logits, ls_dtype logit_dtype, const fl
  * before the article's first traversal, which reads the [batch, k, vocab] logits the
  * projection wrote).  logits = hidden . weight^T are accumulated on the tensor cores a
  * tile at a time and never stored: each tile's epilogue runs the first traversal on it
- * (per beam and 512-token chunk the max, the sum of exp and the group maxima, and the
- * candidates at or above the chunk's R-top-k bound), then the fine rank of ls_beam_step
- * runs on those candidates.
+ * (per beam and chunk of 256 to 1024 tokens the max, the sum of exp and the group
+ * maxima, and the candidates at or above the chunk's R-top-k bound), then the fine rank of
+ * ls_beam_step runs on those candidates.
  *
  *  hidden      [batch, k, dim] row-major, dtype, device, 16-byte aligned: each beam's last
  *              decoder state.

@@ -2,29 +2,32 @@
 // inference article (31duo.com, itemid-283120), hierarchical decoding section, the first
 // traversal reads the [batch, beam, vocab] logits that the projection wrote; here the
 // logits of a tile of 128 beams x 256 tokens are accumulated by the tensor cores in tensor
-// memory and never stored.  The tile's epilogue computes, per beam and 512-token chunk,
-// what K1 (beam_rows.cu) computes from stored logits -- the chunk max, the sum of
-// exp(x - max), the group maxima -- and writes the chunk's candidates at or above its
-// R-top-k bound as slots, in the same record format; K2 (beam_select.cu) finishes the
-// step unchanged.
+// memory and never stored.  The epilogue computes, per beam and chunk (1 to 4 sub-tiles of
+// 256 tokens, the width chosen on the host), what K1 (beam_rows.cu) computes from stored
+// logits -- the chunk max, the sum of exp(x - max), the group maxima -- and writes the
+// chunk's candidates at or above its bound as slots, in the same record format; K2
+// (beam_select.cu) finishes the step unchanged.
 //
 // One CTA per SM, in clusters of two CTAs that take adjacent 128-row blocks of the same
-// chunk, persistent over tiles of 2 x 128 rows x 512 columns (a chunk), 6 warps per CTA:
+// chunk, persistent over tiles of 2 x 128 rows x one chunk, 6 warps per CTA:
 //   warp 0     TMA producer: a ring of [128 x kLgBK] hidden tiles and [256 x kLgBK] weight
 //              tiles (f16 / bf16, swizzled rows of kLgBK elements), 192 KB in all; each
-//              CTA of the pair loads half of the weight tile and multicasts it to both, so a
-//              CTA pulls 32 KB from L2 per stage instead of 48 KB;
+//              CTA of the pair loads half of the weight tile and multicasts it to both (L2
+//              serves 32 KB per CTA and stage instead of 48 KB), and prefetches the half of
+//              the next sub-tile into L2;
 //   warp 1     owns 512 tensor-memory columns; one lane issues tcgen05.mma (M 128, N 256,
 //              K 16) into one of two 256-column accumulators, so one sub-tile's epilogue
 //              overlaps the next sub-tile's products;
-//   warps 2-5  epilogue: a thread is one beam (one tensor-memory lane); it reads its 256
-//              accumulators of a sub-tile twice: max and group maxima, then the sum of exp
-//              and the candidates at or above the bound.
-// A chunk keeps every candidate at or above its bound when they fit its slots, and
-// otherwise its own top k (x descending, then token ascending), so the fine rank never
-// needs the logits.  Every wait is bounded: one that runs out sets the timeout bit of the
-// status word, and the CTA lets its copies and products finish, frees its tensor memory
-// and returns.
+//   warps 2-5  epilogue: a thread is one beam (one tensor-memory lane).  Pass 1 reads its
+//              256 accumulators of a sub-tile once: block and group maxima and the sum of
+//              exp; pass 2 reads again only the blocks whose max reaches the bound and
+//              stores the candidates from survivor bit masks.
+// The bound is the larger of two lower bounds of the chunk's k-th largest x: the k-th
+// largest group maximum and (k <= 8) the k-th largest 32-column block maximum.  A chunk
+// keeps every candidate at or above its bound when they fit its slots, and otherwise its
+// own top k (x descending, then token ascending), so the fine rank never needs the logits.
+// Every wait is bounded: one that runs out sets the timeout bit of the status word, and the
+// CTA lets its copies and products finish, frees its tensor memory and returns.
 #include <cuda.h>
 
 #include <climits>
