@@ -10,6 +10,9 @@ GPU: the beam state and the two cache buffers alternate between two sets
 With ``inplace=True`` the cache is one buffer refreshed in place, copy on change
 (``ls_cache_refresh_inplace``): rows that continue themselves are not moved.
 
+``step_projection`` takes the decoder states and the output projection instead of logits
+(``ls_logits_beam_step``: the logits are made on the tensor cores and never stored).
+
 With ``max_steps`` > 0 every step writes its tokens and parents straight into a
 [max_steps, batch, k] history, and ``finalize`` turns the history into the token
 sequence and length of every final beam (``ls_backtrack``): the n-best list of each
@@ -24,7 +27,7 @@ from __future__ import annotations
 import torch
 
 from . import (check, ls_backtrack, ls_beam_step, ls_beam_step_workspace_size, ls_cache_refresh_inplace,
-               ls_cache_reorder, ls_workspace_init)
+               ls_cache_reorder, ls_logits_beam_step, ls_workspace_init)
 
 
 class BeamSearchLoop:
@@ -85,12 +88,24 @@ class BeamSearchLoop:
     def step(self, logits: torch.Tensor, t: int, bias=None, stream=None) -> int:
         """Decode step t (1-based): beam step on `logits` [batch, k, vocab], then the cache refresh of
         positions [0, t).  Returns the index of the state set holding this step's outputs."""
+        return self._advance(t, stream, lambda s, n, tok, par: check(
+            ls_beam_step(logits, bias, self.scores[s], self.finished[s], self.eos_id, tok, par, self.scores[n],
+                         self.finished[n], self.workspace, stream), "ls_beam_step"))
+
+    def step_projection(self, hidden: torch.Tensor, weight: torch.Tensor, t: int, bias=None, stream=None) -> int:
+        """Decode step t (1-based) from the decoder states `hidden` [batch, k, dim] and the output projection
+        `weight` [vocab, dim] (f16 or bf16; logits = hidden . weight^T, never stored), then the cache refresh
+        of positions [0, t).  Returns the index of the state set holding this step's outputs."""
+        return self._advance(t, stream, lambda s, n, tok, par: check(
+            ls_logits_beam_step(hidden, weight, bias, self.scores[s], self.finished[s], self.eos_id, tok, par,
+                                self.scores[n], self.finished[n], self.workspace, stream), "ls_logits_beam_step"))
+
+    def _advance(self, t: int, stream, beam_step) -> int:
         if self.max_steps > 0 and not 1 <= t <= self.max_steps:
             raise ValueError(f"decode step {t} outside 1..{self.max_steps}")
         s, n = self.cur, 1 - self.cur
         tok, par = self.token_out(t), self.parent_out(t)
-        check(ls_beam_step(logits, bias, self.scores[s], self.finished[s], self.eos_id, tok, par,
-                           self.scores[n], self.finished[n], self.workspace, stream), "ls_beam_step")
+        beam_step(s, n, tok, par)
         if self.cache is not None:
             if self.inplace:
                 check(ls_cache_refresh_inplace(self.cache[0], par, t, self.workspace, stream),

@@ -85,3 +85,66 @@ def test_c5_trajectory_sampled(dev, oracle_mod):
     for i in sorted(alive):
         np.testing.assert_array_equal(seq[i], o_seq[i])
         np.testing.assert_array_equal(ln[i], o_len[i])
+
+
+def test_projection_loop_trajectory(dev, oracle_mod):
+    """8 decode steps of the loop driven by decoder states (step_projection: the beam step fused into
+    the output projection, bf16, hidden size 128), the cache refreshed in place, against the oracle's
+    own trajectory (projection in fp64, then the naive step).  The logits carry the projection's
+    rounding (parity.projection_logit_bound, B per step); a beam score carries it from every step
+    before, so at step t scores agree within t (2B + 1e-5), and a batch leaves the comparison once the
+    oracle's gap at the k-th place falls below twice that."""
+    from parity import projection_logit_bound
+
+    w = synth.Workload("proj_loop", 16, 4, 3000, "bf16", 31, logit_var=2.0, beam_range=(-5.0, 0.0))
+    dim, steps = 128, 8
+    kv = (2, 4, 8, 16)
+    shape = (kv[0], w.rows, kv[1], kv[2], kv[3])
+    weight = synth.projection(w, dim)
+    wv = (weight.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    d_weight = torch.from_numpy(weight).view(torch.int16).view(torch.bfloat16).to(dev)
+    cache0 = synth.kv_cache(shape, w.seed)
+    loop = BeamSearchLoop(w.batch, w.k, w.vocab, w.eos_id, kv_shape=kv, device=dev,
+                          caches=[torch.from_numpy(cache0).to(dev)], max_steps=steps, inplace=True)
+    beam0 = synth.beam_scores(w, 0)
+    loop.reset(torch.from_numpy(beam0).to(dev))
+    o_cache, o_beam = cache0.copy(), beam0.copy()
+    o_fin = np.zeros((w.batch, w.k), np.uint8)
+    alive = set(range(w.batch))
+    compared = 0
+    o_tok, o_par = [], []
+    for t in range(1, steps + 1):
+        hid = synth.hidden_states(w, dim, step=t)
+        idx = loop.step_projection(torch.from_numpy(hid).view(torch.int16).view(torch.bfloat16).to(dev), d_weight, t)
+        out = {key: v.cpu().numpy() for key, v in loop.outputs(idx).items()}
+        ora = oracle_mod.logits_beam_step(hid, weight, o_beam, dtype="bf16", finished=o_fin, eos_id=w.eos_id,
+                                          m_out=w.k + 8)
+        hv = (hid.astype(np.uint32) << 16).view(np.float32).reshape(-1, dim).astype(np.float64)
+        bound = projection_logit_bound(hv, wv).reshape(w.batch, w.k, -1).max(axis=(1, 2))
+        stol = t * (2.0 * bound + 1e-5)
+        gaps = boundary_gaps(ora, w.k)
+        for i in sorted(alive):
+            compare_step(out, ora, w.k, "bf16", finished=o_fin, eos_id=w.eos_id, batches=[i], score_tol=stol,
+                         gap_tol=2.0 * stol)
+            if gaps[i] < 2.0 * stol[i]:
+                alive.discard(i)
+            else:
+                assert (out["token"][i] == ora["token"][i, : w.k]).all()
+                assert (out["parent"][i] == ora["parent"][i, : w.k]).all()
+                compared += 1
+        o_tok.append(ora["token"][:, : w.k].astype(np.int32))
+        o_par.append(ora["parent"][:, : w.k].astype(np.int32))
+        o_cache = oracle_mod.cache_refresh_inplace(o_cache, ora["parent"][:, : w.k], t)
+        o_beam = ora["score"][:, : w.k].astype(np.float32)
+        o_fin = ora["finished"][:, : w.k].astype(np.uint8)
+    assert compared >= w.batch * steps // 2
+    final = loop.current_cache().cpu().numpy()
+    for i in sorted(alive):
+        sl = slice(i * w.k, (i + 1) * w.k)
+        assert np.array_equal(final[:, sl].view(np.int16), o_cache[:, sl].view(np.int16))
+    seq, ln = loop.finalize(steps)
+    o_seq, o_len = oracle_mod.backtrack(np.stack(o_tok), np.stack(o_par), w.eos_id)
+    seq, ln = seq.cpu().numpy(), ln.cpu().numpy()
+    for i in sorted(alive):
+        np.testing.assert_array_equal(seq[i], o_seq[i])
+        np.testing.assert_array_equal(ln[i], o_len[i])
