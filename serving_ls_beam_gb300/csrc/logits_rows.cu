@@ -299,6 +299,9 @@ __global__ void __launch_bounds__(kLgThreads, 1)
   const uint32_t tmem = *tmem_slot;
   // the hidden states may come from the previous kernel of the stream
   grid_dependency_wait();
+  // the fine rank may be scheduled from now on: its CTAs take the SMs this grid's CTAs leave
+  // (they warm up, then wait for the whole grid before reading its records)
+  grid_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
