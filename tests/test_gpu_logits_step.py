@@ -7,7 +7,7 @@ parity.projection_logit_bound: scores agree within twice that bound (the logit a
 log-sum-exp each move by at most the bound) plus 1e-5, and a selected pair may differ
 from the oracle's only where the oracle's score gap is below twice the score tolerance.
 
-The cases span several 128-row blocks and 512-token chunks with ragged tails in rows,
+The cases span several 128-row blocks and chunks (of 1 to 4 sub-tiles of 256 tokens) with ragged tails in rows,
 vocab and hidden size (not a multiple of the 64-element stage), k = 1 ... 32 (group counts
 1 ... 32, k below and equal to its group count), f16 and bf16, bias, finished beams, vocab
 equal to k, ties heavy enough to overflow a chunk's slots (the chunk then keeps its own top
