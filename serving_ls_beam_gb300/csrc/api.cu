@@ -428,7 +428,7 @@ ls_status ls_logits_beam_step(const void* hidden, const void* weight, ls_dtype d
 
   CUtensorMap mh, mw;
   if (!encode_kmajor(&mh, hidden, dtype, dim, rows, kLgM) ||
-      !encode_kmajor(&mw, weight, dtype, dim, vocab, kLgN / 2))  // each CTA of a pair loads half
+      !encode_kmajor(&mw, weight, dtype, dim, vocab, kLgN))
     return cuda_fail(cudaErrorUnknown);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_logits_rows(mh, mw, lp, grid, st);

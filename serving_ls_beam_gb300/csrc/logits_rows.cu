@@ -9,12 +9,12 @@
 // (beam_select.cu) finishes the step unchanged.
 //
 // One CTA per SM, in clusters of two CTAs that take adjacent 128-row blocks of the same
-// chunk, persistent over tiles of 2 x 128 rows x one chunk, 6 warps per CTA:
+// chunk (so the pair reads each weight tile from L2 at about the same time), persistent
+// over tiles of 2 x 128 rows x one chunk, 6 warps per CTA:
 //   warp 0     TMA producer: a ring of [128 x kLgBK] hidden tiles and [256 x kLgBK] weight
-//              tiles (f16 / bf16, swizzled rows of kLgBK elements), 192 KB in all; each
-//              CTA of the pair loads half of the weight tile and multicasts it to both (L2
-//              serves 32 KB per CTA and stage instead of 48 KB), and prefetches the half of
-//              the next sub-tile into L2;
+//              tiles (f16 / bf16, swizzled rows of kLgBK elements), 192 KB in all, each CTA
+//              loading its own tiles; the pair's first CTA prefetches the next sub-tile's
+//              weight tile into L2;
 //   warp 1     owns 512 tensor-memory columns; one lane issues tcgen05.mma (M 128, N 256,
 //              K 16) into one of two 256-column accumulators, so one sub-tile's epilogue
 //              overlaps the next sub-tile's products;
@@ -60,7 +60,6 @@ constexpr long long kLgDrainNs = 2000000000LL;
 // sleep between polls of a waiting thread: the MMA lane reacts within ~30 ns to arrived data
 // (a stage is ~280 ns of tensor work); the producer has 4 stages of slack
 constexpr uint32_t kLgSleepMma = 32, kLgSleepProducer = 128, kLgSleepEpilogue = 64;
-constexpr uint16_t kLgPairMask = 0x3;  // both CTAs of the cluster
 static_assert(kLgABytes % 1024 == 0 && kLgBBytes % 1024 == 0, "tiles must keep 1024-byte alignment");
 static_assert(kLgBK * 2 == kLgSwizzleBytes, "a stage row is one swizzle row");
 
@@ -77,27 +76,10 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// The same load, written to this offset of shared memory in every CTA of cta_mask and
-// completing bytes on the barrier at this offset in each of them.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar,
-                                               uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
-      : "memory");
-}
-
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
-}
-
-// Every thread of both CTAs of the cluster.
-__device__ __forceinline__ void cluster_sync() {
-  __syncwarp();  // .aligned: the warp reaches it converged
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
@@ -128,14 +110,6 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint6
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
-// The same, arriving on the barrier at this offset in every CTA of cta_mask.
-__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t cta_mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                   bar),
-               "h"(cta_mask)
-               : "memory");
-}
-
 // Shared-memory matrix descriptor of a K-major tile written by TMA with the 128- or 64-byte
 // swizzle: rows of kLgSwizzleBytes, 8-row swizzle atoms stacked along M / N.
 __device__ __forceinline__ uint64_t kmajor_desc(uint32_t saddr) {
@@ -276,7 +250,7 @@ __global__ void __launch_bounds__(kLgThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kLgStages; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 2);  // both CTAs' products must be done before the stage refills
+      mbar_init(empty_bar(s), 1);  // this CTA's products are done before the stage refills
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
@@ -293,8 +267,6 @@ __global__ void __launch_bounds__(kLgThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  // the peer's barriers exist before either CTA multicasts into it
-  cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   // the hidden states may come from the previous kernel of the stream
@@ -333,11 +305,10 @@ __global__ void __launch_bounds__(kLgThreads, 1)
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(full_bar(s), kLgABytes + kLgBBytes);  // own A, both halves of B
+            mbar_arrive_expect_tx(full_bar(s), kLgABytes + kLgBBytes);
             tma_load_2d(sA + (uint32_t)s * kLgABytes, &tmap_h, kb * kLgBK, mb * kLgM, full_bar(s));
-            tma_load_2d_mc(sB + (uint32_t)s * kLgBBytes + (uint32_t)crank * (kLgBBytes / 2), &tmap_w, kb * kLgBK,
-                           n0 + crank * (kLgN / 2), full_bar(s), kLgPairMask);
-            if (n_next >= 0) tma_prefetch_2d(&tmap_w, kb * kLgBK, n_next + crank * (kLgN / 2));
+            tma_load_2d(sB + (uint32_t)s * kLgBBytes, &tmap_w, kb * kLgBK, n0, full_bar(s));
+            if (n_next >= 0 && crank == 0) tma_prefetch_2d(&tmap_w, kb * kLgBK, n_next);
           }
         }
       }
@@ -381,7 +352,7 @@ __global__ void __launch_bounds__(kLgThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < kLgBK / 16; ++kk)  // 16 elements = 32 bytes along the swizzled row
               umma_f16(d, a0 + 2u * kk, b0 + 2u * kk, idesc, (uint32_t)((kb | kk) != 0));
-            umma_commit_mc(empty_bar(s), kLgPairMask);  // the stage is free in both CTAs once done
+            umma_commit(empty_bar(s));  // the stage is free once these products are done
           }
           if (!ok) {
             umma_commit(tfull_bar(buf));  // release the epilogue; it sees the abort flag
@@ -668,11 +639,9 @@ __global__ void __launch_bounds__(kLgThreads, 1)
       }
     }
   }
-  // teardown: every product and tensor-memory read is done before the columns are freed,
-  // and neither CTA leaves while the other may still write into its shared memory
+  // teardown: every product and tensor-memory read is done before the columns are freed
   tc_fence_before();
   __syncthreads();
-  cluster_sync();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
