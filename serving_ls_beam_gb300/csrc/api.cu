@@ -26,6 +26,8 @@ struct DeviceInfo {
   int logits_clusters = 0;    // co-resident clusters of two K0 CTAs
   // K1 occupancy per [dtype][bias][vpl index]; 0 = not configured yet
   int step_occ[3][2][3] = {};
+  // K1s occupancy per [dtype][bias][stages]
+  int strip_occ[3][2][kStMaxStages + 1] = {};
   int copy_occ[5] = {};
   int inplace_occ[5] = {};
   int inplace_tma_occ = 0;
@@ -41,13 +43,17 @@ int unit_index(int unit) { return unit == 16 ? 0 : unit == 8 ? 1 : unit == 4 ? 2
 struct Debug {
   int flags = 0;
   long long spin_ns = kDefaultSpinNs;
-  int vpl = 0;  // 0 = plan's choice
+  int vpl = 0;     // 0 = plan's choice
+  int stages = 0;  // K1s stage buffers per warp, 0 = plan's choice
+  int parts = 0;   // K1s strips per row, 0 = plan's choice
   bool check_ptrs = true;
 };
 
-// LS_BEAM_DEBUG: comma-separated "exact", "ipplain", "spin=<ns>", "vpl=<4|8|16>", "nocheck".
+// LS_BEAM_DEBUG: comma-separated "exact", "ipplain", "chunk", "spin=<ns>", "vpl=<4|8|16>",
+// "stages=<2..8>", "parts=<n>", "nocheck".
 Debug read_debug() {
   Debug d;
+  d.flags = kFlagChunkRows;  // K1 by chunks until K1s is measured faster
   const char* env = std::getenv("LS_BEAM_DEBUG");
   if (!env || !*env) return d;
   char buf[256];
@@ -57,11 +63,17 @@ Debug read_debug() {
     if (!std::strcmp(tok, "exact")) d.flags |= kFlagForceExact;
     else if (!std::strcmp(tok, "ipplain")) d.flags |= kFlagPlainInplace;
     else if (!std::strncmp(tok, "spin=", 5)) d.spin_ns = std::atoll(tok + 5);
+    else if (!std::strcmp(tok, "chunk")) d.flags |= kFlagChunkRows;
+    else if (!std::strcmp(tok, "strips")) d.flags &= ~kFlagChunkRows;
     else if (!std::strncmp(tok, "vpl=", 4)) d.vpl = std::atoi(tok + 4);
+    else if (!std::strncmp(tok, "stages=", 7)) d.stages = std::atoi(tok + 7);
+    else if (!std::strncmp(tok, "parts=", 6)) d.parts = std::atoi(tok + 6);
     else if (!std::strcmp(tok, "nocheck")) d.check_ptrs = false;
   }
   if (d.spin_ns < 0) d.spin_ns = 0;
   if (vpl_index(d.vpl) < 0) d.vpl = 0;
+  if (d.stages < 2 || d.stages > kStMaxStages) d.stages = 0;
+  if (d.parts < 0) d.parts = 0;
   return d;
 }
 
@@ -117,6 +129,48 @@ ls_status plan_rows(DeviceInfo* di, const Debug& dbg, int dtype, int es, bool bi
   out->units = rows * nc;
   const long long grid_full = (long long)di->sms * occ;
   const long long grid_need = (out->units + kRowWarps - 1) / kRowWarps;
+  out->grid = grid_need < grid_full ? grid_need : grid_full;
+  return LS_OK;
+}
+
+int strip_occupancy(DeviceInfo* di, int dtype, bool bias, int vpl, int stages) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int& occ = di->strip_occ[dtype][bias ? 1 : 0][stages];
+  if (occ == 0) {
+    int o = 0;
+    if (beam_strips_config(dtype, bias, vpl, stages, &o) != cudaSuccess || o < 1) return 0;
+    occ = o;
+  }
+  return occ;
+}
+
+// K1s's launch plan for `rows` rows of `vocab` logits of `es` bytes: W strips per row (the
+// unit count rows * W fits the resident warps once, W at most the stages of the shortest
+// row, so every strip has at least one stage), one unit per warp.
+struct StripPlan {
+  int vpl, stages, parts;
+  long long units, grid;
+};
+
+ls_status plan_strips(DeviceInfo* di, const Debug& dbg, int dtype, int es, bool bias, int vocab, long long rows,
+                      const WsLayout& wl, StripPlan* out) {
+  const int vpl = (es == 2 && bias) ? 4 : 8;  // 64 packed or 32 float elements per lane and stage
+  const int stages = dbg.stages ? dbg.stages : 4;
+  const int occ = strip_occupancy(di, dtype, bias, vpl, stages);
+  if (occ < 1) return cuda_fail(cudaErrorUnknown);
+  const long long cv = 32ll * vpl;
+  const long long ns_min = ((long long)vocab * es / 16 + cv - 1) / cv;  // stages of a 16-byte aligned row
+  const long long slots = (long long)di->sms * occ * kStWarps;
+  long long w = dbg.parts ? dbg.parts : slots / (rows > 0 ? rows : 1);
+  if (w > ns_min) w = ns_min;
+  if (w > wl.nc_max) w = wl.nc_max;
+  if (w < 1) w = 1;
+  out->vpl = vpl;
+  out->stages = stages;
+  out->parts = (int)w;
+  out->units = rows * w;
+  const long long grid_full = (long long)di->sms * occ;
+  const long long grid_need = (out->units + kStWarps - 1) / kStWarps;
   out->grid = grid_need < grid_full ? grid_need : grid_full;
   return LS_OK;
 }
@@ -285,11 +339,16 @@ ls_status ls_beam_step(const void* logits, ls_dtype logit_dtype, const float* bi
 
   const int dtype = (int)logit_dtype;
   const long long rows = (long long)batch * k;
-  RowPlan plan;
-  const ls_status ps = plan_rows(di, dbg, dtype, es, bias != nullptr, vocab, rows, wl, &plan);
+  // K1s (a warp streams a strip of a row) unless forced to K1 (fixed-size chunks); K1s
+  // holds the group maxima in lanes, so k <= 32
+  const bool strips = !(dbg.flags & kFlagChunkRows) && k <= 32;
+  RowPlan plan{};
+  StripPlan splan{};
+  const ls_status ps = strips ? plan_strips(di, dbg, dtype, es, bias != nullptr, vocab, rows, wl, &splan)
+                              : plan_rows(di, dbg, dtype, es, bias != nullptr, vocab, rows, wl, &plan);
   if (ps != LS_OK) return ps;
-  const int vpl = plan.vpl, nc = plan.nc;
-  const long long units = plan.units, grid = plan.grid;
+  const int vpl = strips ? splan.vpl : plan.vpl, nc = strips ? splan.parts : plan.nc;
+  const long long units = strips ? splan.units : plan.units, grid = strips ? splan.grid : plan.grid;
 
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   StepParams p;
@@ -324,8 +383,9 @@ ls_status ls_beam_step(const void* logits, ls_dtype logit_dtype, const float* bi
   if (!select_configured(di)) return cuda_fail(cudaErrorUnknown);
   p.units = units;
   p.spin_limit_ns = dbg.spin_ns;
+  p.stages = splan.stages;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_beam_rows(p, dtype, vpl, (int)grid, st);
+  cudaError_t e = strips ? launch_beam_strips(p, dtype, vpl, (int)grid, st) : launch_beam_rows(p, dtype, vpl, (int)grid, st);
   if (e == cudaSuccess) e = launch_beam_select(p, dtype, st);
   return e == cudaSuccess ? LS_OK : cuda_fail(e);
 }

@@ -17,6 +17,16 @@ constexpr int kRowWarps = kRowThreads / 32;
 constexpr int kRowListOff = 128;   // per-warp mbarriers in [0, 128), then per-warp item lists
 constexpr int kRowBarBytes = kRowListOff + kRowWarps * 32 * 4;  // start of the stage buffers
 constexpr int kVplMin = 4;         // smallest vectors-per-lane variant built
+// K1s (beam_strips.cu): CTAs of kStWarps independent warps; a warp streams one strip of a
+// beam's row at a time through its own ring of `stages` stage buffers (at most
+// kStMaxStages) and keeps the strip's candidates in a list of kStListCap entries.
+constexpr int kStThreads = 128;
+constexpr int kStWarps = kStThreads / 32;
+constexpr int kStMaxStages = 8;
+constexpr int kStListCap = 128;
+constexpr int kStTighten = 24;   // candidates of one stage above which the bound is tightened
+constexpr int kStListOff = 256;  // per-warp mbarriers in [0, 256), then the per-warp lists
+constexpr int kStBarBytes = kStListOff + kStWarps * kStListCap * 8;  // start of the stage buffers
 // K2 (beam_select.cu): one CTA per batch.
 constexpr int kSelThreads = 256;
 constexpr int kSelWarps = kSelThreads / 32;
@@ -48,6 +58,7 @@ constexpr uint32_t kDevInternal = 1u << 2;
 // Debug flags (LS_BEAM_DEBUG).
 constexpr int kFlagForceExact = 1;
 constexpr int kFlagPlainInplace = 2;  // the in-place refresh without bulk copies
+constexpr int kFlagChunkRows = 4;     // the beam step's first kernel by fixed-size chunks (K1)
 
 // ---------------------------------------------------------------- workspace layout
 struct alignas(16) RowStat {
@@ -152,6 +163,7 @@ struct StepParams {
   int rec_stride;
   int flags;
   int sel_stage_bytes;  // K2: bytes of a batch's slots copied to shared memory, 0 = read in place
+  int stages;           // K1s: stage buffers per warp
   long long units;  // rows * nc
   long long spin_limit_ns;
 };
@@ -247,6 +259,9 @@ size_t beam_rows_smem_bytes(int vpl);
 cudaError_t beam_rows_config(int dtype, bool bias, int vpl, int* occupancy);
 cudaError_t launch_beam_rows(const StepParams& p, int dtype, int vpl, int grid, cudaStream_t stream);
 cudaError_t launch_beam_select(const StepParams& p, int dtype, cudaStream_t stream);
+size_t beam_strips_smem_bytes(int vpl, int stages);
+cudaError_t beam_strips_config(int dtype, bool bias, int vpl, int stages, int* occupancy);
+cudaError_t launch_beam_strips(const StepParams& p, int dtype, int vpl, int grid, cudaStream_t stream);
 size_t logits_rows_smem_bytes();
 int logits_rows_max_clusters();  // co-resident clusters of two K0 CTAs (0 on error)
 cudaError_t logits_rows_config();  // once per device: the kernels' dynamic shared memory
