@@ -23,6 +23,7 @@ struct DeviceInfo {
   int sms = 0;
   bool select_ready = false;  // K2's dynamic shared-memory limit raised
   bool logits_ready = false;  // K0's dynamic shared-memory limit raised
+  bool fused_ready = false;   // K3's dynamic shared-memory limit raised
   int logits_clusters = 0;    // co-resident clusters of two K0 CTAs
   // K1 occupancy per [dtype][bias][vpl index]; 0 = not configured yet
   int step_occ[3][2][3] = {};
@@ -49,11 +50,10 @@ struct Debug {
   bool check_ptrs = true;
 };
 
-// LS_BEAM_DEBUG: comma-separated "exact", "ipplain", "chunk", "spin=<ns>", "vpl=<4|8|16>",
-// "stages=<2..8>", "parts=<n>", "nocheck".
+// LS_BEAM_DEBUG: comma-separated "exact", "ipplain", "chunk", "strips", "fused", "nofused",
+// "spin=<ns>", "vpl=<4|8|16>", "stages=<2..8>", "parts=<n>", "nocheck".
 Debug read_debug() {
   Debug d;
-  d.flags = kFlagChunkRows;  // K1 by chunks until K1s is measured faster
   const char* env = std::getenv("LS_BEAM_DEBUG");
   if (!env || !*env) return d;
   char buf[256];
@@ -65,6 +65,8 @@ Debug read_debug() {
     else if (!std::strncmp(tok, "spin=", 5)) d.spin_ns = std::atoll(tok + 5);
     else if (!std::strcmp(tok, "chunk")) d.flags |= kFlagChunkRows;
     else if (!std::strcmp(tok, "strips")) d.flags &= ~kFlagChunkRows;
+    else if (!std::strcmp(tok, "fused")) d.flags |= kFlagFused;
+    else if (!std::strcmp(tok, "nofused")) d.flags |= kFlagNoFused;
     else if (!std::strncmp(tok, "vpl=", 4)) d.vpl = std::atoi(tok + 4);
     else if (!std::strncmp(tok, "stages=", 7)) d.stages = std::atoi(tok + 7);
     else if (!std::strncmp(tok, "parts=", 6)) d.parts = std::atoi(tok + 6);
@@ -72,7 +74,7 @@ Debug read_debug() {
   }
   if (d.spin_ns < 0) d.spin_ns = 0;
   if (vpl_index(d.vpl) < 0) d.vpl = 0;
-  if (d.stages < 2 || d.stages > kStMaxStages) d.stages = 0;
+  if (d.stages < 0 || d.stages > kStMaxStages) d.stages = 0;
   if (d.parts < 0) d.parts = 0;
   return d;
 }
@@ -155,7 +157,7 @@ struct StripPlan {
 ls_status plan_strips(DeviceInfo* di, const Debug& dbg, int dtype, int es, bool bias, int vocab, long long rows,
                       const WsLayout& wl, StripPlan* out) {
   const int vpl = (es == 2 && bias) ? 4 : 8;  // 64 packed or 32 float elements per lane and stage
-  const int stages = dbg.stages ? dbg.stages : 4;
+  const int stages = dbg.stages ? dbg.stages : 2;
   const int occ = strip_occupancy(di, dtype, bias, vpl, stages);
   if (occ < 1) return cuda_fail(cudaErrorUnknown);
   const long long cv = 32ll * vpl;
@@ -203,6 +205,15 @@ bool select_configured(DeviceInfo* di) {
   if (!di->select_ready) {
     if (beam_select_config() != cudaSuccess) return false;
     di->select_ready = true;
+  }
+  return true;
+}
+
+bool fused_configured(DeviceInfo* di) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!di->fused_ready) {
+    if (beam_fused_config() != cudaSuccess) return false;
+    di->fused_ready = true;
   }
   return true;
 }
@@ -339,6 +350,42 @@ ls_status ls_beam_step(const void* logits, ls_dtype logit_dtype, const float* bi
 
   const int dtype = (int)logit_dtype;
   const long long rows = (long long)batch * k;
+  // K3 (the whole step of a batch in one CTA) when the batches fill the GPU by themselves and
+  // every strip's block maxima fit its shared memory
+  int fu_parts = (kFuThreads / 32) / k;
+  if (dbg.parts > 0 && dbg.parts * k <= kFuThreads / 32) fu_parts = dbg.parts;
+  const int fu_vpl = (dtype == LS_DTYPE_F32 || bias) ? 4 : 8;
+  const long long fu_ns = ((15 + (long long)vocab * es + 15) / 16 + 32ll * fu_vpl - 1) / (32ll * fu_vpl);
+  const bool fused = !(dbg.flags & kFlagNoFused) && k <= kFuMaxK && fu_parts >= 1 &&
+                     (fu_ns + fu_parts - 1) / fu_parts <= kFuMaxStages &&
+                     ((dbg.flags & kFlagFused) || 2ll * batch >= di->sms);
+  if (fused) {
+    if (!fused_configured(di)) return cuda_fail(cudaErrorUnknown);
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    StepParams p = {};
+    p.logits = logits;
+    p.bias = bias;
+    p.beam = beam_scores;
+    p.finished = finished;
+    p.out_token = out_token;
+    p.out_parent = out_parent;
+    p.out_score = out_score;
+    p.out_finished = out_finished;
+    p.status = reinterpret_cast<uint32_t*>(ws + wl.status_off);
+    p.rowstat = reinterpret_cast<RowStat*>(ws + wl.rowstat_off);
+    p.bstat = reinterpret_cast<int32_t*>(ws + wl.bstat_off);
+    p.batch = batch;
+    p.k = k;
+    p.vocab = vocab;
+    p.eos = eos_id;
+    p.rows = (int)rows;
+    p.nc = fu_parts;  // strips per row, one warp each
+    p.stages = (int)((fu_ns + fu_parts - 1) / fu_parts);  // block-max rows per strip    p.groups = wl.groups;
+    p.flags = dbg.flags;
+    p.spin_limit_ns = dbg.spin_ns;
+    const cudaError_t e = launch_beam_fused(p, dtype, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? LS_OK : cuda_fail(e);
+  }
   // K1s (a warp streams a strip of a row) unless forced to K1 (fixed-size chunks); K1s
   // holds the group maxima in lanes, so k <= 32
   const bool strips = !(dbg.flags & kFlagChunkRows) && k <= 32;

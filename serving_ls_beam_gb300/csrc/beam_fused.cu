@@ -1,0 +1,631 @@
+// Beam-step kernel K3: the whole step of one batch in one CTA -- both traversals of the
+// batch's beams and the fine rank -- for batches that fill the GPU on their own.
+//
+// Method: LightSeq inference article (31duo.com, itemid-283120), hierarchical decoding
+// section.  First traversal: split a beam's logits into groups, take each group's max; the
+// k-th largest of those maxima (their min when there are exactly k groups) is the R-top-k
+// bound, never above the true k-th largest; log_sum_exp in the same pass.  Second
+// traversal: keep the logits at or above R-top-k, rescore them as beam_score + logit -
+// log_sum_exp, and one sort of that short queue per batch gives the exact top-k.
+//
+// GB300 design:
+//  * One CTA per batch, kFuWarps warps.  The batch's k rows are cut into k * W strips
+//    (units); a warp streams its strips with plain 16-byte loads (ld.global.cs), the next
+//    stage's loads issued before the current stage is worked on (two register buffers), so
+//    every warp keeps a stage of loads in flight: on this part plain loads sustain more
+//    read bandwidth than one bulk-copy ring per warp.
+//  * First traversal, per stage and in registers: each lane's max of its 64-element block (its
+//    8 vectors of the stage) goes to shared memory, and a running (max, sum of exp(x - max))
+//    per lane accumulates log_sum_exp.  The blocks partition the row, so the k-th largest
+//    block max of a row is its R-top-k bound (groups = blocks: the article's "any split").
+//  * Second traversal, once the CTA has every block max: each row's R is the k-th largest of
+//    its block maxima, and only the blocks whose max reaches R (a handful per row) are read
+//    again -- from L2, 128 bytes each -- for their elements x >= R, rescored and ranked in
+//    shared memory (each key's rank counted against the others; the k of rank < k are the
+//    outputs).  Nothing else goes through global memory between the traversals and the rank.
+//  * More than kFuCap candidates (ties), or the forced exact mode, send the batch to an exact
+//    path: a radix select of every beam's top-k over its logits.
+#include "ls_device.cuh"
+#include "ls_dtype.cuh"
+#include "ls_internal.h"
+#include "ls_strip.cuh"
+
+namespace lsb {
+namespace {
+
+constexpr int kFuWarps = kFuThreads / 32;
+constexpr int kFuCap = 512;  // keys the fine rank holds
+
+enum { FROW_LIVE = 0, FROW_FIN = 1, FROW_DEAD = 2 };
+
+// Dynamic shared memory: the per-warp rings of kFuRing stages (the rank keys reuse them once
+// the first traversal is done), then the block maxima, [strip][stage of the strip][lane].
+constexpr int kFuRing = 3;
+constexpr int kFuList = 32;  // candidates a strip keeps
+constexpr int kFuHits = 64;  // blocks a strip reads again
+
+struct __align__(16) FuSmem {
+  Key* keys;                        // kFuCap keys, over the rings
+  float um[kFuWarps], us[kFuWarps];  // strip max and sum of exp(x - max)
+  float ur[kFuWarps];                // strip bound: k-th largest block max of the strip
+  int ucnt[kFuWarps], uovf[kFuWarps];
+  float2 cand[kFuWarps][kFuList];    // the strip's candidates (x, token)
+  int hits[kFuWarps][kFuHits];       // the strip's blocks reaching its bound (stage * 32 + lane)
+  double c[kFuMaxK];  // beam_score - log_sum_exp of each live row
+  float beam[kFuMaxK], lse[kFuMaxK], R[kFuMaxK];
+  int fin[kFuMaxK], kind[kFuMaxK], ncand[kFuMaxK];
+  int nkeys, path;
+  // exact path
+  unsigned int hist[256];
+  unsigned int prefix, pmask;
+  int need;
+  int wc[kFuWarps];
+};
+
+}  // namespace
+
+size_t beam_fused_smem_bytes(int vpl, int sps) {
+  const size_t ring = (size_t)kFuWarps * kFuRing * 32 * vpl * 16;
+  return (ring > kFuCap * sizeof(Key) ? ring : kFuCap * sizeof(Key)) + (size_t)kFuWarps * sps * 32 * 4;
+}
+
+namespace {
+
+// Append key k (when take) to sm.keys with one shared atomic per warp; returns nothing, the
+// count may exceed kFuCap (then the batch takes the exact path).
+__device__ __forceinline__ void append_key(FuSmem& sm, bool take, const Key& k) {
+  const int lane = threadIdx.x & 31;
+  const unsigned m = __ballot_sync(0xffffffffu, take);
+  if (m == 0u) return;
+  int base = 0;
+  if (lane == 0) base = atomicAdd(&sm.nkeys, __popc(m));
+  base = __shfl_sync(0xffffffffu, base, 0);
+  const int pos = base + __popc(m & ((1u << lane) - 1u));
+  if (take && pos < kFuCap) sm.keys[pos] = k;
+}
+
+// Rank of every key among the keys; ranks 0..K-1 are written as the batch's outputs.
+__device__ void rank_and_write(const StepParams& p, FuSmem& sm, int b) {
+  const int n = sm.nkeys < kFuCap ? sm.nkeys : kFuCap;
+  const int K = p.k;
+  for (int i = threadIdx.x; i < n; i += kFuThreads) {
+    const Key ki = sm.keys[i];
+    int r0 = 0, r1 = 0, q = 0;
+#pragma unroll 1
+    for (; q + 1 < n; q += 2) {
+      r0 += key_less(sm.keys[q], ki);
+      r1 += key_less(sm.keys[q + 1], ki);
+    }
+    if (q < n) r0 += key_less(sm.keys[q], ki);
+    const int rank = r0 + r1;
+    if (rank < K) {
+      const int o = b * K + rank;
+      const int parent = key_parent(ki), token = key_token(ki);
+      p.out_token[o] = token;
+      p.out_parent[o] = parent;
+      p.out_score[o] = key_score(ki);
+      if (p.out_finished) p.out_finished[o] = (sm.fin[parent] || token == p.eos) ? 1 : 0;
+    }
+  }
+}
+
+// Exact top-K of live row j by (x descending, token ascending): a radix select of the K-th
+// order key over the row's logits, 8 bits a pass, then the elements above it and the first
+// `need` equal to it in token order.  All threads call it.
+template <int DT, bool BIAS>
+__device__ void exact_row(const StepParams& p, FuSmem& sm, int b, int j) {
+  constexpr int ES = Traits<DT>::kBytes;
+  const int K = p.k, V = p.vocab;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const unsigned char* rowp = static_cast<const unsigned char*>(p.logits) + (size_t)(b * K + j) * V * ES;
+  auto xat = [&](int i) -> float {
+    float x = load_elem<DT>(rowp + (size_t)i * ES);
+    if constexpr (BIAS) x += __ldg(p.bias + i);
+    return x;
+  };
+  if (tid == 0) {
+    sm.prefix = 0;
+    sm.pmask = 0;
+    sm.need = K;
+  }
+  __syncthreads();
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += kFuThreads) sm.hist[i] = 0;
+    __syncthreads();
+    const uint32_t prefix = sm.prefix, pmask = sm.pmask;
+    for (int i = tid; i < V; i += kFuThreads) {
+      const uint32_t o = float_ord(xat(i));
+      if ((o & pmask) == prefix) atomicAdd(&sm.hist[(o >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      const int need = sm.need;
+      unsigned int cum = 0;
+      int dgt = 255;
+      for (; dgt > 0; --dgt) {
+        if (cum + sm.hist[dgt] >= (unsigned)need) break;
+        cum += sm.hist[dgt];
+      }
+      sm.need = need - (int)cum;
+      sm.prefix = prefix | ((uint32_t)dgt << shift);
+      sm.pmask = pmask | (255u << shift);
+    }
+    __syncthreads();
+  }
+  const uint32_t tkey = sm.prefix;
+  const int need_eq = sm.need;
+  const double c = sm.c[j];
+  for (int base = 0; base < V; base += kFuThreads) {
+    const int i = base + tid;
+    float x = 0.0f;
+    bool take = false;
+    if (i < V) {
+      x = xat(i);
+      take = float_ord(x) > tkey;
+    }
+    append_key(sm, take, make_key((float)(c + (double)x), j, x, i));
+  }
+  __syncthreads();
+  // the first need_eq elements equal to the K-th key, in token order
+  int taken = 0;
+  for (int base = 0; base < V && taken < need_eq; base += kFuThreads) {
+    const int i = base + tid;
+    float x = 0.0f;
+    bool eq = false;
+    if (i < V) {
+      x = xat(i);
+      eq = float_ord(x) == tkey;
+    }
+    const unsigned ballot = __ballot_sync(0xffffffffu, eq);
+    if (lane == 0) sm.wc[warp] = __popc(ballot);
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int w = 0; w < kFuWarps; ++w) {
+      before += (w < warp) ? sm.wc[w] : 0;
+      total += sm.wc[w];
+    }
+    const int off = taken + before + __popc(ballot & ((1u << lane) - 1u));
+    append_key(sm, eq && off < need_eq, make_key((float)(c + (double)x), j, x, i));
+    taken += total;
+    __syncthreads();
+  }
+  __syncthreads();
+}
+
+template <int DT, bool BIAS, int VPL>
+__global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepParams p) {
+  constexpr int VEC = Traits<DT>::kVec;
+  constexpr int ES = Traits<DT>::kBytes;
+  constexpr int CV = 32 * VPL;                       // vectors per stage
+  constexpr bool kPacked = (DT != DT_F32) && !BIAS;  // the block max on packed 16-bit pairs
+  constexpr int EL = VPL * VEC;                      // elements per lane per stage (one block)
+  __shared__ FuSmem sm;
+  extern __shared__ __align__(128) unsigned char fu_dyn[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = blockIdx.x;
+  const int K = p.k, V = p.vocab, W = p.nc;  // W strips per row, one warp per strip
+  const int SPS = p.stages;                  // block-max rows kept per strip
+  unsigned char* ring = fu_dyn + (size_t)warp * kFuRing * CV * 16;
+  float* bmax = reinterpret_cast<float*>(fu_dyn + (size_t)kFuWarps * kFuRing * CV * 16);
+  const int row_bytes = V * ES;
+  const unsigned char* logits = static_cast<const unsigned char*>(p.logits);
+
+  // inputs may come from the previous kernel of the stream
+  grid_dependency_wait();
+  if (tid < K) {
+    sm.beam[tid] = p.beam[b * K + tid];
+    sm.fin[tid] = (p.finished && p.finished[b * K + tid]) ? 1 : 0;
+    sm.ncand[tid] = 0;
+  }
+  if (tid == 0) {
+    sm.keys = reinterpret_cast<Key*>(fu_dyn);
+    sm.nkeys = 0;
+    sm.path = (p.flags & kFlagForceExact) ? 2 : 0;
+  }
+  __syncthreads();
+
+  // Geometry of row j: 16-byte aligned vectors covering it, stages of CV vectors.
+  struct RowGeo {
+    const uint4* rb;  // first vector (16-byte aligned, may start before the row)
+    int lead;         // bytes of that vector before the row
+    int nv, ns;
+  };
+  auto geo = [&](int j) -> RowGeo {
+    RowGeo g;
+    const unsigned char* rowp = logits + (size_t)(b * K + j) * row_bytes;
+    g.lead = (int)(reinterpret_cast<uintptr_t>(rowp) & 15);
+    g.rb = reinterpret_cast<const uint4*>(rowp - g.lead);
+    g.nv = (g.lead + row_bytes + 15) >> 4;
+    g.ns = (g.nv + CV - 1) / CV;
+    return g;
+  };
+  // Block (stage q, lane l) of the row: vectors q * CV + l + 32 r, r < VPL; elements outside
+  // the row read as -inf.
+  auto load_block = [&](const RowGeo& g, uint4 (&d)[VPL], int q, int l) {
+#pragma unroll
+    for (int r = 0; r < VPL; ++r) {
+      const int jv = q * CV + l + 32 * r;
+      const uint32_t w = Traits<DT>::kNegInfWord;
+      d[r] = jv < g.nv ? __ldcs(g.rb + jv) : make_uint4(w, w, w, w);
+    }
+  };
+  auto mask_block = [&](const RowGeo& g, uint4 (&d)[VPL], int q, int l) {
+    const int j0 = q * CV;
+    if (j0 * 16 - g.lead >= 0 && (j0 + CV) * 16 - g.lead <= row_bytes) return;  // interior stage
+#pragma unroll
+    for (int r = 0; r < VPL; ++r) {
+      const int base_b = (j0 + l + 32 * r) * 16 - g.lead;  // row byte offset of element 0
+      if (base_b < 0 || base_b + 16 > row_bytes) {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          const int eb = base_b + e * ES;
+          if (eb < 0 || eb >= row_bytes) set_neg_inf<DT>(d[r], e);
+        }
+      }
+    }
+  };
+  // x = logit + bias of the block as floats (bias and f32 variants)
+  auto block_x = [&](const RowGeo& g, const uint4 (&d)[VPL], int q, int l, float (&xf)[EL]) {
+#pragma unroll
+    for (int r = 0; r < VPL; ++r) {
+      float x[VEC];
+      unpack<DT>(d[r], x);
+      if constexpr (BIAS) {
+        const int base_b = (q * CV + l + 32 * r) * 16 - g.lead;
+        const int v0 = base_b / ES;
+        if (base_b >= 0 && base_b + 16 <= row_bytes && ((reinterpret_cast<uintptr_t>(p.bias + v0) & 15) == 0)) {
+#pragma unroll
+          for (int e = 0; e < VEC; e += 4) {
+            const float4 bb = __ldg(reinterpret_cast<const float4*>(p.bias + v0 + e));
+            x[e] += bb.x;
+            x[e + 1] += bb.y;
+            x[e + 2] += bb.z;
+            x[e + 3] += bb.w;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) {
+            const int eb = base_b + e * ES;
+            if (eb >= 0 && eb < row_bytes) x[e] += __ldg(p.bias + eb / ES);
+          }
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) xf[r * VEC + e] = x[e];
+    }
+  };
+
+  // ---------------------------------------------------------------- first traversal
+  // warp u streams strip s = u mod W of row j = u / W: stages s, s + W, ...
+  const int nunits = K * W;
+  if (warp < nunits) {
+    const int u = warp, j = u / W, s = u - j * W;
+    float ml = -INFINITY;  // lane's running max
+    float cl = 0.0f;       // the lane's sum is sl = sum of 2^(x log2e + cl), cl = -ml log2e rounded
+    float sl = 0.0f;
+    if (!sm.fin[j]) {
+      const RowGeo g = geo(j);
+      // two register buffers: the next stage's loads are in flight while a stage is worked on
+      // the strip's stages go through a ring of kFuRing stage buffers in shared memory,
+      // filled by 16-byte asynchronous copies (each lane copies, then reads, its own
+      // vectors: no barrier), kFuRing - 1 stages in flight while one is worked on
+      const uint64_t pol = l2_evict_first_policy();
+      auto issue = [&](int q, int slot) {
+        if (q < g.ns) {
+#pragma unroll
+          for (int r = 0; r < VPL; ++r) {
+            const int jv = q * CV + lane + 32 * r;
+            if (jv < g.nv) cp_async16(smem_addr(ring + ((slot * VPL + r) * 32 + lane) * 16), g.rb + jv, pol);
+          }
+        }
+        cp_async_commit();
+      };
+      uint4 d[VPL];
+      int q = s, i = 0;
+#pragma unroll
+      for (int a = 0; a < kFuRing - 1; ++a) issue(q + a * W, a);
+#pragma unroll 1
+      for (; q < g.ns; q += W, ++i) {
+        cp_async_wait<kFuRing - 2>();
+        const int slot = i % kFuRing;
+#pragma unroll
+        for (int r = 0; r < VPL; ++r) {
+          const int jv = q * CV + lane + 32 * r;
+          const uint32_t w = Traits<DT>::kNegInfWord;
+          d[r] = jv < g.nv ? *reinterpret_cast<const uint4*>(ring + ((slot * VPL + r) * 32 + lane) * 16)
+                           : make_uint4(w, w, w, w);
+        }
+        issue(q + (kFuRing - 1) * W, (i + kFuRing - 1) % kFuRing);
+        mask_block(g, d, q, lane);
+        float xf[kPacked ? 1 : EL];
+        if constexpr (!kPacked) block_x(g, d, q, lane, xf);
+        // the block max
+        float lm;
+        if constexpr (kPacked) {
+          uint32_t t = hmax2_bits<DT>(hmax2_bits<DT>(d[0].x, d[0].y), hmax2_bits<DT>(d[0].z, d[0].w));
+#pragma unroll
+          for (int r = 1; r < VPL; ++r)
+            t = hmax2_bits<DT>(t, hmax2_bits<DT>(hmax2_bits<DT>(d[r].x, d[r].y), hmax2_bits<DT>(d[r].z, d[r].w)));
+          lm = hpair_max<DT>(t);
+        } else {
+          lm = xf[0];
+#pragma unroll
+          for (int q2 = 1; q2 < EL; ++q2) lm = fmaxf(lm, xf[q2]);
+        }
+        bmax[(u * SPS + i) * 32 + lane] = lm;
+        // log_sum_exp: the lane's sum is kept as sum of 2^(x log2e + c) with c = -max log2e
+        // rounded (one fused multiply-add per term); rescaled by 2^(c_new - c_old) when the
+        // lane's max rises, and corrected for the rounding of c once, at the end of the strip
+        const float mn = fmaxf(ml, lm);
+        const float cn = mn == -INFINITY ? 0.0f : -mn * kLog2e;
+        sl = ml == -INFINITY ? 0.0f : sl * fast_exp2(cn - cl);
+        cl = cn;
+        ml = mn;
+        const float2 L2 = make_float2(kLog2e, kLog2e), c2 = make_float2(cn, cn);
+        float2 a0 = make_float2(0.0f, 0.0f), a1 = make_float2(0.0f, 0.0f);
+        auto term2 = [&](float2 x) {
+          const float2 t = __ffma2_rn(x, L2, c2);
+          return make_float2(fast_exp2(t.x), fast_exp2(t.y));
+        };
+        if constexpr (kPacked) {
+#pragma unroll
+          for (int r = 0; r < VPL; ++r) {
+            const uint32_t w[4] = {d[r].x, d[r].y, d[r].z, d[r].w};
+#pragma unroll
+            for (int e = 0; e < 4; e += 2) {
+              float2 f0, f1;
+              if constexpr (DT == DT_F16) {
+                f0 = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+                f1 = __half22float2(*reinterpret_cast<const __half2*>(&w[e + 1]));
+              } else {
+                f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+                f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e + 1]));
+              }
+              a0 = __fadd2_rn(a0, term2(f0));
+              a1 = __fadd2_rn(a1, term2(f1));
+            }
+          }
+        } else {
+#pragma unroll
+          for (int q2 = 0; q2 < EL; q2 += 4) {
+            a0 = __fadd2_rn(a0, term2(make_float2(xf[q2], xf[q2 + 1])));
+            a1 = __fadd2_rn(a1, term2(make_float2(xf[q2 + 2], xf[q2 + 3])));
+          }
+        }
+        const float2 a = __fadd2_rn(a0, a1);
+        sl += a.x + a.y;
+      }
+      cp_async_wait<0>();  // the ring becomes the key array: no copy may still land in it
+    }
+    // end of the strip: the lanes' (max, sum) merged
+    float M = ml;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    // sl * 2^(-(ml log2e + cl)) is the lane's sum of exp(x - ml); then rescaled to M
+    float S = (ml == -INFINITY) ? 0.0f : sl * fast_exp2(-fmaf(ml, kLog2e, cl) + (ml - M) * kLog2e);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+
+    // the strip's bound: the k-th largest of its block maxima (each lane keeps the 8 largest
+    // of its own blocks, then k rounds of a warp max take them out in order)
+    const RowGeo g = geo(j);
+    const int nst = (!sm.fin[j] && s < g.ns) ? (g.ns - s + W - 1) / W : 0;
+    float t[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) t[i] = -INFINITY;
+    for (int i = 0; i < nst; ++i) {
+      float v = bmax[(u * SPS + i) * 32 + lane];
+      if (v > t[7]) {
+#pragma unroll
+        for (int q2 = 0; q2 < 8; ++q2) {  // insert, keeping t descending
+          const float hi = fmaxf(t[q2], v);
+          v = fminf(t[q2], v);
+          t[q2] = hi;
+        }
+      }
+    }
+    float Rs = -INFINITY;
+    for (int r = 0; r < K; ++r) {
+      float m = t[0];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      const unsigned who = __ballot_sync(0xffffffffu, t[0] == m);
+      if (lane == __ffs(who) - 1) {
+#pragma unroll
+        for (int q2 = 0; q2 < 7; ++q2) t[q2] = t[q2 + 1];
+        t[7] = -INFINITY;
+      }
+      Rs = m;
+    }
+    // second traversal of the strip: its blocks whose max reaches the bound are read again,
+    // all at once (lane h takes hit h), and their elements x >= bound kept as candidates
+    const float thr = fmaxf(Rs, lowest_finite<DT>());  // -inf elements are never candidates
+    int nh = 0;
+    for (int i = 0; i < nst; ++i) {
+      const bool hit = bmax[(u * SPS + i) * 32 + lane] >= thr;
+      const unsigned hm = __ballot_sync(0xffffffffu, hit);
+      const int pos = nh + __popc(hm & ((1u << lane) - 1u));
+      if (hit && pos < kFuHits) sm.hits[u][pos] = i * 32 + lane;
+      nh += __popc(hm);
+    }
+    bool ovf = nh > kFuHits;
+    if (lane == 0) sm.ucnt[u] = 0;
+    __syncwarp();
+    for (int h0 = 0; h0 < nh && !ovf; h0 += 32) {
+      const int h = h0 + lane;
+      if (h < nh) {
+        const int i = sm.hits[u][h] >> 5, l = sm.hits[u][h] & 31;
+        const int q = s + i * W;
+        uint4 d[VPL];
+        load_block(g, d, q, l);
+        mask_block(g, d, q, l);
+        float xf[kPacked ? 1 : EL];
+        if constexpr (!kPacked) block_x(g, d, q, l, xf);
+#pragma unroll
+        for (int r = 0; r < VPL; ++r) {
+          uint32_t m;
+          if constexpr (kPacked) {
+            m = hvec_ge_mask<DT>(d[r], thr);
+          } else {
+            m = 0;
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) m |= (xf[r * VEC + e] >= thr ? 1u : 0u) << e;
+          }
+          while (m) {
+            const int e = __ffs(m) - 1;
+            m &= m - 1;
+            float x;
+            if constexpr (kPacked) {
+              x = vec_elem_f<DT>(d[r], e);
+            } else {
+              float tv = xf[r * VEC];
+#pragma unroll
+              for (int q2 = 1; q2 < VEC; ++q2) tv = q2 == e ? xf[r * VEC + q2] : tv;
+              x = tv;
+            }
+            const int v = ((q * CV + l + 32 * r) * 16 - g.lead) / ES + e;
+            const int pos = atomicAdd(&sm.ucnt[u], 1);
+            if (pos < kFuList) sm.cand[u][pos] = make_float2(x, __int_as_float(v));
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      sm.um[u] = M;
+      sm.us[u] = S;
+      sm.ur[u] = Rs;
+      sm.uovf[u] = (ovf || sm.ucnt[u] > kFuList) ? 1 : 0;
+    }
+  }
+  __syncthreads();
+
+  // ---------------------------------------------------------------- per row: lse and R
+  // R of a row = the largest of its strips' bounds (each is at most the row's k-th largest)
+  if (warp < K) {
+    const int j = warp, u0 = j * W;
+    const float mu = lane < W ? sm.um[u0 + lane] : -INFINITY;
+    float M = mu;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float S = (lane < W && mu != -INFINITY) ? sm.us[u0 + lane] * exp2f((mu - M) * kLog2e) : 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+    float Rr = lane < W ? sm.ur[u0 + lane] : -INFINITY;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Rr = fmaxf(Rr, __shfl_xor_sync(0xffffffffu, Rr, o));
+    const bool ovf = __any_sync(0xffffffffu, lane < W && sm.uovf[u0 + lane] != 0);
+    if (lane == 0) {
+      const float beam = sm.beam[j];
+      int kind = FROW_LIVE;
+      if (sm.fin[j]) {
+        kind = FROW_FIN;
+      } else if (M == -INFINITY || beam == -INFINITY) {
+        kind = FROW_DEAD;
+      }
+      const float log_s = logf(S);
+      sm.kind[j] = kind;
+      sm.R[j] = Rr;
+      sm.lse[j] = kind == FROW_FIN ? __int_as_float(0x7fc00000)
+                                   : (M == -INFINITY ? -INFINITY : (float)((double)M + (double)log_s));
+      sm.c[j] = kind == FROW_LIVE ? (double)beam - (double)M - (double)log_s : 0.0;
+      if (ovf && kind == FROW_LIVE) atomicMax(&sm.path, 1);
+    }
+  }
+  __syncthreads();
+
+  // ---------------------------------------------------------------- rank keys
+  // every strip's candidates at or above its row's R, rescored: beam_score + x - lse
+  if (sm.path == 0) {
+    for (int i0 = 0; i0 < nunits * kFuList; i0 += kFuThreads) {
+      const int idx = i0 + tid;
+      const int u = idx / kFuList, i = idx - u * kFuList;
+      const int j = u < nunits ? u / W : 0;
+      bool take = false;
+      float2 en = make_float2(0.0f, 0.0f);
+      if (u < nunits && sm.kind[j] == FROW_LIVE && i < sm.ucnt[u]) {
+        en = sm.cand[u][i];
+        take = en.x >= sm.R[j];
+      }
+      append_key(sm, take, make_key((float)(sm.c[j] + (double)en.x), j, en.x, __float_as_int(en.y)));
+      if (take) atomicAdd(&sm.ncand[j], 1);
+    }
+  }
+  // finished beams offer (eos_id, beam score); beams with no finite score offer k tokens
+  if (sm.path == 0 && tid < K * K) {
+    const int jr = tid / K, v = tid - jr * K;
+    const int kind = sm.kind[jr];
+    if ((kind == FROW_FIN && v == 0) || kind == FROW_DEAD) {
+      const int pos = atomicAdd(&sm.nkeys, 1);
+      if (pos < kFuCap) sm.keys[pos] = kind == FROW_FIN ? make_key(sm.beam[jr], jr, 0.0f, p.eos) : make_key(-INFINITY, jr, 0.0f, v);
+      if (v == 0) sm.ncand[jr] = kind == FROW_FIN ? 1 : K;
+    }
+  }
+  __syncthreads();
+  if (tid == 0 && sm.path == 0 && sm.nkeys > kFuCap) sm.path = 3;
+  __syncthreads();
+  const int path = sm.path;
+  if (path != 0) {
+    // exact path: every live beam's top-K by radix select over its logits
+    if (tid == 0) sm.nkeys = 0;
+    __syncthreads();
+    for (int j = 0; j < K; ++j) {
+      const int kind = sm.kind[j];
+      if (kind == FROW_LIVE) {
+        exact_row<DT, BIAS>(p, sm, b, j);
+      } else {
+        if (tid < K && (kind == FROW_DEAD || tid == 0)) {
+          const int pos = atomicAdd(&sm.nkeys, 1);
+          sm.keys[pos] = kind == FROW_FIN ? make_key(sm.beam[j], j, 0.0f, p.eos) : make_key(-INFINITY, j, 0.0f, tid);
+        }
+        __syncthreads();
+      }
+    }
+  }
+  rank_and_write(p, sm, b);
+  if (tid < K) {
+    RowStat st;
+    st.lse = sm.lse[tid];
+    st.rtopk = sm.R[tid];
+    st.ncand = path != 0 ? -1 : sm.ncand[tid];
+    st.pad = 0;
+    p.rowstat[b * K + tid] = st;
+  }
+  if (tid == 0) p.bstat[b] = path;
+}
+
+template <int DT, bool BIAS, int VPL>
+cudaError_t launch_t(const StepParams& p, cudaStream_t stream) {
+  PdlLaunch l(dim3((unsigned)p.batch), dim3(kFuThreads), beam_fused_smem_bytes(VPL, p.stages), stream);
+  return cudaLaunchKernelEx(&l.cfg, beam_fused_kernel<DT, BIAS, VPL>, p);
+}
+
+template <int DT, bool BIAS, int VPL>
+cudaError_t config_t() {
+  return cudaFuncSetAttribute(beam_fused_kernel<DT, BIAS, VPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)beam_fused_smem_bytes(VPL, kFuMaxStages));
+}
+
+}  // namespace
+
+cudaError_t beam_fused_config() {
+  cudaError_t e = config_t<DT_F32, false, 4>();
+  if (e == cudaSuccess) e = config_t<DT_F32, true, 4>();
+  if (e == cudaSuccess) e = config_t<DT_F16, false, 8>();
+  if (e == cudaSuccess) e = config_t<DT_F16, true, 4>();
+  if (e == cudaSuccess) e = config_t<DT_BF16, false, 8>();
+  if (e == cudaSuccess) e = config_t<DT_BF16, true, 4>();
+  return e;
+}
+
+cudaError_t launch_beam_fused(const StepParams& p, int dtype, cudaStream_t stream) {
+  const bool bias = p.bias != nullptr;
+  switch (dtype) {
+    case DT_F32: return bias ? launch_t<DT_F32, true, 4>(p, stream) : launch_t<DT_F32, false, 4>(p, stream);
+    case DT_F16: return bias ? launch_t<DT_F16, true, 4>(p, stream) : launch_t<DT_F16, false, 8>(p, stream);
+    case DT_BF16: return bias ? launch_t<DT_BF16, true, 4>(p, stream) : launch_t<DT_BF16, false, 8>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace lsb

@@ -30,6 +30,7 @@
 #include "ls_device.cuh"
 #include "ls_dtype.cuh"
 #include "ls_internal.h"
+#include "ls_strip.cuh"
 
 namespace lsb {
 namespace {
@@ -38,122 +39,8 @@ constexpr long long kDrainLimitNs = 2000000000LL;  // 2 s for copies already in 
 static_assert(kStWarps * kStMaxStages * 8 <= kStListOff, "mbarriers overlap the lists");
 static_assert(kStBarBytes % 16 == 0, "stage buffers must be 16-byte aligned for bulk copies");
 
-// Lowest finite value of the element type: a threshold of -inf is raised to it so that
-// masked (-inf) elements never count as candidates.
-template <int DT>
-__device__ __forceinline__ float lowest_finite() {
-  if constexpr (DT == DT_F16) return -65504.0f;
-  return -3.4028234663852886e38f;  // f32 and bf16
-}
-
-// Packed max of two 16-bit pairs (bit patterns).
-template <int DT>
-__device__ __forceinline__ uint32_t hmax2_bits(uint32_t a, uint32_t b) {
-  if constexpr (DT == DT_F16) {
-    const __half2 m = __hmax2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
-    return *reinterpret_cast<const uint32_t*>(&m);
-  } else {
-    const __nv_bfloat162 m =
-        __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&a), *reinterpret_cast<const __nv_bfloat162*>(&b));
-    return *reinterpret_cast<const uint32_t*>(&m);
-  }
-}
-template <int DT>
-__device__ __forceinline__ float hpair_max(uint32_t a) {
-  if constexpr (DT == DT_F16) {
-    const __half2 h = *reinterpret_cast<const __half2*>(&a);
-    return fmaxf(__low2float(h), __high2float(h));
-  } else {
-    const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&a);
-    return fmaxf(__low2float(h), __high2float(h));
-  }
-}
-// Bits 2i, 2i+1: elements 2i, 2i+1 of the vector are >= t (t an element value of the type,
-// so the packed comparison is exact).
-template <int DT>
-__device__ __forceinline__ uint32_t hvec_ge_mask(const uint4& d, float t) {
-  uint32_t tb;
-  if constexpr (DT == DT_F16) {
-    const __half2 h = __float2half2_rn(t);
-    tb = *reinterpret_cast<const uint32_t*>(&h);
-  } else {
-    const __nv_bfloat162 h = __float2bfloat162_rn(t);
-    tb = *reinterpret_cast<const uint32_t*>(&h);
-  }
-  const uint32_t w[4] = {d.x, d.y, d.z, d.w};
-  uint32_t m = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint32_t g;
-    if constexpr (DT == DT_F16)
-      g = __hge2_mask(*reinterpret_cast<const __half2*>(&w[i]), *reinterpret_cast<const __half2*>(&tb));
-    else
-      g = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&w[i]), *reinterpret_cast<const __nv_bfloat162*>(&tb));
-    m |= ((g & 1u) | ((g >> 15) & 2u)) << (2 * i);
-  }
-  return m;
-}
-
-// The two 16-bit values of a packed word minus m, each exact in f32 (the mixed-precision
-// subtraction rounds once; the difference of two 16-bit values near each other is exact).
-template <int DT>
-__device__ __forceinline__ float2 hpair_minus(uint32_t w, float m) {
-  float lo, hi;
-  const unsigned short a = (unsigned short)(w & 0xffffu), b = (unsigned short)(w >> 16);
-  if constexpr (DT == DT_F16) {
-    asm("sub.rn.f32.f16 %0, %1, %2;" : "=f"(lo) : "h"(a), "f"(m));
-    asm("sub.rn.f32.f16 %0, %1, %2;" : "=f"(hi) : "h"(b), "f"(m));
-  } else {
-    asm("sub.rn.f32.bf16 %0, %1, %2;" : "=f"(lo) : "h"(a), "f"(m));
-    asm("sub.rn.f32.bf16 %0, %1, %2;" : "=f"(hi) : "h"(b), "f"(m));
-  }
-  return make_float2(lo, hi);
-}
-
-// Element e (runtime index) of a 16-byte vector as float, without dynamic register indexing.
-template <int DT>
-__device__ __forceinline__ float vec_elem_f(const uint4& d, int e) {
-  if constexpr (DT == DT_F32) {
-    const uint32_t w = e == 0 ? d.x : e == 1 ? d.y : e == 2 ? d.z : d.w;
-    return __uint_as_float(w);
-  } else {
-    const int i = e >> 1;
-    const uint32_t w = i == 0 ? d.x : i == 1 ? d.y : i == 2 ? d.z : d.w;
-    const unsigned short h = (unsigned short)((e & 1) ? (w >> 16) : (w & 0xffffu));
-    if constexpr (DT == DT_F16)
-      return __half2float(__ushort_as_half(h));
-    else
-      return __bfloat162float(__ushort_as_bfloat16(h));
-  }
-}
-
-// k-th largest (1-based) of the values held by lanes [0, n), n <= 32; all lanes get it.
-__device__ __forceinline__ float kth_of_lanes(float v, int n, int k) {
-  const int lane = threadIdx.x & 31;
-  int rank = 0;
-  for (int q = 0; q < n; ++q) {
-    const float w = __shfl_sync(0xffffffffu, v, q);
-    rank += (w > v) | ((w == v) & (q < lane));
-  }
-  const unsigned hit = __ballot_sync(0xffffffffu, lane < n && rank == k - 1);
-  return __shfl_sync(0xffffffffu, v, __ffs(hit) - 1);
-}
-
-// R from the lanes' running maxima: group g = lanes l with l mod G == g; R = k-th largest
-// of the G group maxima (their min when G == k).  Lanes g < G return their group max in gm.
-__device__ __forceinline__ float strip_bound(float ml, int G, int K, float& gm) {
-  float g = ml;
-  for (int o = 16; o >= G; o >>= 1) g = fmaxf(g, __shfl_xor_sync(0xffffffffu, g, o));
-  gm = g;
-  if (G == K) {
-    for (int o = G >> 1; o > 0; o >>= 1) g = fminf(g, __shfl_xor_sync(0xffffffffu, g, o));
-    return g;
-  }
-  return kth_of_lanes(g, G, K);
-}
-
 template <int DT, bool BIAS, int VPL>
-__global__ void __launch_bounds__(kStThreads) beam_strips_kernel(const StepParams p) {
+__global__ void __launch_bounds__(kStThreads, 3) beam_strips_kernel(const StepParams p) {
   constexpr int VEC = Traits<DT>::kVec;
   constexpr int ES = Traits<DT>::kBytes;
   constexpr int CV = 32 * VPL;  // vectors per stage
@@ -185,115 +72,108 @@ __global__ void __launch_bounds__(kStThreads) beam_strips_kernel(const StepParam
   // inputs may come from the previous kernel of the stream
   grid_dependency_wait();
 
-  auto row_of = [&](int u) -> int { return (int)fast_div((uint32_t)u, p.nc_magic, p.nc_shift); };
-  auto live = [&](int u) -> bool { return !(p.finished && p.finished[row_of(u)]); };
-  struct RowGeo {
+  // A unit's geometry: its row's 16-byte aligned vectors and the stages of its strip.
+  struct Unit {
+    int u;                    // unit index (>= units: none)
     const unsigned char* rb;  // 16-byte aligned start of the row's first vector
     int lead;                 // bytes of that vector before the row starts
     int nv;                   // vectors covering the row
-    int ns;                   // stages of the row
+    int ns;                   // stages of the row; the strip's are part, part + W, ...
+    int part;
   };
-  auto row_geo = [&](int row) -> RowGeo {
-    RowGeo g;
-    const unsigned char* rowp = logits + (size_t)row * row_bytes;
-    g.lead = (int)(reinterpret_cast<uintptr_t>(rowp) & 15);
-    g.rb = rowp - g.lead;
-    g.nv = (g.lead + row_bytes + 15) >> 4;
-    g.ns = (g.nv + CV - 1) / CV;
-    return g;
-  };
-  // The warp's sequence of (unit, stage) items: units gw, gw + nwarps, ... (live rows
-  // only), each unit's stages part, part + W, ...
-  struct Cursor {
-    int u, q;  // unit, stage within the row (u >= units: done)
-  };
-  auto first_stage_from = [&](int u) -> Cursor {
+  // the warp's next live unit at or after u (every strip has a stage: W <= stages of a row)
+  auto unit_from = [&](int u) -> Unit {
+    Unit t;
     for (; u < units; u += nwarps) {
-      if (!live(u)) continue;
-      const int row = row_of(u), part = u - row * W;
-      if (part < row_geo(row).ns) return Cursor{u, part};
+      const int row = (int)fast_div((uint32_t)u, p.nc_magic, p.nc_shift);
+      if (p.finished && p.finished[row]) continue;
+      const unsigned char* rowp = logits + (size_t)row * row_bytes;
+      t.lead = (int)(reinterpret_cast<uintptr_t>(rowp) & 15);
+      t.rb = rowp - t.lead;
+      t.nv = (t.lead + row_bytes + 15) >> 4;
+      t.ns = (t.nv + CV - 1) / CV;
+      t.part = u - row * W;
+      break;
     }
-    return Cursor{units, 0};
-  };
-  auto advance = [&](Cursor c) -> Cursor {
-    const int row = row_of(c.u);
-    if (c.q + W < row_geo(row).ns) return Cursor{c.u, c.q + W};
-    return first_stage_from(c.u + nwarps);
+    t.u = u;
+    return t;
   };
 
-  // producer state (lane 0): the next item to copy and the number of copies issued
-  Cursor pc{units, 0};
-  int n_iss = 0;
+  // producer (lane 0): the next stage to copy and the number of copies issued
+  Unit pu;
+  int pq = 0, n_iss = 0;
   uint64_t policy = 0;
   if (lane == 0) {
     policy = l2_evict_first_policy();
-    pc = first_stage_from(gw);
+    pu = unit_from(gw);
+    pq = pu.part;
   }
   auto issue_one = [&]() {
-    if (pc.u >= units) return;
-    const RowGeo g = row_geo(row_of(pc.u));
-    const int j0 = pc.q * CV;
-    const int nvec = min(CV, g.nv - j0);
+    if (pu.u >= units) return;
+    const int j0 = pq * CV;
+    const uint32_t bytes = (uint32_t)min(CV, pu.nv - j0) * 16u;
     const int s = n_iss % S;
     const uint32_t bar = smem_addr(&bars[s]);
-    mbar_arrive_expect_tx(bar, (uint32_t)nvec * 16u);
-    bulk_load(smem_addr(stages + (size_t)s * kStageBytes), g.rb + (size_t)j0 * 16, (uint32_t)nvec * 16u, bar,
-              policy);
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_load(smem_addr(stages + (size_t)s * kStageBytes), pu.rb + (size_t)j0 * 16, bytes, bar, policy);
     ++n_iss;
-    pc = advance(pc);
+    pq += W;
+    if (pq >= pu.ns) {
+      pu = unit_from(pu.u + nwarps);
+      pq = pu.part;
+    }
   };
   if (lane == 0)
     for (int s = 0; s < S; ++s) issue_one();
 
-  Cursor cc = first_stage_from(gw);  // consumer (all lanes)
   int n_cons = 0;
   bool aborted = false;
-  while (cc.u < units) {
-    const int u = cc.u, row = row_of(u);
-    const RowGeo g = row_geo(row);
+  for (Unit cu = unit_from(gw); cu.u < units && !aborted; cu = unit_from(cu.u + nwarps)) {
     // running state of the unit
     float ml = -INFINITY, sl = 0.0f;  // lane's running max and sum of exp(x - ml)
     float R = -INFINITY, gm = -INFINITY;
     float Rfl = -INFINITY;  // a tighter bound taken when a stage has many candidates
-    int cnt = 0;       // entries in the warp's list
-    bool ovf = false;  // the list could not hold the candidates
-    while (cc.u == u) {
+    int cnt = 0;            // entries in the warp's list
+    bool ovf = false;       // the list could not hold the candidates
+    for (int q = cu.part; q < cu.ns; q += W) {
       const int s = n_cons % S;
       const bool ok = mbar_wait_bounded(smem_addr(&bars[s]), (uint32_t)((n_cons / S) & 1), p.spin_limit_ns);
       if (!__all_sync(0xffffffffu, ok)) {
         aborted = true;
         break;
       }
-      const int j0 = cc.q * CV;
-      const int nvec = min(CV, g.nv - j0);
+      const int j0 = q * CV;
+      const int nvec = min(CV, cu.nv - j0);
       const uint4* sv = reinterpret_cast<const uint4*>(stages + (size_t)s * kStageBytes);
       uint4 d[VPL];
-      const bool interior = nvec == CV && j0 * 16 - g.lead >= 0 && (j0 + CV) * 16 - g.lead <= row_bytes;
+      const bool interior = nvec == CV && j0 * 16 - cu.lead >= 0 && (j0 + CV) * 16 - cu.lead <= row_bytes;
+      if (interior) {
 #pragma unroll
-      for (int r = 0; r < VPL; ++r) {
-        const int jl = lane + 32 * r;
-        if (interior) {
-          d[r] = sv[jl];
-        } else if (jl < nvec) {
-          d[r] = sv[jl];
-          const int base_b = (j0 + jl) * 16 - g.lead;  // row byte offset of element 0
-          if (base_b < 0 || base_b + 16 > row_bytes) {
+        for (int r = 0; r < VPL; ++r) d[r] = sv[lane + 32 * r];
+      } else {
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) {
-              const int eb = base_b + e * ES;
-              if (eb < 0 || eb >= row_bytes) set_neg_inf<DT>(d[r], e);
+        for (int r = 0; r < VPL; ++r) {
+          const int jl = lane + 32 * r;
+          if (jl < nvec) {
+            d[r] = sv[jl];
+            const int base_b = (j0 + jl) * 16 - cu.lead;  // row byte offset of element 0
+            if (base_b < 0 || base_b + 16 > row_bytes) {
+#pragma unroll
+              for (int e = 0; e < VEC; ++e) {
+                const int eb = base_b + e * ES;
+                if (eb < 0 || eb >= row_bytes) set_neg_inf<DT>(d[r], e);
+              }
             }
+          } else {
+            const uint32_t w = Traits<DT>::kNegInfWord;
+            d[r] = make_uint4(w, w, w, w);
           }
-        } else {
-          const uint32_t w = Traits<DT>::kNegInfWord;
-          d[r] = make_uint4(w, w, w, w);
         }
       }
       // the stage is in registers: hand it back to the producer
       __syncwarp();
       ++n_cons;
       if (lane == 0) issue_one();
-      const Cursor next = advance(cc);
 
       // x = logit + bias as floats (bias and f32 variants)
       float xf[kPacked ? 1 : EL];
@@ -303,7 +183,7 @@ __global__ void __launch_bounds__(kStThreads) beam_strips_kernel(const StepParam
           float x[VEC];
           unpack<DT>(d[r], x);
           if constexpr (BIAS) {
-            const int base_b = (j0 + lane + 32 * r) * 16 - g.lead;
+            const int base_b = (j0 + lane + 32 * r) * 16 - cu.lead;
             const int v0 = base_b / ES;
             if (base_b >= 0 && base_b + 16 <= row_bytes && ((reinterpret_cast<uintptr_t>(p.bias + v0) & 15) == 0)) {
 #pragma unroll
@@ -327,31 +207,18 @@ __global__ void __launch_bounds__(kStThreads) beam_strips_kernel(const StepParam
         }
       }
 
-      // first traversal: per-vector maxima, the lane's stage max, the running maxima and R
-      float vmf[VPL];
+      // first traversal: the lane's stage max, the running maxima and R
       float lm;
       if constexpr (kPacked) {
-        uint32_t vm[VPL];
+        uint32_t t = hmax2_bits<DT>(hmax2_bits<DT>(d[0].x, d[0].y), hmax2_bits<DT>(d[0].z, d[0].w));
 #pragma unroll
-        for (int r = 0; r < VPL; ++r)
-          vm[r] = hmax2_bits<DT>(hmax2_bits<DT>(d[r].x, d[r].y), hmax2_bits<DT>(d[r].z, d[r].w));
-        uint32_t t = vm[0];
-#pragma unroll
-        for (int r = 1; r < VPL; ++r) t = hmax2_bits<DT>(t, vm[r]);
+        for (int r = 1; r < VPL; ++r)
+          t = hmax2_bits<DT>(t, hmax2_bits<DT>(hmax2_bits<DT>(d[r].x, d[r].y), hmax2_bits<DT>(d[r].z, d[r].w)));
         lm = hpair_max<DT>(t);
-#pragma unroll
-        for (int r = 0; r < VPL; ++r) vmf[r] = hpair_max<DT>(vm[r]);
       } else {
+        lm = xf[0];
 #pragma unroll
-        for (int r = 0; r < VPL; ++r) {
-          float m = xf[r * VEC];
-#pragma unroll
-          for (int e = 1; e < VEC; ++e) m = fmaxf(m, xf[r * VEC + e]);
-          vmf[r] = m;
-        }
-        lm = vmf[0];
-#pragma unroll
-        for (int r = 1; r < VPL; ++r) lm = fmaxf(lm, vmf[r]);
+        for (int q2 = 1; q2 < EL; ++q2) lm = fmaxf(lm, xf[q2]);
       }
       const float mn = fmaxf(ml, lm);
       R = fmaxf(strip_bound(mn, G, K, gm), Rfl);
@@ -365,17 +232,15 @@ __global__ void __launch_bounds__(kStThreads) beam_strips_kernel(const StepParam
           if (lm >= t) {
 #pragma unroll
             for (int r = 0; r < VPL; ++r) {
-              if (vmf[r] >= t) {
-                uint32_t m;
-                if constexpr (kPacked) {
-                  m = hvec_ge_mask<DT>(d[r], t);
-                } else {
-                  m = 0;
+              uint32_t m;
+              if constexpr (kPacked) {
+                m = hvec_ge_mask<DT>(d[r], t);
+              } else {
+                m = 0;
 #pragma unroll
-                  for (int e = 0; e < VEC; ++e) m |= (xf[r * VEC + e] >= t ? 1u : 0u) << e;
-                }
-                mk |= (uint64_t)m << (r * VEC);
+                for (int e = 0; e < VEC; ++e) m |= (xf[r * VEC + e] >= t ? 1u : 0u) << e;
               }
+              mk |= (uint64_t)m << (r * VEC);
             }
           }
           return mk;
@@ -422,14 +287,14 @@ __global__ void __launch_bounds__(kStThreads) beam_strips_kernel(const StepParam
             while (m) {
               const int e = __ffs(m) - 1;
               m &= m - 1;
-              const int eb = (j0 + lane + 32 * r) * 16 - g.lead + e * ES;
+              const int eb = (j0 + lane + 32 * r) * 16 - cu.lead + e * ES;
               float x;
               if constexpr (kPacked) {
                 x = vec_elem_f<DT>(d[r], e);
               } else {
                 float t = xf[r * VEC];
 #pragma unroll
-                for (int q = 1; q < VEC; ++q) t = q == e ? xf[r * VEC + q] : t;
+                for (int q2 = 1; q2 < VEC; ++q2) t = q2 == e ? xf[r * VEC + q2] : t;
                 x = t;
               }
               list[pos++] = make_float2(x, __int_as_float(eb / ES));
@@ -440,7 +305,10 @@ __global__ void __launch_bounds__(kStThreads) beam_strips_kernel(const StepParam
         __syncwarp();
       }
 
-      // first traversal, log_sum_exp: sum of exp(x - mn) = 2^((x - mn) log2 e)
+      // first traversal, log_sum_exp: sum of exp(x - mn) = 2^((x - mn) log2 e).  For
+      // |mn| < 64, x log2e - mn log2e in one fused multiply-add (the rounding of mn log2e
+      // scales every term of this lane and stage alike, by at most 2^-17 relative);
+      // otherwise the exact difference x - mn first.
       if (mn != ml) {
         sl = (ml == -INFINITY) ? 0.0f : sl * fast_exp2((ml - mn) * kLog2e);
         ml = mn;
@@ -448,32 +316,40 @@ __global__ void __launch_bounds__(kStThreads) beam_strips_kernel(const StepParam
       if (ml != -INFINITY) {
         const float2 L2 = make_float2(kLog2e, kLog2e);
         float2 a0 = make_float2(0.0f, 0.0f), a1 = make_float2(0.0f, 0.0f);
+        const bool fused = fabsf(ml) < 64.0f;
+        const float2 nml = fused ? make_float2(-ml * kLog2e, -ml * kLog2e) : make_float2(-ml, -ml);
+        auto term2 = [&](float2 x) -> float2 {
+          const float2 t = fused ? __ffma2_rn(x, L2, nml) : __fmul2_rn(__fadd2_rn(x, nml), L2);
+          return make_float2(fast_exp2(t.x), fast_exp2(t.y));
+        };
         if constexpr (kPacked) {
 #pragma unroll
           for (int r = 0; r < VPL; ++r) {
             const uint32_t w[4] = {d[r].x, d[r].y, d[r].z, d[r].w};
 #pragma unroll
             for (int i = 0; i < 4; i += 2) {
-              const float2 t0 = __fmul2_rn(hpair_minus<DT>(w[i], ml), L2);
-              const float2 t1 = __fmul2_rn(hpair_minus<DT>(w[i + 1], ml), L2);
-              a0 = __fadd2_rn(a0, make_float2(fast_exp2(t0.x), fast_exp2(t0.y)));
-              a1 = __fadd2_rn(a1, make_float2(fast_exp2(t1.x), fast_exp2(t1.y)));
+              float2 f0, f1;
+              if constexpr (DT == DT_F16) {
+                f0 = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+                f1 = __half22float2(*reinterpret_cast<const __half2*>(&w[i + 1]));
+              } else {
+                f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+                f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i + 1]));
+              }
+              a0 = __fadd2_rn(a0, term2(f0));
+              a1 = __fadd2_rn(a1, term2(f1));
             }
           }
         } else {
-          const float2 nm = make_float2(-ml, -ml);
 #pragma unroll
-          for (int q = 0; q < EL; q += 4) {
-            const float2 t0 = __fmul2_rn(__fadd2_rn(make_float2(xf[q], xf[q + 1]), nm), L2);
-            const float2 t1 = __fmul2_rn(__fadd2_rn(make_float2(xf[q + 2], xf[q + 3]), nm), L2);
-            a0 = __fadd2_rn(a0, make_float2(fast_exp2(t0.x), fast_exp2(t0.y)));
-            a1 = __fadd2_rn(a1, make_float2(fast_exp2(t1.x), fast_exp2(t1.y)));
+          for (int q2 = 0; q2 < EL; q2 += 4) {
+            a0 = __fadd2_rn(a0, term2(make_float2(xf[q2], xf[q2 + 1])));
+            a1 = __fadd2_rn(a1, term2(make_float2(xf[q2 + 2], xf[q2 + 3])));
           }
         }
         const float2 a = __fadd2_rn(a0, a1);
         sl += a.x + a.y;
       }
-      cc = next;
     }
     if (aborted) break;
 
@@ -499,7 +375,7 @@ __global__ void __launch_bounds__(kStThreads) beam_strips_kernel(const StepParam
       R = fmaxf(R, kth_of_lanes(ml, 32, K));
       thr = fmaxf(R, lo_fin);
     }
-    CandSlot* slots = p.slots + (size_t)u * C;
+    CandSlot* slots = p.slots + (size_t)cu.u * C;
     int total = 0;
     for (int b0 = 0; b0 < cnt; b0 += 32) {
       const int i = b0 + lane;
@@ -516,7 +392,7 @@ __global__ void __launch_bounds__(kStThreads) beam_strips_kernel(const StepParam
       total += __popc(bm);
     }
     if (ovf) total = C + 1;  // the fine rank takes its exact path for this batch
-    float* rec = reinterpret_cast<float*>(p.rec + (size_t)u * p.rec_stride);
+    float* rec = reinterpret_cast<float*>(p.rec + (size_t)cu.u * p.rec_stride);
     if (lane < G) rec[4 + lane] = gm;
     if (lane == 0) {
       reinterpret_cast<int*>(rec)[0] = total;

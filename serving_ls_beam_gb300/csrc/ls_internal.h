@@ -20,13 +20,18 @@ constexpr int kVplMin = 4;         // smallest vectors-per-lane variant built
 // K1s (beam_strips.cu): CTAs of kStWarps independent warps; a warp streams one strip of a
 // beam's row at a time through its own ring of `stages` stage buffers (at most
 // kStMaxStages) and keeps the strip's candidates in a list of kStListCap entries.
-constexpr int kStThreads = 128;
+constexpr int kStThreads = 256;
 constexpr int kStWarps = kStThreads / 32;
 constexpr int kStMaxStages = 8;
-constexpr int kStListCap = 128;
+constexpr int kStListCap = 64;
 constexpr int kStTighten = 24;   // candidates of one stage above which the bound is tightened
-constexpr int kStListOff = 256;  // per-warp mbarriers in [0, 256), then the per-warp lists
+constexpr int kStListOff = 512;  // per-warp mbarriers in [0, 512), then the per-warp lists
 constexpr int kStBarBytes = kStListOff + kStWarps * kStListCap * 8;  // start of the stage buffers
+// K3 (beam_fused.cu): one CTA of kFuThreads threads per batch, one warp per strip of a row
+// (k * strips per row <= warps), k <= kFuMaxK, at most kFuMaxStages stages per strip.
+constexpr int kFuThreads = 256;
+constexpr int kFuMaxK = 8;
+constexpr int kFuMaxStages = 32;
 // K2 (beam_select.cu): one CTA per batch.
 constexpr int kSelThreads = 256;
 constexpr int kSelWarps = kSelThreads / 32;
@@ -59,6 +64,8 @@ constexpr uint32_t kDevInternal = 1u << 2;
 constexpr int kFlagForceExact = 1;
 constexpr int kFlagPlainInplace = 2;  // the in-place refresh without bulk copies
 constexpr int kFlagChunkRows = 4;     // the beam step's first kernel by fixed-size chunks (K1)
+constexpr int kFlagNoFused = 8;       // the beam step as two kernels even where K3 applies
+constexpr int kFlagFused = 16;        // the beam step as K3 wherever k allows
 
 // ---------------------------------------------------------------- workspace layout
 struct alignas(16) RowStat {
@@ -259,6 +266,9 @@ size_t beam_rows_smem_bytes(int vpl);
 cudaError_t beam_rows_config(int dtype, bool bias, int vpl, int* occupancy);
 cudaError_t launch_beam_rows(const StepParams& p, int dtype, int vpl, int grid, cudaStream_t stream);
 cudaError_t launch_beam_select(const StepParams& p, int dtype, cudaStream_t stream);
+size_t beam_fused_smem_bytes(int vpl, int sps);
+cudaError_t beam_fused_config();  // once per device: the kernels' dynamic shared memory
+cudaError_t launch_beam_fused(const StepParams& p, int dtype, cudaStream_t stream);
 size_t beam_strips_smem_bytes(int vpl, int stages);
 cudaError_t beam_strips_config(int dtype, bool bias, int vpl, int stages, int* occupancy);
 cudaError_t launch_beam_strips(const StepParams& p, int dtype, int vpl, int grid, cudaStream_t stream);
