@@ -5,6 +5,10 @@ benchmark uses, and are compared with the oracle element by element; the
 multi-step workload c5 is covered in test_gpu_multistep.py.  The sweeps below
 add ragged vocabularies (not a multiple of the 16-byte vector), misaligned
 logits, k = 1 and k = 64, vocab == k, bias, finished beams and bf16.
+
+Every test runs under each implementation of the step (the `impl` fixture):
+the plan's own choice, the one-kernel step K3 forced wherever k <= 8, and the
+two-kernel step (K1 + K2) forced everywhere.
 """
 import os
 
@@ -20,6 +24,21 @@ pytestmark = pytest.mark.gpu
 import serving_ls_beam_gb300 as lsb  # noqa: E402
 
 TORCH_DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+
+# LS_BEAM_DEBUG settings of the implementations every test runs under
+IMPLS = {"plan": "", "onekernel": "fused", "twokernel": "nofused"}
+_impl_env = {"value": ""}
+
+
+@pytest.fixture(autouse=True, params=sorted(IMPLS))
+def impl(request):
+    _impl_env["value"] = IMPLS[request.param]
+    yield request.param
+    _impl_env["value"] = ""
+
+
+def _env(extra=None):
+    return ",".join(e for e in (_impl_env["value"], extra) if e)
 
 
 @pytest.fixture(scope="module")
@@ -68,17 +87,15 @@ def run_gpu(inp, dev, offset_elems=0, workspace=None, env=None):
         workspace = torch.empty(lsb.ls_beam_step_workspace_size(B, K, V), dtype=torch.uint8, device=dev)
         lsb.check(lsb.ls_workspace_init(workspace))
     old = os.environ.get("LS_BEAM_DEBUG")
-    if env is not None:
-        os.environ["LS_BEAM_DEBUG"] = env
+    os.environ["LS_BEAM_DEBUG"] = _env(env)
     try:
         st = lsb.ls_beam_step(t_lg, t_bias, t_beam, t_fin, inp["eos_id"], out_tok, out_par, out_sc, out_fin,
                               workspace)
     finally:
-        if env is not None:
-            if old is None:
-                os.environ.pop("LS_BEAM_DEBUG", None)
-            else:
-                os.environ["LS_BEAM_DEBUG"] = old
+        if old is None:
+            os.environ.pop("LS_BEAM_DEBUG", None)
+        else:
+            os.environ["LS_BEAM_DEBUG"] = old
     lsb.check(st, "ls_beam_step")
     lsb.check(lsb.ls_read_status(workspace), "device status")
     torch.cuda.synchronize()
@@ -266,7 +283,7 @@ def test_device_wait_timeout_is_reported(dev):
     t_beam = torch.from_numpy(inp["beam_scores"]).to(dev)
     tok = torch.empty((B, K), dtype=torch.int32, device=dev)
     par, sc = torch.empty_like(tok), torch.empty((B, K), device=dev)
-    os.environ["LS_BEAM_DEBUG"] = "spin=0"
+    os.environ["LS_BEAM_DEBUG"] = _env("spin=0,nofused")  # the two-kernel step has the bounded waits
     try:
         st = lsb.ls_beam_step(t_lg, None, t_beam, None, 2, tok, par, sc, None, ws)
     finally:
