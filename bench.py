@@ -181,7 +181,7 @@ class ClockSampler:
 # the sources each recorded kernel's traffic depends on: its own kernels plus the shared
 # launch code and headers (a change to any of them makes the recorded counters stale)
 KERNEL_SOURCES = {
-    "beam_step": ("beam_rows.cu", "beam_select.cu"),
+    "beam_step": ("beam_fused.cu", "ls_strip.cuh"),
     "cache_refresh_inplace": ("cache_inplace.cu",),
     "cache_reorder": ("cache_reorder.cu",),
 }
@@ -242,7 +242,17 @@ def time_oracle_sample(w: synth.Workload, batches, steps_list, with_cache: bool)
     return dt, len(batches) * len(steps_list)
 
 
-def cpu_baseline(w: synth.Workload, target_s: float = 12.0):
+def _oracle_worker(name: str, batches, steps):
+    """One process of the all-core baseline: the unmodified oracle on its own batches."""
+    return time_oracle_sample(synth.WORKLOADS[name], batches, steps, True)
+
+
+def cpu_baseline(w: synth.Workload, target_s: float = 12.0, all_cores_s: float = 8.0):
+    """The oracle (single-threaded fp64 C) on the host: on one core, and batch-parallel over
+    every host core (one process per core, each running the same oracle on its own batches)."""
+    import concurrent.futures as cf
+    import multiprocessing as mp
+
     # calibrate on one batch-step, then size the sample to roughly target_s seconds
     dt1, n1 = time_oracle_sample(w, [0], [1], True)
     per = dt1 / n1
@@ -253,9 +263,29 @@ def cpu_baseline(w: synth.Workload, target_s: float = 12.0):
     dt, bs = time_oracle_sample(w, batches, list(range(1, steps + 1)), True)
     per = dt / bs
     value = 1.0 / (per * w.batch)
-    return {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+    host_cores = os.cpu_count() or 1
+    line = {"value": value, "unit": UNIT, "cores": 1, "host_cores": host_cores, "kind": "oracle",
             "sample": f"{nb} batches x {steps} decode steps of {w.name} (beam step + cache refresh), single thread; "
-                      f"{per * 1e3:.1f} ms per batch-step, scaled to all {w.batch} batches"}
+                      f"{per * 1e3:.1f} ms per batch-step, scaled to all {w.batch} batches (extrapolated)"}
+    # batch-parallel on every host core: processes started with spawn (this process holds a
+    # CUDA context), each sample sized to about all_cores_s seconds
+    try:
+        psteps = max(1, min(w.steps, int(all_cores_s / max(per, 1e-4))))
+        nbp = min(w.batch, host_cores)
+        ctx = mp.get_context("spawn")
+        with cf.ProcessPoolExecutor(max_workers=nbp, mp_context=ctx) as ex:
+            list(ex.map(_oracle_worker, [w.name] * nbp, [[b] for b in range(nbp)], [[1]] * nbp))  # warm-up
+            t0 = time.perf_counter()
+            res = list(ex.map(_oracle_worker, [w.name] * nbp, [[b] for b in range(nbp)],
+                              [list(range(1, psteps + 1))] * nbp))
+            wall = time.perf_counter() - t0
+        done = sum(r[1] for r in res)
+        line["all_cores"] = {"value": done / wall / w.batch, "unit": UNIT, "cores": nbp,
+                             "sample": f"{nbp} processes x 1 batch x {psteps} decode steps, wall clock "
+                                       f"{wall:.1f} s, scaled to all {w.batch} batches (extrapolated)"}
+    except Exception as e:  # a baseline, not the measurement: report why it is missing
+        line["all_cores"] = {"unavailable": f"{type(e).__name__}: {e}"[:200]}
+    return line
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -270,6 +300,26 @@ def workload_config(w: synth.Workload, T: int, world: int) -> dict:
             "graph": f"one CUDA graph of the {T}-step loop and the end-of-search backtrack",
             "cache_refresh": "in place, copy on change (out-of-place figures under cache_refresh_out_of_place)",
             "parallelism": f"replicas x{world} (independent batches)"}
+
+
+def beam_step_kernels(w: synth.Workload, dev) -> int:
+    """Kernels one ls_beam_step launches on this workload: 1 where the plan takes the
+    one-kernel step K3 (k <= 8, every strip's stages within 32, two batches per SM at most),
+    else 2 (K1 + K2).  Mirrors the plan in csrc/api.cu."""
+    import torch
+
+    if os.environ.get("LS_BEAM_DEBUG"):
+        flags = os.environ["LS_BEAM_DEBUG"].split(",")
+        if "nofused" in flags:
+            return 2
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    es = 2 if w.dtype in ("f16", "bf16") else 4
+    vpl = 4 if (es == 4 or w.bias_var) else 8
+    parts = max(0, 8 // w.k)
+    if w.k > 8 or parts < 1:
+        return 2
+    ns = ((15 + w.vocab * es + 15) // 16 + 32 * vpl - 1) // (32 * vpl)
+    return 1 if (ns + parts - 1) // parts <= 32 and 2 * w.batch >= sms else 2
 
 
 def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
@@ -404,7 +454,8 @@ def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
         lsb.check(lsb.ls_read_status(lp.workspace, stream), "device status")
         return ms, k1 / reps, k4 / reps, bt / reps
 
-    launches_per_step = T * (3 if loop.cache is not None else 2) + 1  # K1, K2, K4 per decode step + backtrack
+    # kernels per decode step: the beam step (K3 alone, or K1 + K2) and the cache refresh; plus the backtrack
+    launches_per_step = T * (beam_step_kernels(wr, dev) + (1 if loop.cache is not None else 0)) + 1
     g_plain, g_inst = capture(loop)
     with ClockSampler(local) as clk:
         ms_plain, k1_ms, k4_ms, bt_ms = time_graphs(loop, g_plain, g_inst)
@@ -505,7 +556,12 @@ def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": wr.dtype, "data": "synthetic (seeded generators, workload recipe in synth/)", "config": cfg,
         "logit_gbs": k1_gbs, "step_gbs": step_gbs, "step_roofline_frac": step_gbs / peak,
-        "roofline": roof, "roofline_kernels": kern, "gpu_launches": launches_per_step * args.steps,
+        "roofline": roof, "roofline_kernels": kern,
+        "roofline_kernels_note": "per-kernel times come from a second, event-instrumented graph of the same "
+                                 "search (its events sit between the kernels, so each kernel's time includes a "
+                                 "little launch gap and its frac reads slightly low); value comes from the plain "
+                                 "graph",
+        "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks, "e2e": e2e, "sampling": sampling, "projection_step": projection,
         "cache_refresh_out_of_place": oop_line,
         "candidates": cand,
@@ -737,12 +793,14 @@ def bench_reference(args, w: synth.Workload):
     per = total / bs
     value = 1.0 / (per * w.batch)
     sample = (f"{args.steps} samples of 2 batches x 1 decode step of {w.name} (beam step + cache refresh), "
-              f"single thread; {per * 1e3:.1f} ms per batch-step, scaled to all {w.batch} batches")
+              f"single thread; {per * 1e3:.1f} ms per batch-step, scaled to all {w.batch} batches and "
+              f"{T} decode steps (extrapolated)")
     return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": per * w.batch * T * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic (seeded generators)", "impl": "reference",
             "config": workload_config(w, T, 1),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "host_cores": os.cpu_count() or 1,
+                             "kind": "oracle", "sample": sample, "extrapolated": True},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

@@ -254,14 +254,27 @@ LS_API ls_status ls_read_row_stats(const void* workspace, int batch, int k, int 
  *  - The first call on a device looks up that device's address of the array (the
  *    device must be current); make that first call before any stream capture.
  *  - All calls share the one array, which keeps the last call's contents; its status
- *    word is cleared at the start of each call and is not reported.  Calls whose work
- *    overlaps on the GPU (different streams, or threads without ordering) race on it.
+ *    word is cleared at the start of each call, and ls_beam_step_noalloc_status reads it
+ *    for the call before.  Calls whose work overlaps on the GPU (different streams, or
+ *    threads without ordering) race on it.
+ *  - Argument errors return LS_ERR_INVALID_ARG before anything is enqueued, as for
+ *    ls_beam_step.  After cudaDeviceReset the library is not used on that device again
+ *    (its device code, the array included, went with the context).
  */
 LS_API ls_status ls_beam_step_noalloc(const void* logits, ls_dtype logit_dtype, const float* bias,
                                       const float* beam_scores, const uint8_t* finished, int batch,
                                       int k, int vocab, int eos_id, int32_t* out_token,
                                       int32_t* out_parent, float* out_score, uint8_t* out_finished,
                                       void* stream);
+
+/*
+ * Device-detected status of the last ls_beam_step_noalloc on the current device (no
+ * counterpart in the article): synchronises `stream`, returns what the device recorded in
+ * the fixed array's status word since that call began (LS_OK, or e.g. LS_ERR_TIMEOUT when a
+ * bounded device wait ran out) and clears it.  Read it after the call and before the next
+ * one, which clears the word again.  LS_ERR_CUDA if the array cannot be reached.
+ */
+LS_API ls_status ls_beam_step_noalloc_status(void* stream);
 
 #ifdef __cplusplus
 }

@@ -18,7 +18,8 @@ __all__ = [
     "LS_OK", "LS_ERR_INVALID_ARG", "LS_ERR_UNSUPPORTED", "LS_ERR_CUDA", "LS_ERR_TIMEOUT", "LS_ERR_INTERNAL",
     "LS_DTYPE_F32", "LS_DTYPE_F16", "LS_DTYPE_BF16", "LS_MAX_K", "LsBeamError", "library_path", "load_library",
     "check", "ls_beam_step_workspace_size", "ls_workspace_init", "ls_beam_step", "ls_cache_reorder",
-    "ls_read_status", "ls_status_string", "ls_read_row_stats", "ls_beam_step_noalloc", "ls_backtrack",
+    "ls_read_status", "ls_status_string", "ls_read_row_stats", "ls_beam_step_noalloc", "ls_beam_step_noalloc_status",
+    "ls_backtrack",
     "ls_sample_workspace_size", "ls_sample", "ls_cache_refresh_inplace", "ls_logits_beam_step",
 ]
 
@@ -66,6 +67,8 @@ def load_library():
         lib.ls_read_row_stats.restype = ip
         lib.ls_beam_step_noalloc.argtypes = [vp, ip, vp, vp, vp, ip, ip, ip, ip, vp, vp, vp, vp, vp]
         lib.ls_beam_step_noalloc.restype = ip
+        lib.ls_beam_step_noalloc_status.argtypes = [vp]
+        lib.ls_beam_step_noalloc_status.restype = ip
         lib.ls_backtrack.argtypes = [vp, vp, ip, ip, ip, ip, vp, vp, vp, vp]
         lib.ls_backtrack.restype = ip
         lib.ls_sample_workspace_size.argtypes = [ip, ip, ip]
@@ -160,6 +163,12 @@ def ls_beam_step_noalloc(logits, bias, beam_scores, finished, eos_id: int, out_t
     return load_library().ls_beam_step_noalloc(
         _ptr(logits), _dtype_code(logits), _ptr(bias), _ptr(beam_scores), _ptr(finished), batch, k, vocab,
         int(eos_id), _ptr(out_token), _ptr(out_parent), _ptr(out_score), _ptr(out_finished), _stream(stream))
+
+
+def ls_beam_step_noalloc_status(stream=None) -> int:
+    """Device-detected status of the last ls_beam_step_noalloc on the current device (read and
+    cleared; synchronises the stream)."""
+    return load_library().ls_beam_step_noalloc_status(_stream(stream))
 
 
 def ls_cache_reorder(src, dst, parent, length: int, workspace=None, stream=None) -> int:

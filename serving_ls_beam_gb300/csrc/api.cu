@@ -321,29 +321,52 @@ ls_status ls_workspace_init(void* workspace, size_t workspace_bytes, void* strea
   return e == cudaSuccess ? LS_OK : cuda_fail(e);
 }
 
-ls_status ls_beam_step(const void* logits, ls_dtype logit_dtype, const float* bias, const float* beam_scores,
-                       const uint8_t* finished, int batch, int k, int vocab, int eos_id, int32_t* out_token,
-                       int32_t* out_parent, float* out_score, uint8_t* out_finished, void* workspace,
-                       size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace lsb {
+
+// The host-side checks of ls_beam_step's arguments other than the workspace: LS_OK when they
+// pass (batch == 0 included), LS_ERR_INVALID_ARG otherwise.
+ls_status beam_step_check_args(const void* logits, ls_dtype logit_dtype, const float* bias,
+                               const float* beam_scores, const uint8_t* finished, int batch, int k, int vocab,
+                               int eos_id, const int32_t* out_token, const int32_t* out_parent,
+                               const float* out_score, const uint8_t* out_finished) {
   if (batch < 0 || k < 1 || k > LS_MAX_K || vocab < k) return LS_ERR_INVALID_ARG;
   if ((long long)k * vocab >= (1ll << 31) || vocab > (1 << 28)) return LS_ERR_INVALID_ARG;
   if (eos_id < 0 || eos_id >= vocab) return LS_ERR_INVALID_ARG;
   if (!dtype_ok(logit_dtype)) return LS_ERR_INVALID_ARG;
   if (batch == 0) return LS_OK;
-  if (!logits || !beam_scores || !out_token || !out_parent || !out_score || !workspace) return LS_ERR_INVALID_ARG;
-  const WsLayout wl = ws_layout(batch, k, vocab);
-  if (wl.total == 0 || workspace_bytes < wl.total) return LS_ERR_INVALID_ARG;
+  if (!logits || !beam_scores || !out_token || !out_parent || !out_score) return LS_ERR_INVALID_ARG;
   const int es = dtype_bytes(logit_dtype);
   if (!aligned(logits, es) || (bias && !aligned(bias, 4)) || !aligned(beam_scores, 4) || !aligned(out_token, 4) ||
-      !aligned(out_parent, 4) || !aligned(out_score, 4) || !aligned(workspace, 256))
+      !aligned(out_parent, 4) || !aligned(out_score, 4))
     return LS_ERR_INVALID_ARG;
-  const Debug dbg = read_debug();
-  if (dbg.check_ptrs) {
-    const void* ptrs[] = {logits, bias, beam_scores, finished, out_token, out_parent, out_score, out_finished,
-                          workspace};
+  if (read_debug().check_ptrs) {
+    const void* ptrs[] = {logits, bias, beam_scores, finished, out_token, out_parent, out_score, out_finished};
     for (const void* q : ptrs)
       if (q && !device_reachable(q)) return LS_ERR_INVALID_ARG;
   }
+  return LS_OK;
+}
+
+}  // namespace lsb
+
+extern "C" {
+
+ls_status ls_beam_step(const void* logits, ls_dtype logit_dtype, const float* bias, const float* beam_scores,
+                       const uint8_t* finished, int batch, int k, int vocab, int eos_id, int32_t* out_token,
+                       int32_t* out_parent, float* out_score, uint8_t* out_finished, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  const ls_status chk = beam_step_check_args(logits, logit_dtype, bias, beam_scores, finished, batch, k, vocab,
+                                             eos_id, out_token, out_parent, out_score, out_finished);
+  if (chk != LS_OK || batch == 0) return chk;
+  if (!workspace) return LS_ERR_INVALID_ARG;
+  const WsLayout wl = ws_layout(batch, k, vocab);
+  if (wl.total == 0 || workspace_bytes < wl.total) return LS_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return LS_ERR_INVALID_ARG;
+  const Debug dbg = read_debug();
+  if (dbg.check_ptrs && !device_reachable(workspace)) return LS_ERR_INVALID_ARG;
+  const int es = dtype_bytes(logit_dtype);
   int dev = 0;
   DeviceInfo* di = device_info(&dev);
   if (!di) return cuda_fail(cudaErrorUnknown);

@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "ls_beam.h"
+
 namespace lsb {
 
 // ---------------------------------------------------------------- kernel shape constants
@@ -260,6 +262,12 @@ struct PdlLaunch {
     cfg.numAttrs = 1;
   }
 };
+
+// Host-side checks of ls_beam_step's arguments other than the workspace (api.cu).
+ls_status beam_step_check_args(const void* logits, ls_dtype logit_dtype, const float* bias,
+                               const float* beam_scores, const uint8_t* finished, int batch, int k, int vocab,
+                               int eos_id, const int32_t* out_token, const int32_t* out_parent,
+                               const float* out_score, const uint8_t* out_finished);
 
 // Launchers (defined next to their kernels).
 size_t beam_rows_smem_bytes(int vpl);

@@ -10,9 +10,13 @@
 //
 // Limits and sharing: shapes whose scratch (ls_beam_step_workspace_size) exceeds
 // kNoAllocScratchBytes are rejected.  Every call uses the same array and leaves its
-// contents behind; the status word is cleared at the start of each call.  Calls whose
-// work overlaps on the GPU (different streams, or different host threads without
-// ordering) race on the array and must not be issued.
+// contents behind; the status word (device-detected errors, e.g. a bounded wait that ran
+// out) is cleared at the start of each call and read with ls_beam_step_noalloc_status
+// before the next one.  Calls whose work overlaps on the GPU (different streams, or
+// different host threads without ordering) race on the array and must not be issued.
+// The array's device address is looked up once per device; a cudaDeviceReset unloads the
+// library's device code with the context, so the library is not used on a device after
+// one.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -54,8 +58,10 @@ extern "C" ls_status ls_beam_step_noalloc(const void* logits, ls_dtype logit_dty
                                           const float* beam_scores, const uint8_t* finished, int batch, int k,
                                           int vocab, int eos_id, int32_t* out_token, int32_t* out_parent,
                                           float* out_score, uint8_t* out_finished, void* stream) {
-  if (batch < 0 || k < 1 || k > LS_MAX_K || vocab < k) return LS_ERR_INVALID_ARG;
-  if (batch == 0) return LS_OK;
+  // every argument check of ls_beam_step first: a rejected call touches nothing on the GPU
+  const ls_status chk = lsb::beam_step_check_args(logits, logit_dtype, bias, beam_scores, finished, batch, k,
+                                                  vocab, eos_id, out_token, out_parent, out_score, out_finished);
+  if (chk != LS_OK || batch == 0) return chk;
   const size_t need = ls_beam_step_workspace_size(batch, k, vocab);
   if (need == 0) return LS_ERR_INVALID_ARG;
   if (need > kNoAllocScratchBytes) return LS_ERR_UNSUPPORTED;  // beyond the fixed scratch
@@ -69,4 +75,10 @@ extern "C" ls_status ls_beam_step_noalloc(const void* logits, ls_dtype logit_dty
   }
   return ls_beam_step(logits, logit_dtype, bias, beam_scores, finished, batch, k, vocab, eos_id, out_token,
                       out_parent, out_score, out_finished, scratch, kNoAllocScratchBytes, stream);
+}
+
+extern "C" ls_status ls_beam_step_noalloc_status(void* stream) {
+  void* scratch = scratch_address();
+  if (!scratch) return LS_ERR_CUDA;
+  return ls_read_status(scratch, stream);  // the status word is the array's first word
 }

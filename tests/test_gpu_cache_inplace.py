@@ -116,8 +116,10 @@ def test_bad_parent_leaves_the_row_and_is_reported(dev, oracle_mod, env):
 
 def test_c5_loop_refreshed_in_place(dev, oracle_mod):
     """16 decode steps of c5 with the cache refreshed in place; sampled batches against the
-    oracle's own trajectory (compared while no near-tie lets the trajectories part)."""
-    from parity import GAP_TOL, boundary_gaps
+    oracle's own trajectory.  A batch leaves the comparison only when the oracle shows a
+    near-tie at the k-th place (the trajectories may then part legitimately); until then
+    every step's selection must equal the oracle's, and the final cache rows must match."""
+    from parity import GAP_TOL, boundary_gaps, compare_step
 
     w = synth.WORKLOADS["c5"]
     layers, heads, max_len, head_dim = w.kv_shape
@@ -133,6 +135,7 @@ def test_c5_loop_refreshed_in_place(dev, oracle_mod):
     o_beam = synth.beam_scores(w, 0)[sample].copy()
     o_fin = np.zeros((len(sample), w.k), np.uint8)
     alive = set(range(len(sample)))
+    compared = 0
     for t in range(1, steps + 1):
         lg = synth.logits(w, t)
         idx = loop.step(torch.from_numpy(lg).to(dev), t)
@@ -140,13 +143,39 @@ def test_c5_loop_refreshed_in_place(dev, oracle_mod):
         ora = oracle_mod.beam_step(lg[sample], o_beam, finished=o_fin, eos_id=w.eos_id, m_out=w.k + 8)
         gaps = boundary_gaps(ora, w.k)
         for i in sorted(alive):
-            if gaps[i] < GAP_TOL or not (out["parent"][i] == ora["parent"][i, : w.k]).all():
+            compare_step(out, ora, w.k, w.dtype, finished=o_fin, eos_id=w.eos_id, batches=[i])
+            if gaps[i] < GAP_TOL:
                 alive.discard(i)
+            else:
+                assert (out["token"][i] == ora["token"][i, : w.k]).all()
+                assert (out["parent"][i] == ora["parent"][i, : w.k]).all()
+                compared += 1
         o_cache = oracle_mod.cache_refresh_inplace(o_cache, ora["parent"][:, : w.k].astype(np.int32), t)
         o_beam = ora["score"][:, : w.k].astype(np.float32)
         o_fin = ora["finished"][:, : w.k].astype(np.uint8)
-    assert alive
+    assert alive and compared >= len(sample) * steps // 2
     final = loop.current_cache()[:, rows].cpu().numpy()
     for i in sorted(alive):
         sl = slice(i * w.k, (i + 1) * w.k)
         assert np.array_equal(final[:, sl, :, :steps].view(np.int16), o_cache[:, sl, :, :steps].view(np.int16))
+
+
+def test_bulk_copy_wait_timeout_is_reported(dev, oracle_mod):
+    """A zero wait budget makes the bulk-copy kernel's bounded waits run out: it records a
+    timeout in the workspace and returns after the copies it issued have landed; the context
+    stays usable and, on a restored cache, the same call gives the oracle's result."""
+    g = np.random.default_rng(11)
+    dtype, layers, batch, k, heads, max_len, length, head_dim = ("f16", 2, 10, 4, 3, 16, 16, 64)
+    shape = (layers, batch * k, heads, max_len, head_dim)
+    cache = _cache(g, shape, dtype)
+    parent = torch.from_numpy(_parents(g, batch, k)).to(dev)
+    ws = torch.zeros(lsb.ls_beam_step_workspace_size(1, 1, 1), dtype=torch.uint8, device=dev)
+    t = _to_dev(cache, dtype, dev)
+    _with_env("spin=0", lambda: lsb.check(lsb.ls_cache_refresh_inplace(t, parent, length, ws)))
+    assert lsb.ls_read_status(ws) == lsb.LS_ERR_TIMEOUT
+    lsb.check(lsb.ls_workspace_init(ws))
+    t = _to_dev(cache, dtype, dev)
+    lsb.check(lsb.ls_cache_refresh_inplace(t, parent, length, ws))
+    assert lsb.ls_read_status(ws) == lsb.LS_OK
+    want = oracle_mod.cache_refresh_inplace(cache, parent.cpu().numpy(), length)
+    assert np.array_equal(_bits(t, dtype), want.view(np.int16))

@@ -233,3 +233,32 @@ def test_full_size_p5_sampled(dev, oracle_mod):
     assert np.all(np.diff(gpu["score"], axis=1) <= 0)
     assert np.all((gpu["parent"] >= 0) & (gpu["parent"] < w.k))
     assert np.all((gpu["token"] >= 0) & (gpu["token"] < w.vocab))
+
+
+def test_device_wait_timeout_is_reported(dev, oracle_mod):
+    """A zero wait budget makes the projection kernel's bounded waits run out: every CTA sets
+    the timeout bit, lets the copies and products it issued finish, frees its tensor memory and
+    returns; the status is reported and the next call on a fresh workspace matches the oracle."""
+    inp = make(40, 4, 5000, 200, "bf16", seed=23)
+    H, W = inp["hidden"], inp["weight"]
+    B, K, D = H.shape
+    V = W.shape[0]
+    th, tw = dev_tensor(H, "bf16", dev), dev_tensor(W, "bf16", dev)
+    beam = torch.from_numpy(np.ascontiguousarray(inp["beam_scores"], dtype=np.float32)).to(dev)
+    tok = torch.empty((B, K), dtype=torch.int32, device=dev)
+    par, sc = torch.empty_like(tok), torch.empty((B, K), dtype=torch.float32, device=dev)
+    ws = torch.empty(lsb.ls_beam_step_workspace_size(B, K, V), dtype=torch.uint8, device=dev)
+    lsb.check(lsb.ls_workspace_init(ws))
+    old = os.environ.get("LS_BEAM_DEBUG")
+    os.environ["LS_BEAM_DEBUG"] = "spin=0"
+    try:
+        st = lsb.ls_logits_beam_step(th, tw, None, beam, None, inp["eos_id"], tok, par, sc, None, ws)
+    finally:
+        if old is None:
+            os.environ.pop("LS_BEAM_DEBUG", None)
+        else:
+            os.environ["LS_BEAM_DEBUG"] = old
+    assert st == lsb.LS_OK
+    assert lsb.ls_read_status(ws) == lsb.LS_ERR_TIMEOUT
+    gpu = run_gpu(inp, dev)
+    check(oracle_mod, inp, gpu)

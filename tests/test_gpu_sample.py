@@ -4,8 +4,9 @@ ties (all-equal logits, the exact fallback), the forced exact path, and argument
 
 A token must equal the oracle's unless the oracle's uniform lies within 1e-5 of a
 cumulative-probability boundary of the kept candidates (both sides then round legitimately
-either way); the log-probability of an agreeing token is within 1e-5 (fp32 logits) or
-2e-3 (fp16, bf16) of the oracle's."""
+either way); at most MAX_EXCUSED rows of a call may be excused that way.  The
+log-probability of an agreeing token is within 1e-5 (fp32 logits) or 2e-3 (fp16, bf16) of
+the oracle's."""
 import os
 
 import numpy as np
@@ -19,6 +20,7 @@ pytestmark = pytest.mark.gpu
 import serving_ls_beam_gb300 as lsb  # noqa: E402
 
 MARGIN = 1e-5
+MAX_EXCUSED = 2  # rows of one call whose token may differ at a boundary
 TOL = {"f32": 1e-5, "f16": 2e-3, "bf16": 2e-3}
 
 
@@ -66,6 +68,8 @@ def compare(oracle_mod, lg, dtype, bias, u, top_k, top_p, tok, lp):
     near = ora["margin"] < MARGIN
     bad = np.nonzero(~same & ~near)[0]
     assert bad.size == 0, f"rows {bad[:8]}: GPU {tok[bad[:8]]} vs oracle {ora['token'][bad[:8]]}"
+    excused = int((~same & near).sum())
+    assert excused <= MAX_EXCUSED, f"{excused} rows differ at a cumulative boundary"
     err = np.abs(lp[same].astype(np.float64) - ora["logprob"][same])
     assert err.size == 0 or err.max() <= TOL[dtype], f"logprob error {err.max()}"
     return int(same.sum())
@@ -148,3 +152,29 @@ def test_sample_argument_checks(dev):
     small = torch.zeros(64, dtype=torch.uint8, device=dev)
     assert lsb.ls_sample(lg, None, u, 8, 1.0, tok, None, small) == lsb.LS_ERR_INVALID_ARG
     assert lsb.ls_sample_workspace_size(4, 101, 100) == 0
+
+
+def test_device_wait_timeout_is_reported(dev, oracle_mod):
+    """A zero wait budget makes the first traversal's bounded waits run out: the timeout is
+    reported by ls_read_status, and a re-initialised workspace gives the oracle's draws again."""
+    lg, dtype, bias, u, top_k, top_p = _case(7)
+    rows, vocab = lg.shape
+    t_lg = _logits_dev(lg, dtype, dev)
+    t_b = None if bias is None else torch.from_numpy(bias).to(dev)
+    t_u = torch.from_numpy(u).to(dev)
+    tok = torch.full((rows,), -1, dtype=torch.int32, device=dev)
+    ws = torch.empty(lsb.ls_sample_workspace_size(rows, top_k, vocab), dtype=torch.uint8, device=dev)
+    lsb.check(lsb.ls_workspace_init(ws))
+    old = os.environ.get("LS_BEAM_DEBUG")
+    os.environ["LS_BEAM_DEBUG"] = "spin=0"
+    try:
+        st = lsb.ls_sample(t_lg, t_b, t_u, top_k, top_p, tok, None, ws)
+    finally:
+        if old is None:
+            os.environ.pop("LS_BEAM_DEBUG", None)
+        else:
+            os.environ["LS_BEAM_DEBUG"] = old
+    assert st == lsb.LS_OK
+    assert lsb.ls_read_status(ws) == lsb.LS_ERR_TIMEOUT
+    tok2, lp2 = run_gpu(dev, lg, dtype, bias, u, top_k, top_p)
+    compare(oracle_mod, lg, dtype, bias, u, top_k, top_p, tok2, lp2)

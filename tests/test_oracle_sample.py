@@ -99,3 +99,26 @@ def test_bad_arguments_are_rejected():
         oracle.sample(np.zeros((1, 4), np.float32), [0.5], top_k=5)
     with pytest.raises(ValueError):
         oracle.sample(np.zeros((1, 4), np.float32), [0.5], top_k=2, top_p=0.0)
+
+
+def test_margin_is_the_distance_to_the_nearest_boundary():
+    """The margin the GPU comparison excuses by: the distance of u from the nearest cumulative
+    boundary of the kept set (and of top_p from one of the top_k's), on hand-made probabilities
+    whose normalised cumulative sums are known: 0.5, 0.8, 1.0."""
+    x = np.log(np.array([0.5, 0.3, 0.2, 1e-30], np.float64)).astype(np.float32)
+    rows = np.tile(x, (6, 1))
+    u = np.array([0.45, 0.79, 0.62, 0.1, 0.999, 0.5001])
+    r = oracle.sample(rows, u, top_k=3)
+    # kept boundaries at 0.5 and 0.8 (the last, 1.0, is not a boundary)
+    want = [0.05, 0.01, 0.12, 0.4, 0.199, 0.0001]
+    np.testing.assert_allclose(r["margin"], want, rtol=0, atol=1e-6)
+    np.testing.assert_array_equal(r["token"], [0, 1, 1, 0, 2, 1])
+    # top_p 0.75 keeps tokens 0, 1 (cumulative 0.625 inside the kept set); the cut's own
+    # margin is min |{0.5, 0.8, 1.0} - 0.75| = 0.05
+    r = oracle.sample(rows[:3], np.array([0.6, 0.1, 0.64]), top_k=3, top_p=0.75)
+    np.testing.assert_allclose(r["margin"], [0.025, 0.05, 0.015], rtol=0, atol=1e-6)
+    # a single kept candidate has no boundary: the margin is its ceiling, 1
+    r = oracle.sample(rows[:2], np.array([0.3, 0.9]), top_k=1)
+    np.testing.assert_array_equal(r["margin"], [1.0, 1.0])
+    # a planted mistake a margin of 0 everywhere would excuse every row: the pins above fail it
+    assert (oracle.sample(rows, u, top_k=3)["margin"] > 0).all()
