@@ -1,8 +1,9 @@
 """GPU parity of ls_beam_step against the oracle (called through the C ABI).
 
 Workloads c1-c4 run at their full sizes, in the launch configuration the
-benchmark uses, and are compared with the oracle element by element; the
-multi-step workload c5 is covered in test_gpu_multistep.py.  The sweeps below
+benchmark uses, and are compared with the oracle element by element, and so
+does one step of the multi-step workload c5 (all 256 batches); its whole
+decode loop is covered in test_gpu_multistep.py.  The sweeps below
 add ragged vocabularies (not a multiple of the 16-byte vector), misaligned
 logits, k = 1 and k = 64, vocab == k, bias, finished beams and bf16.
 
@@ -110,12 +111,19 @@ def run_oracle(oracle_mod, inp, m_extra=8):
                                 eos_id=inp["eos_id"], m_out=K + m_extra, dtype=inp["dtype"])
 
 
-@pytest.mark.parametrize("name", ["c1", "c2", "c3", "c4"])
-def test_workload_parity(dev, oracle_mod, name):
+_oracle_cache = {}
+
+
+@pytest.mark.parametrize("name", ["c1", "c2", "c3", "c4", "c5"])
+def test_workload_parity(dev, oracle_mod, impl, name):
+    """Every batch of each workload at its full size (c5: one step of its decode loop, step 1,
+    whose beams are no longer tied, all 256 batches)."""
     w = synth.WORKLOADS[name]
-    inp = synth.step_inputs(w, 0)
+    inp = synth.step_inputs(w, 1 if name == "c5" else 0)
     gpu, ws = run_gpu(inp, dev)
-    ora = run_oracle(oracle_mod, inp)
+    if name not in _oracle_cache:  # the same inputs under every implementation
+        _oracle_cache[name] = run_oracle(oracle_mod, inp)
+    ora = _oracle_cache[name]
     compare_step(gpu, ora, w.k, w.dtype, finished=inp["finished"], eos_id=w.eos_id)
     # diagnostics: lse per beam and the R-top-k lower bound against the true k-th largest
     lse, rtopk, ncand, path = lsb.ls_read_row_stats(ws, w.batch, w.k, w.vocab)

@@ -222,7 +222,9 @@ def test_full_size_p5_sampled(dev, oracle_mod):
     w = synth.PROJ_WORKLOADS["p5"]
     inp = synth.projection_inputs(w)
     gpu = run_gpu(inp, dev)
-    batches = [0, 31, 32, 100, 160, 255]  # rows in 6 of the 8 row blocks
+    # both batches on each side of every 128-row block edge (32 batches of 4 beams a block),
+    # so every row block and every pair of adjacent blocks is compared
+    batches = [0, 1] + [e + d for e in range(32, 256, 32) for d in (-1, 0)] + [254, 255]
     sub = {"hidden": inp["hidden"][batches], "weight": inp["weight"], "bias": inp["bias"],
            "beam_scores": inp["beam_scores"][batches], "finished": None, "eos_id": inp["eos_id"],
            "dtype": inp["dtype"]}
