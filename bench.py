@@ -57,6 +57,9 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--decode-steps", type=int, default=0,
                     help="run only the first N decode steps of the workload (for small profiling runs)")
+    ap.add_argument("--kernel", choices=["beam_step", "cache_refresh_inplace", "cache_reorder"], default=None,
+                    help="profiling driver: time one kernel of the loop alone on the last decode steps of the "
+                         "workload (inputs of a few hundred MB to 1.6 GB) and print its per-launch figures")
     return ap.parse_args()
 
 
@@ -302,6 +305,121 @@ def workload_config(w: synth.Workload, T: int, world: int) -> dict:
             "parallelism": f"replicas x{world} (independent batches)"}
 
 
+def moved_rows(par: np.ndarray, K: int) -> np.ndarray:
+    """Rows the in-place refresh moves per step, from parents [steps, batch, k]: each changed beam
+    is written once and each parent a changed beam needs is read once per batch."""
+    steps, B = par.shape[:2]
+    changed = par != np.arange(K)[None, None, :]
+    needed = np.zeros((steps, B, K), bool)
+    for j in range(K):
+        needed[np.arange(steps)[:, None], np.arange(B)[None, :], par[:, :, j]] |= changed[:, :, j]
+    return changed.sum(axis=(1, 2)) + needed.sum(axis=(1, 2))
+
+
+def bench_kernel(args, w: synth.Workload):
+    """Profiling driver: one kernel of the decode loop, alone, at the workload's last three decode
+    steps.  It walks the search's own trajectory with one step's logits on the device at a time
+    (beam state carried from step to step as in the benchmark loop, so the parents are the loop's),
+    then launches the kernel on those three steps: the beam step on their logits (3 x 82 MB at c5),
+    the cache refresh at len = step on one seeded cache (in place, 805 MB) or two (out of place,
+    1.6 GB).  Each of --warmup + --steps rounds launches the kernel once per step; the JSON line gives
+    each step's event-timed microseconds and algorithmic bytes (one round is 3 launches, so
+    `ncu -k <kernel> -s <launches before> -c 3` captures the three full-size launches)."""
+    import torch
+
+    import serving_ls_beam_gb300 as lsb
+    from serving_ls_beam_gb300 import _build
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device")
+    dev = torch.device("cuda", 0)
+    _build.build()
+    lsb.load_library()
+    B, K, V = w.batch, w.k, w.vocab
+    es = 2 if w.dtype in ("f16", "bf16") else 4
+    multi = w.steps > 1
+    last = w.steps if multi else 0
+    steps = list(range(max(1 if multi else 0, last - 2), last + 1))
+    ws = torch.empty(lsb.ls_beam_step_workspace_size(B, K, V), dtype=torch.uint8, device=dev)
+    lsb.check(lsb.ls_workspace_init(ws))
+    bias_np = synth.bias(w)
+    bias = None if bias_np is None else torch.from_numpy(bias_np).to(dev)
+    fin_np = synth.finished(w)
+    scores = [torch.from_numpy(synth.beam_scores(w, 0)).to(dev), torch.empty((B, K), dtype=torch.float32, device=dev)]
+    fins = [torch.zeros((B, K), dtype=torch.uint8, device=dev) if fin_np is None
+            else torch.from_numpy(fin_np).to(dev), torch.empty((B, K), dtype=torch.uint8, device=dev)]
+    tok = torch.empty((B, K), dtype=torch.int32, device=dev)
+    ins, parents = [], []
+    cur = 0
+    for t in (range(1, last + 1) if multi else [0]):
+        lg = torch.from_numpy(synth.logits(w, t)).to(dev)
+        par = torch.empty((B, K), dtype=torch.int32, device=dev)
+        if t in steps:
+            ins.append((lg, scores[cur].clone(), fins[cur].clone()))
+        lsb.check(lsb.ls_beam_step(lg, bias, scores[cur], fins[cur], w.eos_id, tok, par, scores[1 - cur],
+                                   fins[1 - cur], ws), "ls_beam_step")
+        if t in steps:
+            parents.append(par)
+        cur = 1 - cur
+    torch.cuda.synchronize()
+    lsb.check(lsb.ls_read_status(ws), "device status")
+    sc = torch.empty((B, K), dtype=torch.float32, device=dev)
+    fo = torch.empty((B, K), dtype=torch.uint8, device=dev)
+    if args.kernel == "beam_step":
+        nbytes = [(w.rows - int(f.sum())) * V * es + (V * 4 if bias is not None else 0) + w.rows * 13
+                  for (_, _, f) in ins]
+
+        def launch(i):
+            lg, beam, fin = ins[i]
+            return lsb.ls_beam_step(lg, bias, beam, fin, w.eos_id, tok, parents[i], sc, fo, ws)
+    else:
+        ins.clear()
+        if w.kv_shape is None:
+            raise SystemExit(f"bench.py: workload {w.name} has no cache")
+        layers, heads, max_len, head_dim = w.kv_shape
+        shape = (layers, w.rows, heads, max_len, head_dim)
+        lens = [t if multi else max_len for t in steps]
+        slabs = [layers * heads * n * head_dim * 2 for n in lens]
+        caches = [torch.from_numpy(synth.kv_cache(shape, w.seed, which=i)).to(dev)
+                  for i in range(1 if args.kernel == "cache_refresh_inplace" else 2)]
+        if args.kernel == "cache_refresh_inplace":
+            par_np = np.stack([p.cpu().numpy() for p in parents])
+            nbytes = [int(m) * sl for m, sl in zip(moved_rows(par_np, K), slabs)]
+
+            def launch(i):
+                return lsb.ls_cache_refresh_inplace(caches[0], parents[i], lens[i], ws)
+        else:
+            nbytes = [2 * w.rows * sl for sl in slabs]
+
+            def launch(i):
+                return lsb.ls_cache_reorder(caches[i % 2], caches[1 - i % 2], parents[i], lens[i])
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in steps]
+    us = [[] for _ in steps]
+    for rnd in range(args.warmup + args.steps):
+        torch.cuda.synchronize()
+        torch.cuda._sleep(1 << 20)  # ~0.5 ms of GPU time, so every launch below is queued before it starts
+        for i in range(len(steps)):
+            ev[i][0].record()
+            lsb.check(launch(i), args.kernel)
+            ev[i][1].record()
+        torch.cuda.synchronize()
+        if rnd >= args.warmup:
+            for i in range(len(steps)):
+                us[i].append(ev[i][0].elapsed_time(ev[i][1]) * 1e3)
+    lsb.check(lsb.ls_read_status(ws), "device status")
+    peak, peak_src = hbm_peak()
+    launches = []
+    for i, t in enumerate(steps):
+        u = statistics.median(us[i]) if us[i] else None
+        launches.append({"decode_step": t, "us": u, "algorithmic_bytes": nbytes[i],
+                         "gbs": None if not u else nbytes[i] / (u * 1e-6) / 1e9})
+    return {"kernel": args.kernel, "workload": w.name, "warmup": args.warmup, "steps": args.steps,
+            "peak": peak, "peak_source": peak_src, "launches": launches,
+            "note": "each launch timed with CUDA events around it, the three launches of a round queued "
+                    "back to back behind a GPU sleep (no host launch time inside); no L2 flush between "
+                    "launches, each launch reads inputs larger than L2 or those of the previous step"}
+
+
 def beam_step_kernels(w: synth.Workload, dev) -> int:
     """Kernels one ls_beam_step launches on this workload: 1 where the plan takes the
     one-kernel step K3 (k <= 8, every strip's stages within 32, two batches per SM at most),
@@ -480,15 +598,10 @@ def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
         layers, heads, max_len, head_dim = wr.kv_shape
         # in place: each batch reads the slabs of the parents its changed beams need and writes
         # the changed beams (exact, from the run's parents); out of place: every row both ways
-        par = parents_run.reshape(T, B, K)
-        changed = par != np.arange(K)[None, None, :]
-        needed = np.zeros((T, B, K), bool)
-        for j in range(K):
-            needed[np.arange(T)[:, None], np.arange(B)[None, :], par[:, :, j]] |= changed[:, :, j]
-        moved_rows = changed.sum(axis=(1, 2)) + needed.sum(axis=(1, 2))
+        moved = moved_rows(parents_run.reshape(T, B, K), K)
         for t in range(1, T + 1):
             slab = layers * heads * lens(t) * head_dim * 2
-            k4_bytes += int(moved_rows[t - 1]) * slab
+            k4_bytes += int(moved[t - 1]) * slab
             k4_dense_bytes += 2 * wr.rows * slab
     peak, peak_src = hbm_peak()
     k1_gbs = k1_bytes / (k1_ms / 1e3) / 1e9
@@ -818,6 +931,10 @@ def main():
         if args.impl == "reference":
             if rank == 0:
                 print(json.dumps(bench_reference(args, w)))
+            return
+        if args.kernel:
+            if rank == 0:
+                print(json.dumps(bench_kernel(args, w)))
             return
         line = bench_gpu(args, w, world, rank, local)
         if rank == 0:

@@ -9,22 +9,28 @@
 // log_sum_exp, and one sort of that short queue per batch gives the exact top-k.
 //
 // GB300 design:
-//  * One CTA per batch, kFuWarps warps.  The batch's k rows are cut into k * W strips
-//    (units); a warp streams its strips with plain 16-byte loads (ld.global.cs), the next
-//    stage's loads issued before the current stage is worked on (two register buffers), so
-//    every warp keeps a stage of loads in flight: on this part plain loads sustain more
-//    read bandwidth than one bulk-copy ring per warp.
-//  * First traversal, per stage and in registers: each lane's max of its 64-element block (its
-//    8 vectors of the stage) goes to shared memory, and a running (max, sum of exp(x - max))
-//    per lane accumulates log_sum_exp.  The blocks partition the row, so the k-th largest
-//    block max of a row is its R-top-k bound (groups = blocks: the article's "any split").
-//  * Second traversal, once the CTA has every block max: each row's R is the k-th largest of
-//    its block maxima, and only the blocks whose max reaches R (a handful per row) are read
-//    again -- from L2, 128 bytes each -- for their elements x >= R, rescored and ranked in
-//    shared memory (each key's rank counted against the others; the k of rank < k are the
-//    outputs).  Nothing else goes through global memory between the traversals and the rank.
-//  * More than kFuCap candidates (ties), or the forced exact mode, send the batch to an exact
-//    path: a radix select of every beam's top-k over its logits.
+//  * One CTA per batch, kFuWarps warps.  The batch's k rows are cut into k * W strips; a warp
+//    streams its strip through a ring of kFuRing stages in shared memory, filled by 16-byte
+//    asynchronous copies (each lane copies, then reads, its own vectors: no barrier), with
+//    kFuRing - 1 stages in flight while one is worked on.
+//  * First traversal, per stage and in registers: a running (max, sum of exp(x - max)) per
+//    lane accumulates log_sum_exp.  The lanes' running maxima give the strip's R-top-k bound as
+//    the traversal goes (groups = lanes mod G, G the power of two >= k: the k-th largest group
+//    max, the least one when G = k); on the first stage the k-th largest of the lanes' block
+//    maxima tightens it.  The bound only rises, and at every point it is at most the strip's
+//    k-th largest element, so the elements of a stage at or above it (read from registers,
+//    only in lanes whose block max reaches it) hold every element of the row's top-k in the
+//    stage.  They go to the strip's short candidate list; when the list fills, entries below
+//    the current bound are dropped.  No logit is read twice.
+//  * Per row: lse from the strips' (max, sum); R = the largest of the strips' bounds.  The
+//    candidates at or above R are rescored (beam_score + x - lse) into 128-bit keys in shared
+//    memory and ranked (each key's rank counted against the others; the k of rank < k are the
+//    outputs).  Nothing goes through global memory between the traversals and the rank.
+//  * More than kFuList candidates in a strip's list, more than kFuCap keys, or the forced
+//    exact mode send the batch to an exact path: a radix select of every beam's top-k over its
+//    logits.
+#include <type_traits>
+
 #include "ls_device.cuh"
 #include "ls_dtype.cuh"
 #include "ls_internal.h"
@@ -38,20 +44,22 @@ constexpr int kFuCap = 512;  // keys the fine rank holds
 
 enum { FROW_LIVE = 0, FROW_FIN = 1, FROW_DEAD = 2 };
 
-// Dynamic shared memory: the per-warp rings of kFuRing stages (the rank keys reuse them once
-// the first traversal is done), then the block maxima, [strip][stage of the strip][lane].
+// Dynamic shared memory: the per-warp rings of kFuRing stages; the rank keys reuse them once
+// the first traversal is done.
 constexpr int kFuRing = 3;
-constexpr int kFuList = 32;  // candidates a strip keeps
-constexpr int kFuHits = 64;  // blocks a strip reads again
+constexpr int kFuList = 32;     // candidates a strip keeps
+constexpr int kFuVecs = 32;     // 16-byte vectors a strip saves for its candidates
+constexpr int kFuCompact = 16;  // saved vectors past which those below the bound are dropped
 
 struct __align__(16) FuSmem {
+  uint4 hv[kFuWarps][kFuVecs];      // saved vectors holding elements at or above the bound
+  int hi[kFuWarps][kFuVecs];        // their vector index in the row
   Key* keys;                        // kFuCap keys, over the rings
   float um[kFuWarps], us[kFuWarps];  // strip max and sum of exp(x - max)
-  float ur[kFuWarps];                // strip bound: k-th largest block max of the strip
-  int ucnt[kFuWarps], uovf[kFuWarps];
+  float ur[kFuWarps];                // strip bound (running R-top-k at the end of the strip)
+  int ucnt[kFuWarps], uovf[kFuWarps], hcnt[kFuWarps];
   float2 cand[kFuWarps][kFuList];    // the strip's candidates (x, token)
-  int hits[kFuWarps][kFuHits];       // the strip's blocks reaching its bound (stage * 32 + lane)
-  double c[kFuMaxK];  // beam_score - log_sum_exp of each live row
+  ScoreBase c[kFuMaxK];  // beam_score - log_sum_exp of each live row
   float beam[kFuMaxK], lse[kFuMaxK], R[kFuMaxK];
   int fin[kFuMaxK], kind[kFuMaxK], ncand[kFuMaxK];
   int nkeys, path;
@@ -64,9 +72,9 @@ struct __align__(16) FuSmem {
 
 }  // namespace
 
-size_t beam_fused_smem_bytes(int vpl, int sps) {
+size_t beam_fused_smem_bytes(int vpl) {
   const size_t ring = (size_t)kFuWarps * kFuRing * 32 * vpl * 16;
-  return (ring > kFuCap * sizeof(Key) ? ring : kFuCap * sizeof(Key)) + (size_t)kFuWarps * sps * 32 * 4;
+  return ring > kFuCap * sizeof(Key) ? ring : kFuCap * sizeof(Key);
 }
 
 namespace {
@@ -154,7 +162,7 @@ __device__ void exact_row(const StepParams& p, FuSmem& sm, int b, int j) {
   }
   const uint32_t tkey = sm.prefix;
   const int need_eq = sm.need;
-  const double c = sm.c[j];
+  const ScoreBase c = sm.c[j];
   for (int base = 0; base < V; base += kFuThreads) {
     const int i = base + tid;
     float x = 0.0f;
@@ -163,7 +171,7 @@ __device__ void exact_row(const StepParams& p, FuSmem& sm, int b, int j) {
       x = xat(i);
       take = float_ord(x) > tkey;
     }
-    append_key(sm, take, make_key((float)(c + (double)x), j, x, i));
+    append_key(sm, take, make_key(score_of(c, x), j, x, i));
   }
   __syncthreads();
   // the first need_eq elements equal to the K-th key, in token order
@@ -185,7 +193,7 @@ __device__ void exact_row(const StepParams& p, FuSmem& sm, int b, int j) {
       total += sm.wc[w];
     }
     const int off = taken + before + __popc(ballot & ((1u << lane) - 1u));
-    append_key(sm, eq && off < need_eq, make_key((float)(c + (double)x), j, x, i));
+    append_key(sm, eq && off < need_eq, make_key(score_of(c, x), j, x, i));
     taken += total;
     __syncthreads();
   }
@@ -204,9 +212,7 @@ __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepPar
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = blockIdx.x;
   const int K = p.k, V = p.vocab, W = p.nc;  // W strips per row, one warp per strip
-  const int SPS = p.stages;                  // block-max rows kept per strip
   unsigned char* ring = fu_dyn + (size_t)warp * kFuRing * CV * 16;
-  float* bmax = reinterpret_cast<float*>(fu_dyn + (size_t)kFuWarps * kFuRing * CV * 16);
   const int row_bytes = V * ES;
   const unsigned char* logits = static_cast<const unsigned char*>(p.logits);
 
@@ -296,19 +302,50 @@ __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepPar
   };
 
   // ---------------------------------------------------------------- first traversal
-  // warp u streams strip s = u mod W of row j = u / W: stages s, s + W, ...
+  // warp u streams strip s = u mod W of row j = u / W: stages s, s + W, ...; G = groups of the
+  // running bound (lanes mod G), a power of two >= K
   const int nunits = K * W;
-  if (warp < nunits) {
+  // x = logit + bias of vector jv of row j (elements outside the row read as -inf)
+  auto vec_x = [&](const RowGeo& g, uint4 dv, int jv, float (&x)[VEC]) {
+    unpack<DT>(dv, x);
+    const int base_b = jv * 16 - g.lead;
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
+      const int eb = base_b + e * ES;
+      if (eb < 0 || eb >= row_bytes) {
+        x[e] = -INFINITY;
+      } else if constexpr (BIAS) {
+        x[e] += __ldg(p.bias + eb / ES);
+      }
+    }
+  };
+  // max of saved vector (hv, jv) when lane < n, else -inf: the saved vectors are disjoint
+  // pieces of the strip, so the k-th largest of their maxima never exceeds its k-th largest
+  auto saved_max = [&](const RowGeo& g, int n, uint4 hv, int jv) -> float {
+    float m = -INFINITY;
+    if (lane < n) {
+      float x[VEC];
+      vec_x(g, hv, jv, x);
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) m = fmaxf(m, x[e]);
+    }
+    return m;
+  };
+  auto traverse = [&](auto gc) {
+    constexpr int G = decltype(gc)::value;
     const int u = warp, j = u / W, s = u - j * W;
     float ml = -INFINITY;  // lane's running max
     float cl = 0.0f;       // the lane's sum is sl = sum of 2^(x log2e + cl), cl = -ml log2e rounded
     float sl = 0.0f;
+    float Rw = -INFINITY;  // the strip's running R-top-k bound (warp-uniform)
+    if (lane == 0) {
+      sm.ucnt[u] = 0;
+      sm.uovf[u] = 0;
+      sm.hcnt[u] = 0;
+    }
+    __syncwarp();
+    const RowGeo g = geo(j);
     if (!sm.fin[j]) {
-      const RowGeo g = geo(j);
-      // two register buffers: the next stage's loads are in flight while a stage is worked on
-      // the strip's stages go through a ring of kFuRing stage buffers in shared memory,
-      // filled by 16-byte asynchronous copies (each lane copies, then reads, its own
-      // vectors: no barrier), kFuRing - 1 stages in flight while one is worked on
       const uint64_t pol = l2_evict_first_policy();
       auto issue = [&](int q, int slot) {
         if (q < g.ns) {
@@ -337,22 +374,23 @@ __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepPar
         }
         issue(q + (kFuRing - 1) * W, (i + kFuRing - 1) % kFuRing);
         mask_block(g, d, q, lane);
-        float xf[kPacked ? 1 : EL];
+        [[maybe_unused]] float xf[kPacked ? 1 : EL];
         if constexpr (!kPacked) block_x(g, d, q, lane, xf);
-        // the block max
+        // the block max, keeping each vector's (packed) max
         float lm;
+        [[maybe_unused]] uint32_t vm[kPacked ? VPL : 1];
         if constexpr (kPacked) {
-          uint32_t t = hmax2_bits<DT>(hmax2_bits<DT>(d[0].x, d[0].y), hmax2_bits<DT>(d[0].z, d[0].w));
 #pragma unroll
-          for (int r = 1; r < VPL; ++r)
-            t = hmax2_bits<DT>(t, hmax2_bits<DT>(hmax2_bits<DT>(d[r].x, d[r].y), hmax2_bits<DT>(d[r].z, d[r].w)));
+          for (int r = 0; r < VPL; ++r) vm[r] = hmax2_bits<DT>(hmax2_bits<DT>(d[r].x, d[r].y), hmax2_bits<DT>(d[r].z, d[r].w));
+          uint32_t t = vm[0];
+#pragma unroll
+          for (int r = 1; r < VPL; ++r) t = hmax2_bits<DT>(t, vm[r]);
           lm = hpair_max<DT>(t);
         } else {
           lm = xf[0];
 #pragma unroll
           for (int q2 = 1; q2 < EL; ++q2) lm = fmaxf(lm, xf[q2]);
         }
-        bmax[(u * SPS + i) * 32 + lane] = lm;
         // log_sum_exp: the lane's sum is kept as sum of 2^(x log2e + c) with c = -max log2e
         // rounded (one fused multiply-add per term); rescaled by 2^(c_new - c_old) when the
         // lane's max rises, and corrected for the rounding of c once, at the end of the strip
@@ -361,6 +399,62 @@ __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepPar
         sl = ml == -INFINITY ? 0.0f : sl * fast_exp2(cn - cl);
         cl = cn;
         ml = mn;
+        // the running bound: k-th largest of the G group maxima of the lanes' running maxima;
+        // on the first stage also the k-th largest of the 32 block maxima
+        float gmx;
+        Rw = fmaxf(Rw, strip_bound_g<G>(ml, K, gmx));
+        if (i == 0) Rw = fmaxf(Rw, kth_of_lanes(lm, 32, K));
+        const float thr = fmaxf(Rw, lowest_finite<DT>());  // -inf elements are never candidates
+        const bool hit = lm >= thr;
+        if (__any_sync(0xffffffffu, hit)) {
+          // a lane whose block reaches the bound saves the vectors that do
+          if (hit) {
+            [[maybe_unused]] uint32_t tb = 0;
+            if constexpr (kPacked) tb = hpack_thr<DT>(thr);
+#pragma unroll
+            for (int r = 0; r < VPL; ++r) {
+              bool has;
+              if constexpr (kPacked) {
+                has = hpair_any_ge<DT>(vm[r], tb);
+              } else {
+                has = false;
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) has |= xf[r * VEC + e] >= thr;
+              }
+              if (has) {
+                const int pos = atomicAdd(&sm.hcnt[u], 1);
+                if (pos < kFuVecs) {
+                  sm.hv[u][pos] = d[r];
+                  sm.hi[u][pos] = q * CV + lane + 32 * r;
+                } else {
+                  sm.uovf[u] = 1;  // a vector was lost: the batch takes the exact path
+                }
+              }
+            }
+          }
+          __syncwarp();
+          // many saved vectors: the bound rises to the k-th largest of their maxima and the
+          // vectors below it are dropped; all lanes read the same count after the barrier
+          const int n = min(sm.hcnt[u], kFuVecs);
+          if (n > kFuCompact) {
+            const uint4 hv = sm.hv[u][lane];
+            const int hiv = sm.hi[u][lane];
+            const float vmx = saved_max(g, n, hv, hiv);
+            Rw = fmaxf(Rw, kth_of_lanes(vmx, 32, K));
+            const bool keep = vmx >= fmaxf(Rw, lowest_finite<DT>());
+            const unsigned kb = __ballot_sync(0xffffffffu, keep);
+            __syncwarp();
+            if (keep) {
+              const int dst = __popc(kb & ((1u << lane) - 1u));
+              sm.hv[u][dst] = hv;
+              sm.hi[u][dst] = hiv;
+            }
+            __syncwarp();
+            if (lane == 0) sm.hcnt[u] = __popc(kb);
+            __syncwarp();
+          }
+        }
+        // the lse terms of the stage
         const float2 L2 = make_float2(kLog2e, kLog2e), c2 = make_float2(cn, cn);
         float2 a0 = make_float2(0.0f, 0.0f), a1 = make_float2(0.0f, 0.0f);
         auto term2 = [&](float2 x) {
@@ -405,103 +499,52 @@ __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepPar
     float S = (ml == -INFINITY) ? 0.0f : sl * fast_exp2(-fmaf(ml, kLog2e, cl) + (ml - M) * kLog2e);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
-
-    // the strip's bound: the k-th largest of its block maxima (each lane keeps the 8 largest
-    // of its own blocks, then k rounds of a warp max take them out in order)
-    const RowGeo g = geo(j);
-    const int nst = (!sm.fin[j] && s < g.ns) ? (g.ns - s + W - 1) / W : 0;
-    float t[8];
+    // the final bound: the k-th largest of the saved vectors' maxima (they hold every element
+    // at or above the running bound); their elements at or above it are the strip's
+    // candidates (lane h takes vector h)
+    const int n = min(sm.hcnt[u], kFuVecs);
+    const uint4 hv = sm.hv[u][lane];
+    const int jv = sm.hi[u][lane];
+    Rw = fmaxf(Rw, kth_of_lanes(saved_max(g, n, hv, jv), 32, K));
+    const float thr = fmaxf(Rw, lowest_finite<DT>());
+    if (lane < n) {
+      float x[VEC];
+      vec_x(g, hv, jv, x);
+      const int v0 = (jv * 16 - g.lead) / ES;  // token of element 0 (elements outside the row are -inf)
 #pragma unroll
-    for (int i = 0; i < 8; ++i) t[i] = -INFINITY;
-    for (int i = 0; i < nst; ++i) {
-      float v = bmax[(u * SPS + i) * 32 + lane];
-      if (v > t[7]) {
-#pragma unroll
-        for (int q2 = 0; q2 < 8; ++q2) {  // insert, keeping t descending
-          const float hi = fmaxf(t[q2], v);
-          v = fminf(t[q2], v);
-          t[q2] = hi;
-        }
-      }
-    }
-    float Rs = -INFINITY;
-    for (int r = 0; r < K; ++r) {
-      float m = t[0];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      const unsigned who = __ballot_sync(0xffffffffu, t[0] == m);
-      if (lane == __ffs(who) - 1) {
-#pragma unroll
-        for (int q2 = 0; q2 < 7; ++q2) t[q2] = t[q2 + 1];
-        t[7] = -INFINITY;
-      }
-      Rs = m;
-    }
-    // second traversal of the strip: its blocks whose max reaches the bound are read again,
-    // all at once (lane h takes hit h), and their elements x >= bound kept as candidates
-    const float thr = fmaxf(Rs, lowest_finite<DT>());  // -inf elements are never candidates
-    int nh = 0;
-    for (int i = 0; i < nst; ++i) {
-      const bool hit = bmax[(u * SPS + i) * 32 + lane] >= thr;
-      const unsigned hm = __ballot_sync(0xffffffffu, hit);
-      const int pos = nh + __popc(hm & ((1u << lane) - 1u));
-      if (hit && pos < kFuHits) sm.hits[u][pos] = i * 32 + lane;
-      nh += __popc(hm);
-    }
-    bool ovf = nh > kFuHits;
-    if (lane == 0) sm.ucnt[u] = 0;
-    __syncwarp();
-    for (int h0 = 0; h0 < nh && !ovf; h0 += 32) {
-      const int h = h0 + lane;
-      if (h < nh) {
-        const int i = sm.hits[u][h] >> 5, l = sm.hits[u][h] & 31;
-        const int q = s + i * W;
-        uint4 d[VPL];
-        load_block(g, d, q, l);
-        mask_block(g, d, q, l);
-        float xf[kPacked ? 1 : EL];
-        if constexpr (!kPacked) block_x(g, d, q, l, xf);
-#pragma unroll
-        for (int r = 0; r < VPL; ++r) {
-          uint32_t m;
-          if constexpr (kPacked) {
-            m = hvec_ge_mask<DT>(d[r], thr);
+      for (int e = 0; e < VEC; ++e) {
+        if (x[e] >= thr) {
+          const int pos = atomicAdd(&sm.ucnt[u], 1);
+          if (pos < kFuList) {
+            sm.cand[u][pos] = make_float2(x[e], __int_as_float(v0 + e));
           } else {
-            m = 0;
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) m |= (xf[r * VEC + e] >= thr ? 1u : 0u) << e;
-          }
-          while (m) {
-            const int e = __ffs(m) - 1;
-            m &= m - 1;
-            float x;
-            if constexpr (kPacked) {
-              x = vec_elem_f<DT>(d[r], e);
-            } else {
-              float tv = xf[r * VEC];
-#pragma unroll
-              for (int q2 = 1; q2 < VEC; ++q2) tv = q2 == e ? xf[r * VEC + q2] : tv;
-              x = tv;
-            }
-            const int v = ((q * CV + l + 32 * r) * 16 - g.lead) / ES + e;
-            const int pos = atomicAdd(&sm.ucnt[u], 1);
-            if (pos < kFuList) sm.cand[u][pos] = make_float2(x, __int_as_float(v));
+            sm.uovf[u] = 1;
           }
         }
       }
     }
-    __syncwarp();
     if (lane == 0) {
       sm.um[u] = M;
       sm.us[u] = S;
-      sm.ur[u] = Rs;
-      sm.uovf[u] = (ovf || sm.ucnt[u] > kFuList) ? 1 : 0;
+      sm.ur[u] = Rw;
+    }
+  };
+  if (warp < nunits) {
+    const int G = K <= 1 ? 1 : K <= 2 ? 2 : K <= 4 ? 4 : 8;
+    switch (G) {
+      case 1: traverse(std::integral_constant<int, 1>{}); break;
+      case 2: traverse(std::integral_constant<int, 2>{}); break;
+      case 4: traverse(std::integral_constant<int, 4>{}); break;
+      default: traverse(std::integral_constant<int, 8>{}); break;
     }
   }
   __syncthreads();
 
-  // ---------------------------------------------------------------- per row: lse and R
-  // R of a row = the largest of its strips' bounds (each is at most the row's k-th largest)
+  // ---------------------------------------------------------------- per row: lse, R, keys
+  // warp j merges row j's strips -- lse from their (max, sum), R = the largest of their
+  // bounds (each is at most the row's k-th largest) -- and appends the row's keys: the strips'
+  // candidates at or above R, rescored as beam_score + x - lse; a finished beam offers
+  // (eos_id, beam score), a beam with no finite score k tokens
   if (warp < K) {
     const int j = warp, u0 = j * W;
     const float mu = lane < W ? sm.um[u0 + lane] : -INFINITY;
@@ -515,58 +558,44 @@ __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepPar
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) Rr = fmaxf(Rr, __shfl_xor_sync(0xffffffffu, Rr, o));
     const bool ovf = __any_sync(0xffffffffu, lane < W && sm.uovf[u0 + lane] != 0);
+    const float beam = sm.beam[j];
+    const int kind = sm.fin[j] ? FROW_FIN : ((M == -INFINITY || beam == -INFINITY) ? FROW_DEAD : FROW_LIVE);
+    const float log_s = logf(S);
+    const ScoreBase c = kind == FROW_LIVE ? score_base(beam, M, log_s) : ScoreBase{0.0f, 0.0f};
     if (lane == 0) {
-      const float beam = sm.beam[j];
-      int kind = FROW_LIVE;
-      if (sm.fin[j]) {
-        kind = FROW_FIN;
-      } else if (M == -INFINITY || beam == -INFINITY) {
-        kind = FROW_DEAD;
-      }
-      const float log_s = logf(S);
       sm.kind[j] = kind;
       sm.R[j] = Rr;
-      sm.lse[j] = kind == FROW_FIN ? __int_as_float(0x7fc00000)
-                                   : (M == -INFINITY ? -INFINITY : (float)((double)M + (double)log_s));
-      sm.c[j] = kind == FROW_LIVE ? (double)beam - (double)M - (double)log_s : 0.0;
+      sm.lse[j] = kind == FROW_FIN ? __int_as_float(0x7fc00000) : (M == -INFINITY ? -INFINITY : __fadd_rn(M, log_s));
+      sm.c[j] = c;
       if (ovf && kind == FROW_LIVE) atomicMax(&sm.path, 1);
     }
-  }
-  __syncthreads();
-
-  // ---------------------------------------------------------------- rank keys
-  // every strip's candidates at or above its row's R, rescored: beam_score + x - lse
-  if (sm.path == 0) {
-    for (int i0 = 0; i0 < nunits * kFuList; i0 += kFuThreads) {
-      const int idx = i0 + tid;
-      const int u = idx / kFuList, i = idx - u * kFuList;
-      const int j = u < nunits ? u / W : 0;
-      bool take = false;
-      float2 en = make_float2(0.0f, 0.0f);
-      if (u < nunits && sm.kind[j] == FROW_LIVE && i < sm.ucnt[u]) {
-        en = sm.cand[u][i];
-        take = en.x >= sm.R[j];
+    int nc = 0;
+    if (kind == FROW_LIVE) {
+      if (!ovf) {
+        for (int t = 0; t < W; ++t) {
+          const int u = u0 + t;
+          const int n = min(sm.ucnt[u], kFuList);
+          float2 en = make_float2(0.0f, 0.0f);
+          if (lane < n) en = sm.cand[u][lane];
+          const bool take = lane < n && en.x >= Rr;
+          append_key(sm, take, make_key(score_of(c, en.x), j, en.x, __float_as_int(en.y)));
+          nc += __popc(__ballot_sync(0xffffffffu, take));
+        }
       }
-      append_key(sm, take, make_key((float)(sm.c[j] + (double)en.x), j, en.x, __float_as_int(en.y)));
-      if (take) atomicAdd(&sm.ncand[j], 1);
+    } else {
+      const bool take = kind == FROW_DEAD ? lane < K : lane == 0;
+      append_key(sm, take, kind == FROW_FIN ? make_key(beam, j, 0.0f, p.eos) : make_key(-INFINITY, j, 0.0f, lane));
+      nc = kind == FROW_FIN ? 1 : K;
     }
-  }
-  // finished beams offer (eos_id, beam score); beams with no finite score offer k tokens
-  if (sm.path == 0 && tid < K * K) {
-    const int jr = tid / K, v = tid - jr * K;
-    const int kind = sm.kind[jr];
-    if ((kind == FROW_FIN && v == 0) || kind == FROW_DEAD) {
-      const int pos = atomicAdd(&sm.nkeys, 1);
-      if (pos < kFuCap) sm.keys[pos] = kind == FROW_FIN ? make_key(sm.beam[jr], jr, 0.0f, p.eos) : make_key(-INFINITY, jr, 0.0f, v);
-      if (v == 0) sm.ncand[jr] = kind == FROW_FIN ? 1 : K;
-    }
+    if (lane == 0) sm.ncand[j] = nc;
   }
   __syncthreads();
-  if (tid == 0 && sm.path == 0 && sm.nkeys > kFuCap) sm.path = 3;
-  __syncthreads();
-  const int path = sm.path;
+  // any strip that lost a candidate, or more keys than the rank holds: the exact path
+  const int path = sm.path != 0 ? sm.path : (sm.nkeys > kFuCap ? 3 : 0);
   if (path != 0) {
-    // exact path: every live beam's top-K by radix select over its logits
+    // exact path: every live beam's top-K by radix select over its logits (the barrier first:
+    // every thread has read the key count that chose the path)
+    __syncthreads();
     if (tid == 0) sm.nkeys = 0;
     __syncthreads();
     for (int j = 0; j < K; ++j) {
@@ -596,14 +625,14 @@ __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepPar
 
 template <int DT, bool BIAS, int VPL>
 cudaError_t launch_t(const StepParams& p, cudaStream_t stream) {
-  PdlLaunch l(dim3((unsigned)p.batch), dim3(kFuThreads), beam_fused_smem_bytes(VPL, p.stages), stream);
+  PdlLaunch l(dim3((unsigned)p.batch), dim3(kFuThreads), beam_fused_smem_bytes(VPL), stream);
   return cudaLaunchKernelEx(&l.cfg, beam_fused_kernel<DT, BIAS, VPL>, p);
 }
 
 template <int DT, bool BIAS, int VPL>
 cudaError_t config_t() {
   return cudaFuncSetAttribute(beam_fused_kernel<DT, BIAS, VPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)beam_fused_smem_bytes(VPL, kFuMaxStages));
+                              (int)beam_fused_smem_bytes(VPL));
 }
 
 }  // namespace

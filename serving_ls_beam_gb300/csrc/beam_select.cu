@@ -23,7 +23,7 @@ namespace {
 enum { ROW_LIVE = 0, ROW_FIN = 1, ROW_DEAD = 2 };
 
 struct RowSel {
-  double c;  // beam_score - log_sum_exp
+  ScoreBase c;  // beam_score - log_sum_exp
   float rtopk;
   float lse;
   int kind;
@@ -246,7 +246,7 @@ __device__ void exact_select(const StepParams& p, SelSmem& sm, int b, int path) 
       if (!src(i, x, v)) continue;
       if (float_ord(x) > tkey) {
         const int pos = atomicAdd(&sm.nrl, 1);
-        if (pos < kMaxK) sm.rl[pos] = make_key((float)(rs.c + (double)x), j, x, v);
+        if (pos < kMaxK) sm.rl[pos] = make_key(score_of(rs.c, x), j, x, v);
       }
     }
     __syncthreads();
@@ -268,7 +268,7 @@ __device__ void exact_select(const StepParams& p, SelSmem& sm, int b, int path) 
       const int off = taken + before + __popc(ballot & ((1u << lane) - 1u));
       if (eq && off < need_eq) {
         const int pos = atomicAdd(&sm.nrl, 1);
-        if (pos < kMaxK) sm.rl[pos] = make_key((float)(rs.c + (double)x), j, x, v);
+        if (pos < kMaxK) sm.rl[pos] = make_key(score_of(rs.c, x), j, x, v);
       }
       taken += total;
       __syncthreads();
@@ -320,7 +320,7 @@ __device__ __forceinline__ int queue_select(const StepParams& p, SelSmem& sm, un
     if (sm.fin[j]) {
       if (lane == 0) {
         RowSel rs;
-        rs.c = 0.0;
+        rs.c = ScoreBase{0.0f, 0.0f};
         rs.rtopk = __int_as_float(0x7fc00000);
         rs.lse = __int_as_float(0x7fc00000);
         rs.kind = ROW_FIN;
@@ -409,13 +409,13 @@ __device__ __forceinline__ int queue_select(const StepParams& p, SelSmem& sm, un
         rs.ncand = 0;
         if (M == -INFINITY || beam == -INFINITY) {
           rs.kind = ROW_DEAD;
-          rs.c = -(double)INFINITY;
+          rs.c = ScoreBase{-INFINITY, 0.0f};
           rs.lse = M == -INFINITY ? -INFINITY : M + logf(S);
         } else {
           const float log_s = logf(S);
           rs.kind = ROW_LIVE;
-          rs.c = (double)beam - (double)M - (double)log_s;  // beam - lse, lse = M + log S
-          rs.lse = (float)((double)M + (double)log_s);
+          rs.c = score_base(beam, M, log_s);  // beam - lse, lse = M + log S
+          rs.lse = __fadd_rn(M, log_s);
         }
         sm.row[j] = rs;
         if (ovf) sm.ovf = 1;
@@ -508,7 +508,7 @@ __device__ __forceinline__ int queue_select(const StepParams& p, SelSmem& sm, un
         if (lane == 0) base = atomicAdd(&sm.nsel, __popc(m));
         base = __shfl_sync(0xffffffffu, base, 0);
         const int pos = base + __popc(m & lt_mask);
-        if (surv & (pos < kSelCap)) sm.sel[pos] = make_key((float)(rs.c + (double)x), jr, x, raw[t].y);
+        if (surv & (pos < kSelCap)) sm.sel[pos] = make_key(score_of(rs.c, x), jr, x, raw[t].y);
         // survivors per beam: the first lane of each beam's group adds the group's count
         const unsigned same = __match_any_sync(0xffffffffu, surv ? jr : -1);
         if (surv & ((same & lt_mask) == 0u)) atomicAdd(&sm.row[jr].ncand, __popc(same));
@@ -595,7 +595,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) beam_select_kernel(const StepP
     if (fin) {
       if (lane == 0) {
         RowSel rs;
-        rs.c = 0.0;
+        rs.c = ScoreBase{0.0f, 0.0f};
         rs.rtopk = __int_as_float(0x7fc00000);
         rs.lse = __int_as_float(0x7fc00000);
         rs.kind = ROW_FIN;
@@ -694,13 +694,13 @@ __global__ void __launch_bounds__(kSelThreads, 1) beam_select_kernel(const StepP
       rs.ncand = 0;
       if (M == -INFINITY || beam == -INFINITY) {
         rs.kind = ROW_DEAD;
-        rs.c = -(double)INFINITY;
+        rs.c = ScoreBase{-INFINITY, 0.0f};
         rs.lse = M == -INFINITY ? -INFINITY : M + logf(S);
       } else {
         const float log_s = logf(S);
         rs.kind = ROW_LIVE;
-        rs.c = (double)beam - (double)M - (double)log_s;  // beam - lse, lse = M + log S
-        rs.lse = (float)((double)M + (double)log_s);
+        rs.c = score_base(beam, M, log_s);  // beam - lse, lse = M + log S
+        rs.lse = __fadd_rn(M, log_s);
       }
       sm.row[j] = rs;
       if (ovf) sm.ovf = 1;
@@ -798,7 +798,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) beam_select_kernel(const StepP
           const float x = __int_as_float(raw[t].x);
           const RowSel& rs = sm.row[j];
           if (x >= rs.rtopk) {
-            const Key key = make_key((float)(rs.c + (double)x), j, x, raw[t].y);
+            const Key key = make_key(score_of(rs.c, x), j, x, raw[t].y);
             const int pos = atomicAdd(&sm.nsel, 1);
             if (pos < kSelCap)
               sm.sel[pos] = key;

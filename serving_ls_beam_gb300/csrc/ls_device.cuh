@@ -157,6 +157,38 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// The rescored candidate beam_score + x - lse in fp32 arithmetic only (FP64 runs at a small
+// fraction of the fp32 rate on this part): c = beam_score - lse is kept as an unevaluated pair
+// hi + lo of floats (error-free sums, Knuth's two-sum), and hi + x + lo is rounded once more,
+// so the score is within about one ulp of the exact value.
+struct ScoreBase {
+  float hi, lo;
+};
+__device__ __forceinline__ float2 two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  const float err = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+  return make_float2(s, err);
+}
+// beam_score - (M + log_s), the row's lse being M + log(S); -inf when either is -inf
+__device__ __forceinline__ ScoreBase score_base(float beam, float M, float log_s) {
+  const float2 a = two_sum(beam, -M);
+  const float2 b = two_sum(a.x, -log_s);
+  ScoreBase c;
+  c.hi = b.x;
+  c.lo = __fadd_rn(a.y, b.y);
+  if (!isfinite(c.hi)) {
+    c.hi = -INFINITY;
+    c.lo = 0.0f;
+  }
+  return c;
+}
+__device__ __forceinline__ float score_of(const ScoreBase& c, float x) {
+  const float2 t = two_sum(c.hi, x);
+  if (!isfinite(t.x)) return c.hi == -INFINITY ? -INFINITY : t.x;
+  return __fadd_rn(t.x, __fadd_rn(t.y, c.lo));
+}
+
 // q = n / d for n < 2^31 with a multiplier prepared on the host (Granlund & Montgomery,
 // "Division by invariant integers using multiplication", 1994, round-up variant).
 __device__ __forceinline__ uint32_t fast_div(uint32_t n, uint32_t magic, int shift) {

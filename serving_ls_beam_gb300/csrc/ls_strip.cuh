@@ -16,7 +16,8 @@ namespace lsb {
 template <int DT>
 __device__ __forceinline__ float lowest_finite() {
   if constexpr (DT == DT_F16) return -65504.0f;
-  return -3.4028234663852886e38f;  // f32 and bf16
+  if constexpr (DT == DT_BF16) return -3.3895313892515355e38f;  // 0xff7f: rounds to itself in bf16
+  return -3.4028234663852886e38f;
 }
 
 // Packed max of two 16-bit pairs (bit patterns).
@@ -65,6 +66,26 @@ __device__ __forceinline__ uint32_t hvec_ge_mask(const uint4& d, float t) {
     m |= ((g & 1u) | ((g >> 15) & 2u)) << (2 * i);
   }
   return m;
+}
+
+// The packed threshold t, t an element value of the type (so packed comparisons are exact).
+template <int DT>
+__device__ __forceinline__ uint32_t hpack_thr(float t) {
+  if constexpr (DT == DT_F16) {
+    const __half2 h = __float2half2_rn(t);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  } else {
+    const __nv_bfloat162 h = __float2bfloat162_rn(t);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+}
+// Either element of the 16-bit pair w is >= the packed threshold tb.
+template <int DT>
+__device__ __forceinline__ bool hpair_any_ge(uint32_t w, uint32_t tb) {
+  if constexpr (DT == DT_F16)
+    return __hge2_mask(*reinterpret_cast<const __half2*>(&w), *reinterpret_cast<const __half2*>(&tb)) != 0u;
+  else
+    return __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&w), *reinterpret_cast<const __nv_bfloat162*>(&tb)) != 0u;
 }
 
 // Element e (runtime index) of a 16-byte vector as float, without dynamic register indexing.
