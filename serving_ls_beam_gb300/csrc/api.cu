@@ -373,10 +373,14 @@ ls_status ls_beam_step(const void* logits, ls_dtype logit_dtype, const float* bi
 
   const int dtype = (int)logit_dtype;
   const long long rows = (long long)batch * k;
-  // K3 (the whole step of a batch in one CTA) when the batches fill the GPU by themselves
+  // K3 (the whole step of a batch in one CTA) when the batches fill the GPU by themselves and
+  // every strip's block maxima fit its shared memory
   int fu_parts = (kFuThreads / 32) / k;
   if (dbg.parts > 0 && dbg.parts * k <= kFuThreads / 32) fu_parts = dbg.parts;
+  const int fu_vpl = (dtype == LS_DTYPE_F32 || bias) ? 4 : 8;
+  const long long fu_ns = ((15 + (long long)vocab * es + 15) / 16 + 32ll * fu_vpl - 1) / (32ll * fu_vpl);
   const bool fused = !(dbg.flags & kFlagNoFused) && k <= kFuMaxK && fu_parts >= 1 &&
+                     (fu_ns + fu_parts - 1) / fu_parts <= kFuMaxStages &&
                      ((dbg.flags & kFlagFused) || 2ll * batch >= di->sms);
   if (fused) {
     if (!fused_configured(di)) return cuda_fail(cudaErrorUnknown);
@@ -398,7 +402,8 @@ ls_status ls_beam_step(const void* logits, ls_dtype logit_dtype, const float* bi
     p.vocab = vocab;
     p.eos = eos_id;
     p.rows = (int)rows;
-    p.nc = fu_parts;  // strips per row, one warp each
+    p.nc = fu_parts;                                       // strips per row, one warp each
+    p.stages = (int)((fu_ns + fu_parts - 1) / fu_parts);  // block-max rows per strip
     p.flags = dbg.flags;
     p.spin_limit_ns = dbg.spin_ns;
     const cudaError_t e = launch_beam_fused(p, dtype, static_cast<cudaStream_t>(stream));

@@ -12,25 +12,24 @@
 //  * One CTA per batch, kFuWarps warps.  The batch's k rows are cut into k * W strips; a warp
 //    streams its strip through a ring of kFuRing stages in shared memory, filled by 16-byte
 //    asynchronous copies (each lane copies, then reads, its own vectors: no barrier), with
-//    kFuRing - 1 stages in flight while one is worked on.
-//  * First traversal, per stage and in registers: a running (max, sum of exp(x - max)) per
-//    lane accumulates log_sum_exp.  The lanes' running maxima give the strip's R-top-k bound as
-//    the traversal goes (groups = lanes mod G, G the power of two >= k: the k-th largest group
-//    max, the least one when G = k); on the first stage the k-th largest of the lanes' block
-//    maxima tightens it.  The bound only rises, and at every point it is at most the strip's
-//    k-th largest element, so the elements of a stage at or above it (read from registers,
-//    only in lanes whose block max reaches it) hold every element of the row's top-k in the
-//    stage.  They go to the strip's short candidate list; when the list fills, entries below
-//    the current bound are dropped.  No logit is read twice.
-//  * Per row: lse from the strips' (max, sum); R = the largest of the strips' bounds.  The
-//    candidates at or above R are rescored (beam_score + x - lse) into 128-bit keys in shared
-//    memory and ranked (each key's rank counted against the others; the k of rank < k are the
-//    outputs).  Nothing goes through global memory between the traversals and the rank.
-//  * More than kFuList candidates in a strip's list, more than kFuCap keys, or the forced
-//    exact mode send the batch to an exact path: a radix select of every beam's top-k over its
-//    logits.
-#include <type_traits>
-
+//    kFuRing - 1 stages in flight while one is worked on.  Stages lying wholly inside the row
+//    (all but a row's first and last) skip the per-vector range tests and the masking.
+//  * First traversal, per stage and in registers: each lane's max of its 64-element block (its
+//    8 vectors of the stage) goes to shared memory and into the lane's sorted 8 largest, and
+//    a running (max, sum of exp(x - max)) per lane accumulates log_sum_exp.  The blocks
+//    partition the row, so the k-th largest block max of a strip is an R-top-k bound for it
+//    (groups = blocks: the article's "any split"); at the end of the strip k rounds of a warp
+//    max over the lanes' sorted lists give it.
+//  * Second traversal: only the blocks whose max reaches the strip's bound (a handful) are
+//    read again -- from L2, 128 bytes each -- for their elements x >= bound.  Per row, lse
+//    comes from the strips' (max, sum) and R is the largest of the strips' bounds; the
+//    candidates at or above R are rescored (beam_score + x - lse, in compensated fp32) into
+//    128-bit keys in shared memory and ranked (each key's rank counted against the others;
+//    the k of rank < k are the outputs).  Nothing else goes through global memory between
+//    the traversals and the rank.
+//  * More than kFuList candidates in a strip, more than kFuCap keys (ties), or the forced
+//    exact mode send the batch to an exact path: a radix select of every beam's top-k over
+//    its logits.
 #include "ls_device.cuh"
 #include "ls_dtype.cuh"
 #include "ls_internal.h"
@@ -44,21 +43,19 @@ constexpr int kFuCap = 512;  // keys the fine rank holds
 
 enum { FROW_LIVE = 0, FROW_FIN = 1, FROW_DEAD = 2 };
 
-// Dynamic shared memory: the per-warp rings of kFuRing stages; the rank keys reuse them once
-// the first traversal is done.
+// Dynamic shared memory: the per-warp rings of kFuRing stages (the rank keys reuse them once
+// the first traversal is done), then the block maxima, [strip][stage of the strip][lane].
 constexpr int kFuRing = 3;
-constexpr int kFuList = 32;     // candidates a strip keeps
-constexpr int kFuVecs = 32;     // 16-byte vectors a strip saves for its candidates
-constexpr int kFuCompact = 16;  // saved vectors past which those below the bound are dropped
+constexpr int kFuList = 32;  // candidates a strip keeps
+constexpr int kFuHits = 64;  // blocks a strip reads again
 
 struct __align__(16) FuSmem {
-  uint4 hv[kFuWarps][kFuVecs];      // saved vectors holding elements at or above the bound
-  int hi[kFuWarps][kFuVecs];        // their vector index in the row
   Key* keys;                        // kFuCap keys, over the rings
   float um[kFuWarps], us[kFuWarps];  // strip max and sum of exp(x - max)
-  float ur[kFuWarps];                // strip bound (running R-top-k at the end of the strip)
-  int ucnt[kFuWarps], uovf[kFuWarps], hcnt[kFuWarps];
+  float ur[kFuWarps];                // strip bound: k-th largest block max of the strip
+  int ucnt[kFuWarps], uovf[kFuWarps];
   float2 cand[kFuWarps][kFuList];    // the strip's candidates (x, token)
+  int hits[kFuWarps][kFuHits];       // the strip's blocks reaching its bound (stage * 32 + lane)
   ScoreBase c[kFuMaxK];  // beam_score - log_sum_exp of each live row
   float beam[kFuMaxK], lse[kFuMaxK], R[kFuMaxK];
   int fin[kFuMaxK], kind[kFuMaxK], ncand[kFuMaxK];
@@ -72,9 +69,9 @@ struct __align__(16) FuSmem {
 
 }  // namespace
 
-size_t beam_fused_smem_bytes(int vpl) {
+size_t beam_fused_smem_bytes(int vpl, int sps) {
   const size_t ring = (size_t)kFuWarps * kFuRing * 32 * vpl * 16;
-  return ring > kFuCap * sizeof(Key) ? ring : kFuCap * sizeof(Key);
+  return (ring > kFuCap * sizeof(Key) ? ring : kFuCap * sizeof(Key)) + (size_t)kFuWarps * sps * 32 * 4;
 }
 
 namespace {
@@ -212,7 +209,9 @@ __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepPar
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = blockIdx.x;
   const int K = p.k, V = p.vocab, W = p.nc;  // W strips per row, one warp per strip
+  const int SPS = p.stages;                  // block-max rows kept per strip
   unsigned char* ring = fu_dyn + (size_t)warp * kFuRing * CV * 16;
+  float* bmax = reinterpret_cast<float*>(fu_dyn + (size_t)kFuWarps * kFuRing * CV * 16);
   const int row_bytes = V * ES;
   const unsigned char* logits = static_cast<const unsigned char*>(p.logits);
 
@@ -302,57 +301,37 @@ __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepPar
   };
 
   // ---------------------------------------------------------------- first traversal
-  // warp u streams strip s = u mod W of row j = u / W: stages s, s + W, ...; G = groups of the
-  // running bound (lanes mod G), a power of two >= K
+  // warp u streams strip s = u mod W of row j = u / W: stages s, s + W, ...
   const int nunits = K * W;
-  // x = logit + bias of vector jv of row j (elements outside the row read as -inf)
-  auto vec_x = [&](const RowGeo& g, uint4 dv, int jv, float (&x)[VEC]) {
-    unpack<DT>(dv, x);
-    const int base_b = jv * 16 - g.lead;
-#pragma unroll
-    for (int e = 0; e < VEC; ++e) {
-      const int eb = base_b + e * ES;
-      if (eb < 0 || eb >= row_bytes) {
-        x[e] = -INFINITY;
-      } else if constexpr (BIAS) {
-        x[e] += __ldg(p.bias + eb / ES);
-      }
-    }
-  };
-  // max of saved vector (hv, jv) when lane < n, else -inf: the saved vectors are disjoint
-  // pieces of the strip, so the k-th largest of their maxima never exceeds its k-th largest
-  auto saved_max = [&](const RowGeo& g, int n, uint4 hv, int jv) -> float {
-    float m = -INFINITY;
-    if (lane < n) {
-      float x[VEC];
-      vec_x(g, hv, jv, x);
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) m = fmaxf(m, x[e]);
-    }
-    return m;
-  };
-  auto traverse = [&](auto gc) {
-    constexpr int G = decltype(gc)::value;
+  if (warp < nunits) {
     const int u = warp, j = u / W, s = u - j * W;
     float ml = -INFINITY;  // lane's running max
     float cl = 0.0f;       // the lane's sum is sl = sum of 2^(x log2e + cl), cl = -ml log2e rounded
     float sl = 0.0f;
-    float Rw = -INFINITY;  // the strip's running R-top-k bound (warp-uniform)
-    if (lane == 0) {
-      sm.ucnt[u] = 0;
-      sm.uovf[u] = 0;
-      sm.hcnt[u] = 0;
-    }
-    __syncwarp();
-    const RowGeo g = geo(j);
+    float t[8];  // the lane's 8 largest block maxima, descending (insertion as the stages stream)
+#pragma unroll
+    for (int i8 = 0; i8 < 8; ++i8) t[i8] = -INFINITY;
     if (!sm.fin[j]) {
+      const RowGeo g = geo(j);
+      // the strip's stages go through a ring of kFuRing stage buffers in shared memory,
+      // filled by 16-byte asynchronous copies (each lane copies, then reads, its own
+      // vectors: no barrier), kFuRing - 1 stages in flight while one is worked on.  A stage
+      // whose vectors all lie inside the row (every one but a row's first and last) takes
+      // the short path: no per-vector range test, no masking.
       const uint64_t pol = l2_evict_first_policy();
+      const int in_lo = (g.lead + CV * 16 - 1) / (CV * 16);     // first stage starting inside the row
+      const int in_hi = (g.lead + row_bytes) / (CV * 16) - 1;  // last stage ending inside the row
       auto issue = [&](int q, int slot) {
-        if (q < g.ns) {
+        unsigned char* dst = ring + (slot * VPL * 32 + lane) * 16;
+        const uint4* src = g.rb + q * CV + lane;
+        if (q >= in_lo && q <= in_hi) {
+#pragma unroll
+          for (int r = 0; r < VPL; ++r) cp_async16(smem_addr(dst + r * 512), src + 32 * r, pol);
+        } else if (q < g.ns) {
 #pragma unroll
           for (int r = 0; r < VPL; ++r) {
             const int jv = q * CV + lane + 32 * r;
-            if (jv < g.nv) cp_async16(smem_addr(ring + ((slot * VPL + r) * 32 + lane) * 16), g.rb + jv, pol);
+            if (jv < g.nv) cp_async16(smem_addr(dst + r * 512), src + 32 * r, pol);
           }
         }
         cp_async_commit();
@@ -361,35 +340,51 @@ __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepPar
       int q = s, i = 0;
 #pragma unroll
       for (int a = 0; a < kFuRing - 1; ++a) issue(q + a * W, a);
+      int slot = 0, islot = kFuRing - 1;  // the stage worked on, the stage being issued
 #pragma unroll 1
       for (; q < g.ns; q += W, ++i) {
         cp_async_wait<kFuRing - 2>();
-        const int slot = i % kFuRing;
+        const unsigned char* src = ring + (slot * VPL * 32 + lane) * 16;
+        const bool inner = q >= in_lo && q <= in_hi;
+        if (inner) {
 #pragma unroll
-        for (int r = 0; r < VPL; ++r) {
-          const int jv = q * CV + lane + 32 * r;
-          const uint32_t w = Traits<DT>::kNegInfWord;
-          d[r] = jv < g.nv ? *reinterpret_cast<const uint4*>(ring + ((slot * VPL + r) * 32 + lane) * 16)
-                           : make_uint4(w, w, w, w);
+          for (int r = 0; r < VPL; ++r) d[r] = *reinterpret_cast<const uint4*>(src + r * 512);
+        } else {
+#pragma unroll
+          for (int r = 0; r < VPL; ++r) {
+            const int jv = q * CV + lane + 32 * r;
+            const uint32_t w = Traits<DT>::kNegInfWord;
+            d[r] = jv < g.nv ? *reinterpret_cast<const uint4*>(src + r * 512) : make_uint4(w, w, w, w);
+          }
         }
-        issue(q + (kFuRing - 1) * W, (i + kFuRing - 1) % kFuRing);
-        mask_block(g, d, q, lane);
-        [[maybe_unused]] float xf[kPacked ? 1 : EL];
+        issue(q + (kFuRing - 1) * W, islot);
+        slot = slot == kFuRing - 1 ? 0 : slot + 1;
+        islot = islot == kFuRing - 1 ? 0 : islot + 1;
+        if (!inner) mask_block(g, d, q, lane);
+        float xf[kPacked ? 1 : EL];
         if constexpr (!kPacked) block_x(g, d, q, lane, xf);
-        // the block max, keeping each vector's (packed) max
+        // the block max
         float lm;
-        [[maybe_unused]] uint32_t vm[kPacked ? VPL : 1];
         if constexpr (kPacked) {
+          uint32_t t = hmax2_bits<DT>(hmax2_bits<DT>(d[0].x, d[0].y), hmax2_bits<DT>(d[0].z, d[0].w));
 #pragma unroll
-          for (int r = 0; r < VPL; ++r) vm[r] = hmax2_bits<DT>(hmax2_bits<DT>(d[r].x, d[r].y), hmax2_bits<DT>(d[r].z, d[r].w));
-          uint32_t t = vm[0];
-#pragma unroll
-          for (int r = 1; r < VPL; ++r) t = hmax2_bits<DT>(t, vm[r]);
+          for (int r = 1; r < VPL; ++r)
+            t = hmax2_bits<DT>(t, hmax2_bits<DT>(hmax2_bits<DT>(d[r].x, d[r].y), hmax2_bits<DT>(d[r].z, d[r].w)));
           lm = hpair_max<DT>(t);
         } else {
           lm = xf[0];
 #pragma unroll
           for (int q2 = 1; q2 < EL; ++q2) lm = fmaxf(lm, xf[q2]);
+        }
+        bmax[(u * SPS + i) * 32 + lane] = lm;
+        if (lm > t[7]) {
+          float v = lm;
+#pragma unroll
+          for (int q2 = 0; q2 < 8; ++q2) {  // insert, keeping t descending
+            const float hi = fmaxf(t[q2], v);
+            v = fminf(t[q2], v);
+            t[q2] = hi;
+          }
         }
         // log_sum_exp: the lane's sum is kept as sum of 2^(x log2e + c) with c = -max log2e
         // rounded (one fused multiply-add per term); rescaled by 2^(c_new - c_old) when the
@@ -399,62 +394,6 @@ __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepPar
         sl = ml == -INFINITY ? 0.0f : sl * fast_exp2(cn - cl);
         cl = cn;
         ml = mn;
-        // the running bound: k-th largest of the G group maxima of the lanes' running maxima;
-        // on the first stage also the k-th largest of the 32 block maxima
-        float gmx;
-        Rw = fmaxf(Rw, strip_bound_g<G>(ml, K, gmx));
-        if (i == 0) Rw = fmaxf(Rw, kth_of_lanes(lm, 32, K));
-        const float thr = fmaxf(Rw, lowest_finite<DT>());  // -inf elements are never candidates
-        const bool hit = lm >= thr;
-        if (__any_sync(0xffffffffu, hit)) {
-          // a lane whose block reaches the bound saves the vectors that do
-          if (hit) {
-            [[maybe_unused]] uint32_t tb = 0;
-            if constexpr (kPacked) tb = hpack_thr<DT>(thr);
-#pragma unroll
-            for (int r = 0; r < VPL; ++r) {
-              bool has;
-              if constexpr (kPacked) {
-                has = hpair_any_ge<DT>(vm[r], tb);
-              } else {
-                has = false;
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) has |= xf[r * VEC + e] >= thr;
-              }
-              if (has) {
-                const int pos = atomicAdd(&sm.hcnt[u], 1);
-                if (pos < kFuVecs) {
-                  sm.hv[u][pos] = d[r];
-                  sm.hi[u][pos] = q * CV + lane + 32 * r;
-                } else {
-                  sm.uovf[u] = 1;  // a vector was lost: the batch takes the exact path
-                }
-              }
-            }
-          }
-          __syncwarp();
-          // many saved vectors: the bound rises to the k-th largest of their maxima and the
-          // vectors below it are dropped; all lanes read the same count after the barrier
-          const int n = min(sm.hcnt[u], kFuVecs);
-          if (n > kFuCompact) {
-            const uint4 hv = sm.hv[u][lane];
-            const int hiv = sm.hi[u][lane];
-            const float vmx = saved_max(g, n, hv, hiv);
-            Rw = fmaxf(Rw, kth_of_lanes(vmx, 32, K));
-            const bool keep = vmx >= fmaxf(Rw, lowest_finite<DT>());
-            const unsigned kb = __ballot_sync(0xffffffffu, keep);
-            __syncwarp();
-            if (keep) {
-              const int dst = __popc(kb & ((1u << lane) - 1u));
-              sm.hv[u][dst] = hv;
-              sm.hi[u][dst] = hiv;
-            }
-            __syncwarp();
-            if (lane == 0) sm.hcnt[u] = __popc(kb);
-            __syncwarp();
-          }
-        }
-        // the lse terms of the stage
         const float2 L2 = make_float2(kLog2e, kLog2e), c2 = make_float2(cn, cn);
         float2 a0 = make_float2(0.0f, 0.0f), a1 = make_float2(0.0f, 0.0f);
         auto term2 = [&](float2 x) {
@@ -499,43 +438,83 @@ __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepPar
     float S = (ml == -INFINITY) ? 0.0f : sl * fast_exp2(-fmaf(ml, kLog2e, cl) + (ml - M) * kLog2e);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
-    // the final bound: the k-th largest of the saved vectors' maxima (they hold every element
-    // at or above the running bound); their elements at or above it are the strip's
-    // candidates (lane h takes vector h)
-    const int n = min(sm.hcnt[u], kFuVecs);
-    const uint4 hv = sm.hv[u][lane];
-    const int jv = sm.hi[u][lane];
-    Rw = fmaxf(Rw, kth_of_lanes(saved_max(g, n, hv, jv), 32, K));
-    const float thr = fmaxf(Rw, lowest_finite<DT>());
-    if (lane < n) {
-      float x[VEC];
-      vec_x(g, hv, jv, x);
-      const int v0 = (jv * 16 - g.lead) / ES;  // token of element 0 (elements outside the row are -inf)
+
+    // the strip's bound: the k-th largest of its block maxima (each lane has kept the 8
+    // largest of its own blocks; k rounds of a warp max take them out in order)
+    const RowGeo g = geo(j);
+    const int nst = (!sm.fin[j] && s < g.ns) ? (g.ns - s + W - 1) / W : 0;
+    float Rs = -INFINITY;
+    for (int r = 0; r < K; ++r) {
+      float m = t[0];
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        if (x[e] >= thr) {
-          const int pos = atomicAdd(&sm.ucnt[u], 1);
-          if (pos < kFuList) {
-            sm.cand[u][pos] = make_float2(x[e], __int_as_float(v0 + e));
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      const unsigned who = __ballot_sync(0xffffffffu, t[0] == m);
+      if (lane == __ffs(who) - 1) {
+#pragma unroll
+        for (int q2 = 0; q2 < 7; ++q2) t[q2] = t[q2 + 1];
+        t[7] = -INFINITY;
+      }
+      Rs = m;
+    }
+    // second traversal of the strip: its blocks whose max reaches the bound are read again,
+    // all at once (lane h takes hit h), and their elements x >= bound kept as candidates
+    const float thr = fmaxf(Rs, lowest_finite<DT>());  // -inf elements are never candidates
+    int nh = 0;
+    for (int i = 0; i < nst; ++i) {
+      const bool hit = bmax[(u * SPS + i) * 32 + lane] >= thr;
+      const unsigned hm = __ballot_sync(0xffffffffu, hit);
+      const int pos = nh + __popc(hm & ((1u << lane) - 1u));
+      if (hit && pos < kFuHits) sm.hits[u][pos] = i * 32 + lane;
+      nh += __popc(hm);
+    }
+    bool ovf = nh > kFuHits;
+    if (lane == 0) sm.ucnt[u] = 0;
+    __syncwarp();
+    for (int h0 = 0; h0 < nh && !ovf; h0 += 32) {
+      const int h = h0 + lane;
+      if (h < nh) {
+        const int i = sm.hits[u][h] >> 5, l = sm.hits[u][h] & 31;
+        const int q = s + i * W;
+        uint4 d[VPL];
+        load_block(g, d, q, l);
+        mask_block(g, d, q, l);
+        float xf[kPacked ? 1 : EL];
+        if constexpr (!kPacked) block_x(g, d, q, l, xf);
+#pragma unroll
+        for (int r = 0; r < VPL; ++r) {
+          uint32_t m;
+          if constexpr (kPacked) {
+            m = hvec_ge_mask<DT>(d[r], thr);
           } else {
-            sm.uovf[u] = 1;
+            m = 0;
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) m |= (xf[r * VEC + e] >= thr ? 1u : 0u) << e;
+          }
+          while (m) {
+            const int e = __ffs(m) - 1;
+            m &= m - 1;
+            float x;
+            if constexpr (kPacked) {
+              x = vec_elem_f<DT>(d[r], e);
+            } else {
+              float tv = xf[r * VEC];
+#pragma unroll
+              for (int q2 = 1; q2 < VEC; ++q2) tv = q2 == e ? xf[r * VEC + q2] : tv;
+              x = tv;
+            }
+            const int v = ((q * CV + l + 32 * r) * 16 - g.lead) / ES + e;
+            const int pos = atomicAdd(&sm.ucnt[u], 1);
+            if (pos < kFuList) sm.cand[u][pos] = make_float2(x, __int_as_float(v));
           }
         }
       }
     }
+    __syncwarp();
     if (lane == 0) {
       sm.um[u] = M;
       sm.us[u] = S;
-      sm.ur[u] = Rw;
-    }
-  };
-  if (warp < nunits) {
-    const int G = K <= 1 ? 1 : K <= 2 ? 2 : K <= 4 ? 4 : 8;
-    switch (G) {
-      case 1: traverse(std::integral_constant<int, 1>{}); break;
-      case 2: traverse(std::integral_constant<int, 2>{}); break;
-      case 4: traverse(std::integral_constant<int, 4>{}); break;
-      default: traverse(std::integral_constant<int, 8>{}); break;
+      sm.ur[u] = Rs;
+      sm.uovf[u] = (ovf || sm.ucnt[u] > kFuList) ? 1 : 0;
     }
   }
   __syncthreads();
@@ -625,14 +604,14 @@ __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepPar
 
 template <int DT, bool BIAS, int VPL>
 cudaError_t launch_t(const StepParams& p, cudaStream_t stream) {
-  PdlLaunch l(dim3((unsigned)p.batch), dim3(kFuThreads), beam_fused_smem_bytes(VPL), stream);
+  PdlLaunch l(dim3((unsigned)p.batch), dim3(kFuThreads), beam_fused_smem_bytes(VPL, p.stages), stream);
   return cudaLaunchKernelEx(&l.cfg, beam_fused_kernel<DT, BIAS, VPL>, p);
 }
 
 template <int DT, bool BIAS, int VPL>
 cudaError_t config_t() {
   return cudaFuncSetAttribute(beam_fused_kernel<DT, BIAS, VPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)beam_fused_smem_bytes(VPL));
+                              (int)beam_fused_smem_bytes(VPL, kFuMaxStages));
 }
 
 }  // namespace

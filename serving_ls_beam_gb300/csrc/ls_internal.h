@@ -30,9 +30,11 @@ constexpr int kStTighten = 24;   // candidates of one stage above which the boun
 constexpr int kStListOff = 512;  // per-warp mbarriers in [0, 512), then the per-warp lists
 constexpr int kStBarBytes = kStListOff + kStWarps * kStListCap * 8;  // start of the stage buffers
 // K3 (beam_fused.cu): one CTA of kFuThreads threads per batch, one warp per strip of a row
-// (k * strips per row <= warps), k <= kFuMaxK.
+// (k * strips per row <= warps), k <= kFuMaxK, at most kFuMaxStages stages per strip (their
+// block maxima are kept in shared memory).
 constexpr int kFuThreads = 256;
 constexpr int kFuMaxK = 8;
+constexpr int kFuMaxStages = 32;
 // K2 (beam_select.cu): one CTA per batch.
 constexpr int kSelThreads = 256;
 constexpr int kSelWarps = kSelThreads / 32;
@@ -273,7 +275,7 @@ size_t beam_rows_smem_bytes(int vpl);
 cudaError_t beam_rows_config(int dtype, bool bias, int vpl, int* occupancy);
 cudaError_t launch_beam_rows(const StepParams& p, int dtype, int vpl, int grid, cudaStream_t stream);
 cudaError_t launch_beam_select(const StepParams& p, int dtype, cudaStream_t stream);
-size_t beam_fused_smem_bytes(int vpl);
+size_t beam_fused_smem_bytes(int vpl, int sps);
 cudaError_t beam_fused_config();  // once per device: the kernels' dynamic shared memory
 cudaError_t launch_beam_fused(const StepParams& p, int dtype, cudaStream_t stream);
 size_t beam_strips_smem_bytes(int vpl, int stages);

@@ -117,6 +117,21 @@ __device__ __forceinline__ float kth_of_lanes(float v, int n, int k) {
   return __shfl_sync(0xffffffffu, v, __ffs(hit) - 1);
 }
 
+// k-th largest (1-based, k <= 32) of the 32 lanes' values by k rounds of a warp max, each
+// taking one lane's value out; all lanes get it.  Cheaper than kth_of_lanes for small k.
+__device__ __forceinline__ float kth_by_rounds(float v, int k) {
+  const int lane = threadIdx.x & 31;
+  float m = -INFINITY;
+  for (int r = 0; r < k; ++r) {
+    m = v;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const unsigned who = __ballot_sync(0xffffffffu, v == m);
+    if (lane == __ffs(who) - 1) v = -INFINITY;
+  }
+  return m;
+}
+
 // Max over the lanes congruent modulo G (offsets 16 .. G), then min over G consecutive
 // lanes (offsets G/2 .. 1): with G known at compile time only the needed shuffles run.
 template <int G>
