@@ -31,6 +31,8 @@ struct DeviceInfo {
   int strip_occ[3][2][kStMaxStages + 1] = {};
   int copy_occ[5] = {};
   int inplace_occ[5] = {};
+  int words_occ[10] = {};  // word kernel per [unit index][k <= 4 or <= 8]
+  long long words_parents[10] = {};  // the batch * k that occupancy was computed for
   int inplace_tma_occ = 0;
   size_t inplace_tma_smem = 0;
 };
@@ -47,11 +49,12 @@ struct Debug {
   int vpl = 0;     // 0 = plan's choice
   int stages = 0;  // K1s stage buffers per warp, 0 = plan's choice
   int parts = 0;   // K1s strips per row, 0 = plan's choice
+  int ipw = 0;     // in-place word kernel: words per item, 0 = plan's choice
   bool check_ptrs = true;
 };
 
-// LS_BEAM_DEBUG: comma-separated "exact", "ipplain", "chunk", "strips", "fused", "nofused",
-// "spin=<ns>", "vpl=<4|8|16>", "stages=<2..8>", "parts=<n>", "nocheck".
+// LS_BEAM_DEBUG: comma-separated "exact", "ipplain", "iptma", "ipwords", "chunk", "strips", "fused", "nofused",
+// "spin=<ns>", "vpl=<4|8|16>", "stages=<2..8>", "parts=<n>", "ipw=<words>", "nocheck".
 Debug read_debug() {
   Debug d;
   const char* env = std::getenv("LS_BEAM_DEBUG");
@@ -62,6 +65,8 @@ Debug read_debug() {
   for (char* tok = std::strtok(buf, ","); tok; tok = std::strtok(nullptr, ",")) {
     if (!std::strcmp(tok, "exact")) d.flags |= kFlagForceExact;
     else if (!std::strcmp(tok, "ipplain")) d.flags |= kFlagPlainInplace;
+    else if (!std::strcmp(tok, "iptma")) d.flags |= kFlagTmaInplace;
+    else if (!std::strcmp(tok, "ipwords")) d.flags |= kFlagWordInplace;
     else if (!std::strncmp(tok, "spin=", 5)) d.spin_ns = std::atoll(tok + 5);
     else if (!std::strcmp(tok, "chunk")) d.flags |= kFlagChunkRows;
     else if (!std::strcmp(tok, "strips")) d.flags &= ~kFlagChunkRows;
@@ -70,6 +75,7 @@ Debug read_debug() {
     else if (!std::strncmp(tok, "vpl=", 4)) d.vpl = std::atoi(tok + 4);
     else if (!std::strncmp(tok, "stages=", 7)) d.stages = std::atoi(tok + 7);
     else if (!std::strncmp(tok, "parts=", 6)) d.parts = std::atoi(tok + 6);
+    else if (!std::strncmp(tok, "ipw=", 4)) d.ipw = std::atoi(tok + 4);
     else if (!std::strcmp(tok, "nocheck")) d.check_ptrs = false;
   }
   if (d.spin_ns < 0) d.spin_ns = 0;
@@ -184,6 +190,22 @@ int inplace_occupancy(DeviceInfo* di, int unit) {
     int o = 0;
     if (cache_inplace_occupancy(unit, &o) != cudaSuccess || o < 1) return 0;
     occ = o;
+  }
+  return occ;
+}
+
+// occupancy of the word kernel for (unit, k <= 4 or <= 8), computed once per device
+int inplace_words_occupancy(DeviceInfo* di, int unit, int batch, int k) {
+  // the shared memory (the parents) varies with batch * k: looked up again when it grows
+  std::lock_guard<std::mutex> lk(g_mu);
+  const int slot = unit_index(unit) * 2 + (k <= 4 ? 0 : 1);
+  int& occ = di->words_occ[slot];
+  long long& parents = di->words_parents[slot];
+  if (occ == 0 || (long long)batch * k > parents) {
+    int o = 0;
+    if (cache_inplace_words_occupancy(unit, batch, k, &o) != cudaSuccess || o < 1) return 0;
+    occ = o;
+    parents = (long long)batch * k;
   }
   return occ;
 }
@@ -666,6 +688,33 @@ ls_status ls_cache_refresh_inplace(void* cache, ls_dtype dtype, const int32_t* p
   p.layers = layers;
   p.units = units;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // short slabs (< 1 KB: the first decode steps) and k <= 8: the word kernel (a warp per
+  // item, a lane per word position), about 256 words per item.  Measured at c5 against the
+  // bulk-copy kernel: 9-15 us against 18-19 us at len 1-4, even at len 8, 10% slower from
+  // len 16 on.  Without bulk copies (unaligned slabs) it serves every length.
+  const long long slab_words = slab_bytes / unit;
+  const bool words_fit = k <= kIpWordMaxK && (long long)heads * slab_words < (1ll << 31) &&
+                         (long long)batch * k <= kIpTmaMaxParents;
+  const bool tma_fit = unit == 16 && (long long)batch * k <= kIpTmaMaxParents;
+  const bool words = words_fit && !(dbg.flags & (kFlagPlainInplace | kFlagTmaInplace)) &&
+                     (slab_bytes < 1024 || !tma_fit || (dbg.flags & kFlagWordInplace));
+  if (words) {
+    long long wh = (dbg.ipw > 0 ? dbg.ipw : 256) / slab_words;
+    wh = wh < 1 ? 1 : (wh > heads ? heads : wh);
+    p.slab_words = slab_words;
+    p.word_heads = (int)wh;
+    make_divisor((uint32_t)slab_words, &p.word_magic, &p.word_shift);
+    p.word_items = (long long)layers * batch * ((heads + wh - 1) / wh);
+    p.tile_bytes = 0;
+    p.heads_per_item = 0;
+    const int wocc = inplace_words_occupancy(di, unit, batch, k);
+    if (wocc < 1) return cuda_fail(cudaErrorUnknown);
+    const long long warps_full = (long long)di->sms * wocc * (kIpWordThreads / 32);
+    const long long warps = p.word_items < warps_full ? p.word_items : warps_full;
+    const long long grid = (warps + kIpWordThreads / 32 - 1) / (kIpWordThreads / 32);
+    const cudaError_t e = launch_cache_inplace_words(p, unit, (int)grid, st);
+    return e == cudaSuccess ? LS_OK : cuda_fail(e);
+  }
   // bulk copies when every slab and tile is 16-byte aligned and the parents fit in shared memory
   const bool tma = unit == 16 && (long long)batch * k <= kIpTmaMaxParents && !(dbg.flags & kFlagPlainInplace);
   const int occ = tma ? inplace_tma_occupancy(di, batch, k) : inplace_occupancy(di, unit);

@@ -6,11 +6,15 @@
 // inference time.  The out-of-place refresh moves every row; here a row that continues
 // itself is not moved at all, and a parent is read once for all the beams that continue it.
 //
-// GB300 design: a persistent grid walks (layer, batch, head) units.  For a unit, the slabs
-// of the parents that changed rows need are staged in shared memory first (several
-// independent 16-byte loads per thread), then the changed rows are written from there, so
-// rows that are both read and overwritten (swaps, cycles) need no ordering and no global
-// temporary.  Slabs longer than the staging space are done a tile of positions at a time.
+// GB300 design, three kernels (the host picks one):
+//  * the bulk-copy kernel (aligned slabs, the long ones): one lane per CTA pipelines 1-D bulk
+//    copies of the needed parents' slabs into shared memory and of the changed rows out;
+//  * the word kernel (k <= 8, short slabs): a lane owns word positions and, per position,
+//    loads every needed parent's word before writing any changed row;
+//  * the staged CTA kernel (any shape): a persistent grid walks (layer, batch, head) units,
+//    staging the needed parents' slabs in shared memory before writing the changed rows.
+// In each, every row reads the state before the step, so swaps and cycles need no ordering
+// and no global temporary.
 #include "ls_device.cuh"
 #include "ls_dtype.cuh"
 #include "ls_internal.h"
@@ -249,6 +253,99 @@ __global__ void __launch_bounds__(32) cache_inplace_tma_kernel(const InplacePara
   if (bad && p.status) atomicOr(p.status, kDevBadParent);
 }
 
+// The same refresh by plain word copies, for k <= KT: a warp takes an item (heads
+// [h0, h0 + word_heads) of one (layer, batch)), and each lane owns a set of word positions in
+// it.  For a position, the lane first loads that word of every needed parent into registers,
+// then writes it to every changed row whose parent it is.  A word position belongs to one lane
+// in every row of the item, so rows that are both read and overwritten (swaps, cycles) need
+// no staging, no barrier and no ordering between lanes.  U positions are in flight per lane.
+template <int KT, int UNIT>
+__global__ void __launch_bounds__(kIpWordThreads) cache_inplace_words_kernel(const InplaceParams p) {
+  using Wd = typename IpWord<UNIT>::T;
+  constexpr int U = KT <= 4 ? 4 : 2;  // word positions per lane and round
+  const int K = p.k, lane = threadIdx.x & 31;
+  const long long warp0 = ((long long)blockIdx.x * kIpWordThreads + threadIdx.x) >> 5;
+  const long long nwarps = ((long long)gridDim.x * kIpWordThreads) >> 5;
+  extern __shared__ int wpar[];  // every batch's parents, [batch * k]
+  const int HG = p.word_heads;
+  const long long groups = (p.heads + HG - 1) / HG;
+  const long long bg = (long long)p.batch * groups;
+  grid_launch_dependents();
+  grid_dependency_wait();  // the parents come from the beam step just before
+  for (int i = threadIdx.x; i < p.batch * K; i += kIpWordThreads) wpar[i] = __ldg(p.parent + i);
+  __syncthreads();
+  bool bad = false;
+  for (long long item = warp0; item < p.word_items; item += nwarps) {
+    const int l = (int)(item / bg);
+    const long long rem = item - (long long)l * bg;
+    const int b = (int)(rem / groups);
+    const int h0 = (int)(rem - (long long)b * groups) * HG;
+    const int hg = min(HG, p.heads - h0);
+    // the batch's parents: which rows change (changed) and, per parent q, the rows it feeds
+    const int myq = lane < K ? wpar[b * K + lane] : lane;
+    unsigned tgt[KT];
+#pragma unroll
+    for (int q = 0; q < KT; ++q) tgt[q] = 0u;
+    unsigned changed = 0u;
+#pragma unroll
+    for (int j = 0; j < KT; ++j) {
+      const int q = __shfl_sync(0xffffffffu, myq, j);
+      if (j < K) {
+        if (q < 0 || q >= K) {
+          bad = true;  // that row is left as it is
+        } else if (q != j) {
+          changed |= 1u << j;
+#pragma unroll
+          for (int qq = 0; qq < KT; ++qq) tgt[qq] |= (qq == q ? 1u : 0u) << j;
+        }
+      }
+    }
+    if (changed == 0u) continue;  // warp-uniform: nothing moves in this item
+    unsigned char* base = p.cache + (size_t)l * p.layer_stride + (size_t)b * K * p.row_stride +
+                          (size_t)h0 * p.slab_stride;
+    const uint32_t nw = (uint32_t)(hg * p.slab_words);
+    for (uint32_t w0 = lane; w0 < nw; w0 += 32 * U) {
+      Wd v[U][KT];
+      size_t off[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const uint32_t w = w0 + 32u * u;
+        const uint32_t h = fast_div(w, p.word_magic, p.word_shift);
+        const uint32_t e = w - h * (uint32_t)p.slab_words;
+        off[u] = (size_t)h * p.slab_stride + (size_t)e * UNIT;
+        if (w < nw) {
+#pragma unroll
+          for (int q = 0; q < KT; ++q)
+            if (tgt[q]) v[u][q] = *reinterpret_cast<const Wd*>(base + (size_t)q * p.row_stride + off[u]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (w0 + 32u * u < nw) {
+#pragma unroll
+          for (int q = 0; q < KT; ++q) {
+            unsigned m = tgt[q];
+            while (m) {
+              const int j = __ffs(m) - 1;
+              m &= m - 1u;
+              *reinterpret_cast<Wd*>(base + (size_t)j * p.row_stride + off[u]) = v[u][q];
+            }
+          }
+        }
+      }
+    }
+  }
+  if (bad && lane == 0 && p.status) atomicOr(p.status, kDevBadParent);
+}
+
+size_t words_smem(int batch, int k) { return align_up((size_t)batch * k * sizeof(int32_t), 16); }
+
+template <int KT, int UNIT>
+cudaError_t launch_w(const InplaceParams& p, int grid, cudaStream_t stream) {
+  PdlLaunch l(dim3((unsigned)grid), dim3(kIpWordThreads), words_smem(p.batch, p.k), stream);
+  return cudaLaunchKernelEx(&l.cfg, cache_inplace_words_kernel<KT, UNIT>, p);
+}
+
 template <int UNIT>
 cudaError_t launch_u(const InplaceParams& p, int grid, size_t smem, cudaStream_t stream) {
   PdlLaunch l(dim3((unsigned)grid), dim3(kIpThreads), smem, stream);
@@ -289,6 +386,40 @@ cudaError_t launch_cache_inplace(const InplaceParams& p, int unit, int grid, cud
     case 4: return launch_u<4>(p, grid, smem, stream);
     case 2: return launch_u<2>(p, grid, smem, stream);
     case 1: return launch_u<1>(p, grid, smem, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_cache_inplace_words(const InplaceParams& p, int unit, int grid, cudaStream_t stream) {
+  const bool k4 = p.k <= 4;
+  switch (unit) {
+    case 16: return k4 ? launch_w<4, 16>(p, grid, stream) : launch_w<8, 16>(p, grid, stream);
+    case 8: return k4 ? launch_w<4, 8>(p, grid, stream) : launch_w<8, 8>(p, grid, stream);
+    case 4: return k4 ? launch_w<4, 4>(p, grid, stream) : launch_w<8, 4>(p, grid, stream);
+    case 2: return k4 ? launch_w<4, 2>(p, grid, stream) : launch_w<8, 2>(p, grid, stream);
+    case 1: return k4 ? launch_w<4, 1>(p, grid, stream) : launch_w<8, 1>(p, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int KT, int UNIT>
+cudaError_t occ_w(int batch, int k, int* occ) {
+  const size_t smem = words_smem(batch, k);
+  cudaError_t e = cudaFuncSetAttribute(cache_inplace_words_kernel<KT, UNIT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, cache_inplace_words_kernel<KT, UNIT>, kIpWordThreads,
+                                                       smem);
+}
+
+cudaError_t cache_inplace_words_occupancy(int unit, int batch, int k, int* occ) {
+  const bool k4 = k <= 4;
+  switch (unit) {
+    case 16: return k4 ? occ_w<4, 16>(batch, k, occ) : occ_w<8, 16>(batch, k, occ);
+    case 8: return k4 ? occ_w<4, 8>(batch, k, occ) : occ_w<8, 8>(batch, k, occ);
+    case 4: return k4 ? occ_w<4, 4>(batch, k, occ) : occ_w<8, 4>(batch, k, occ);
+    case 2: return k4 ? occ_w<4, 2>(batch, k, occ) : occ_w<8, 2>(batch, k, occ);
+    case 1: return k4 ? occ_w<4, 1>(batch, k, occ) : occ_w<8, 1>(batch, k, occ);
     default: return cudaErrorInvalidValue;
   }
 }

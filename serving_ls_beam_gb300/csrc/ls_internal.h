@@ -65,7 +65,9 @@ constexpr uint32_t kDevInternal = 1u << 2;
 
 // Debug flags (LS_BEAM_DEBUG).
 constexpr int kFlagForceExact = 1;
-constexpr int kFlagPlainInplace = 2;  // the in-place refresh without bulk copies
+constexpr int kFlagPlainInplace = 2;  // the in-place refresh by the staged CTA kernel
+constexpr int kFlagTmaInplace = 32;   // the in-place refresh by bulk copies
+constexpr int kFlagWordInplace = 64;  // the in-place refresh by the word kernel (k <= 8)
 constexpr int kFlagChunkRows = 4;     // the beam step's first kernel by fixed-size chunks (K1)
 constexpr int kFlagNoFused = 8;       // the beam step as two kernels even where K3 applies
 constexpr int kFlagFused = 16;        // the beam step as K3 wherever k allows
@@ -244,6 +246,13 @@ struct InplaceParams {
   int heads_per_item;     // bulk-copy kernel: heads of one (layer, batch) moved together
   int batch, k, heads, layers;
   long long units;        // layers * batch * heads
+  // word kernel: an item is heads [h0, h0 + word_heads) of one (layer, batch); its words are
+  // word_heads * slab_words, divided by slab_words with (word_magic, word_shift)
+  long long slab_words;   // slab_bytes / word size
+  int word_heads;
+  uint32_t word_magic;
+  int word_shift;
+  long long word_items;   // layers * batch * ceil(heads / word_heads)
 };
 
 // Launch configuration with programmatic dependent launch: the kernel may be scheduled
@@ -295,6 +304,12 @@ cudaError_t launch_backtrack(const BacktrackParams& p, cudaStream_t stream);
 cudaError_t launch_sample_select(const SampleParams& p, int dtype, cudaStream_t stream);
 cudaError_t launch_cache_inplace(const InplaceParams& p, int unit, int grid, cudaStream_t stream);
 cudaError_t cache_inplace_occupancy(int unit, int* occupancy);
+// word kernel (k <= kIpWordMaxK): a warp per item, each lane owning word positions
+constexpr int kIpWordMaxK = 8;
+constexpr int kIpWordThreads = 256;
+cudaError_t launch_cache_inplace_words(const InplaceParams& p, int unit, int grid, cudaStream_t stream);
+// every batch's parents are staged in shared memory: batch * k <= kIpTmaMaxParents
+cudaError_t cache_inplace_words_occupancy(int unit, int batch, int k, int* occupancy);
 size_t cache_inplace_tma_smem(int batch, int k);
 cudaError_t launch_cache_inplace_tma(const InplaceParams& p, int grid, cudaStream_t stream);
 cudaError_t cache_inplace_tma_occupancy(int batch, int k, int* occupancy);

@@ -2,7 +2,8 @@
 oracle, bitwise: parent patterns that make in-place writing hazardous (swaps, cycles, one
 parent for all), every element width, odd head sizes, k up to 64 (slabs staged in several
 tiles), len < max_len, a bad parent reported through the workspace, and a c5 decode loop
-refreshed in place against the oracle's trajectory."""
+refreshed in place against the oracle's trajectory.  The cases run under each implementation:
+the plan's choice, the word kernel, bulk copies and the staged CTA kernel."""
 import numpy as np
 import pytest
 
@@ -61,7 +62,15 @@ CASES = [  # (dtype, layers, batch, k, heads, max_len, len, head_dim)
     ("f32", 2, 3, 5, 1, 10, 1, 16),
     ("f16", 1, 3, 4, 16, 64, 20, 64),  # short slabs: 3 heads per item, a last group of 1
     ("f16", 2, 5, 4, 7, 64, 3, 64),    # all 7 heads in one item
+    ("f16", 2, 6, 4, 16, 64, 6, 64),   # word kernel: 48 words a slab, items of 5 heads (5, 5, 5, 1)
+    ("bf16", 1, 9, 8, 3, 32, 32, 64),  # word kernel, k = 8, 1 head per item
+    ("f16", 1, 5, 2, 4, 16, 1, 8),     # one 16-byte word per slab
 ]
+
+# LS_BEAM_DEBUG settings of the implementations: the plan's choice (the word kernel for short
+# slabs and k <= 8, bulk copies otherwise), the word kernel, bulk copies and the staged CTA
+# kernel forced
+IMPLS = [None, "ipwords", "iptma", "ipplain"]
 
 
 def _with_env(env, fn):
@@ -80,7 +89,7 @@ def _with_env(env, fn):
                 os.environ["LS_BEAM_DEBUG"] = old
 
 
-@pytest.mark.parametrize("env", [None, "ipplain"])  # bulk copies where aligned; the plain kernel
+@pytest.mark.parametrize("env", IMPLS)
 @pytest.mark.parametrize("case", CASES)
 def test_inplace_matches_oracle(dev, oracle_mod, case, env):
     dtype, layers, batch, k, heads, max_len, length, head_dim = case
@@ -97,7 +106,7 @@ def test_inplace_matches_oracle(dev, oracle_mod, case, env):
     assert np.array_equal(got, exp)
 
 
-@pytest.mark.parametrize("env", [None, "ipplain"])
+@pytest.mark.parametrize("env", IMPLS)
 def test_bad_parent_leaves_the_row_and_is_reported(dev, oracle_mod, env):
     g = np.random.default_rng(3)
     shape = (1, 8, 2, 4, 16)
@@ -171,7 +180,7 @@ def test_bulk_copy_wait_timeout_is_reported(dev, oracle_mod):
     parent = torch.from_numpy(_parents(g, batch, k)).to(dev)
     ws = torch.zeros(lsb.ls_beam_step_workspace_size(1, 1, 1), dtype=torch.uint8, device=dev)
     t = _to_dev(cache, dtype, dev)
-    _with_env("spin=0", lambda: lsb.check(lsb.ls_cache_refresh_inplace(t, parent, length, ws)))
+    _with_env("spin=0,iptma", lambda: lsb.check(lsb.ls_cache_refresh_inplace(t, parent, length, ws)))
     assert lsb.ls_read_status(ws) == lsb.LS_ERR_TIMEOUT
     lsb.check(lsb.ls_workspace_init(ws))
     t = _to_dev(cache, dtype, dev)
