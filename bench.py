@@ -572,12 +572,62 @@ def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
         lsb.check(lsb.ls_read_status(lp.workspace, stream), "device status")
         return ms, k1 / reps, k4 / reps, bt / reps
 
+    def time_alone(lp):
+        """us per launch of the beam step and of the cache refresh, each timed in a graph of the
+        search's launches of that kernel alone (chained with programmatic dependent launch, no
+        events between them; the refreshes use the parents the loop recorded)."""
+        def beams():
+            lp.reset(beam0, fin0)
+            for t in range(T):
+                s, n = lp.cur, 1 - lp.cur
+                lsb.check(lsb.ls_beam_step(d_logits[t], d_bias, lp.scores[s], lp.finished[s], wr.eos_id,
+                                           lp.token_out(t + 1), lp.parent_out(t + 1), lp.scores[n], lp.finished[n],
+                                           lp.workspace), "ls_beam_step")
+                lp.cur = n
+
+        def refreshes():
+            for t in range(T):
+                par = lp.parent_out(t + 1)
+                if lp.inplace:
+                    lsb.check(lsb.ls_cache_refresh_inplace(lp.cache[0], par, lens(t + 1), lp.workspace),
+                              "ls_cache_refresh_inplace")
+                else:
+                    lsb.check(lsb.ls_cache_reorder(lp.cache[t % 2], lp.cache[1 - t % 2], par, lens(t + 1)),
+                              "ls_cache_reorder")
+
+        out = {}
+        for name, fn in (("beam_step", beams), ("refresh", refreshes)):
+            if name == "refresh" and lp.cache is None:
+                continue
+            with torch.cuda.stream(stream):
+                fn()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+            torch.cuda.synchronize()
+            ts = []
+            with torch.cuda.stream(stream):
+                for r in range(4):
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record()
+                    g.replay()
+                    b.record()
+                    torch.cuda.synchronize()
+                    if r > 0:
+                        ts.append(a.elapsed_time(b) * 1e3 / T)
+            del g
+            out[name] = statistics.median(ts)
+        lsb.check(lsb.ls_read_status(lp.workspace, stream), "device status")
+        return out
+
     # kernels per decode step: the beam step (K3 alone, or K1 + K2) and the cache refresh; plus the backtrack
     launches_per_step = T * (beam_step_kernels(wr, dev) + (1 if loop.cache is not None else 0)) + 1
     g_plain, g_inst = capture(loop)
     with ClockSampler(local) as clk:
         ms_plain, k1_ms, k4_ms, bt_ms = time_graphs(loop, g_plain, g_inst)
         parents_run = loop.parent_hist.cpu().numpy() if loop.cache is not None else None
+        alone = time_alone(loop)
         oop = None
         if loop_oop is not None:
             del g_plain, g_inst
@@ -605,10 +655,15 @@ def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
             k4_dense_bytes += 2 * wr.rows * slab
     peak, peak_src = hbm_peak()
     k1_gbs = k1_bytes / (k1_ms / 1e3) / 1e9
+    def alone_fields(us, nbytes):
+        gbs = nbytes / (us * 1e-6) / 1e9
+        return {"us_per_launch_alone": us, "achieved_alone": gbs, "frac_alone": gbs / peak}
+
     kern = {"beam_step": {"bound": "hbm", "achieved": k1_gbs, "peak": peak, "unit": "GB/s", "frac": k1_gbs / peak,
                           "traffic": recorded_traffic("beam_step", wr.name),
                           "us_per_launch": k1_ms * 1e3 / T,
-                          "algorithmic_bytes_per_launch": k1_bytes / T}}
+                          "algorithmic_bytes_per_launch": k1_bytes / T,
+                          **alone_fields(alone["beam_step"], k1_bytes / T)}}
     oop_line = None
     if loop.cache is not None:
         k4_gbs = k4_bytes / (k4_ms / 1e3) / 1e9
@@ -617,7 +672,8 @@ def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
             "traffic": recorded_traffic("cache_refresh_inplace", wr.name), "us_per_launch": k4_ms * 1e3 / T,
             "algorithmic_bytes_per_launch": k4_bytes / T,
             "note": "copy on change: bytes of the parents read and the beams written, from the run's parents; "
-                    f"{k4_dense_bytes / T:.0f} B per launch if every row were moved"}
+                    f"{k4_dense_bytes / T:.0f} B per launch if every row were moved",
+            **alone_fields(alone["refresh"], k4_bytes / T)}
         if oop is not None:
             o_ms, o_k1, o_k4, o_bt = oop
             o_ms = max_over_ranks(o_ms, world, dev)
@@ -670,10 +726,11 @@ def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
         "dtype": wr.dtype, "data": "synthetic (seeded generators, workload recipe in synth/)", "config": cfg,
         "logit_gbs": k1_gbs, "step_gbs": step_gbs, "step_roofline_frac": step_gbs / peak,
         "roofline": roof, "roofline_kernels": kern,
-        "roofline_kernels_note": "per-kernel times come from a second, event-instrumented graph of the same "
-                                 "search (its events sit between the kernels, so each kernel's time includes a "
-                                 "little launch gap and its frac reads slightly low); value comes from the plain "
-                                 "graph",
+        "roofline_kernels_note": "us_per_launch and frac: a second, event-instrumented graph of the same search "
+                                 "(an event between every two kernels, so each kernel's time includes a launch "
+                                 "gap and its frac reads low); us_per_launch_alone and frac_alone: a graph of the "
+                                 "search's launches of that kernel alone, chained with programmatic dependent "
+                                 "launch, events only around the graph; value comes from the plain graph",
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks, "e2e": e2e, "sampling": sampling, "projection_step": projection,
         "cache_refresh_out_of_place": oop_line,
