@@ -168,6 +168,28 @@ LS_API ls_status ls_cache_refresh_inplace(void* cache, ls_dtype dtype, const int
                                           void* workspace, void* stream);
 
 /*
+ * One beam-search step followed by the in-place cache refresh by its parents (article:
+ * hierarchical decoding, then "update the cache"): the result equals ls_beam_step and then
+ * ls_cache_refresh_inplace(cache, ..., out_parent, ...) on the same stream.  The arguments
+ * are those of the two calls; out_parent is required.
+ *
+ * By default the two run as two launches.  With LS_BEAM_DEBUG=steprefresh, where the step
+ * of each batch runs in one CTA (k <= 8 and batch large enough to fill the GPU), that CTA
+ * refreshes its own batch's rows as soon as it has ranked them, so the refresh of early
+ * batches overlaps the step of the others.  On c5 that form measured slower (7.49 against
+ * 6.83 ms per 64-step search: the per-batch refresh inherits the step's two batches per
+ * SM, while the standalone refresh spreads over every SM).  A bounded wait of that refresh
+ * that runs out sets LS_ERR_TIMEOUT in the workspace's status word (read with
+ * ls_read_status).  The cache must not overlap any other argument.  Nothing is allocated.
+ */
+LS_API ls_status ls_beam_step_refresh_inplace(const void* logits, ls_dtype logit_dtype, const float* bias,
+                                              const float* beam_scores, const uint8_t* finished, int batch, int k,
+                                              int vocab, int eos_id, int32_t* out_token, int32_t* out_parent,
+                                              float* out_score, uint8_t* out_finished, void* cache,
+                                              ls_dtype cache_dtype, int layers, int heads, int max_len, int len,
+                                              int head_dim, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Workspace bytes for ls_sample on `rows` rows of `vocab` logits keeping top_k candidates
  * (0 for unsupported shapes: top_k outside [1, LS_MAX_K] or above vocab).
  */

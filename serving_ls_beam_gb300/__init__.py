@@ -21,6 +21,7 @@ __all__ = [
     "ls_read_status", "ls_status_string", "ls_read_row_stats", "ls_beam_step_noalloc", "ls_beam_step_noalloc_status",
     "ls_backtrack",
     "ls_sample_workspace_size", "ls_sample", "ls_cache_refresh_inplace", "ls_logits_beam_step",
+    "ls_beam_step_refresh_inplace",
 ]
 
 LS_OK, LS_ERR_INVALID_ARG, LS_ERR_UNSUPPORTED, LS_ERR_CUDA, LS_ERR_TIMEOUT, LS_ERR_INTERNAL = range(6)
@@ -79,6 +80,9 @@ def load_library():
         lib.ls_cache_refresh_inplace.restype = ip
         lib.ls_logits_beam_step.argtypes = [vp, vp, ip, ip, vp, vp, vp, ip, ip, ip, ip, vp, vp, vp, vp, vp, sz, vp]
         lib.ls_logits_beam_step.restype = ip
+        lib.ls_beam_step_refresh_inplace.argtypes = [vp, ip, vp, vp, vp, ip, ip, ip, ip, vp, vp, vp, vp, vp, ip, ip,
+                                                     ip, ip, ip, ip, vp, sz, vp]
+        lib.ls_beam_step_refresh_inplace.restype = ip
         _lib = lib
         return lib
 
@@ -137,6 +141,21 @@ def ls_beam_step(logits, bias, beam_scores, finished, eos_id: int, out_token, ou
     return load_library().ls_beam_step(
         _ptr(logits), _dtype_code(logits), _ptr(bias), _ptr(beam_scores), _ptr(finished), batch, k, vocab,
         int(eos_id), _ptr(out_token), _ptr(out_parent), _ptr(out_score), _ptr(out_finished), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+
+
+def ls_beam_step_refresh_inplace(logits, bias, beam_scores, finished, eos_id: int, out_token, out_parent, out_score,
+                                 out_finished, cache, length: int, workspace, stream=None) -> int:
+    """ls_beam_step, then the in-place refresh of cache [layers, batch*k, heads, max_len, head_dim] by
+    out_parent over positions [0, length); one kernel where the step runs a batch per CTA."""
+    batch, k, vocab = logits.shape
+    layers, rows, heads, max_len, head_dim = cache.shape
+    if rows != batch * k:
+        raise ValueError("cache rows do not match batch * k")
+    return load_library().ls_beam_step_refresh_inplace(
+        _ptr(logits), _dtype_code(logits), _ptr(bias), _ptr(beam_scores), _ptr(finished), batch, k, vocab,
+        int(eos_id), _ptr(out_token), _ptr(out_parent), _ptr(out_score), _ptr(out_finished), _ptr(cache),
+        _dtype_code(cache), layers, heads, max_len, int(length), head_dim, _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream))
 
 

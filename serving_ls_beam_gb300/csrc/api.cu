@@ -50,11 +50,12 @@ struct Debug {
   int stages = 0;  // K1s stage buffers per warp, 0 = plan's choice
   int parts = 0;   // K1s strips per row, 0 = plan's choice
   int ipw = 0;     // in-place word kernel: words per item, 0 = plan's choice
+  int stage = -1;  // K2 after K0: 1 = stage the batch's slots, 0 = read them in place, -1 = plan
   bool check_ptrs = true;
 };
 
-// LS_BEAM_DEBUG: comma-separated "exact", "ipplain", "iptma", "ipwords", "chunk", "strips", "fused", "nofused",
-// "spin=<ns>", "vpl=<4|8|16>", "stages=<2..8>", "parts=<n>", "ipw=<words>", "nocheck".
+// LS_BEAM_DEBUG: comma-separated "exact", "ipplain", "iptma", "ipwords", "steprefresh", "chunk", "strips", "fused", "nofused",
+// "spin=<ns>", "vpl=<4|8|16>", "stages=<2..8>", "parts=<n>", "ipw=<words>", "stage=<0|1>", "nocheck".
 Debug read_debug() {
   Debug d;
   const char* env = std::getenv("LS_BEAM_DEBUG");
@@ -67,6 +68,7 @@ Debug read_debug() {
     else if (!std::strcmp(tok, "ipplain")) d.flags |= kFlagPlainInplace;
     else if (!std::strcmp(tok, "iptma")) d.flags |= kFlagTmaInplace;
     else if (!std::strcmp(tok, "ipwords")) d.flags |= kFlagWordInplace;
+    else if (!std::strcmp(tok, "steprefresh")) d.flags |= kFlagFusedRefresh;
     else if (!std::strncmp(tok, "spin=", 5)) d.spin_ns = std::atoll(tok + 5);
     else if (!std::strcmp(tok, "chunk")) d.flags |= kFlagChunkRows;
     else if (!std::strcmp(tok, "strips")) d.flags &= ~kFlagChunkRows;
@@ -76,6 +78,7 @@ Debug read_debug() {
     else if (!std::strncmp(tok, "stages=", 7)) d.stages = std::atoi(tok + 7);
     else if (!std::strncmp(tok, "parts=", 6)) d.parts = std::atoi(tok + 6);
     else if (!std::strncmp(tok, "ipw=", 4)) d.ipw = std::atoi(tok + 4);
+    else if (!std::strncmp(tok, "stage=", 6)) d.stage = std::atoi(tok + 6);
     else if (!std::strcmp(tok, "nocheck")) d.check_ptrs = false;
   }
   if (d.spin_ns < 0) d.spin_ns = 0;
@@ -371,14 +374,41 @@ ls_status beam_step_check_args(const void* logits, ls_dtype logit_dtype, const f
   return LS_OK;
 }
 
+// The argument checks of ls_cache_refresh_inplace (an empty shape passes).
+ls_status inplace_check_args(void* cache, ls_dtype dtype, const int32_t* parent, int layers, int batch, int k,
+                             int heads, int max_len, int len, int head_dim, void* workspace) {
+  if (layers < 0 || batch < 0 || k < 1 || k > LS_MAX_K || heads < 0 || max_len < 0 || len < 0 || len > max_len ||
+      head_dim < 0)
+    return LS_ERR_INVALID_ARG;
+  if (!dtype_ok(dtype)) return LS_ERR_INVALID_ARG;
+  if (layers == 0 || batch == 0 || heads == 0 || len == 0 || head_dim == 0) return LS_OK;
+  if (!cache || !parent) return LS_ERR_INVALID_ARG;
+  if (!aligned(parent, 4) || (workspace && !aligned(workspace, 256))) return LS_ERR_INVALID_ARG;
+  if (read_debug().check_ptrs) {
+    if (!device_reachable(cache) || !device_reachable(parent)) return LS_ERR_INVALID_ARG;
+    if (workspace && !device_reachable(workspace)) return LS_ERR_INVALID_ARG;
+  }
+  return LS_OK;
+}
+
 }  // namespace lsb
 
 extern "C" {
 
-ls_status ls_beam_step(const void* logits, ls_dtype logit_dtype, const float* bias, const float* beam_scores,
-                       const uint8_t* finished, int batch, int k, int vocab, int eos_id, int32_t* out_token,
-                       int32_t* out_parent, float* out_score, uint8_t* out_finished, void* workspace,
-                       size_t workspace_bytes, void* stream) {
+// The in-place cache refresh a step may run in its own kernel (K3), as the host planned it.
+struct FusedRefresh {
+  unsigned char* cache;
+  int es;  // element size of the cache
+  int layers, heads, max_len, len, head_dim;
+};
+
+// ls_beam_step; with rf != nullptr, K3 also refreshes the cache when its plan is taken and
+// the cache suits the bulk copies (*refreshed is set then).
+static ls_status beam_step_impl(const void* logits, ls_dtype logit_dtype, const float* bias, const float* beam_scores,
+                         const uint8_t* finished, int batch, int k, int vocab, int eos_id, int32_t* out_token,
+                         int32_t* out_parent, float* out_score, uint8_t* out_finished, void* workspace,
+                         size_t workspace_bytes, void* stream, const FusedRefresh* rf, bool* refreshed) {
+  if (refreshed) *refreshed = false;
   const ls_status chk = beam_step_check_args(logits, logit_dtype, bias, beam_scores, finished, batch, k, vocab,
                                              eos_id, out_token, out_parent, out_score, out_finished);
   if (chk != LS_OK || batch == 0) return chk;
@@ -428,6 +458,33 @@ ls_status ls_beam_step(const void* logits, ls_dtype logit_dtype, const float* bi
     p.stages = (int)((fu_ns + fu_parts - 1) / fu_parts);  // block-max rows per strip
     p.flags = dbg.flags;
     p.spin_limit_ns = dbg.spin_ns;
+    if (rf && (dbg.flags & kFlagFusedRefresh)) {
+      // the batch's refresh in K3: bulk copies of 16-byte aligned slabs through two buffers
+      // per warp; a tile of a slab (positions) per parent, or several heads' whole slabs
+      const long long slab_stride = (long long)rf->max_len * rf->head_dim * rf->es;
+      const long long slab_bytes = (long long)rf->len * rf->head_dim * rf->es;
+      const long long buf = beam_fused_refresh_buffer(dtype, bias != nullptr);
+      long long tile = (buf / k) / 16 * 16;
+      const bool fits = aligned(rf->cache, 16) && slab_stride % 16 == 0 && slab_bytes % 16 == 0 && tile >= 16;
+      if (fits) {
+        long long hg = 1;
+        if (slab_bytes <= tile) {
+          tile = slab_bytes;
+          hg = buf / ((long long)k * slab_bytes);
+          hg = hg < 1 ? 1 : (hg > rf->heads ? rf->heads : hg);
+        }
+        p.rf_cache = rf->cache;
+        p.rf_slab_stride = slab_stride;
+        p.rf_row_stride = slab_stride * rf->heads;
+        p.rf_layer_stride = p.rf_row_stride * rows;
+        p.rf_slab_bytes = slab_bytes;
+        p.rf_layers = rf->layers;
+        p.rf_heads = rf->heads;
+        p.rf_tile = (int)tile;
+        p.rf_hg = (int)hg;
+        if (refreshed) *refreshed = true;
+      }
+    }
     const cudaError_t e = launch_beam_fused(p, dtype, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? LS_OK : cuda_fail(e);
   }
@@ -480,6 +537,37 @@ ls_status ls_beam_step(const void* logits, ls_dtype logit_dtype, const float* bi
   cudaError_t e = strips ? launch_beam_strips(p, dtype, vpl, (int)grid, st) : launch_beam_rows(p, dtype, vpl, (int)grid, st);
   if (e == cudaSuccess) e = launch_beam_select(p, dtype, st);
   return e == cudaSuccess ? LS_OK : cuda_fail(e);
+}
+
+ls_status ls_beam_step(const void* logits, ls_dtype logit_dtype, const float* bias, const float* beam_scores,
+                       const uint8_t* finished, int batch, int k, int vocab, int eos_id, int32_t* out_token,
+                       int32_t* out_parent, float* out_score, uint8_t* out_finished, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  return beam_step_impl(logits, logit_dtype, bias, beam_scores, finished, batch, k, vocab, eos_id, out_token,
+                        out_parent, out_score, out_finished, workspace, workspace_bytes, stream, nullptr, nullptr);
+}
+
+ls_status ls_beam_step_refresh_inplace(const void* logits, ls_dtype logit_dtype, const float* bias,
+                                       const float* beam_scores, const uint8_t* finished, int batch, int k,
+                                       int vocab, int eos_id, int32_t* out_token, int32_t* out_parent,
+                                       float* out_score, uint8_t* out_finished, void* cache, ls_dtype cache_dtype,
+                                       int layers, int heads, int max_len, int len, int head_dim, void* workspace,
+                                       size_t workspace_bytes, void* stream) {
+  // every argument of both calls is checked before anything is queued
+  if (!out_parent) return LS_ERR_INVALID_ARG;
+  const ls_status ci = inplace_check_args(cache, cache_dtype, out_parent, layers, batch, k, heads, max_len, len,
+                                          head_dim, workspace);
+  if (ci != LS_OK) return ci;
+  const bool empty_cache = layers == 0 || batch == 0 || heads == 0 || len == 0 || head_dim == 0;
+  FusedRefresh rf{static_cast<unsigned char*>(cache), dtype_bytes(cache_dtype), layers, heads, max_len, len,
+                  head_dim};
+  bool refreshed = false;
+  const ls_status st = beam_step_impl(logits, logit_dtype, bias, beam_scores, finished, batch, k, vocab, eos_id,
+                                      out_token, out_parent, out_score, out_finished, workspace, workspace_bytes,
+                                      stream, empty_cache ? nullptr : &rf, &refreshed);
+  if (st != LS_OK || refreshed || empty_cache) return st;
+  return ls_cache_refresh_inplace(cache, cache_dtype, out_parent, layers, batch, k, heads, max_len, len, head_dim,
+                                  workspace, stream);
 }
 
 ls_status ls_logits_beam_step(const void* hidden, const void* weight, ls_dtype dtype, int dim, const float* bias,
@@ -566,6 +654,7 @@ ls_status ls_logits_beam_step(const void* hidden, const void* weight, ls_dtype d
   p.flags = dbg.flags;
   const long long stage = (long long)k * nc * wl.slot_cap * (long long)sizeof(CandSlot);
   p.sel_stage_bytes = (k <= 8 && nc <= 128 && (long long)k * nc <= 1024 && stage <= kSelStageMax) ? (int)stage : 0;
+  if (dbg.stage == 0) p.sel_stage_bytes = 0;
   p.units = rows * nc;
   p.spin_limit_ns = dbg.spin_ns;
   lp.idesc = umma_idesc(dtype == LS_DTYPE_BF16);
@@ -648,18 +737,11 @@ ls_status ls_cache_reorder(const void* src, void* dst, ls_dtype dtype, const int
 
 ls_status ls_cache_refresh_inplace(void* cache, ls_dtype dtype, const int32_t* parent, int layers, int batch, int k,
                                    int heads, int max_len, int len, int head_dim, void* workspace, void* stream) {
-  if (layers < 0 || batch < 0 || k < 1 || k > LS_MAX_K || heads < 0 || max_len < 0 || len < 0 || len > max_len ||
-      head_dim < 0)
-    return LS_ERR_INVALID_ARG;
-  if (!dtype_ok(dtype)) return LS_ERR_INVALID_ARG;
+  const ls_status ci = inplace_check_args(cache, dtype, parent, layers, batch, k, heads, max_len, len, head_dim,
+                                          workspace);
+  if (ci != LS_OK) return ci;
   if (layers == 0 || batch == 0 || heads == 0 || len == 0 || head_dim == 0) return LS_OK;
-  if (!cache || !parent) return LS_ERR_INVALID_ARG;
-  if (!aligned(parent, 4) || (workspace && !aligned(workspace, 256))) return LS_ERR_INVALID_ARG;
   const Debug dbg = read_debug();
-  if (dbg.check_ptrs) {
-    if (!device_reachable(cache) || !device_reachable(parent)) return LS_ERR_INVALID_ARG;
-    if (workspace && !device_reachable(workspace)) return LS_ERR_INVALID_ARG;
-  }
   const long long es = dtype_bytes(dtype);
   const long long slab_stride = (long long)max_len * head_dim * es;
   const long long row_stride = slab_stride * heads;

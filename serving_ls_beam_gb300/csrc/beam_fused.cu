@@ -65,6 +65,10 @@ struct __align__(16) FuSmem {
   unsigned int prefix, pmask;
   int need;
   int wc[kFuWarps];
+  // the batch's new parent of each output row (rank order), and each warp's two bulk-copy
+  // barriers of the cache refresh
+  int opar[kFuMaxK];
+  unsigned long long rbar[kFuWarps][2];
 };
 
 }  // namespace
@@ -106,6 +110,7 @@ __device__ void rank_and_write(const StepParams& p, FuSmem& sm, int b) {
     if (rank < K) {
       const int o = b * K + rank;
       const int parent = key_parent(ki), token = key_token(ki);
+      sm.opar[rank] = parent;
       p.out_token[o] = token;
       p.out_parent[o] = parent;
       p.out_score[o] = key_score(ki);
@@ -197,6 +202,95 @@ __device__ void exact_row(const StepParams& p, FuSmem& sm, int b, int j) {
   __syncthreads();
 }
 
+// The in-place cache refresh of batch b by the parents in sm.opar, after the step: the
+// warps take the batch's items (layer, heads [h0, h0 + rf_hg), one tile of their slabs) in
+// turn, and lane 0 of each runs a two-buffer pipeline in the warp's part of the rings, as the
+// standalone bulk-copy refresh does: the bulk loads of the slabs item i needs are issued
+// before the bulk stores of item i-1's changed rows, and a buffer is refilled only after the
+// stores that read it.  Every row reads the state before the step: an item's stores start
+// only once all of its loads have landed, and items touch disjoint bytes.  Waits are bounded;
+// one that runs out sets the timeout bit and lets the copies in flight land.
+__device__ void refresh_batch(const StepParams& p, FuSmem& sm, unsigned char* wbuf, uint32_t buf_bytes, int b) {
+  const int K = p.k, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned changed = 0u, needed = 0u;
+  for (int j = 0; j < K; ++j) {
+    const int q = sm.opar[j];
+    if (q != j) {
+      changed |= 1u << j;
+      needed |= 1u << q;
+    }
+  }
+  if (changed == 0u || lane != 0) return;
+  const int HG = p.rf_hg, TB = p.rf_tile;
+  const long long groups = (p.rf_heads + HG - 1) / HG;
+  const long long ntiles = (p.rf_slab_bytes + TB - 1) / TB;
+  const long long nitems = (long long)p.rf_layers * groups * ntiles;
+  const uint32_t bar0 = smem_addr(&sm.rbar[warp][0]), bar1 = smem_addr(&sm.rbar[warp][1]);
+  uint32_t uses0 = 0u, uses1 = 0u;  // completed-or-pending fills of each buffer
+  int cur = 0;
+  bool aborted = false, have_prev = false;
+  unsigned char* pv_base = nullptr;
+  int pv_tb = 0, pv_hg = 0, pv_buf = 0;
+  uint32_t pv_parity = 0;
+  auto finish_prev = [&]() {
+    if (!mbar_wait_bounded(pv_buf ? bar1 : bar0, pv_parity, p.spin_limit_ns)) {
+      aborted = true;
+      return;
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    const unsigned char* src = wbuf + (size_t)pv_buf * buf_bytes;
+    for (int j = 0; j < K; ++j) {
+      if (!((changed >> j) & 1u)) continue;
+      const int slot = __popc(needed & ((1u << sm.opar[j]) - 1u));
+      for (int hh = 0; hh < pv_hg; ++hh)
+        bulk_store(pv_base + (size_t)j * p.rf_row_stride + (size_t)hh * p.rf_slab_stride,
+                   smem_addr(src + ((size_t)slot * pv_hg + hh) * pv_tb), (uint32_t)pv_tb);
+    }
+    bulk_commit();
+  };
+  const int nneed = __popc(needed);
+  for (long long it = warp; it < nitems && !aborted; it += kFuWarps) {
+    const long long unit = it / ntiles;
+    const long long tile = it - unit * ntiles;
+    const int l = (int)(unit / groups);
+    const int h0 = (int)(unit - (long long)l * groups) * HG;
+    const int hg = min(HG, p.rf_heads - h0);
+    const long long t0 = tile * TB;
+    const int tb = (int)min((long long)TB, p.rf_slab_bytes - t0);
+    unsigned char* base = p.rf_cache + (size_t)l * p.rf_layer_stride + (size_t)b * K * p.rf_row_stride +
+                          (size_t)h0 * p.rf_slab_stride + t0;
+    bulk_wait_read<0>();  // buffer `cur` was last read by the stores of the item before the previous one
+    const uint32_t bcur = cur ? bar1 : bar0;
+    mbar_arrive_expect_tx(bcur, (uint32_t)(nneed * hg * tb));
+    unsigned char* dst = wbuf + (size_t)cur * buf_bytes;
+    int slot = 0;
+    for (int q = 0; q < K; ++q) {
+      if (!((needed >> q) & 1u)) continue;
+      for (int hh = 0; hh < hg; ++hh)
+        bulk_load_plain(smem_addr(dst + ((size_t)slot * hg + hh) * tb),
+                        base + (size_t)q * p.rf_row_stride + (size_t)hh * p.rf_slab_stride, (uint32_t)tb, bcur);
+      ++slot;
+    }
+    if (have_prev) finish_prev();
+    have_prev = true;
+    pv_base = base;
+    pv_tb = tb;
+    pv_hg = hg;
+    pv_buf = cur;
+    uint32_t& uses = cur ? uses1 : uses0;
+    pv_parity = uses & 1u;
+    ++uses;
+    cur ^= 1;
+  }
+  if (have_prev && !aborted) finish_prev();
+  if (aborted) {
+    atomicOr(p.status, kDevTimeout);
+    if (uses0 > 0) mbar_wait_bounded(bar0, (uses0 - 1) & 1u, 2000000000LL);
+    if (uses1 > 0) mbar_wait_bounded(bar1, (uses1 - 1) & 1u, 2000000000LL);
+  }
+  bulk_wait_all();
+}
+
 template <int DT, bool BIAS, int VPL>
 __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepParams p) {
   constexpr int VEC = Traits<DT>::kVec;
@@ -226,6 +320,13 @@ __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepPar
     sm.keys = reinterpret_cast<Key*>(fu_dyn);
     sm.nkeys = 0;
     sm.path = (p.flags & kFlagForceExact) ? 2 : 0;
+  }
+  if (p.rf_cache && tid == 0) {
+    for (int w = 0; w < kFuWarps; ++w) {
+      mbar_init(smem_addr(&sm.rbar[w][0]), 1);
+      mbar_init(smem_addr(&sm.rbar[w][1]), 1);
+    }
+    fence_barrier_init();
   }
   __syncthreads();
 
@@ -600,6 +701,14 @@ __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepPar
     p.rowstat[b * K + tid] = st;
   }
   if (tid == 0) p.bstat[b] = path;
+  if (p.rf_cache) {
+    // every thread's reads of the keys and the rings are done before they become buffers of
+    // bulk copies (the async proxy)
+    __syncthreads();
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    const uint32_t wbytes = (uint32_t)(kFuRing * CV * 16);
+    refresh_batch(p, sm, fu_dyn + (size_t)warp * wbytes, wbytes / 2, b);
+  }
 }
 
 template <int DT, bool BIAS, int VPL>
@@ -624,6 +733,11 @@ cudaError_t beam_fused_config() {
   if (e == cudaSuccess) e = config_t<DT_BF16, false, 8>();
   if (e == cudaSuccess) e = config_t<DT_BF16, true, 4>();
   return e;
+}
+
+int beam_fused_refresh_buffer(int dtype, bool bias) {
+  const int vpl = (dtype == DT_F32 || bias) ? 4 : 8;  // as launch_beam_fused picks it
+  return kFuRing * 32 * vpl * 16 / 2;
 }
 
 cudaError_t launch_beam_fused(const StepParams& p, int dtype, cudaStream_t stream) {

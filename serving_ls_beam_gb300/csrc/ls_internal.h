@@ -68,6 +68,7 @@ constexpr int kFlagForceExact = 1;
 constexpr int kFlagPlainInplace = 2;  // the in-place refresh by the staged CTA kernel
 constexpr int kFlagTmaInplace = 32;   // the in-place refresh by bulk copies
 constexpr int kFlagWordInplace = 64;  // the in-place refresh by the word kernel (k <= 8)
+constexpr int kFlagFusedRefresh = 128;  // ls_beam_step_refresh_inplace in one kernel where K3 applies
 constexpr int kFlagChunkRows = 4;     // the beam step's first kernel by fixed-size chunks (K1)
 constexpr int kFlagNoFused = 8;       // the beam step as two kernels even where K3 applies
 constexpr int kFlagFused = 16;        // the beam step as K3 wherever k allows
@@ -178,6 +179,13 @@ struct StepParams {
   int stages;           // K1s: stage buffers per warp
   long long units;  // rows * nc
   long long spin_limit_ns;
+  // K3 followed, in the same CTA, by the in-place cache refresh of its batch (the cache
+  // [layers, batch * k, heads, max_len, head_dim] by the batch's new parents, positions
+  // [0, len)); rf_cache == nullptr: no refresh.  An item is heads [h0, h0 + rf_hg) of one
+  // layer and one tile of rf_tile bytes of their slabs.
+  unsigned char* rf_cache;
+  long long rf_layer_stride, rf_row_stride, rf_slab_stride, rf_slab_bytes;
+  int rf_layers, rf_heads, rf_tile, rf_hg;
 };
 
 struct LogitsParams {
@@ -287,6 +295,8 @@ cudaError_t launch_beam_select(const StepParams& p, int dtype, cudaStream_t stre
 size_t beam_fused_smem_bytes(int vpl, int sps);
 cudaError_t beam_fused_config();  // once per device: the kernels' dynamic shared memory
 cudaError_t launch_beam_fused(const StepParams& p, int dtype, cudaStream_t stream);
+// bytes of one of a warp's two refresh buffers in K3 for these logits (its VPL)
+int beam_fused_refresh_buffer(int dtype, bool bias);
 size_t beam_strips_smem_bytes(int vpl, int stages);
 cudaError_t beam_strips_config(int dtype, bool bias, int vpl, int stages, int* occupancy);
 cudaError_t launch_beam_strips(const StepParams& p, int dtype, int vpl, int grid, cudaStream_t stream);

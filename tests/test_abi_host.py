@@ -96,6 +96,14 @@ def test_host_argument_checks(lib):
     assert lib.ls_backtrack(p, p, 4, 2, 65, 0, p, p, None, None) == E  # k > 64
     assert lib.ls_backtrack(None, p, 4, 2, 3, 0, p, p, None, None) == E  # no history
     assert lib.ls_backtrack(None, None, 0, 2, 3, 0, None, None, None, None) == 0  # no steps: no-op
+    # the step followed by the in-place refresh: the refresh's checks run before anything is queued
+    R = lib.ls_beam_step_refresh_inplace
+    R.argtypes = [ctypes.c_void_p, ctypes.c_int] + [ctypes.c_void_p] * 3 + [ctypes.c_int] * 4 + \
+        [ctypes.c_void_p] * 5 + [ctypes.c_int] * 6 + [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    assert R(p, 0, None, p, None, 2, 4, 100, 0, p, p, p, None, p, 1, 1, 1, 4, 5, 8, p, 1 << 20, None) == E  # len
+    assert R(p, 0, None, p, None, 2, 4, 100, 0, p, None, p, None, p, 1, 1, 1, 4, 2, 8, p, 1 << 20, None) == E
+    assert R(p, 0, None, p, None, 2, 4, 100, 0, p, p, p, None, p, 7, 1, 1, 4, 2, 8, p, 1 << 20, None) == E  # dtype
+    assert R(p, 0, None, p, None, 2, 4, 100, 0, p, p, p, None, None, 1, 1, 1, 4, 2, 8, p, 1 << 20, None) == E
     assert lib.ls_read_status(None, None) == E
     assert lib.ls_workspace_init(None, 0, None) == E
 
