@@ -741,8 +741,9 @@ def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
 
 
 def bench_sampling(dev, peak, calls: int = 16):
-    """Sampling decoding (ls_sample: K1 then K5) on workload s1: one CUDA graph of `calls` calls over as
-    many distinct logit sets (1.3 GB in all, larger than L2), timed with CUDA events."""
+    """Sampling decoding (ls_sample: the one-kernel sampler for top_k <= 8, else K1 then K5) on
+    workload s1: one CUDA graph of `calls` calls over as many distinct logit sets (1.3 GB in all,
+    larger than L2), timed with CUDA events."""
     import torch
 
     import serving_ls_beam_gb300 as lsb
@@ -785,7 +786,10 @@ def bench_sampling(dev, peak, calls: int = 16):
     gbs = nbytes / (us * 1e-6) / 1e9
     return {"workload": f"s1: {rows} rows, vocab {vocab}, f16 logits N(0,2), top_k {top_k}, top_p {top_p}",
             "us_per_call": us, "rows_per_s": rows / (us * 1e-6), "achieved": gbs, "peak": peak, "unit": "GB/s",
-            "frac": gbs / peak, "algorithmic_bytes_per_call": nbytes, "launches_per_call": 2,
+            "frac": gbs / peak, "algorithmic_bytes_per_call": nbytes,
+            # the one-kernel sampler for top_k <= 8 with rows enough to fill the GPU, else K1 then K5
+            "launches_per_call": 1 if top_k <= 8 and 2 * ((rows + 3) // 4) >= torch.cuda.get_device_properties(
+                dev).multi_processor_count else 2,
             "l2": f"{calls} distinct logit sets per graph ({calls * rows * vocab * 2 / 1e9:.2f} GB)"}
 
 

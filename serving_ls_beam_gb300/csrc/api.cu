@@ -848,6 +848,42 @@ ls_status ls_sample(const void* logits, ls_dtype logit_dtype, const float* bias,
   DeviceInfo* di = device_info(&dev);
   if (!di) return cuda_fail(cudaErrorUnknown);
   const int dtype = (int)logit_dtype;
+  // the one-kernel sampler (K3's traversal, kFuSampRows rows per CTA, two strips a row) when
+  // top_k <= 8, the CTAs fill the GPU by themselves and a strip's block maxima fit in shared
+  // memory; otherwise K1 then K5
+  {
+    const int fu_parts = (kFuThreads / 32) / kFuSampRows;
+    const int fu_vpl = (dtype == LS_DTYPE_F32 || bias) ? 4 : 8;
+    const long long fu_ns = ((15 + (long long)vocab * es + 15) / 16 + 32ll * fu_vpl - 1) / (32ll * fu_vpl);
+    const long long ctas = ((long long)rows + kFuSampRows - 1) / kFuSampRows;
+    const bool one = !(dbg.flags & kFlagNoFused) && top_k <= kFuMaxK &&
+                     (fu_ns + fu_parts - 1) / fu_parts <= kFuMaxStages &&
+                     ((dbg.flags & kFlagFused) || 2 * ctas >= di->sms);
+    if (one) {
+      if (!fused_configured(di)) return cuda_fail(cudaErrorUnknown);
+      unsigned char* ws = static_cast<unsigned char*>(workspace);
+      StepParams p = {};
+      p.logits = logits;
+      p.bias = bias;
+      p.u = u;
+      p.out_token = out_token;
+      p.out_logprob = out_logprob;
+      p.top_p = top_p;
+      p.status = reinterpret_cast<uint32_t*>(ws + wl.status_off);
+      p.rowstat = reinterpret_cast<RowStat*>(ws + wl.rowstat_off);
+      p.bstat = reinterpret_cast<int32_t*>(ws + wl.bstat_off);
+      p.batch = (int)ctas;
+      p.k = top_k;
+      p.vocab = vocab;
+      p.rows = rows;
+      p.nc = fu_parts;
+      p.stages = (int)((fu_ns + fu_parts - 1) / fu_parts);
+      p.flags = dbg.flags;
+      p.spin_limit_ns = dbg.spin_ns;
+      const cudaError_t e = launch_sample_fused(p, dtype, static_cast<cudaStream_t>(stream));
+      return e == cudaSuccess ? LS_OK : cuda_fail(e);
+    }
+  }
   RowPlan plan;
   const ls_status ps = plan_rows(di, dbg, dtype, es, bias != nullptr, vocab, rows, wl, &plan);
   if (ps != LS_OK) return ps;

@@ -1,5 +1,8 @@
 // Beam-step kernel K3: the whole step of one batch in one CTA -- both traversals of the
-// batch's beams and the fine rank -- for batches that fill the GPU on their own.
+// batch's beams and the fine rank -- for batches that fill the GPU on their own.  The same
+// kernel is the one-kernel sampler of sampling decoding (SAMP): a CTA takes kFuSampRows
+// independent rows, and per row the candidates at or above its bound give its exact top k,
+// from which one token is drawn at the caller's uniform (ls_draw.cuh).
 //
 // Method: LightSeq inference article (31duo.com, itemid-283120), hierarchical decoding
 // section.  First traversal: split a beam's logits into groups, take each group's max; the
@@ -31,6 +34,7 @@
 //    exact mode send the batch to an exact path: a radix select of every beam's top-k over
 //    its logits.
 #include "ls_device.cuh"
+#include "ls_draw.cuh"
 #include "ls_dtype.cuh"
 #include "ls_internal.h"
 #include "ls_strip.cuh"
@@ -69,6 +73,10 @@ struct __align__(16) FuSmem {
   // barriers of the cache refresh
   int opar[kFuMaxK];
   unsigned long long rbar[kFuWarps][2];
+  // the one-kernel sampler: each row's top k (best first) and whether it needs the exact path
+  float tx[kFuSampRows][kFuMaxK];
+  int tv[kFuSampRows][kFuMaxK];
+  int spath[kFuSampRows];
 };
 
 }  // namespace
@@ -123,11 +131,11 @@ __device__ void rank_and_write(const StepParams& p, FuSmem& sm, int b) {
 // order key over the row's logits, 8 bits a pass, then the elements above it and the first
 // `need` equal to it in token order.  All threads call it.
 template <int DT, bool BIAS>
-__device__ void exact_row(const StepParams& p, FuSmem& sm, int b, int j) {
+__device__ void exact_row(const StepParams& p, FuSmem& sm, long long row, int j) {
   constexpr int ES = Traits<DT>::kBytes;
   const int K = p.k, V = p.vocab;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const unsigned char* rowp = static_cast<const unsigned char*>(p.logits) + (size_t)(b * K + j) * V * ES;
+  const unsigned char* rowp = static_cast<const unsigned char*>(p.logits) + (size_t)row * V * ES;
   auto xat = [&](int i) -> float {
     float x = load_elem<DT>(rowp + (size_t)i * ES);
     if constexpr (BIAS) x += __ldg(p.bias + i);
@@ -291,7 +299,7 @@ __device__ void refresh_batch(const StepParams& p, FuSmem& sm, unsigned char* wb
   bulk_wait_all();
 }
 
-template <int DT, bool BIAS, int VPL>
+template <int DT, bool BIAS, int VPL, bool SAMP>
 __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepParams p) {
   constexpr int VEC = Traits<DT>::kVec;
   constexpr int ES = Traits<DT>::kBytes;
@@ -303,6 +311,8 @@ __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepPar
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = blockIdx.x;
   const int K = p.k, V = p.vocab, W = p.nc;  // W strips per row, one warp per strip
+  // rows per CTA: the batch's k beams, or kFuSampRows independent rows for the sampler
+  const int NR = SAMP ? kFuSampRows : K;
   const int SPS = p.stages;                  // block-max rows kept per strip
   unsigned char* ring = fu_dyn + (size_t)warp * kFuRing * CV * 16;
   float* bmax = reinterpret_cast<float*>(fu_dyn + (size_t)kFuWarps * kFuRing * CV * 16);
@@ -311,7 +321,14 @@ __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepPar
 
   // inputs may come from the previous kernel of the stream
   grid_dependency_wait();
-  if (tid < K) {
+  if constexpr (SAMP) {
+    if (tid < NR) {
+      sm.beam[tid] = 0.0f;
+      sm.fin[tid] = (long long)b * NR + tid >= p.rows ? 1 : 0;  // past the last row: skipped
+      sm.ncand[tid] = 0;
+      sm.spath[tid] = 0;
+    }
+  } else if (tid < K) {
     sm.beam[tid] = p.beam[b * K + tid];
     sm.fin[tid] = (p.finished && p.finished[b * K + tid]) ? 1 : 0;
     sm.ncand[tid] = 0;
@@ -338,7 +355,7 @@ __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepPar
   };
   auto geo = [&](int j) -> RowGeo {
     RowGeo g;
-    const unsigned char* rowp = logits + (size_t)(b * K + j) * row_bytes;
+    const unsigned char* rowp = logits + ((size_t)b * NR + j) * row_bytes;
     g.lead = (int)(reinterpret_cast<uintptr_t>(rowp) & 15);
     g.rb = reinterpret_cast<const uint4*>(rowp - g.lead);
     g.nv = (g.lead + row_bytes + 15) >> 4;
@@ -403,7 +420,7 @@ __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepPar
 
   // ---------------------------------------------------------------- first traversal
   // warp u streams strip s = u mod W of row j = u / W: stages s, s + W, ...
-  const int nunits = K * W;
+  const int nunits = NR * W;
   if (warp < nunits) {
     const int u = warp, j = u / W, s = u - j * W;
     float ml = -INFINITY;  // lane's running max
@@ -620,6 +637,108 @@ __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepPar
   }
   __syncthreads();
 
+  if constexpr (SAMP) {
+    // ---------------------------------------------------------------- per row: the draw
+    // warp j takes row j: lse from its strips' (max, sum), R = the largest strip bound, the
+    // row's candidates at or above R ranked (larger x, then smaller token) into its top k,
+    // and the draw at u[row]
+    if (warp < NR && !sm.fin[warp]) {
+      const int j = warp, u0 = j * W;
+      const long long row = (long long)b * NR + j;
+      const float mu = lane < W ? sm.um[u0 + lane] : -INFINITY;
+      float M = mu;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      float S = (lane < W && mu != -INFINITY) ? sm.us[u0 + lane] * exp2f((mu - M) * kLog2e) : 0.0f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+      float Rr = lane < W ? sm.ur[u0 + lane] : -INFINITY;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) Rr = fmaxf(Rr, __shfl_xor_sync(0xffffffffu, Rr, o));
+      const bool ovf = __any_sync(0xffffffffu, lane < W && sm.uovf[u0 + lane] != 0);
+      const float lse = M == -INFINITY ? -INFINITY : __fadd_rn(M, logf(S));
+      // candidate `lane` of each strip of the row, kept when at or above R
+      float cx[kFuWarps / kFuSampRows];
+      int cv[kFuWarps / kFuSampRows];
+      bool ck[kFuWarps / kFuSampRows];
+      int ntot = 0;
+#pragma unroll
+      for (int t = 0; t < kFuWarps / kFuSampRows; ++t) {
+        const int n = t < W ? min(sm.ucnt[u0 + t], kFuList) : 0;
+        const float2 en = lane < n ? sm.cand[u0 + t][lane] : make_float2(-INFINITY, 0.0f);
+        ck[t] = lane < n && en.x >= Rr;
+        cx[t] = en.x;
+        cv[t] = __float_as_int(en.y);
+        ntot += __popc(__ballot_sync(0xffffffffu, ck[t]));
+      }
+      const bool forced = (p.flags & kFlagForceExact) != 0;
+      const bool exact = forced || ovf || ntot < K;
+      if (!exact) {
+#pragma unroll
+        for (int t = 0; t < kFuWarps / kFuSampRows; ++t) {
+          if (ck[t]) {
+            int rank = 0;
+            for (int t2 = 0; t2 < W; ++t2) {
+              const int n2 = min(sm.ucnt[u0 + t2], kFuList);
+              for (int i = 0; i < n2; ++i) {
+                const float2 e = sm.cand[u0 + t2][i];
+                const int ev = __float_as_int(e.y);
+                rank += (e.x >= Rr) & ((e.x > cx[t]) | ((e.x == cx[t]) & (ev < cv[t])));
+              }
+            }
+            if (rank < K) {
+              sm.tx[j][rank] = cx[t];
+              sm.tv[j][rank] = cv[t];
+            }
+          }
+        }
+        __syncwarp();
+        draw_topk(sm.tx[j], sm.tv[j], K, p.top_p, lse, p.u[row], (int)row, p.out_token, p.out_logprob);
+      }
+      if (lane == 0) {
+        sm.spath[j] = exact ? 1 : 0;
+        sm.lse[j] = lse;
+        RowStat st;
+        st.lse = lse;
+        st.rtopk = Rr;
+        st.ncand = exact ? -1 : ntot;
+        st.pad = 0;
+        p.rowstat[row] = st;
+        p.bstat[row] = forced ? 2 : (exact ? 1 : 0);
+      }
+    }
+    __syncthreads();
+    // a row that lost a candidate, or holds fewer than k at or above R: its exact top k by a
+    // radix select over the row (the whole CTA), ranked by x (the keys' score is x here), then
+    // the draw
+    for (int j = 0; j < NR; ++j) {
+      if (!sm.spath[j] || sm.fin[j]) continue;  // CTA-uniform
+      if (tid == 0) {
+        sm.nkeys = 0;
+        sm.c[j] = ScoreBase{0.0f, 0.0f};
+      }
+      __syncthreads();
+      const long long row = (long long)b * NR + j;
+      exact_row<DT, BIAS>(p, sm, row, j);
+      if (warp == 0) {
+        const int n = min(sm.nkeys, kFuCap);
+        for (int i = lane; i < n; i += 32) {
+          const Key ki = sm.keys[i];
+          int rank = 0;
+          for (int q = 0; q < n; ++q) rank += key_less(sm.keys[q], ki);
+          if (rank < K) {
+            sm.tx[j][rank] = key_score(ki);
+            sm.tv[j][rank] = key_token(ki);
+          }
+        }
+        __syncwarp();
+        draw_topk(sm.tx[j], sm.tv[j], K, p.top_p, sm.lse[j], p.u[row], (int)row, p.out_token, p.out_logprob);
+      }
+      __syncthreads();
+    }
+    return;
+  }
+
   // ---------------------------------------------------------------- per row: lse, R, keys
   // warp j merges row j's strips -- lse from their (max, sum), R = the largest of their
   // bounds (each is at most the row's k-th largest) -- and appends the row's keys: the strips'
@@ -681,7 +800,7 @@ __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepPar
     for (int j = 0; j < K; ++j) {
       const int kind = sm.kind[j];
       if (kind == FROW_LIVE) {
-        exact_row<DT, BIAS>(p, sm, b, j);
+        exact_row<DT, BIAS>(p, sm, (long long)b * K + j, j);
       } else {
         if (tid < K && (kind == FROW_DEAD || tid == 0)) {
           const int pos = atomicAdd(&sm.nkeys, 1);
@@ -711,15 +830,20 @@ __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepPar
   }
 }
 
-template <int DT, bool BIAS, int VPL>
+template <int DT, bool BIAS, int VPL, bool SAMP>
 cudaError_t launch_t(const StepParams& p, cudaStream_t stream) {
-  PdlLaunch l(dim3((unsigned)p.batch), dim3(kFuThreads), beam_fused_smem_bytes(VPL, p.stages), stream);
-  return cudaLaunchKernelEx(&l.cfg, beam_fused_kernel<DT, BIAS, VPL>, p);
+  const unsigned grid = SAMP ? (unsigned)((p.rows + kFuSampRows - 1) / kFuSampRows) : (unsigned)p.batch;
+  PdlLaunch l(dim3(grid), dim3(kFuThreads), beam_fused_smem_bytes(VPL, p.stages), stream);
+  return cudaLaunchKernelEx(&l.cfg, beam_fused_kernel<DT, BIAS, VPL, SAMP>, p);
 }
 
 template <int DT, bool BIAS, int VPL>
 cudaError_t config_t() {
-  return cudaFuncSetAttribute(beam_fused_kernel<DT, BIAS, VPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(beam_fused_kernel<DT, BIAS, VPL, false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)beam_fused_smem_bytes(VPL, kFuMaxStages));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(beam_fused_kernel<DT, BIAS, VPL, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)beam_fused_smem_bytes(VPL, kFuMaxStages));
 }
 
@@ -740,14 +864,26 @@ int beam_fused_refresh_buffer(int dtype, bool bias) {
   return kFuRing * 32 * vpl * 16 / 2;
 }
 
-cudaError_t launch_beam_fused(const StepParams& p, int dtype, cudaStream_t stream) {
+template <bool SAMP>
+cudaError_t launch_any(const StepParams& p, int dtype, cudaStream_t stream) {
   const bool bias = p.bias != nullptr;
   switch (dtype) {
-    case DT_F32: return bias ? launch_t<DT_F32, true, 4>(p, stream) : launch_t<DT_F32, false, 4>(p, stream);
-    case DT_F16: return bias ? launch_t<DT_F16, true, 4>(p, stream) : launch_t<DT_F16, false, 8>(p, stream);
-    case DT_BF16: return bias ? launch_t<DT_BF16, true, 4>(p, stream) : launch_t<DT_BF16, false, 8>(p, stream);
+    case DT_F32:
+      return bias ? launch_t<DT_F32, true, 4, SAMP>(p, stream) : launch_t<DT_F32, false, 4, SAMP>(p, stream);
+    case DT_F16:
+      return bias ? launch_t<DT_F16, true, 4, SAMP>(p, stream) : launch_t<DT_F16, false, 8, SAMP>(p, stream);
+    case DT_BF16:
+      return bias ? launch_t<DT_BF16, true, 4, SAMP>(p, stream) : launch_t<DT_BF16, false, 8, SAMP>(p, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_beam_fused(const StepParams& p, int dtype, cudaStream_t stream) {
+  return launch_any<false>(p, dtype, stream);
+}
+
+cudaError_t launch_sample_fused(const StepParams& p, int dtype, cudaStream_t stream) {
+  return launch_any<true>(p, dtype, stream);
 }
 
 }  // namespace lsb

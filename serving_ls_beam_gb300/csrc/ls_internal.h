@@ -35,6 +35,7 @@ constexpr int kStBarBytes = kStListOff + kStWarps * kStListCap * 8;  // start of
 constexpr int kFuThreads = 256;
 constexpr int kFuMaxK = 8;
 constexpr int kFuMaxStages = 32;
+constexpr int kFuSampRows = 4;  // rows per CTA of the one-kernel sampler
 // K2 (beam_select.cu): one CTA per batch.
 constexpr int kSelThreads = 256;
 constexpr int kSelWarps = kSelThreads / 32;
@@ -186,6 +187,11 @@ struct StepParams {
   unsigned char* rf_cache;
   long long rf_layer_stride, rf_row_stride, rf_slab_stride, rf_slab_bytes;
   int rf_layers, rf_heads, rf_tile, rf_hg;
+  // K3 as the one-kernel sampler (sampling decoding): rows are independent sequences, kFuSampRows
+  // per CTA, k = top_k; the draw at u[row] writes out_token[row] and out_logprob[row]
+  const float* u;
+  float* out_logprob;
+  float top_p;
 };
 
 struct LogitsParams {
@@ -295,6 +301,8 @@ cudaError_t launch_beam_select(const StepParams& p, int dtype, cudaStream_t stre
 size_t beam_fused_smem_bytes(int vpl, int sps);
 cudaError_t beam_fused_config();  // once per device: the kernels' dynamic shared memory
 cudaError_t launch_beam_fused(const StepParams& p, int dtype, cudaStream_t stream);
+// the one-kernel sampler: ceil(rows / kFuSampRows) CTAs
+cudaError_t launch_sample_fused(const StepParams& p, int dtype, cudaStream_t stream);
 // bytes of one of a warp's two refresh buffers in K3 for these logits (its VPL)
 int beam_fused_refresh_buffer(int dtype, bool bias);
 size_t beam_strips_smem_bytes(int vpl, int stages);

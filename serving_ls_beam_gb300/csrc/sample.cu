@@ -1,5 +1,7 @@
 // Sampling kernel K5: the draw of one token per sequence from the top-k (optionally
-// top-p) candidates of its logits, after K1 has streamed every row once.
+// top-p) candidates of its logits, after K1 has streamed every row once.  This two-kernel
+// sampler serves top_k > 8 and row counts too small to fill the GPU; otherwise the one-kernel
+// sampler in beam_fused.cu runs.
 //
 // Method: LightSeq inference article (31duo.com, itemid-283120), decoding section: besides
 // beam search, decoding by sampling.  The hierarchical first traversal applies unchanged:
@@ -17,6 +19,7 @@
 // overflowed, or with more survivors than a warp holds, is flagged and its exact top-k
 // taken afterwards by the whole CTA (a radix select over its logits).
 #include "ls_device.cuh"
+#include "ls_draw.cuh"
 #include "ls_dtype.cuh"
 #include "ls_internal.h"
 
@@ -62,44 +65,10 @@ __device__ __forceinline__ bool before(float xa, int va, float xb, int vb) {
   return (xa > xb) | ((xa == xb) & (va < vb));
 }
 
-__device__ __forceinline__ float warp_incl_scan(float v) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float t = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += t;
-  }
-  return v;
-}
-
-// The draw of one row by one warp from its top-k (tx/tv, best first): probabilities
-// exp(x - x_0) renormalised over the k, the top-p prefix, the inverse CDF at u.
+// The draw of one row by one warp from its top-k (tx/tv, best first).
 __device__ __forceinline__ void draw(const SampleParams& p, const float* tx, const int* tv, float lse, float u,
                                      int r) {
-  const int lane = threadIdx.x & 31, K = p.k;
-  const float x0 = tx[0];
-  const float e0 = lane < K ? expf(tx[lane] - x0) : 0.0f;
-  const float e1 = lane + 32 < K ? expf(tx[lane + 32] - x0) : 0.0f;
-  const float c0 = warp_incl_scan(e0);
-  const float t0 = __shfl_sync(0xffffffffu, c0, 31);
-  const float c1 = warp_incl_scan(e1) + t0;
-  const float tot = __shfl_sync(0xffffffffu, c1, 31);
-  int mk = K;  // kept prefix
-  if (p.top_p < 1.0f) {
-    const float lim = p.top_p * tot;
-    const unsigned b0 = __ballot_sync(0xffffffffu, (lane < K) & (c0 >= lim));
-    const unsigned b1 = __ballot_sync(0xffffffffu, (lane + 32 < K) & (c1 >= lim));
-    mk = b0 ? __ffs(b0) : (b1 ? 32 + __ffs(b1) : K);
-  }
-  const float totm = mk <= 32 ? __shfl_sync(0xffffffffu, c0, mk - 1) : __shfl_sync(0xffffffffu, c1, (mk - 33) & 31);
-  const float target = u * totm;
-  const unsigned h0 = __ballot_sync(0xffffffffu, (lane < mk) & (c0 > target));
-  const unsigned h1 = __ballot_sync(0xffffffffu, (lane + 32 < mk) & (c1 > target));
-  const int pick = h0 ? __ffs(h0) - 1 : (h1 ? 31 + __ffs(h1) : mk - 1);
-  if (lane == 0) {
-    p.out_token[r] = tv[pick];
-    if (p.out_logprob) p.out_logprob[r] = tx[pick] - lse;
-  }
+  draw_topk(tx, tv, p.k, p.top_p, lse, u, r, p.out_token, p.out_logprob);
 }
 
 // Exact top-k of row r without the candidate slots, by the whole CTA: radix select of the

@@ -1,6 +1,7 @@
 """Sampling decoding on the GPU (ls_sample) against the oracle on the same seeded inputs:
 the 1024-row workload s1 in full, random shapes over dtypes, bias, top_k 1..64 and top_p,
-ties (all-equal logits, the exact fallback), the forced exact path, and argument checks.
+ties (all-equal logits, the exact fallback), the forced exact path, and argument checks,
+each under the plan's choice, the one-kernel sampler and the two-kernel sampler.
 
 A token must equal the oracle's unless the oracle's uniform lies within 1e-5 of a
 cumulative-probability boundary of the kept candidates (both sides then round legitimately
@@ -22,6 +23,23 @@ import serving_ls_beam_gb300 as lsb  # noqa: E402
 MARGIN = 1e-5
 MAX_EXCUSED = 2  # rows of one call whose token may differ at a boundary
 TOL = {"f32": 1e-5, "f16": 2e-3, "bf16": 2e-3}
+
+
+# LS_BEAM_DEBUG settings of the implementations every test runs under: the plan's choice, the
+# one-kernel sampler forced wherever top_k <= 8, and the two-kernel sampler (K1 then K5)
+IMPLS = {"plan": "", "onekernel": "fused", "twokernel": "nofused"}
+_impl_env = {"value": ""}
+
+
+@pytest.fixture(autouse=True, params=sorted(IMPLS))
+def impl(request):
+    _impl_env["value"] = IMPLS[request.param]
+    yield request.param
+    _impl_env["value"] = ""
+
+
+def _env(extra=None):
+    return ",".join(e for e in (_impl_env["value"], extra) if e)
 
 
 @pytest.fixture(scope="module")
@@ -49,15 +67,13 @@ def run_gpu(dev, lg, dtype, bias, u, top_k, top_p, env=None):
     lsb.check(lsb.ls_workspace_init(ws))
     old = os.environ.get("LS_BEAM_DEBUG")
     try:
-        if env is not None:
-            os.environ["LS_BEAM_DEBUG"] = env
+        os.environ["LS_BEAM_DEBUG"] = _env(env)
         lsb.check(lsb.ls_sample(t_lg, t_b, t_u, top_k, top_p, tok, lp, ws), "ls_sample")
     finally:
-        if env is not None:
-            if old is None:
-                os.environ.pop("LS_BEAM_DEBUG", None)
-            else:
-                os.environ["LS_BEAM_DEBUG"] = old
+        if old is None:
+            os.environ.pop("LS_BEAM_DEBUG", None)
+        else:
+            os.environ["LS_BEAM_DEBUG"] = old
     lsb.check(lsb.ls_read_status(ws), "device status")
     return tok.cpu().numpy(), lp.cpu().numpy()
 
@@ -166,7 +182,7 @@ def test_device_wait_timeout_is_reported(dev, oracle_mod):
     ws = torch.empty(lsb.ls_sample_workspace_size(rows, top_k, vocab), dtype=torch.uint8, device=dev)
     lsb.check(lsb.ls_workspace_init(ws))
     old = os.environ.get("LS_BEAM_DEBUG")
-    os.environ["LS_BEAM_DEBUG"] = "spin=0"
+    os.environ["LS_BEAM_DEBUG"] = "spin=0,nofused"  # the two-kernel sampler has the bounded waits
     try:
         st = lsb.ls_sample(t_lg, t_b, t_u, top_k, top_p, tok, None, ws)
     finally:
