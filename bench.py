@@ -57,7 +57,7 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--decode-steps", type=int, default=0,
                     help="run only the first N decode steps of the workload (for small profiling runs)")
-    ap.add_argument("--kernel", choices=["beam_step", "cache_refresh_inplace", "cache_reorder"], default=None,
+    ap.add_argument("--kernel", choices=["beam_step", "cache_refresh_inplace", "cache_reorder", "sample"], default=None,
                     help="profiling driver: time one kernel of the loop alone on the last decode steps of the "
                          "workload (inputs of a few hundred MB to 1.6 GB) and print its per-launch figures")
     return ap.parse_args()
@@ -335,6 +335,8 @@ def bench_kernel(args, w: synth.Workload):
     dev = torch.device("cuda", 0)
     _build.build()
     lsb.load_library()
+    if args.kernel == "sample":
+        return bench_kernel_sample(args, dev)
     B, K, V = w.batch, w.k, w.vocab
     es = 2 if w.dtype in ("f16", "bf16") else 4
     multi = w.steps > 1
@@ -418,6 +420,49 @@ def bench_kernel(args, w: synth.Workload):
             "note": "each launch timed with CUDA events around it, the three launches of a round queued "
                     "back to back behind a GPU sleep (no host launch time inside); no L2 flush between "
                     "launches, each launch reads inputs larger than L2 or those of the previous step"}
+
+
+def bench_kernel_sample(args, dev):
+    """Profiling driver for sampling decoding: ls_sample on three of workload s1's logit sets
+    (3 x 82 MB), each of --warmup + --steps rounds launching it once per set."""
+    import torch
+
+    import serving_ls_beam_gb300 as lsb
+
+    w = synth.SAMPLE_WORKLOADS["s1"]
+    ins = [synth.sample_inputs(w, step=i) for i in range(3)]
+    rows, vocab, top_k, top_p = w.batch, w.vocab, ins[0]["top_k"], ins[0]["top_p"]
+    lg = [torch.from_numpy(x["logits"]).to(dev) for x in ins]
+    u = [torch.from_numpy(x["u"]).to(dev) for x in ins]
+    tok = torch.empty(rows, dtype=torch.int32, device=dev)
+    lp = torch.empty(rows, dtype=torch.float32, device=dev)
+    ws = torch.empty(lsb.ls_sample_workspace_size(rows, top_k, vocab), dtype=torch.uint8, device=dev)
+    lsb.check(lsb.ls_workspace_init(ws))
+    nbytes = rows * vocab * 2
+    us = [[] for _ in ins]
+    for rnd in range(args.warmup + args.steps):
+        torch.cuda.synchronize()
+        torch.cuda._sleep(1 << 20)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in ins]
+        for i in range(len(ins)):
+            ev[i][0].record()
+            lsb.check(lsb.ls_sample(lg[i], None, u[i], top_k, top_p, tok, lp, ws), "ls_sample")
+            ev[i][1].record()
+        torch.cuda.synchronize()
+        if rnd >= args.warmup:
+            for i in range(len(ins)):
+                us[i].append(ev[i][0].elapsed_time(ev[i][1]) * 1e3)
+    lsb.check(lsb.ls_read_status(ws), "device status")
+    peak, peak_src = hbm_peak()
+    launches = []
+    for i in range(len(ins)):
+        t = statistics.median(us[i]) if us[i] else None
+        launches.append({"call": i, "us": t, "algorithmic_bytes": nbytes,
+                         "gbs": None if not t else nbytes / (t * 1e-6) / 1e9})
+    return {"kernel": "sample", "workload": "s1", "warmup": args.warmup, "steps": args.steps, "peak": peak,
+            "peak_source": peak_src, "launches": launches,
+            "note": "each call timed with CUDA events around it, the three calls of a round queued back to back "
+                    "behind a GPU sleep"}
 
 
 def beam_step_kernels(w: synth.Workload, dev) -> int:
