@@ -728,7 +728,10 @@ def bench_gpu(args, w: synth.Workload, world: int, rank: int, local: int):
                                           "frac": o_gbs / peak,
                                           "traffic": recorded_traffic("cache_reorder", wr.name),
                                           "us_per_launch": o_k4 * 1e3 / T,
-                                          "algorithmic_bytes_per_launch": k4_dense_bytes / T},
+                                          "algorithmic_bytes_per_launch": k4_dense_bytes / T,
+                                          "note": "algorithmic bytes count every row both ways; a parent "
+                                                  "shared by several beams is read again from L2, so frac "
+                                                  "may exceed 1 (traffic is the DRAM bytes moved)"},
                         "beam_step_us_per_launch": o_k1 * 1e3 / T,
                         "note": "the same search with the out-of-place (ping-pong) cache refresh"}
     bt_bytes = 2 * T * B * K * 4 + B * K * (T + 1) * 4  # history read, sequences and lengths written
