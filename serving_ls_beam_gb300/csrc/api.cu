@@ -54,8 +54,8 @@ struct Debug {
   bool check_ptrs = true;
 };
 
-// LS_BEAM_DEBUG: comma-separated "exact", "ipplain", "iptma", "ipwords", "steprefresh", "chunk", "strips", "fused", "nofused",
-// "spin=<ns>", "vpl=<4|8|16>", "stages=<2..8>", "parts=<n>", "ipw=<words>", "stage=<0|1>", "nocheck".
+// LS_BEAM_DEBUG: comma-separated "exact", "ipplain", "iptma", "ipwords", "steprefresh", "chunk", "strips", "fused",
+// "nofused", "cluster", "nocluster", "spin=<ns>", "vpl=<4|8|16>", "stages=<2..8>", "parts=<n>", "ipw=<words>", "stage=<0|1>", "nocheck".
 Debug read_debug() {
   Debug d;
   const char* env = std::getenv("LS_BEAM_DEBUG");
@@ -74,6 +74,8 @@ Debug read_debug() {
     else if (!std::strcmp(tok, "strips")) d.flags &= ~kFlagChunkRows;
     else if (!std::strcmp(tok, "fused")) d.flags |= kFlagFused;
     else if (!std::strcmp(tok, "nofused")) d.flags |= kFlagNoFused;
+    else if (!std::strcmp(tok, "nocluster")) d.flags |= kFlagNoCluster;
+    else if (!std::strcmp(tok, "cluster")) d.flags |= kFlagCluster;
     else if (!std::strncmp(tok, "vpl=", 4)) d.vpl = std::atoi(tok + 4);
     else if (!std::strncmp(tok, "stages=", 7)) d.stages = std::atoi(tok + 7);
     else if (!std::strncmp(tok, "parts=", 6)) d.parts = std::atoi(tok + 6);
@@ -434,7 +436,12 @@ static ls_status beam_step_impl(const void* logits, ls_dtype logit_dtype, const 
   const bool fused = !(dbg.flags & kFlagNoFused) && k <= kFuMaxK && fu_parts >= 1 &&
                      (fu_ns + fu_parts - 1) / fu_parts <= kFuMaxStages &&
                      ((dbg.flags & kFlagFused) || 2ll * batch >= di->sms);
-  if (fused) {
+  // otherwise K3's cluster form for k a power of two up to 8: a CTA (eight strips) per row,
+  // a batch's k CTAs one cluster
+  constexpr int kClParts = kFuThreads / 32;
+  const bool cluster = (!fused || (dbg.flags & kFlagCluster)) && !(dbg.flags & (kFlagNoFused | kFlagNoCluster)) &&
+                       k <= kFuMaxK && (k & (k - 1)) == 0 && (fu_ns + kClParts - 1) / kClParts <= kFuMaxStages;
+  if (fused || cluster) {
     if (!fused_configured(di)) return cuda_fail(cudaErrorUnknown);
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     StepParams p = {};
@@ -454,10 +461,15 @@ static ls_status beam_step_impl(const void* logits, ls_dtype logit_dtype, const 
     p.vocab = vocab;
     p.eos = eos_id;
     p.rows = (int)rows;
-    p.nc = fu_parts;                                       // strips per row, one warp each
-    p.stages = (int)((fu_ns + fu_parts - 1) / fu_parts);  // block-max rows per strip
+    const int parts = cluster ? kClParts : fu_parts;
+    p.nc = parts;                                    // strips per row, one warp each
+    p.stages = (int)((fu_ns + parts - 1) / parts);  // block-max rows per strip
     p.flags = dbg.flags;
     p.spin_limit_ns = dbg.spin_ns;
+    if (cluster) {
+      const cudaError_t e = launch_beam_cluster(p, dtype, static_cast<cudaStream_t>(stream));
+      return e == cudaSuccess ? LS_OK : cuda_fail(e);
+    }
     if (rf && (dbg.flags & kFlagFusedRefresh)) {
       // the batch's refresh in K3: bulk copies of 16-byte aligned slabs through two buffers
       // per warp; a tile of a slab (positions) per parent, or several heads' whole slabs

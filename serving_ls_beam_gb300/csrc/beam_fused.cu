@@ -33,6 +33,8 @@
 //  * More than kFuList candidates in a strip, more than kFuCap keys (ties), or the forced
 //    exact mode send the batch to an exact path: a radix select of every beam's top-k over
 //    its logits.
+#include <cooperative_groups.h>
+
 #include "ls_device.cuh"
 #include "ls_draw.cuh"
 #include "ls_dtype.cuh"
@@ -77,6 +79,11 @@ struct __align__(16) FuSmem {
   float tx[kFuSampRows][kFuMaxK];
   int tv[kFuSampRows][kFuMaxK];
   int spath[kFuSampRows];
+  // the cluster step: this CTA's row's top k keys (best first), their count, the row's path,
+  // and on the batch's first CTA the gathered rows' offsets and the batch's path
+  Key tk[kFuMaxK];
+  int ntk, cpath, gpath;
+  int goff[kFuMaxK];
 };
 
 }  // namespace
@@ -299,8 +306,14 @@ __device__ void refresh_batch(const StepParams& p, FuSmem& sm, unsigned char* wb
   bulk_wait_all();
 }
 
-template <int DT, bool BIAS, int VPL, bool SAMP>
+// Modes of the kernel: the batch step (one CTA per batch), the sampler (kFuSampRows rows per
+// CTA), and the cluster step (one CTA per row, a batch's k CTAs a thread-block cluster).
+enum { kModeBatch = 0, kModeSample = 1, kModeCluster = 2 };
+
+template <int DT, bool BIAS, int VPL, int MODE>
 __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepParams p) {
+  constexpr bool SAMP = MODE == kModeSample;
+  constexpr bool CL = MODE == kModeCluster;
   constexpr int VEC = Traits<DT>::kVec;
   constexpr int ES = Traits<DT>::kBytes;
   constexpr int CV = 32 * VPL;                       // vectors per stage
@@ -309,10 +322,13 @@ __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepPar
   __shared__ FuSmem sm;
   extern __shared__ __align__(128) unsigned char fu_dyn[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int b = blockIdx.x;
   const int K = p.k, V = p.vocab, W = p.nc;  // W strips per row, one warp per strip
-  // rows per CTA: the batch's k beams, or kFuSampRows independent rows for the sampler
-  const int NR = SAMP ? kFuSampRows : K;
+  // rows per CTA: the batch's k beams, kFuSampRows independent rows for the sampler, or one
+  // beam of the batch in the cluster step (its rank in the cluster)
+  const int NR = SAMP ? kFuSampRows : (CL ? 1 : K);
+  const int crank = CL ? (int)cooperative_groups::this_cluster().block_rank() : 0;
+  const int b = CL ? (int)blockIdx.x / K : (int)blockIdx.x;  // the batch (the row group when SAMP)
+  const int jb = CL ? crank : 0;                            // the batch row of this CTA's first row
   const int SPS = p.stages;                  // block-max rows kept per strip
   unsigned char* ring = fu_dyn + (size_t)warp * kFuRing * CV * 16;
   float* bmax = reinterpret_cast<float*>(fu_dyn + (size_t)kFuWarps * kFuRing * CV * 16);
@@ -347,7 +363,8 @@ __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepPar
   }
   __syncthreads();
 
-  // Geometry of row j: 16-byte aligned vectors covering it, stages of CV vectors.
+  // Geometry of row j (the row's index in the batch, or in the CTA's group for the sampler):
+  // 16-byte aligned vectors covering it, stages of CV vectors.
   struct RowGeo {
     const uint4* rb;  // first vector (16-byte aligned, may start before the row)
     int lead;         // bytes of that vector before the row
@@ -355,7 +372,7 @@ __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepPar
   };
   auto geo = [&](int j) -> RowGeo {
     RowGeo g;
-    const unsigned char* rowp = logits + ((size_t)b * NR + j) * row_bytes;
+    const unsigned char* rowp = logits + (SAMP ? (size_t)b * NR + j : (size_t)b * K + j) * row_bytes;
     g.lead = (int)(reinterpret_cast<uintptr_t>(rowp) & 15);
     g.rb = reinterpret_cast<const uint4*>(rowp - g.lead);
     g.nv = (g.lead + row_bytes + 15) >> 4;
@@ -422,7 +439,7 @@ __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepPar
   // warp u streams strip s = u mod W of row j = u / W: stages s, s + W, ...
   const int nunits = NR * W;
   if (warp < nunits) {
-    const int u = warp, j = u / W, s = u - j * W;
+    const int u = warp, j = u / W + jb, s = u - (j - jb) * W;  // j: the row's index in the batch
     float ml = -INFINITY;  // lane's running max
     float cl = 0.0f;       // the lane's sum is sl = sum of 2^(x log2e + cl), cl = -ml log2e rounded
     float sl = 0.0f;
@@ -744,8 +761,8 @@ __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepPar
   // bounds (each is at most the row's k-th largest) -- and appends the row's keys: the strips'
   // candidates at or above R, rescored as beam_score + x - lse; a finished beam offers
   // (eos_id, beam score), a beam with no finite score k tokens
-  if (warp < K) {
-    const int j = warp, u0 = j * W;
+  if (warp < NR) {
+    const int j = jb + warp, u0 = warp * W;  // j: the row's index in the batch
     const float mu = lane < W ? sm.um[u0 + lane] : -INFINITY;
     float M = mu;
 #pragma unroll
@@ -797,7 +814,8 @@ __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepPar
     __syncthreads();
     if (tid == 0) sm.nkeys = 0;
     __syncthreads();
-    for (int j = 0; j < K; ++j) {
+    for (int jl = 0; jl < NR; ++jl) {
+      const int j = jb + jl;
       const int kind = sm.kind[j];
       if (kind == FROW_LIVE) {
         exact_row<DT, BIAS>(p, sm, (long long)b * K + j, j);
@@ -810,17 +828,59 @@ __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepPar
       }
     }
   }
-  rank_and_write(p, sm, b);
-  if (tid < K) {
-    RowStat st;
-    st.lse = sm.lse[tid];
-    st.rtopk = sm.R[tid];
-    st.ncand = path != 0 ? -1 : sm.ncand[tid];
-    st.pad = 0;
-    p.rowstat[b * K + tid] = st;
+  if constexpr (CL) {
+    // this row's top k keys, best first (the batch's top k holds no other key of the row)
+    const int n = min(sm.nkeys, kFuCap);
+    for (int i = tid; i < n; i += kFuThreads) {
+      const Key ki = sm.keys[i];
+      int r0 = 0;
+      for (int q = 0; q < n; ++q) r0 += key_less(sm.keys[q], ki);
+      if (r0 < K) sm.tk[r0] = ki;
+    }
+    if (tid == 0) {
+      sm.ntk = min(n, K);
+      sm.cpath = path;
+    }
+    cooperative_groups::cluster_group cl = cooperative_groups::this_cluster();
+    cl.sync();  // every row of the batch has its top k
+    if (crank == 0) {
+      // the batch's first CTA gathers the rows' top k (distributed shared memory) and ranks them
+      if (tid == 0) {
+        int off = 0, pm = 0;
+        for (int r = 0; r < K; ++r) {
+          const FuSmem* ps = cl.map_shared_rank(&sm, (unsigned)r);
+          sm.goff[r] = off;
+          off += ps->ntk;
+          pm = max(pm, ps->cpath);
+        }
+        sm.nkeys = off;
+        sm.gpath = pm;
+      }
+      __syncthreads();
+      for (int idx = tid; idx < K * K; idx += kFuThreads) {
+        const int r = idx / K, i = idx - r * K;
+        const FuSmem* ps = cl.map_shared_rank(&sm, (unsigned)r);
+        if (i < ps->ntk) sm.keys[sm.goff[r] + i] = ps->tk[i];
+      }
+      __syncthreads();
+      rank_and_write(p, sm, b);
+      if (tid == 0) p.bstat[b] = sm.gpath;
+    }
+    cl.sync();  // a row's shared memory stays until the gather has read it
+  } else {
+    rank_and_write(p, sm, b);
+    if (tid == 0) p.bstat[b] = path;
   }
-  if (tid == 0) p.bstat[b] = path;
-  if (p.rf_cache) {
+  if (tid < NR) {
+    const int j = jb + tid;
+    RowStat st;
+    st.lse = sm.lse[j];
+    st.rtopk = sm.R[j];
+    st.ncand = path != 0 ? -1 : sm.ncand[j];
+    st.pad = 0;
+    p.rowstat[b * K + j] = st;
+  }
+  if (!CL && p.rf_cache) {
     // every thread's reads of the keys and the rings are done before they become buffers of
     // bulk copies (the async proxy)
     __syncthreads();
@@ -830,21 +890,38 @@ __global__ void __launch_bounds__(kFuThreads, 2) beam_fused_kernel(const StepPar
   }
 }
 
-template <int DT, bool BIAS, int VPL, bool SAMP>
+template <int DT, bool BIAS, int VPL, int MODE>
 cudaError_t launch_t(const StepParams& p, cudaStream_t stream) {
-  const unsigned grid = SAMP ? (unsigned)((p.rows + kFuSampRows - 1) / kFuSampRows) : (unsigned)p.batch;
+  const unsigned grid = MODE == kModeSample    ? (unsigned)((p.rows + kFuSampRows - 1) / kFuSampRows)
+                        : MODE == kModeCluster ? (unsigned)p.batch * (unsigned)p.k
+                                               : (unsigned)p.batch;
   PdlLaunch l(dim3(grid), dim3(kFuThreads), beam_fused_smem_bytes(VPL, p.stages), stream);
-  return cudaLaunchKernelEx(&l.cfg, beam_fused_kernel<DT, BIAS, VPL, SAMP>, p);
+  cudaLaunchAttribute attr[2];
+  if (MODE == kModeCluster) {
+    // a batch's k CTAs form one cluster (k a power of two up to 8)
+    attr[0] = l.attr[0];
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)p.k;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    l.cfg.attrs = attr;
+    l.cfg.numAttrs = 2;
+  }
+  return cudaLaunchKernelEx(&l.cfg, beam_fused_kernel<DT, BIAS, VPL, MODE>, p);
 }
 
 template <int DT, bool BIAS, int VPL>
 cudaError_t config_t() {
-  cudaError_t e = cudaFuncSetAttribute(beam_fused_kernel<DT, BIAS, VPL, false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)beam_fused_smem_bytes(VPL, kFuMaxStages));
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(beam_fused_kernel<DT, BIAS, VPL, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)beam_fused_smem_bytes(VPL, kFuMaxStages));
+  const int smem = (int)beam_fused_smem_bytes(VPL, kFuMaxStages);
+  cudaError_t e = cudaFuncSetAttribute(beam_fused_kernel<DT, BIAS, VPL, kModeBatch>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(beam_fused_kernel<DT, BIAS, VPL, kModeSample>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(beam_fused_kernel<DT, BIAS, VPL, kModeCluster>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  return e;
 }
 
 }  // namespace
@@ -864,26 +941,30 @@ int beam_fused_refresh_buffer(int dtype, bool bias) {
   return kFuRing * 32 * vpl * 16 / 2;
 }
 
-template <bool SAMP>
+template <int MODE>
 cudaError_t launch_any(const StepParams& p, int dtype, cudaStream_t stream) {
   const bool bias = p.bias != nullptr;
   switch (dtype) {
     case DT_F32:
-      return bias ? launch_t<DT_F32, true, 4, SAMP>(p, stream) : launch_t<DT_F32, false, 4, SAMP>(p, stream);
+      return bias ? launch_t<DT_F32, true, 4, MODE>(p, stream) : launch_t<DT_F32, false, 4, MODE>(p, stream);
     case DT_F16:
-      return bias ? launch_t<DT_F16, true, 4, SAMP>(p, stream) : launch_t<DT_F16, false, 8, SAMP>(p, stream);
+      return bias ? launch_t<DT_F16, true, 4, MODE>(p, stream) : launch_t<DT_F16, false, 8, MODE>(p, stream);
     case DT_BF16:
-      return bias ? launch_t<DT_BF16, true, 4, SAMP>(p, stream) : launch_t<DT_BF16, false, 8, SAMP>(p, stream);
+      return bias ? launch_t<DT_BF16, true, 4, MODE>(p, stream) : launch_t<DT_BF16, false, 8, MODE>(p, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
 cudaError_t launch_beam_fused(const StepParams& p, int dtype, cudaStream_t stream) {
-  return launch_any<false>(p, dtype, stream);
+  return launch_any<kModeBatch>(p, dtype, stream);
 }
 
 cudaError_t launch_sample_fused(const StepParams& p, int dtype, cudaStream_t stream) {
-  return launch_any<true>(p, dtype, stream);
+  return launch_any<kModeSample>(p, dtype, stream);
+}
+
+cudaError_t launch_beam_cluster(const StepParams& p, int dtype, cudaStream_t stream) {
+  return launch_any<kModeCluster>(p, dtype, stream);
 }
 
 }  // namespace lsb

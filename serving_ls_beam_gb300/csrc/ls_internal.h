@@ -73,6 +73,8 @@ constexpr int kFlagFusedRefresh = 128;  // ls_beam_step_refresh_inplace in one k
 constexpr int kFlagChunkRows = 4;     // the beam step's first kernel by fixed-size chunks (K1)
 constexpr int kFlagNoFused = 8;       // the beam step as two kernels even where K3 applies
 constexpr int kFlagFused = 16;        // the beam step as K3 wherever k allows
+constexpr int kFlagNoCluster = 256;   // no cluster form of K3 for small batches (K1s and K2 there)
+constexpr int kFlagCluster = 512;     // the cluster form of K3 wherever k allows, whatever the batch
 
 // ---------------------------------------------------------------- workspace layout
 struct alignas(16) RowStat {
@@ -303,6 +305,9 @@ cudaError_t beam_fused_config();  // once per device: the kernels' dynamic share
 cudaError_t launch_beam_fused(const StepParams& p, int dtype, cudaStream_t stream);
 // the one-kernel sampler: ceil(rows / kFuSampRows) CTAs
 cudaError_t launch_sample_fused(const StepParams& p, int dtype, cudaStream_t stream);
+// the cluster step: one CTA per row (p.nc = 8 strips), a batch's k CTAs one cluster; k a
+// power of two up to kFuMaxK
+cudaError_t launch_beam_cluster(const StepParams& p, int dtype, cudaStream_t stream);
 // bytes of one of a warp's two refresh buffers in K3 for these logits (its VPL)
 int beam_fused_refresh_buffer(int dtype, bool bias);
 size_t beam_strips_smem_bytes(int vpl, int stages);

@@ -26,8 +26,9 @@ import serving_ls_beam_gb300 as lsb  # noqa: E402
 
 TORCH_DT = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
 
-# LS_BEAM_DEBUG settings of the implementations every test runs under
-IMPLS = {"plan": "", "onekernel": "fused", "twokernel": "nofused"}
+# LS_BEAM_DEBUG settings of the implementations every test runs under: the plan's choice, K3
+# (a CTA per batch), K3's cluster form (a CTA per row, a cluster per batch), K1s then K2
+IMPLS = {"plan": "", "onekernel": "fused", "cluster": "cluster", "twokernel": "nofused"}
 _impl_env = {"value": ""}
 
 
