@@ -318,7 +318,7 @@ def moved_rows(par: np.ndarray, K: int) -> np.ndarray:
 
 def bench_kernel(args, w: synth.Workload):
     """Profiling driver: one kernel of the decode loop, alone, at the workload's last three decode
-    steps.  It walks the search's own trajectory with one step's logits on the device at a time
+    steps (with --decode-steps N, steps N-2..N).  It walks the search's own trajectory with one step's logits on the device at a time
     (beam state carried from step to step as in the benchmark loop, so the parents are the loop's),
     then launches the kernel on those three steps: the beam step on their logits (3 x 82 MB at c5),
     the cache refresh at len = step on one seeded cache (in place, 805 MB) or two (out of place,
@@ -340,7 +340,7 @@ def bench_kernel(args, w: synth.Workload):
     B, K, V = w.batch, w.k, w.vocab
     es = 2 if w.dtype in ("f16", "bf16") else 4
     multi = w.steps > 1
-    last = w.steps if multi else 0
+    last = (min(w.steps, args.decode_steps) if args.decode_steps > 0 else w.steps) if multi else 0
     steps = list(range(max(1 if multi else 0, last - 2), last + 1))
     ws = torch.empty(lsb.ls_beam_step_workspace_size(B, K, V), dtype=torch.uint8, device=dev)
     lsb.check(lsb.ls_workspace_init(ws))

@@ -160,8 +160,11 @@ LS_API ls_status ls_cache_reorder(const void* src, void* dst, ls_dtype dtype, co
  * cache [layers, batch*k, heads, max_len, head_dim] of dtype, device; parent [batch, k]
  * int32 in [0, k), device; k <= LS_MAX_K.  An out-of-range parent leaves that row as it is
  * and, when `workspace` is not NULL, sets LS_ERR_INTERNAL in its status word.  workspace:
- * NULL or a workspace initialised by ls_workspace_init (only its status word is used).
- * len == 0 or an empty shape is a no-op.  Nothing is allocated.
+ * NULL or a workspace initialised by ls_workspace_init.  Of it the call uses the status word
+ * and, for the bulk-copy kernel, a work counter in bytes 64-71 from which its CTAs take their
+ * items; each launch leaves the counter at zero, so calls that share a workspace must be
+ * ordered (one stream, or events).  Without a workspace each CTA takes a fixed share of the
+ * items.  len == 0 or an empty shape is a no-op.  Nothing is allocated.
  */
 LS_API ls_status ls_cache_refresh_inplace(void* cache, ls_dtype dtype, const int32_t* parent, int layers,
                                           int batch, int k, int heads, int max_len, int len, int head_dim,

@@ -54,8 +54,9 @@ struct Debug {
   bool check_ptrs = true;
 };
 
-// LS_BEAM_DEBUG: comma-separated "exact", "ipplain", "iptma", "ipwords", "steprefresh", "chunk", "strips", "fused",
-// "nofused", "cluster", "nocluster", "spin=<ns>", "vpl=<4|8|16>", "stages=<2..8>", "parts=<n>", "ipw=<words>", "stage=<0|1>", "nocheck".
+// LS_BEAM_DEBUG: comma-separated "exact", "ipplain", "iptma", "ipwords", "ipstatic", "steprefresh", "chunk", "strips",
+// "fused", "nofused", "cluster", "nocluster", "spin=<ns>", "vpl=<4|8|16>", "stages=<2..8>", "parts=<n>", "ipw=<words>",
+// "stage=<0|1>", "nocheck".
 Debug read_debug() {
   Debug d;
   const char* env = std::getenv("LS_BEAM_DEBUG");
@@ -67,6 +68,7 @@ Debug read_debug() {
     if (!std::strcmp(tok, "exact")) d.flags |= kFlagForceExact;
     else if (!std::strcmp(tok, "ipplain")) d.flags |= kFlagPlainInplace;
     else if (!std::strcmp(tok, "iptma")) d.flags |= kFlagTmaInplace;
+    else if (!std::strcmp(tok, "ipstatic")) d.flags |= kFlagStaticItems;
     else if (!std::strcmp(tok, "ipwords")) d.flags |= kFlagWordInplace;
     else if (!std::strcmp(tok, "steprefresh")) d.flags |= kFlagFusedRefresh;
     else if (!std::strncmp(tok, "spin=", 5)) d.spin_ns = std::atoll(tok + 5);
@@ -771,6 +773,7 @@ ls_status ls_cache_refresh_inplace(void* cache, ls_dtype dtype, const int32_t* p
   p.cache = static_cast<unsigned char*>(cache);
   p.parent = parent;
   p.status = workspace ? reinterpret_cast<uint32_t*>(workspace) : nullptr;
+  p.work = nullptr;
   p.spin_limit_ns = dbg.spin_ns;
   p.layer_stride = layer_stride;
   p.row_stride = row_stride;
@@ -825,6 +828,9 @@ ls_status ls_cache_refresh_inplace(void* cache, ls_dtype dtype, const int32_t* p
                               : units;
   const long long grid_full = (long long)di->sms * occ;
   const long long grid = items < grid_full ? items : grid_full;
+  // with a workspace, the bulk-copy kernel's CTAs take items from a counter in it
+  if (tma && workspace && items < (1ll << 31) && !(dbg.flags & kFlagStaticItems))
+    p.work = reinterpret_cast<uint32_t*>(static_cast<unsigned char*>(workspace) + kIpWorkOff);
   const cudaError_t e = tma ? launch_cache_inplace_tma(p, (int)grid, st) : launch_cache_inplace(p, unit, (int)grid, st);
   return e == cudaSuccess ? LS_OK : cuda_fail(e);
 }

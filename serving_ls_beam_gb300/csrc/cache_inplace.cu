@@ -143,7 +143,11 @@ __global__ void __launch_bounds__(kIpThreads) cache_inplace_kernel(const Inplace
 // lanes load the batches' parents into shared memory, after which lane 0 alone runs a
 // two-stage pipeline over its (layer, batch, head, tile) items: the bulk loads of the slabs
 // item i needs are issued before the bulk stores of item i-1's changed rows, so a copy in
-// each direction is always in flight.  Requires 16-byte aligned slabs and tiles.
+// each direction is always in flight.  Items differ in size (the rows a batch changes), so
+// with a work counter (p.work) a CTA takes its next item when it is ready for one: the CTAs
+// then finish together instead of with the sum of their items' sizes.  The last CTA to finish
+// sets the counter back to zero for the next launch.  Requires 16-byte aligned slabs and
+// tiles.
 __global__ void __launch_bounds__(32) cache_inplace_tma_kernel(const InplaceParams p) {
   extern __shared__ __align__(128) unsigned char tsm[];
   __shared__ __align__(8) unsigned long long bar[2];
@@ -193,9 +197,18 @@ __global__ void __launch_bounds__(32) cache_inplace_tma_kernel(const InplacePara
     bulk_commit();
   };
 
-  for (long long it = blockIdx.x; it < (long long)p.layers * bg * ntiles && !aborted; it += gridDim.x) {
-    const long long unit = it / ntiles;
-    const long long tile = it - unit * ntiles;
+  const long long total = (long long)p.layers * bg * ntiles;
+  uint32_t* const work = p.work;  // null: CTA c takes items c, c + grid, c + 2 grid, ...
+  // the item after the current one, asked for one item ahead so that the atomic's latency
+  // is hidden behind the current item's copies
+  long long it = blockIdx.x;
+  long long nxt = work ? (long long)gridDim.x + atomicAdd(work, 1u) : it + gridDim.x;
+  while (it < total && !aborted) {
+    const long long item = it;
+    it = nxt;
+    if (it < total) nxt = work ? (long long)gridDim.x + atomicAdd(work, 1u) : it + gridDim.x;
+    const long long unit = item / ntiles;
+    const long long tile = item - unit * ntiles;
     const int l = (int)(unit / bg);
     const long long rem = unit - (long long)l * bg;
     const int b = (int)(rem / groups);
@@ -251,6 +264,14 @@ __global__ void __launch_bounds__(32) cache_inplace_tma_kernel(const InplacePara
   }
   bulk_wait_all();
   if (bad && p.status) atomicOr(p.status, kDevBadParent);
+  if (work) {
+    // every CTA has taken its last item once all have counted themselves out here
+    __threadfence();
+    if (atomicAdd(work + 1, 1u) == gridDim.x - 1u) {
+      work[0] = 0u;
+      work[1] = 0u;
+    }
+  }
 }
 
 // The same refresh by plain word copies, for k <= KT: a warp takes an item (heads

@@ -74,6 +74,7 @@ constexpr int kFlagChunkRows = 4;     // the beam step's first kernel by fixed-s
 constexpr int kFlagNoFused = 8;       // the beam step as two kernels even where K3 applies
 constexpr int kFlagFused = 16;        // the beam step as K3 wherever k allows
 constexpr int kFlagNoCluster = 256;   // no cluster form of K3 for small batches (K1s and K2 there)
+constexpr int kFlagStaticItems = 2048;  // the bulk-copy refresh without its work counter
 constexpr int kFlagCluster = 512;     // the cluster form of K3 wherever k allows, whatever the batch
 
 // ---------------------------------------------------------------- workspace layout
@@ -249,6 +250,7 @@ struct SampleParams {
 // stage of the bulk-copy kernel (two stages), and the parents the bulk-copy kernel stages.
 constexpr int kIpStageBytes = 48 * 1024;
 constexpr int kIpTmaStage = 32 * 1024;
+constexpr int kIpWorkOff = 64;  // byte offset of the bulk-copy kernel's work counter in a workspace
 constexpr int kIpTmaMaxParents = 8192;
 
 struct InplaceParams {
@@ -258,6 +260,7 @@ struct InplaceParams {
   long long spin_limit_ns;  // bounded waits of the bulk-copy kernel
   long long layer_stride, row_stride, slab_stride;  // bytes
   long long slab_bytes;   // len * head_dim * es
+  uint32_t* work;         // bulk-copy kernel: {next item, CTAs done}, zero between launches; or null
   int tile_bytes;         // positions staged at a time, in bytes (<= stage / k)
   int heads_per_item;     // bulk-copy kernel: heads of one (layer, batch) moved together
   int batch, k, heads, layers;

@@ -68,9 +68,9 @@ CASES = [  # (dtype, layers, batch, k, heads, max_len, len, head_dim)
 ]
 
 # LS_BEAM_DEBUG settings of the implementations: the plan's choice (the word kernel for short
-# slabs and k <= 8, bulk copies otherwise), the word kernel, bulk copies and the staged CTA
-# kernel forced
-IMPLS = [None, "ipwords", "iptma", "ipplain"]
+# slabs and k <= 8, bulk copies otherwise), the word kernel, bulk copies (with a workspace,
+# also with a fixed share of items per CTA) and the staged CTA kernel forced
+IMPLS = [None, "ipwords", "iptma", "iptma,ipstatic", "ipplain"]
 
 
 def _with_env(env, fn):
@@ -89,21 +89,34 @@ def _with_env(env, fn):
                 os.environ["LS_BEAM_DEBUG"] = old
 
 
+@pytest.mark.parametrize("with_ws", [False, True])
 @pytest.mark.parametrize("env", IMPLS)
 @pytest.mark.parametrize("case", CASES)
-def test_inplace_matches_oracle(dev, oracle_mod, case, env):
+def test_inplace_matches_oracle(dev, oracle_mod, case, env, with_ws):
+    """Bitwise against the oracle.  With a workspace the bulk-copy kernel's CTAs take items from
+    a counter in it (twice in a row here, so the second call starts from the counter the first
+    left); without one each CTA takes a fixed share."""
     dtype, layers, batch, k, heads, max_len, length, head_dim = case
     g = np.random.default_rng(CASES.index(case))
     shape = (layers, batch * k, heads, max_len, head_dim)
     cache = _cache(g, shape, dtype)
     parent = _parents(g, batch, k)
+    parent2 = _parents(g, batch, k)
     t = _to_dev(cache, dtype, dev)
-    _with_env(env, lambda: lsb.check(lsb.ls_cache_refresh_inplace(t, torch.from_numpy(parent).to(dev), length),
-                                     "ls_cache_refresh_inplace"))
-    want = oracle_mod.cache_refresh_inplace(cache, parent, length)
+    ws = None
+    if with_ws:
+        ws = torch.empty(lsb.ls_beam_step_workspace_size(1, 1, 1), dtype=torch.uint8, device=dev)
+        lsb.check(lsb.ls_workspace_init(ws))
+    for par in (parent, parent2):
+        _with_env(env, lambda: lsb.check(lsb.ls_cache_refresh_inplace(t, torch.from_numpy(par).to(dev), length, ws),
+                                         "ls_cache_refresh_inplace"))
+    want = oracle_mod.cache_refresh_inplace(oracle_mod.cache_refresh_inplace(cache, parent, length), parent2, length)
     got = _bits(t, dtype)
     exp = want.view(got.dtype) if want.dtype != got.dtype else want
     assert np.array_equal(got, exp)
+    if with_ws:
+        assert lsb.ls_read_status(ws) == lsb.LS_OK
+        assert (ws[:256].cpu().numpy() == 0).all()  # the status word and the work counter are back to zero
 
 
 @pytest.mark.parametrize("env", IMPLS)
