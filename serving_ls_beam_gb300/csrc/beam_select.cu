@@ -34,7 +34,7 @@ constexpr int kPairTile = 1024;  // (beam, chunk) pairs whose slot counts are sc
 
 struct __align__(16) SelSmem {
   unsigned long long sbar;  // completion of the slot staging copy
-  int nsel, big, ovf, nbest, nrl, ptotal;
+  int nsel, big, ovf, nbest, nrl, ptotal, ecnt;
   int pc[kPairTile];   // slots to read per pair of the tile, then their exclusive prefix sums
   float pm[kPairTile];  // chunk max of each (beam, chunk) pair (first tile only)
   int pn[kPairTile];    // survivor count of each pair (first tile only)
@@ -151,17 +151,30 @@ __device__ void merge_into_best(SelSmem& sm, int K) {
   __syncthreads();
 }
 
-// Exact fine rank of batch b without the candidate queue: per live beam, a radix select
-// of its top-K logits (order: larger x first, then smaller token id), merged across beams.
-// Without logits (p.logits null: the chunk records and slots came from the projection's
-// epilogue, whose chunks keep every candidate at or above their bound, or else their own
-// top-K, in token order) the select runs over the beam's slots instead of its row.
+// Exact fine rank of batch b without the candidate queue: per live beam its top-K entries
+// (order: larger x first, then smaller token id), merged across beams.
+//  1. One pass over the beam's source keeps the entries x >= R (the beam's R-top-k, never
+//     above its K-th largest, so its top-K are among them) in a shared-memory list.  The
+//     source is the beam's slots when they hold every entry at or above R -- the queue only
+//     outgrew the fine rank (path 3), or there are no logits (the projection's epilogue wrote
+//     the slots) -- and its row otherwise (a chunk's slots overflowed, or the exact path is
+//     forced), read in 16-byte vectors.
+//  2. The top-K of that list: by counting ranks when it is short, else by a radix select of
+//     the K-th largest order key over it; entries equal to that key are taken by smallest
+//     token.  A list longer than the buffer (massive ties at R) falls back to the radix
+//     select over the whole source, in token order.
+constexpr int kExactBuf = 4096;  // entries (x, token) of a beam's list in dynamic shared memory
+constexpr int kExactRankMax = 256;  // lists up to this long are ranked by counting
+
 template <int DT, bool BIAS>
-__device__ void exact_select(const StepParams& p, SelSmem& sm, int b, int path) {
+__device__ void exact_select(const StepParams& p, SelSmem& sm, int b, int path, float2* buf) {
   constexpr int ES = Traits<DT>::kBytes;
+  constexpr int VEC = Traits<DT>::kVec;
+  constexpr int NT = kSelThreads;
   const int K = p.k, V = p.vocab, C = p.slot_cap, nc = p.nc;
-  const bool from_slots = p.logits == nullptr;
+  const bool from_slots = p.logits == nullptr || path == 3;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const unsigned lt_mask = (1u << lane) - 1u;
   if (tid == 0) {
     sm.nbest = 0;
     sm.nrl = 0;
@@ -180,17 +193,16 @@ __device__ void exact_select(const StepParams& p, SelSmem& sm, int b, int path) 
       continue;
     }
     if (rs.kind == ROW_DEAD) {
-      for (int v = tid; v < K; v += kSelThreads) sm.rl[v] = make_key(-INFINITY, j, 0.0f, v);
+      for (int v = tid; v < K; v += NT) sm.rl[v] = make_key(-INFINITY, j, 0.0f, v);
       if (tid == 0) sm.nrl = K;
       __syncthreads();
       merge_into_best(sm, K);
       continue;
     }
-    const unsigned char* rowp =
-        from_slots ? nullptr : static_cast<const unsigned char*>(p.logits) + (size_t)row * V * ES;
+    const unsigned char* rowp = p.logits ? static_cast<const unsigned char*>(p.logits) + (size_t)row * V * ES : nullptr;
     const long long u0 = (long long)row * nc;
     const int n_src = from_slots ? nc * C : V;
-    // element i of the beam's source, in token order: (x, token), or false when i is empty
+    // entry i of the beam's source, in token order: (x, token), or false when i is empty
     auto src = [&](int i, float& x, int& v) -> bool {
       if (from_slots) {
         const int c = i / C, sl = i - c * C;
@@ -205,79 +217,184 @@ __device__ void exact_select(const StepParams& p, SelSmem& sm, int b, int path) 
       v = i;
       return true;
     };
-    // radix select of the K-th largest order key, 8 bits at a time from the top
-    if (tid == 0) {
-      sm.prefix = 0;
-      sm.pmask = 0;
-      sm.need = K;
+    // 1. the entries at or above R, appended a warp at a time
+    const float R = rs.rtopk;
+    if (tid == 0) sm.ecnt = 0;
+    __syncthreads();
+    auto append = [&](bool take, float x, int v) {
+      const unsigned m = __ballot_sync(0xffffffffu, take);
+      if (m == 0u) return;
+      int base = 0;
+      if (lane == 0) base = atomicAdd(&sm.ecnt, __popc(m));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      const int pos = base + __popc(m & lt_mask);
+      if (take && pos < kExactBuf) buf[pos] = make_float2(x, __int_as_float(v));
+    };
+    if (from_slots) {
+      for (int i0 = warp * 32; i0 < n_src; i0 += NT) {
+        float x = 0.0f;
+        int v = 0;
+        const int i = i0 + lane;
+        const bool take = i < n_src && src(i, x, v) && x >= R;
+        append(take, x, v);
+      }
+    } else {
+      // 16-byte vectors covering the row (the first may start before it, the last end after
+      // it), four per thread in flight
+      const int lead = (int)(reinterpret_cast<uintptr_t>(rowp) & 15);
+      const uint4* rb = reinterpret_cast<const uint4*>(rowp - lead);
+      const int row_bytes = V * ES;
+      const int nv = (lead + row_bytes + 15) >> 4;
+      for (int v0 = warp * 128; v0 < nv; v0 += NT * 4) {
+        uint4 d[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int jv = v0 + 32 * r + lane;
+          d[r] = jv < nv ? __ldcs(rb + jv) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int jv = v0 + 32 * r + lane;
+          float xs[VEC];
+          unpack<DT>(d[r], xs);
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) {
+            const int byte = jv * 16 + e * ES - lead;
+            const bool in = jv < nv && byte >= 0 && byte < row_bytes;
+            const int v = byte / ES;
+            float x = xs[e];
+            if constexpr (BIAS) x += in ? __ldg(p.bias + v) : 0.0f;
+            append(in && x >= R, x, v);
+          }
+        }
+      }
     }
     __syncthreads();
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int i = tid; i < 256; i += kSelThreads) sm.hist[i] = 0;
+    const int n = sm.ecnt;
+    if (tid == 0) sm.nrl = 0;
+    __syncthreads();
+    if (n <= kExactRankMax) {
+      // 2a. short list: each entry's rank among the others
+      for (int i = tid; i < n; i += NT) {
+        const float2 ei = buf[i];
+        const int vi = __float_as_int(ei.y);
+        int rank = 0;
+        for (int q = 0; q < n; ++q) {
+          const float2 eq = buf[q];
+          const int vq = __float_as_int(eq.y);
+          rank += (eq.x > ei.x) | ((eq.x == ei.x) & (vq < vi));
+        }
+        if (rank < K) sm.rl[rank] = make_key(score_of(rs.c, ei.x), j, ei.x, vi);
+      }
+      if (tid == 0) sm.nrl = n < K ? n : K;
+    } else {
+      // 2b. radix select of the K-th largest order key, 8 bits at a time from the top, over
+      // the list (n <= kExactBuf) or, when it overflowed, over the whole source
+      const bool over_buf = n <= kExactBuf;
+      const int n_sel = over_buf ? n : n_src;
+      auto entry = [&](int i, float& x, int& v) -> bool {
+        if (over_buf) {
+          const float2 e = buf[i];
+          x = e.x;
+          v = __float_as_int(e.y);
+          return true;
+        }
+        return src(i, x, v);
+      };
+      if (tid == 0) {
+        sm.prefix = 0;
+        sm.pmask = 0;
+        sm.need = K;
+      }
       __syncthreads();
-      const uint32_t prefix = sm.prefix, pmask = sm.pmask;
-      for (int i = tid; i < n_src; i += kSelThreads) {
+      for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int i = tid; i < 256; i += NT) sm.hist[i] = 0;
+        __syncthreads();
+        const uint32_t prefix = sm.prefix, pmask = sm.pmask;
+        for (int i = tid; i < n_sel; i += NT) {
+          float x;
+          int v;
+          if (!entry(i, x, v)) continue;
+          const uint32_t o = float_ord(x);
+          if ((o & pmask) == prefix) atomicAdd(&sm.hist[(o >> shift) & 255u], 1u);
+        }
+        __syncthreads();
+        if (tid == 0) {
+          const int need = sm.need;
+          unsigned int cum = 0;
+          int dgt = 255;
+          for (; dgt > 0; --dgt) {
+            if (cum + sm.hist[dgt] >= (unsigned)need) break;
+            cum += sm.hist[dgt];
+          }
+          sm.need = need - (int)cum;
+          sm.prefix = prefix | ((uint32_t)dgt << shift);
+          sm.pmask = pmask | (255u << shift);
+        }
+        __syncthreads();
+      }
+      const uint32_t tkey = sm.prefix;
+      const int need_eq = sm.need;  // entries equal to the threshold to take, smallest tokens first
+      for (int i = tid; i < n_sel; i += NT) {
         float x;
         int v;
-        if (!src(i, x, v)) continue;
-        const uint32_t o = float_ord(x);
-        if ((o & pmask) == prefix) atomicAdd(&sm.hist[(o >> shift) & 255u], 1u);
-      }
-      __syncthreads();
-      if (tid == 0) {
-        const int need = sm.need;
-        unsigned int cum = 0;
-        int dgt = 255;
-        for (; dgt > 0; --dgt) {
-          if (cum + sm.hist[dgt] >= (unsigned)need) break;
-          cum += sm.hist[dgt];
+        if (!entry(i, x, v)) continue;
+        if (float_ord(x) > tkey) {
+          const int pos = atomicAdd(&sm.nrl, 1);
+          if (pos < kMaxK) sm.rl[pos] = make_key(score_of(rs.c, x), j, x, v);
         }
-        sm.need = need - (int)cum;
-        sm.prefix = prefix | ((uint32_t)dgt << shift);
-        sm.pmask = pmask | (255u << shift);
       }
       __syncthreads();
-    }
-    const uint32_t tkey = sm.prefix;
-    const int need_eq = sm.need;  // elements equal to the threshold to take, in token order
-    for (int i = tid; i < n_src; i += kSelThreads) {
-      float x;
-      int v;
-      if (!src(i, x, v)) continue;
-      if (float_ord(x) > tkey) {
-        const int pos = atomicAdd(&sm.nrl, 1);
-        if (pos < kMaxK) sm.rl[pos] = make_key(score_of(rs.c, x), j, x, v);
+      if (over_buf) {
+        // the list is in no particular order: an equal entry is taken when fewer than need_eq
+        // equal entries have a smaller token
+        for (int i = tid; i < n_sel; i += NT) {
+          const float2 ei = buf[i];
+          if (float_ord(ei.x) != tkey) continue;
+          const int vi = __float_as_int(ei.y);
+          int before = 0;
+          for (int q = 0; q < n_sel; ++q) {
+            const float2 eq = buf[q];
+            before += (float_ord(eq.x) == tkey) & (__float_as_int(eq.y) < vi);
+          }
+          if (before < need_eq) {
+            const int pos = atomicAdd(&sm.nrl, 1);
+            if (pos < kMaxK) sm.rl[pos] = make_key(score_of(rs.c, ei.x), j, ei.x, vi);
+          }
+        }
+      } else {
+        // the source is in token order: the first need_eq equal entries
+        int taken = 0;
+        for (int base = 0; base < n_sel && taken < need_eq; base += NT) {
+          const int i = base + tid;
+          float x = 0.0f;
+          int v = 0;
+          bool eq = false;
+          if (i < n_sel && entry(i, x, v)) eq = float_ord(x) == tkey;
+          const unsigned ballot = __ballot_sync(0xffffffffu, eq);
+          if (lane == 0) sm.wc[warp] = __popc(ballot);
+          __syncthreads();
+          int before = 0, total = 0;
+          for (int w = 0; w < kSelWarps; ++w) {
+            before += (w < warp) ? sm.wc[w] : 0;
+            total += sm.wc[w];
+          }
+          const int off = taken + before + __popc(ballot & lt_mask);
+          if (eq && off < need_eq) {
+            const int pos = atomicAdd(&sm.nrl, 1);
+            if (pos < kMaxK) sm.rl[pos] = make_key(score_of(rs.c, x), j, x, v);
+          }
+          taken += total;
+          __syncthreads();
+        }
       }
-    }
-    __syncthreads();
-    int taken = 0;
-    for (int base = 0; base < n_src && taken < need_eq; base += kSelThreads) {
-      const int i = base + tid;
-      float x = 0.0f;
-      int v = 0;
-      bool eq = false;
-      if (i < n_src && src(i, x, v)) eq = float_ord(x) == tkey;
-      const unsigned ballot = __ballot_sync(0xffffffffu, eq);
-      if (lane == 0) sm.wc[warp] = __popc(ballot);
       __syncthreads();
-      int before = 0, total = 0;
-      for (int w = 0; w < kSelWarps; ++w) {
-        before += (w < warp) ? sm.wc[w] : 0;
-        total += sm.wc[w];
-      }
-      const int off = taken + before + __popc(ballot & ((1u << lane) - 1u));
-      if (eq && off < need_eq) {
-        const int pos = atomicAdd(&sm.nrl, 1);
-        if (pos < kMaxK) sm.rl[pos] = make_key(score_of(rs.c, x), j, x, v);
-      }
-      taken += total;
-      __syncthreads();
+      if (tid == 0 && sm.nrl > kMaxK) sm.nrl = kMaxK;  // greater + taken equal == K, cannot exceed
     }
-    if (tid == 0 && sm.nrl > kMaxK) sm.nrl = kMaxK;  // greater + ties == K, cannot exceed
     __syncthreads();
     merge_into_best(sm, K);
   }
-  for (int r = tid; r < K && r < sm.nbest; r += kSelThreads) write_output(p, sm, b, r, sm.best[r]);
+  for (int r = tid; r < K && r < sm.nbest; r += NT) write_output(p, sm, b, r, sm.best[r]);
   write_row_stats(p, sm, b, true);
   if (tid == 0) p.bstat[b] = path;
 }
@@ -584,7 +701,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) beam_select_kernel(const StepP
   __syncthreads();
   if (queue_path) {
     const int path = queue_select<DT, BIAS>(p, sm, sel_stage, b, false);
-    if (path > 0) exact_select<DT, BIAS>(p, sm, b, path);
+    if (path > 0) exact_select<DT, BIAS>(p, sm, b, path, reinterpret_cast<float2*>(sel_stage));
     return;
   }
   const bool keep_pairs = K * nc <= kPairTile;
@@ -832,7 +949,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) beam_select_kernel(const StepP
     if (sm.big) path = 3;
   }
   if (path != 0) {
-    exact_select<DT, BIAS>(p, sm, b, path);
+    exact_select<DT, BIAS>(p, sm, b, path, reinterpret_cast<float2*>(sel_stage));
     return;
   }
   // 3. rank of every survivor among the survivors; ranks 0..K-1 are the output
@@ -852,7 +969,9 @@ cudaError_t launch_t(const StepParams& p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.batch);
   cfg.blockDim = dim3(kSelThreads);
-  cfg.dynamicSmemBytes = (size_t)p.sel_stage_bytes;
+  // the slots' staging copy, or the exact path's list (the two are never in use at once)
+  const size_t list_bytes = kExactBuf * sizeof(float2);
+  cfg.dynamicSmemBytes = (size_t)p.sel_stage_bytes > list_bytes ? (size_t)p.sel_stage_bytes : list_bytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
