@@ -36,6 +36,36 @@ namespace lsb {
 namespace {
 
 constexpr long long kDrainLimitNs = 2000000000LL;  // 2 s for copies already in flight
+
+// Order keys of the values a stage compares, so that a threshold found by bisection converts
+// to the compared type exactly: the 16-bit patterns for packed 16-bit logits, the fp32
+// patterns otherwise (x = logit + bias in fp32).
+template <int DT, bool PACKED>
+struct OrderKey {
+  static __device__ __forceinline__ uint32_t of(float x) {
+    if constexpr (PACKED) {
+      uint32_t h;
+      if constexpr (DT == DT_F16)
+        h = __half_as_ushort(__float2half_rn(x));
+      else
+        h = __bfloat16_as_ushort(__float2bfloat16_rn(x));
+      return (h & 0x8000u) ? (~h & 0xffffu) : (h | 0x8000u);
+    } else {
+      return float_ord(x);
+    }
+  }
+  static __device__ __forceinline__ float val(uint32_t k) {
+    if constexpr (PACKED) {
+      const unsigned short h = (unsigned short)((k & 0x8000u) ? (k & 0x7fffu) : (~k & 0xffffu));
+      if constexpr (DT == DT_F16)
+        return __half2float(__ushort_as_half(h));
+      else
+        return __bfloat162float(__ushort_as_bfloat16(h));
+    } else {
+      return ord_float(k);
+    }
+  }
+};
 static_assert(kStWarps * kStMaxStages * 8 <= kStListOff, "mbarriers overlap the lists");
 static_assert(kStBarBytes % 16 == 0, "stage buffers must be 16-byte aligned for bulk copies");
 
@@ -135,6 +165,21 @@ __global__ void __launch_bounds__(kStThreads, 3) beam_strips_kernel(const StepPa
     float Rfl = -INFINITY;  // a tighter bound taken when a stage has many candidates
     int cnt = 0;            // entries in the warp's list
     bool ovf = false;       // the list could not hold the candidates
+    // keep the list's entries x >= t, in order; returns their count
+    auto drop_below = [&](int n_in, float t) -> int {
+      int out = 0;
+      for (int b0 = 0; b0 < n_in; b0 += 32) {
+        const int i = b0 + lane;
+        const float2 en = i < n_in ? list[i] : make_float2(-INFINITY, 0.0f);
+        const bool keep = i < n_in && en.x >= t;
+        const unsigned bm = __ballot_sync(0xffffffffu, keep);
+        __syncwarp();
+        if (keep) list[out + __popc(bm & ((1u << lane) - 1u))] = en;
+        out += __popc(bm);
+        __syncwarp();
+      }
+      return out;
+    };
     for (int q = cu.part; q < cu.ns; q += W) {
       const int s = n_cons % S;
       const bool ok = mbar_wait_bounded(smem_addr(&bars[s]), (uint32_t)((n_cons / S) & 1), p.spin_limit_ns);
@@ -256,28 +301,54 @@ __global__ void __launch_bounds__(kStThreads, 3) beam_strips_kernel(const StepPa
           mk = stage_mask(thr);
           n = __reduce_add_sync(0xffffffffu, __popcll(mk));
         }
+        if (!ovf && cnt + n > kStListCap) {
+          // drop the entries below the current bound (it only rises along the strip)
+          cnt = drop_below(cnt, thr);
+          if (cnt + n > kStListCap) {
+            // still more than the list holds: the k-th largest of the list and the stage's
+            // candidates together is itself a lower bound of the row's k-th largest (they are
+            // elements of the row).  Raise the bound to it -- the largest value t of the
+            // compared type with at least k of them >= t, by bisection on its order key.
+            auto count_ge = [&](float t) -> int {
+              int nge = __reduce_add_sync(0xffffffffu, __popcll(stage_mask(t)));
+              for (int b0 = 0; b0 < cnt; b0 += 32) {
+                const int i = b0 + lane;
+                nge += __popc(__ballot_sync(0xffffffffu, i < cnt && list[i].x >= t));
+              }
+              return nge;
+            };
+            float hv = lm;
+            for (int i = lane; i < cnt; i += 32) hv = fmaxf(hv, list[i].x);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) hv = fmaxf(hv, __shfl_xor_sync(0xffffffffu, hv, o));
+            using OK = OrderKey<DT, kPacked>;
+            float kb = hv;
+            if (count_ge(hv) < K) {
+              uint32_t lo = OK::of(thr), hi = OK::of(hv);  // count_ge(lo) >= k > count_ge(hi)
+              while (hi - lo > 1u) {
+                const uint32_t mid = lo + ((hi - lo) >> 1);
+                if (count_ge(OK::val(mid)) >= K)
+                  lo = mid;
+                else
+                  hi = mid;
+              }
+              kb = OK::val(lo);
+            }
+            Rfl = fmaxf(Rfl, kb);
+            R = fmaxf(R, Rfl);
+            thr = fmaxf(R, lo_fin);
+            cnt = drop_below(cnt, thr);
+            mk = stage_mask(thr);
+            n = __reduce_add_sync(0xffffffffu, __popcll(mk));
+          }
+          if (cnt + n > kStListCap) ovf = true;  // ties at the bound beyond the list
+        }
         const int c = __popcll(mk);
         int incl = c;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const int t = __shfl_up_sync(0xffffffffu, incl, o);
           if (lane >= o) incl += t;
-        }
-        if (!ovf && cnt + n > kStListCap) {
-          // drop the entries below the current bound (it only rises along the strip)
-          int out = 0;
-          for (int b0 = 0; b0 < cnt; b0 += 32) {
-            const int i = b0 + lane;
-            const float2 en = i < cnt ? list[i] : make_float2(-INFINITY, 0.0f);
-            const bool keep = i < cnt && en.x >= thr;
-            const unsigned bm = __ballot_sync(0xffffffffu, keep);
-            __syncwarp();
-            if (keep) list[out + __popc(bm & ((1u << lane) - 1u))] = en;
-            out += __popc(bm);
-            __syncwarp();
-          }
-          cnt = out;
-          if (cnt + n > kStListCap) ovf = true;
         }
         if (!ovf) {
           int pos = cnt + incl - c;
@@ -371,9 +442,31 @@ __global__ void __launch_bounds__(kStThreads, 3) beam_strips_kernel(const StepPa
       return n;
     };
     if (!ovf && count_above(thr) > C) {
-      // more than the slots hold: the tighter bound of the 32 lanes' maxima
+      // more than the slots hold: the tighter bound of the 32 lanes' maxima, then, if still
+      // too many, the k-th largest of the list itself (bisection as above)
       R = fmaxf(R, kth_of_lanes(ml, 32, K));
       thr = fmaxf(R, lo_fin);
+      if (count_above(thr) > C) {
+        using OK = OrderKey<DT, kPacked>;
+        float hv = -INFINITY;
+        for (int i = lane; i < cnt; i += 32) hv = fmaxf(hv, list[i].x);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) hv = fmaxf(hv, __shfl_xor_sync(0xffffffffu, hv, o));
+        float kb = hv;
+        if (count_above(hv) < K) {
+          uint32_t lo = OK::of(thr), hi = OK::of(hv);
+          while (hi - lo > 1u) {
+            const uint32_t mid = lo + ((hi - lo) >> 1);
+            if (count_above(OK::val(mid)) >= K)
+              lo = mid;
+            else
+              hi = mid;
+          }
+          kb = OK::val(lo);
+        }
+        R = fmaxf(R, kb);
+        thr = fmaxf(R, lo_fin);
+      }
     }
     CandSlot* slots = p.slots + (size_t)cu.u * C;
     int total = 0;
