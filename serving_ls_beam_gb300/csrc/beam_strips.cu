@@ -37,35 +37,6 @@ namespace {
 
 constexpr long long kDrainLimitNs = 2000000000LL;  // 2 s for copies already in flight
 
-// Order keys of the values a stage compares, so that a threshold found by bisection converts
-// to the compared type exactly: the 16-bit patterns for packed 16-bit logits, the fp32
-// patterns otherwise (x = logit + bias in fp32).
-template <int DT, bool PACKED>
-struct OrderKey {
-  static __device__ __forceinline__ uint32_t of(float x) {
-    if constexpr (PACKED) {
-      uint32_t h;
-      if constexpr (DT == DT_F16)
-        h = __half_as_ushort(__float2half_rn(x));
-      else
-        h = __bfloat16_as_ushort(__float2bfloat16_rn(x));
-      return (h & 0x8000u) ? (~h & 0xffffu) : (h | 0x8000u);
-    } else {
-      return float_ord(x);
-    }
-  }
-  static __device__ __forceinline__ float val(uint32_t k) {
-    if constexpr (PACKED) {
-      const unsigned short h = (unsigned short)((k & 0x8000u) ? (k & 0x7fffu) : (~k & 0xffffu));
-      if constexpr (DT == DT_F16)
-        return __half2float(__ushort_as_half(h));
-      else
-        return __bfloat162float(__ushort_as_bfloat16(h));
-    } else {
-      return ord_float(k);
-    }
-  }
-};
 static_assert(kStWarps * kStMaxStages * 8 <= kStListOff, "mbarriers overlap the lists");
 static_assert(kStBarBytes % 16 == 0, "stage buffers must be 16-byte aligned for bulk copies");
 

@@ -7,6 +7,7 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include "ls_device.cuh"
 #include "ls_dtype.cuh"
 
 namespace lsb {
@@ -165,5 +166,35 @@ __device__ __forceinline__ float strip_bound(float ml, int G, int K, float& gm) 
     default: return strip_bound_g<32>(ml, K, gm);
   }
 }
+
+// Order keys of the values a strip or chunk compares, so that a threshold found by bisection
+// converts to the compared type exactly: the 16-bit patterns for 16-bit logits compared as
+// they are (PACKED), the fp32 patterns otherwise (x = logit + bias in fp32).
+template <int DT, bool PACKED>
+struct OrderKey {
+  static __device__ __forceinline__ uint32_t of(float x) {
+    if constexpr (PACKED) {
+      uint32_t h;
+      if constexpr (DT == DT_F16)
+        h = __half_as_ushort(__float2half_rn(x));
+      else
+        h = __bfloat16_as_ushort(__float2bfloat16_rn(x));
+      return (h & 0x8000u) ? (~h & 0xffffu) : (h | 0x8000u);
+    } else {
+      return float_ord(x);
+    }
+  }
+  static __device__ __forceinline__ float val(uint32_t k) {
+    if constexpr (PACKED) {
+      const unsigned short h = (unsigned short)((k & 0x8000u) ? (k & 0x7fffu) : (~k & 0xffffu));
+      if constexpr (DT == DT_F16)
+        return __half2float(__ushort_as_half(h));
+      else
+        return __bfloat162float(__ushort_as_bfloat16(h));
+    } else {
+      return ord_float(k);
+    }
+  }
+};
 
 }  // namespace lsb
