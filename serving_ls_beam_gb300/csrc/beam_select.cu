@@ -165,6 +165,174 @@ __device__ void merge_into_best(SelSmem& sm, int K) {
 //     select over the whole source, in token order.
 constexpr int kExactBuf = 4096;  // entries (x, token) of a beam's list in dynamic shared memory
 constexpr int kExactRankMax = 256;  // lists up to this long are ranked by counting
+constexpr int kExactWarpList = kExactBuf / kSelWarps;  // a warp's list in the beam-parallel form
+
+__host__ __device__ constexpr int pow2_at_least(int x) {
+  int n = 1;
+  while (n < x) n <<= 1;
+  return n;
+}
+
+// Dynamic shared memory of K2 for k: the exact path's lists, then k * k rank keys.
+__host__ __device__ constexpr size_t exact_smem_bytes(int k) {
+  return kExactBuf * sizeof(float2) + (size_t)pow2_at_least(k * k) * sizeof(Key);
+}
+
+static_assert(exact_smem_bytes(kMaxK) <= (size_t)kSelStageMax, "the exact path's shared memory exceeds K2's limit");
+
+// The exact path one warp per beam: each warp keeps its beam's entries x >= R in its own list
+// -- from the beam's slots when they are complete, else from its row in 16-byte vectors -- and
+// ranks them, writing the beam's top-k as rank keys; the batch's top-k are then the first k of
+// the k * k keys, sorted once.  Returns false, with nothing written, when some beam has more
+// such entries than a warp's list holds.
+template <int DT, bool BIAS>
+__device__ bool exact_parallel(const StepParams& p, SelSmem& sm, int b, int path, unsigned char* dyn,
+                               bool from_slots) {
+  constexpr int ES = Traits<DT>::kBytes;
+  constexpr int VEC = Traits<DT>::kVec;
+  const int K = p.k, C = p.slot_cap, nc = p.nc, V = p.vocab;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  float2* list = reinterpret_cast<float2*>(dyn) + warp * kExactWarpList;
+  Key* keys = reinterpret_cast<Key*>(dyn + kExactBuf * sizeof(float2));
+  const int nk = pow2_at_least(K * K);
+  Key pad;
+  pad.hi = ~0ull;
+  pad.lo = ~0ull;
+  if (tid == 0) sm.big = 0;
+  __syncthreads();
+  for (int j = warp; j < K; j += kSelWarps) {
+    const RowSel rs = sm.row[j];
+    const int row = b * K + j;
+    Key* out = keys + j * K;
+    if (rs.kind == ROW_FIN) {
+      for (int r = lane; r < K; r += 32) out[r] = r == 0 ? make_key(p.beam[row], j, 0.0f, p.eos) : pad;
+      continue;
+    }
+    if (rs.kind == ROW_DEAD) {
+      for (int r = lane; r < K; r += 32) out[r] = make_key(-INFINITY, j, 0.0f, r);
+      continue;
+    }
+    float R = rs.rtopk;
+    int n = 0;
+    bool full = false;  // ties at the bound beyond the list: the serial path takes the batch
+    // The list is full: raise R to the k-th largest of its entries (elements of the row, so
+    // still a lower bound of its k-th largest) and keep the entries at or above it.
+    auto tighten = [&]() {
+      float kth = -INFINITY;
+      for (int i = lane; i < n; i += 32) {
+        const float xi = list[i].x;
+        int gt = 0, ge = 0;
+        for (int q = 0; q < n; ++q) {
+          const float xq = list[q].x;
+          gt += xq > xi;
+          ge += xq >= xi;
+        }
+        if (gt < K && ge >= K) kth = xi;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) kth = fmaxf(kth, __shfl_xor_sync(0xffffffffu, kth, o));
+      R = fmaxf(R, kth);
+      int out = 0;
+      for (int b0 = 0; b0 < n; b0 += 32) {
+        const int i = b0 + lane;
+        const float2 en = i < n ? list[i] : make_float2(-INFINITY, 0.0f);
+        const bool keep = i < n && en.x >= R;
+        const unsigned bm = __ballot_sync(0xffffffffu, keep);
+        __syncwarp();
+        if (keep) list[out + __popc(bm & lt_mask)] = en;
+        out += __popc(bm);
+        __syncwarp();
+      }
+      n = out;
+    };
+    auto append = [&](bool take, float x, int v) {
+      unsigned m = __ballot_sync(0xffffffffu, take);
+      if (n + __popc(m) > kExactWarpList) {
+        tighten();
+        m = __ballot_sync(0xffffffffu, take && x >= R);
+        if (n + __popc(m) > kExactWarpList) {
+          full = true;
+          return;
+        }
+      }
+      const int pos = n + __popc(m & lt_mask);
+      if ((m >> lane) & 1u) list[pos] = make_float2(x, __int_as_float(v));
+      n += __popc(m);
+    };
+    if (from_slots) {
+      const long long u0 = (long long)row * nc;
+      for (int c = 0; c < nc && !full; ++c) {
+        const int cnt = min(__float_as_int(rec_ptr(p, u0 + c)[0]), C);
+        const CandSlot* sl = p.slots + (u0 + c) * C;
+        for (int s0 = 0; s0 < cnt; s0 += 32) {
+          const int i = s0 + lane;
+          CandSlot cs;
+          cs.x = -INFINITY;
+          cs.v = 0;
+          if (i < cnt) cs = sl[i];
+          append(i < cnt && cs.x >= R, cs.x, cs.v);
+        }
+      }
+    } else {
+      // 16-byte vectors covering the row (the first may start before it, the last end after
+      // it), four per lane in flight
+      const unsigned char* rowp = static_cast<const unsigned char*>(p.logits) + (size_t)row * V * ES;
+      const int lead = (int)(reinterpret_cast<uintptr_t>(rowp) & 15);
+      const uint4* rb = reinterpret_cast<const uint4*>(rowp - lead);
+      const int row_bytes = V * ES;
+      const int nv = (lead + row_bytes + 15) >> 4;
+      for (int v0 = 0; v0 < nv && !full; v0 += 128) {
+        uint4 d[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int jv = v0 + 32 * r + lane;
+          d[r] = jv < nv ? __ldcs(rb + jv) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int jv = v0 + 32 * r + lane;
+          float xs[VEC];
+          unpack<DT>(d[r], xs);
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) {
+            const int byte = jv * 16 + e * ES - lead;
+            const bool in = jv < nv && byte >= 0 && byte < row_bytes;
+            const int v = byte / ES;
+            float x = xs[e];
+            if constexpr (BIAS) x += in ? __ldg(p.bias + v) : 0.0f;
+            append(in && x >= R, x, v);
+          }
+        }
+      }
+    }
+    if (full) {
+      if (lane == 0) sm.big = 1;
+      continue;
+    }
+    __syncwarp();
+    for (int r = n + lane; r < K; r += 32) out[r] = pad;  // fewer than k entries (cannot happen for a live beam)
+    for (int i = lane; i < n; i += 32) {
+      const float2 ei = list[i];
+      const int vi = __float_as_int(ei.y);
+      int rank = 0;
+      for (int q = 0; q < n; ++q) {
+        const float2 eq = list[q];
+        rank += (eq.x > ei.x) | ((eq.x == ei.x) & (__float_as_int(eq.y) < vi));
+      }
+      if (rank < K) out[rank] = make_key(score_of(rs.c, ei.x), j, ei.x, vi);
+    }
+  }
+  __syncthreads();
+  if (sm.big) return false;
+  for (int i = K * K + tid; i < nk; i += kSelThreads) keys[i] = pad;
+  __syncthreads();
+  bitonic_sort(keys, nk);
+  for (int r = tid; r < K; r += kSelThreads) write_output(p, sm, b, r, keys[r]);
+  write_row_stats(p, sm, b, true);
+  if (tid == 0) p.bstat[b] = path;
+  return true;
+}
 
 template <int DT, bool BIAS>
 __device__ void exact_select(const StepParams& p, SelSmem& sm, int b, int path, float2* buf) {
@@ -173,6 +341,7 @@ __device__ void exact_select(const StepParams& p, SelSmem& sm, int b, int path, 
   constexpr int NT = kSelThreads;
   const int K = p.k, V = p.vocab, C = p.slot_cap, nc = p.nc;
   const bool from_slots = p.logits == nullptr || path == 3;
+  if (exact_parallel<DT, BIAS>(p, sm, b, path, reinterpret_cast<unsigned char*>(buf), from_slots)) return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const unsigned lt_mask = (1u << lane) - 1u;
   if (tid == 0) {
@@ -970,8 +1139,8 @@ cudaError_t launch_t(const StepParams& p, cudaStream_t stream) {
   cfg.gridDim = dim3((unsigned)p.batch);
   cfg.blockDim = dim3(kSelThreads);
   // the slots' staging copy, or the exact path's list (the two are never in use at once)
-  const size_t list_bytes = kExactBuf * sizeof(float2);
-  cfg.dynamicSmemBytes = (size_t)p.sel_stage_bytes > list_bytes ? (size_t)p.sel_stage_bytes : list_bytes;
+  const size_t exact_bytes = exact_smem_bytes(p.k);
+  cfg.dynamicSmemBytes = (size_t)p.sel_stage_bytes > exact_bytes ? (size_t)p.sel_stage_bytes : exact_bytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
