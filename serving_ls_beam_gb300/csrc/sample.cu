@@ -29,6 +29,7 @@ namespace {
 constexpr int kSampThreads = 256;
 constexpr int kSampWarps = kSampThreads / 32;  // rows per CTA
 constexpr int kSampWarpCap = 128;              // survivors a warp holds for its row
+constexpr int kSampRounds = 4;                  // gathers of a row's survivors, each with a higher bound
 constexpr int kSampHdr = 128;                  // chunk headers a warp keeps in shared memory
 
 struct __align__(16) SampSmem {
@@ -157,6 +158,114 @@ __device__ void exact_candidates(const SampleParams& p, SampSmem& sm, int r) {
   }
 }
 
+// Exact top-k of row r by warp w alone: one pass over the row in 16-byte vectors keeps the
+// entries x >= R (the row's R-top-k, never above its k-th largest) in the warp's list; a full
+// list raises R to the k-th largest of its entries (elements of the row, so still a lower bound)
+// and keeps those at or above it.  The list's top-k (larger x, then smaller token) go to
+// sm.tx / sm.tv[w].  Returns false when ties at the bound overflow the list.
+template <int DT, bool BIAS>
+__device__ bool exact_row_warp(const SampleParams& p, SampSmem& sm, int w, int r) {
+  constexpr int ES = Traits<DT>::kBytes;
+  constexpr int VEC = Traits<DT>::kVec;
+  const int K = p.k, V = p.vocab, lane = threadIdx.x & 31;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  float* lx = sm.cx[w];
+  int* lv = sm.cv[w];
+  float R = sm.R[w];
+  int n = 0;
+  bool full = false;
+  auto tighten = [&]() {
+    float kth = -INFINITY;
+    for (int i = lane; i < n; i += 32) {
+      const float xi = lx[i];
+      int gt = 0, ge = 0;
+      for (int q = 0; q < n; ++q) {
+        gt += lx[q] > xi;
+        ge += lx[q] >= xi;
+      }
+      if (gt < K && ge >= K) kth = xi;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) kth = fmaxf(kth, __shfl_xor_sync(0xffffffffu, kth, o));
+    R = fmaxf(R, kth);
+    int out = 0;
+    for (int b0 = 0; b0 < n; b0 += 32) {
+      const int i = b0 + lane;
+      const float xi = i < n ? lx[i] : -INFINITY;
+      const int vi = i < n ? lv[i] : 0;
+      const bool keep = i < n && xi >= R;
+      const unsigned bm = __ballot_sync(0xffffffffu, keep);
+      __syncwarp();
+      if (keep) {
+        lx[out + __popc(bm & lt_mask)] = xi;
+        lv[out + __popc(bm & lt_mask)] = vi;
+      }
+      out += __popc(bm);
+      __syncwarp();
+    }
+    n = out;
+  };
+  auto append = [&](bool take, float x, int v) {
+    unsigned m = __ballot_sync(0xffffffffu, take);
+    if (n + __popc(m) > kSampWarpCap) {
+      tighten();
+      m = __ballot_sync(0xffffffffu, take && x >= R);
+      if (n + __popc(m) > kSampWarpCap) {
+        full = true;
+        return;
+      }
+    }
+    if ((m >> lane) & 1u) {
+      lx[n + __popc(m & lt_mask)] = x;
+      lv[n + __popc(m & lt_mask)] = v;
+    }
+    n += __popc(m);
+  };
+  const unsigned char* rowp = static_cast<const unsigned char*>(p.logits) + (size_t)r * V * ES;
+  const int lead = (int)(reinterpret_cast<uintptr_t>(rowp) & 15);
+  const uint4* rb = reinterpret_cast<const uint4*>(rowp - lead);
+  const int row_bytes = V * ES;
+  const int nv = (lead + row_bytes + 15) >> 4;
+  // 16-byte vectors covering the row (the first may start before it, the last end after it),
+  // four per lane in flight
+  for (int v0 = 0; v0 < nv && !full; v0 += 128) {
+    uint4 d[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int jv = v0 + 32 * q + lane;
+      d[q] = jv < nv ? __ldcs(rb + jv) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int jv = v0 + 32 * q + lane;
+      float xs[VEC];
+      unpack<DT>(d[q], xs);
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        const int byte = jv * 16 + e * ES - lead;
+        const bool in = jv < nv && byte >= 0 && byte < row_bytes;
+        const int v = byte / ES;
+        float x = xs[e];
+        if constexpr (BIAS) x += in ? __ldg(p.bias + v) : 0.0f;
+        append(in && x >= R, x, v);
+      }
+    }
+  }
+  if (full || n < K) return false;
+  __syncwarp();
+  for (int i = lane; i < n; i += 32) {
+    const float xi = lx[i];
+    const int vi = lv[i];
+    int rank = 0;
+    for (int q = 0; q < n; ++q) rank += before(lx[q], lv[q], xi, vi);
+    if (rank < K) {
+      sm.tx[w][rank] = xi;
+      sm.tv[w][rank] = vi;
+    }
+  }
+  return true;
+}
+
 template <int DT, bool BIAS>
 __global__ void __launch_bounds__(kSampThreads, 1) sample_select_kernel(const SampleParams p) {
   __shared__ SampSmem sm;
@@ -258,8 +367,31 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_select_kernel(const Sa
     const float lse = m == -INFINITY ? -INFINITY : m + logf(s);
     path = ovf ? 1 : 0;
     if (p.flags & kFlagForceExact) path = 2;
-    if (path == 0) {
-      // 2. survivors of the row's bound from the chunks whose max reaches it
+    // 2. survivors of the row's bound from the chunks whose max reaches it.  When they
+    // outnumber the warp's list, the k-th largest of the entries it holds (elements of the
+    // row, so still a lower bound of its k-th largest) becomes the bound and the gather runs
+    // again, a few times at most.
+    for (int round = 0; path == 0 && round < kSampRounds; ++round) {
+      if (round > 0) {
+        const int held = min(sm.n[w], kSampWarpCap);
+        float kth = -INFINITY;
+        for (int i = lane; i < held; i += 32) {
+          const float xi = sm.cx[w][i];
+          int gt = 0, ge = 0;
+          for (int q = 0; q < held; ++q) {
+            const float xq = sm.cx[w][q];
+            gt += xq > xi;
+            ge += xq >= xi;
+          }
+          if (gt < K && ge >= K) kth = xi;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) kth = fmaxf(kth, __shfl_xor_sync(0xffffffffu, kth, o));
+        R = fmaxf(R, kth);
+        __syncwarp();
+        if (lane == 0) sm.n[w] = 0;
+        __syncwarp();
+      }
       for (int c = lane; c < nc; c += 32) {
         float mc;
         int cnt;
@@ -292,6 +424,9 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_select_kernel(const Sa
         }
       }
       __syncwarp();
+      if (sm.n[w] <= kSampWarpCap) break;
+    }
+    if (path == 0) {
       const int n = sm.n[w];
       if (n > kSampWarpCap || n < K) path = 3;
       if (path == 0) {
@@ -326,9 +461,19 @@ __global__ void __launch_bounds__(kSampThreads, 1) sample_select_kernel(const Sa
       p.bstat[r] = path;
       sm.path[w] = path;
       sm.lse[w] = lse;
+      sm.R[w] = R;
     }
   }
-  // rows that need the exact top-k: the whole CTA, one row at a time
+  // rows that need the exact top-k: first each warp alone over its own row (its entries
+  // x >= R in the warp's list, the bound raised to the k-th largest of the list whenever it
+  // fills); only a row whose ties at the bound overflow the list takes the whole CTA after.
+  __syncwarp();
+  if (row_ok && sm.path[w] != 0 && exact_row_warp<DT, BIAS>(p, sm, w, r)) {
+    __syncwarp();
+    draw(p, sm.tx[w], sm.tv[w], sm.lse[w], u, r);
+    __syncwarp();
+    if (lane == 0) sm.path[w] = 0;
+  }
   __syncthreads();
   for (int w2 = 0; w2 < kSampWarps; ++w2) {
     if (sm.path[w2] == 0) continue;  // CTA-uniform
