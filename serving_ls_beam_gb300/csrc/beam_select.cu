@@ -180,6 +180,40 @@ __host__ __device__ constexpr size_t exact_smem_bytes(int k) {
 
 static_assert(exact_smem_bytes(kMaxK) <= (size_t)kSelStageMax, "the exact path's shared memory exceeds K2's limit");
 
+// A warp's full list of entries (x, token): the k-th largest x among list[0..n) (n >= k), the
+// larger of it and R as the new bound, and the entries at or above that bound kept in order.
+// Returns (bound, kept count as int bits).  Out of line: it is called from unrolled loops.
+__device__ __noinline__ float2 list_tighten(float2* list, int n, int K, float R) {
+  const int lane = threadIdx.x & 31;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  float kth = -INFINITY;
+  for (int i = lane; i < n; i += 32) {
+    const float xi = list[i].x;
+    int gt = 0, ge = 0;
+    for (int q = 0; q < n; ++q) {
+      const float xq = list[q].x;
+      gt += xq > xi;
+      ge += xq >= xi;
+    }
+    if (gt < K && ge >= K) kth = xi;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) kth = fmaxf(kth, __shfl_xor_sync(0xffffffffu, kth, o));
+  R = fmaxf(R, kth);
+  int out = 0;
+  for (int b0 = 0; b0 < n; b0 += 32) {
+    const int i = b0 + lane;
+    const float2 en = i < n ? list[i] : make_float2(-INFINITY, 0.0f);
+    const bool keep = i < n && en.x >= R;
+    const unsigned bm = __ballot_sync(0xffffffffu, keep);
+    __syncwarp();
+    if (keep) list[out + __popc(bm & lt_mask)] = en;
+    out += __popc(bm);
+    __syncwarp();
+  }
+  return make_float2(R, __int_as_float(out));
+}
+
 // The exact path one warp per beam: each warp keeps its beam's entries x >= R in its own list
 // -- from the beam's slots when they are complete, else from its row in 16-byte vectors -- and
 // ranks them, writing the beam's top-k as rank keys; the batch's top-k are then the first k of
@@ -219,32 +253,9 @@ __device__ bool exact_parallel(const StepParams& p, SelSmem& sm, int b, int path
     // The list is full: raise R to the k-th largest of its entries (elements of the row, so
     // still a lower bound of its k-th largest) and keep the entries at or above it.
     auto tighten = [&]() {
-      float kth = -INFINITY;
-      for (int i = lane; i < n; i += 32) {
-        const float xi = list[i].x;
-        int gt = 0, ge = 0;
-        for (int q = 0; q < n; ++q) {
-          const float xq = list[q].x;
-          gt += xq > xi;
-          ge += xq >= xi;
-        }
-        if (gt < K && ge >= K) kth = xi;
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) kth = fmaxf(kth, __shfl_xor_sync(0xffffffffu, kth, o));
-      R = fmaxf(R, kth);
-      int out = 0;
-      for (int b0 = 0; b0 < n; b0 += 32) {
-        const int i = b0 + lane;
-        const float2 en = i < n ? list[i] : make_float2(-INFINITY, 0.0f);
-        const bool keep = i < n && en.x >= R;
-        const unsigned bm = __ballot_sync(0xffffffffu, keep);
-        __syncwarp();
-        if (keep) list[out + __popc(bm & lt_mask)] = en;
-        out += __popc(bm);
-        __syncwarp();
-      }
-      n = out;
+      const float2 rn = list_tighten(list, n, K, R);
+      R = rn.x;
+      n = __float_as_int(rn.y);
     };
     auto append = [&](bool take, float x, int v) {
       unsigned m = __ballot_sync(0xffffffffu, take);
@@ -289,11 +300,12 @@ __device__ bool exact_parallel(const StepParams& p, SelSmem& sm, int b, int path
           const int jv = v0 + 32 * r + lane;
           d[r] = jv < nv ? __ldcs(rb + jv) : make_uint4(0u, 0u, 0u, 0u);
         }
-#pragma unroll
+#pragma unroll 1
         for (int r = 0; r < 4; ++r) {
           const int jv = v0 + 32 * r + lane;
           float xs[VEC];
-          unpack<DT>(d[r], xs);
+          const uint4 dv = r == 0 ? d[0] : (r == 1 ? d[1] : (r == 2 ? d[2] : d[3]));  // no local array
+          unpack<DT>(dv, xs);
 #pragma unroll
           for (int e = 0; e < VEC; ++e) {
             const int byte = jv * 16 + e * ES - lead;
@@ -421,11 +433,12 @@ __device__ void exact_select(const StepParams& p, SelSmem& sm, int b, int path, 
           const int jv = v0 + 32 * r + lane;
           d[r] = jv < nv ? __ldcs(rb + jv) : make_uint4(0u, 0u, 0u, 0u);
         }
-#pragma unroll
+#pragma unroll 1
         for (int r = 0; r < 4; ++r) {
           const int jv = v0 + 32 * r + lane;
           float xs[VEC];
-          unpack<DT>(d[r], xs);
+          const uint4 dv = r == 0 ? d[0] : (r == 1 ? d[1] : (r == 2 ? d[2] : d[3]));  // no local array
+          unpack<DT>(dv, xs);
 #pragma unroll
           for (int e = 0; e < VEC; ++e) {
             const int byte = jv * 16 + e * ES - lead;

@@ -158,6 +158,44 @@ __device__ void exact_candidates(const SampleParams& p, SampSmem& sm, int r) {
   }
 }
 
+// A warp's full list of entries (lx, lv): the k-th largest x among its n entries (n >= k),
+// the larger of it and R as the new bound, and the entries at or above that bound kept in
+// order.  Returns (bound, kept count as int bits).  Out of line: it is called from unrolled
+// loops.
+__device__ __noinline__ float2 list_tighten(float* lx, int* lv, int n, int K, float R) {
+  const int lane = threadIdx.x & 31;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  float kth = -INFINITY;
+  for (int i = lane; i < n; i += 32) {
+    const float xi = lx[i];
+    int gt = 0, ge = 0;
+    for (int q = 0; q < n; ++q) {
+      gt += lx[q] > xi;
+      ge += lx[q] >= xi;
+    }
+    if (gt < K && ge >= K) kth = xi;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) kth = fmaxf(kth, __shfl_xor_sync(0xffffffffu, kth, o));
+  R = fmaxf(R, kth);
+  int out = 0;
+  for (int b0 = 0; b0 < n; b0 += 32) {
+    const int i = b0 + lane;
+    const float xi = i < n ? lx[i] : -INFINITY;
+    const int vi = i < n ? lv[i] : 0;
+    const bool keep = i < n && xi >= R;
+    const unsigned bm = __ballot_sync(0xffffffffu, keep);
+    __syncwarp();
+    if (keep) {
+      lx[out + __popc(bm & lt_mask)] = xi;
+      lv[out + __popc(bm & lt_mask)] = vi;
+    }
+    out += __popc(bm);
+    __syncwarp();
+  }
+  return make_float2(R, __int_as_float(out));
+}
+
 // Exact top-k of row r by warp w alone: one pass over the row in 16-byte vectors keeps the
 // entries x >= R (the row's R-top-k, never above its k-th largest) in the warp's list; a full
 // list raises R to the k-th largest of its entries (elements of the row, so still a lower bound)
@@ -175,35 +213,9 @@ __device__ bool exact_row_warp(const SampleParams& p, SampSmem& sm, int w, int r
   int n = 0;
   bool full = false;
   auto tighten = [&]() {
-    float kth = -INFINITY;
-    for (int i = lane; i < n; i += 32) {
-      const float xi = lx[i];
-      int gt = 0, ge = 0;
-      for (int q = 0; q < n; ++q) {
-        gt += lx[q] > xi;
-        ge += lx[q] >= xi;
-      }
-      if (gt < K && ge >= K) kth = xi;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) kth = fmaxf(kth, __shfl_xor_sync(0xffffffffu, kth, o));
-    R = fmaxf(R, kth);
-    int out = 0;
-    for (int b0 = 0; b0 < n; b0 += 32) {
-      const int i = b0 + lane;
-      const float xi = i < n ? lx[i] : -INFINITY;
-      const int vi = i < n ? lv[i] : 0;
-      const bool keep = i < n && xi >= R;
-      const unsigned bm = __ballot_sync(0xffffffffu, keep);
-      __syncwarp();
-      if (keep) {
-        lx[out + __popc(bm & lt_mask)] = xi;
-        lv[out + __popc(bm & lt_mask)] = vi;
-      }
-      out += __popc(bm);
-      __syncwarp();
-    }
-    n = out;
+    const float2 rn = list_tighten(lx, lv, n, K, R);
+    R = rn.x;
+    n = __float_as_int(rn.y);
   };
   auto append = [&](bool take, float x, int v) {
     unsigned m = __ballot_sync(0xffffffffu, take);
@@ -235,11 +247,12 @@ __device__ bool exact_row_warp(const SampleParams& p, SampSmem& sm, int w, int r
       const int jv = v0 + 32 * q + lane;
       d[q] = jv < nv ? __ldcs(rb + jv) : make_uint4(0u, 0u, 0u, 0u);
     }
-#pragma unroll
+#pragma unroll 1
     for (int q = 0; q < 4; ++q) {
       const int jv = v0 + 32 * q + lane;
       float xs[VEC];
-      unpack<DT>(d[q], xs);
+      const uint4 dv = q == 0 ? d[0] : (q == 1 ? d[1] : (q == 2 ? d[2] : d[3]));  // no local array
+      unpack<DT>(dv, xs);
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
         const int byte = jv * 16 + e * ES - lead;
