@@ -186,6 +186,25 @@ def test_forced_exact_path(dev, oracle_mod, seed):
         assert (gpu_q[key] == gpu_x[key]).all()
 
 
+@pytest.mark.parametrize("k", [16, 32, 64])
+def test_large_k_exact_path(dev, oracle_mod, k):
+    """Large beams at a full vocabulary: the k-group bound lets hundreds of candidates per beam
+    through, the queue overflows and the exact path selects from the slots (or, where a chunk's
+    slots overflowed, from the rows), one warp per beam.  Outputs against the oracle, and the
+    path taken is the exact one for at least one batch."""
+    g = np.random.default_rng(k)
+    B, V = 4, 40000
+    lg = (g.standard_normal((B, k, V)) * 2).astype(np.float16)
+    inp = {"logits": lg, "bias": None, "beam_scores": g.uniform(-10, 0, (B, k)).astype(np.float32),
+           "finished": None, "eos_id": 2, "dtype": "f16"}
+    gpu, ws = run_gpu(inp, dev)
+    _, _, _, path = lsb.ls_read_row_stats(ws, B, k, V)
+    if _impl_env["value"] in ("", "nofused"):
+        assert (np.asarray(path) != 0).any()
+    ora = run_oracle(oracle_mod, inp)
+    compare_step(gpu, ora, k, "f16", eos_id=2)
+
+
 def test_all_equal_logits_overflow(dev, oracle_mod):
     """Every logit ties with R-top-k: the chunk slots overflow and the exact fallback answers."""
     B, K, V = 3, 4, 40000

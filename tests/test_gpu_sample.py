@@ -133,6 +133,19 @@ def test_forced_exact_path_agrees(dev, oracle_mod, seed):
     compare(oracle_mod, lg, dtype, bias, u, top_k, top_p, *b)
 
 
+@pytest.mark.parametrize("top_k", [16, 32, 64])
+def test_large_top_k_full_vocab(dev, oracle_mod, top_k):
+    """Large top_k at a full vocabulary, where the rows' survivors outnumber a warp's list (the
+    bound is raised and the survivors gathered again) or the chunks' slots overflow (each row is
+    scanned by its warp): against the oracle."""
+    g = np.random.default_rng(top_k)
+    rows, vocab = 96, 40000
+    lg = (g.standard_normal((rows, vocab)) * 2).astype(np.float16)
+    u = g.random(rows).astype(np.float32)
+    tok, lp = run_gpu(dev, lg, "f16", None, u, top_k, 0.9)
+    compare(oracle_mod, lg, "f16", None, u, top_k, 0.9, tok, lp)
+
+
 def test_all_equal_logits_take_the_first_tokens(dev, oracle_mod):
     rows, vocab, top_k = 64, 40000, 8
     lg = np.zeros((rows, vocab), np.float16)
