@@ -50,13 +50,14 @@ struct Debug {
   int stages = 0;  // K1s stage buffers per warp, 0 = plan's choice
   int parts = 0;   // K1s strips per row, 0 = plan's choice
   int ipw = 0;     // in-place word kernel: words per item, 0 = plan's choice
+  int ipkeff = 0;  // in-place bulk-copy kernel: parents an item is sized for, 0 = plan's choice
   int stage = -1;  // K2 after K0: 1 = stage the batch's slots, 0 = read them in place, -1 = plan
   bool check_ptrs = true;
 };
 
 // LS_BEAM_DEBUG: comma-separated "exact", "ipplain", "iptma", "ipwords", "ipstatic", "steprefresh", "chunk", "strips",
 // "fused", "nofused", "cluster", "nocluster", "spin=<ns>", "vpl=<4|8|16>", "stages=<2..8>", "parts=<n>", "ipw=<words>",
-// "stage=<0|1>", "nocheck".
+// "ipkeff=<parents>", "stage=<0|1>", "nocheck".
 Debug read_debug() {
   Debug d;
   const char* env = std::getenv("LS_BEAM_DEBUG");
@@ -82,6 +83,7 @@ Debug read_debug() {
     else if (!std::strncmp(tok, "stages=", 7)) d.stages = std::atoi(tok + 7);
     else if (!std::strncmp(tok, "parts=", 6)) d.parts = std::atoi(tok + 6);
     else if (!std::strncmp(tok, "ipw=", 4)) d.ipw = std::atoi(tok + 4);
+    else if (!std::strncmp(tok, "ipkeff=", 7)) d.ipkeff = std::atoi(tok + 7);
     else if (!std::strncmp(tok, "stage=", 6)) d.stage = std::atoi(tok + 6);
     else if (!std::strcmp(tok, "nocheck")) d.check_ptrs = false;
   }
@@ -819,8 +821,13 @@ ls_status ls_cache_refresh_inplace(void* cache, ls_dtype dtype, const int32_t* p
   const long long stage = tma ? kIpTmaStage : kIpStageBytes;
   const long long tile = (stage / k) / unit * unit;  // every row's tile fits one staging buffer
   p.tile_bytes = (int)(tile < slab_bytes ? tile : slab_bytes);
-  // short slabs: the bulk-copy kernel moves as many heads of a (layer, batch) as fit at once
-  long long hg = slab_bytes <= tile ? stage / ((long long)k * slab_bytes) : 1;
+  // short slabs: an item of the bulk-copy kernel is as many heads of a (layer, batch) as fit a
+  // buffer for ceil(k / 2) needed parents -- about what a beam-search batch needs -- and the
+  // kernel moves an item in steps that fit the parents its batch actually needs (c5 loop, one
+  // launch timed alone: 82.5 us sized for 2 parents, 83.5 for 3, 90.5 for all 4, 86.5 for 1);
+  // the staged CTA kernel stages all k
+  const long long k_item = !tma ? k : (dbg.ipkeff > 0 && dbg.ipkeff <= k ? dbg.ipkeff : (k + 1) / 2);
+  long long hg = slab_bytes <= tile ? stage / (k_item * slab_bytes) : 1;
   hg = hg < 1 ? 1 : (hg > heads ? heads : hg);
   p.heads_per_item = (int)hg;
   const long long items = tma ? (long long)layers * batch * ((heads + hg - 1) / hg) *

@@ -141,9 +141,11 @@ __global__ void __launch_bounds__(kIpThreads) cache_inplace_kernel(const Inplace
 
 // The same refresh driven by bulk (TMA) copies from one thread: a CTA is one warp whose
 // lanes load the batches' parents into shared memory, after which lane 0 alone runs a
-// two-stage pipeline over its (layer, batch, head, tile) items: the bulk loads of the slabs
-// item i needs are issued before the bulk stores of item i-1's changed rows, so a copy in
-// each direction is always in flight.  Items differ in size (the rows a batch changes), so
+// two-stage pipeline over its (layer, batch, head group, tile) items, a step at a time: the
+// bulk loads of the slabs step i needs are issued before the bulk stores of step i-1's changed
+// rows, so a copy in each direction is always in flight.  A step takes as many of the item's
+// heads as the slabs of the parents its batch actually needs fit a 32 KB buffer (the host
+// sizes items for a typical count of needed parents, not for all k).  Items differ in size (the rows a batch changes), so
 // with a work counter (p.work) a CTA takes its next item when it is ready for one: the CTAs
 // then finish together instead of with the sum of their items' sizes.  The last CTA to finish
 // sets the counter back to zero for the next launch.  Requires 16-byte aligned slabs and
@@ -227,33 +229,39 @@ __global__ void __launch_bounds__(32) cache_inplace_tma_kernel(const InplacePara
     if (changed == 0ull) continue;
     const long long t0 = tile * p.tile_bytes;
     const int tb = (int)min((long long)p.tile_bytes, p.slab_bytes - t0);
-    unsigned char* base = p.cache + (size_t)l * p.layer_stride + (size_t)b * K * p.row_stride +
-                          (size_t)h0 * p.slab_stride + t0;
-    // buffer `cur` was last read by the stores of the item before the previous one
-    bulk_wait_read<0>();
-    const uint32_t b_addr = smem_addr(&bar[cur]);
-    mbar_arrive_expect_tx(b_addr, (uint32_t)(__popcll(needed) * hg * tb));
-    unsigned char* dst = tsm + (size_t)cur * kIpTmaStage;
-    int slot = 0;
-    for (int q = 0; q < K; ++q) {
-      if (!((needed >> q) & 1ull)) continue;
-      for (int hh = 0; hh < hg; ++hh)
-        bulk_load_plain(smem_addr(dst + ((size_t)slot * hg + hh) * tb),
-                        base + (size_t)q * p.row_stride + (size_t)hh * p.slab_stride, (uint32_t)tb, b_addr);
-      ++slot;
+    // a step moves as many of the item's heads as the needed parents' slabs fit a buffer
+    const int nn = __popcll(needed);
+    const int hsub = max(1, min(hg, kIpTmaStage / (nn * tb)));
+    for (int hs = 0; hs < hg && !aborted; hs += hsub) {
+      const int hn = min(hsub, hg - hs);
+      unsigned char* base = p.cache + (size_t)l * p.layer_stride + (size_t)b * K * p.row_stride +
+                            (size_t)(h0 + hs) * p.slab_stride + t0;
+      // buffer `cur` was last read by the stores of the step before the previous one
+      bulk_wait_read<0>();
+      const uint32_t b_addr = smem_addr(&bar[cur]);
+      mbar_arrive_expect_tx(b_addr, (uint32_t)(nn * hn * tb));
+      unsigned char* dst = tsm + (size_t)cur * kIpTmaStage;
+      int slot = 0;
+      for (int q = 0; q < K; ++q) {
+        if (!((needed >> q) & 1ull)) continue;
+        for (int hh = 0; hh < hn; ++hh)
+          bulk_load_plain(smem_addr(dst + ((size_t)slot * hn + hh) * tb),
+                          base + (size_t)q * p.row_stride + (size_t)hh * p.slab_stride, (uint32_t)tb, b_addr);
+        ++slot;
+      }
+      if (have_prev) finish_prev();
+      have_prev = true;
+      pv_base = base;
+      pv_changed = changed;
+      pv_needed = needed;
+      pv_b = b;
+      pv_tb = tb;
+      pv_hg = hn;
+      pv_buf = cur;
+      pv_parity = uses[cur] & 1u;
+      ++uses[cur];
+      cur ^= 1;
     }
-    if (have_prev) finish_prev();
-    have_prev = true;
-    pv_base = base;
-    pv_changed = changed;
-    pv_needed = needed;
-    pv_b = b;
-    pv_tb = tb;
-    pv_hg = hg;
-    pv_buf = cur;
-    pv_parity = uses[cur] & 1u;
-    ++uses[cur];
-    cur ^= 1;
   }
   if (have_prev && !aborted) finish_prev();
   if (aborted) {

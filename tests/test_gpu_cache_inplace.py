@@ -69,8 +69,9 @@ CASES = [  # (dtype, layers, batch, k, heads, max_len, len, head_dim)
 
 # LS_BEAM_DEBUG settings of the implementations: the plan's choice (the word kernel for short
 # slabs and k <= 8, bulk copies otherwise), the word kernel, bulk copies (with a workspace,
-# also with a fixed share of items per CTA) and the staged CTA kernel forced
-IMPLS = [None, "ipwords", "iptma", "iptma,ipstatic", "ipplain"]
+# also with a fixed share of items per CTA, and with items sized for one needed parent, so
+# that an item takes several steps) and the staged CTA kernel forced
+IMPLS = [None, "ipwords", "iptma", "iptma,ipstatic", "iptma,ipkeff=1", "ipplain"]
 
 
 def _with_env(env, fn):
