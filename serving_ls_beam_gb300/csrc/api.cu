@@ -51,13 +51,14 @@ struct Debug {
   int parts = 0;   // K1s strips per row, 0 = plan's choice
   int ipw = 0;     // in-place word kernel: words per item, 0 = plan's choice
   int ipkeff = 0;  // in-place bulk-copy kernel: parents an item is sized for, 0 = plan's choice
+  int ipstage = 0; // in-place bulk-copy kernel: bytes of each staging buffer, 0 = plan's choice
   int stage = -1;  // K2 after K0: 1 = stage the batch's slots, 0 = read them in place, -1 = plan
   bool check_ptrs = true;
 };
 
 // LS_BEAM_DEBUG: comma-separated "exact", "ipplain", "iptma", "ipwords", "ipstatic", "steprefresh", "chunk", "strips",
 // "fused", "nofused", "cluster", "nocluster", "spin=<ns>", "vpl=<4|8|16>", "stages=<2..8>", "parts=<n>", "ipw=<words>",
-// "ipkeff=<parents>", "stage=<0|1>", "nocheck".
+// "ipkeff=<parents>", "ipstage=<bytes>", "stage=<0|1>", "nocheck".
 Debug read_debug() {
   Debug d;
   const char* env = std::getenv("LS_BEAM_DEBUG");
@@ -84,6 +85,7 @@ Debug read_debug() {
     else if (!std::strncmp(tok, "parts=", 6)) d.parts = std::atoi(tok + 6);
     else if (!std::strncmp(tok, "ipw=", 4)) d.ipw = std::atoi(tok + 4);
     else if (!std::strncmp(tok, "ipkeff=", 7)) d.ipkeff = std::atoi(tok + 7);
+    else if (!std::strncmp(tok, "ipstage=", 8)) d.ipstage = std::atoi(tok + 8);
     else if (!std::strncmp(tok, "stage=", 6)) d.stage = std::atoi(tok + 6);
     else if (!std::strcmp(tok, "nocheck")) d.check_ptrs = false;
   }
@@ -219,12 +221,12 @@ int inplace_words_occupancy(DeviceInfo* di, int unit, int batch, int k) {
   return occ;
 }
 
-int inplace_tma_occupancy(DeviceInfo* di, int batch, int k) {
+int inplace_tma_occupancy(DeviceInfo* di, int stage_bytes, int batch, int k) {
   std::lock_guard<std::mutex> lk(g_mu);
-  const size_t smem = cache_inplace_tma_smem(batch, k);
+  const size_t smem = cache_inplace_tma_smem(stage_bytes, batch, k);
   if (di->inplace_tma_occ == 0 || di->inplace_tma_smem != smem) {
     int o = 0;
-    if (cache_inplace_tma_occupancy(batch, k, &o) != cudaSuccess || o < 1) return 0;
+    if (cache_inplace_tma_occupancy(stage_bytes, batch, k, &o) != cudaSuccess || o < 1) return 0;
     di->inplace_tma_occ = o;
     di->inplace_tma_smem = smem;
   }
@@ -816,9 +818,11 @@ ls_status ls_cache_refresh_inplace(void* cache, ls_dtype dtype, const int32_t* p
   }
   // bulk copies when every slab and tile is 16-byte aligned and the parents fit in shared memory
   const bool tma = unit == 16 && (long long)batch * k <= kIpTmaMaxParents && !(dbg.flags & kFlagPlainInplace);
-  const int occ = tma ? inplace_tma_occupancy(di, batch, k) : inplace_occupancy(di, unit);
+  const int tma_stage = dbg.ipstage >= 4096 && dbg.ipstage <= 64 * 1024 && dbg.ipstage % 16 == 0 ? dbg.ipstage : kIpTmaStage;
+  const int occ = tma ? inplace_tma_occupancy(di, tma_stage, batch, k) : inplace_occupancy(di, unit);
   if (occ < 1) return cuda_fail(cudaErrorUnknown);
-  const long long stage = tma ? kIpTmaStage : kIpStageBytes;
+  const long long stage = tma ? tma_stage : kIpStageBytes;
+  p.stage_bytes = tma_stage;
   const long long tile = (stage / k) / unit * unit;  // every row's tile fits one staging buffer
   p.tile_bytes = (int)(tile < slab_bytes ? tile : slab_bytes);
   // short slabs: an item of the bulk-copy kernel is as many heads of a (layer, batch) as fit a

@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(kIpThreads) cache_inplace_kernel(const Inplace
 // two-stage pipeline over its (layer, batch, head group, tile) items, a step at a time: the
 // bulk loads of the slabs step i needs are issued before the bulk stores of step i-1's changed
 // rows, so a copy in each direction is always in flight.  A step takes as many of the item's
-// heads as the slabs of the parents its batch actually needs fit a 32 KB buffer (the host
+// heads as the slabs of the parents its batch actually needs fit a buffer (the host
 // sizes items for a typical count of needed parents, not for all k).  Items differ in size (the rows a batch changes), so
 // with a work counter (p.work) a CTA takes its next item when it is ready for one: the CTAs
 // then finish together instead of with the sum of their items' sizes.  The last CTA to finish
@@ -154,7 +154,8 @@ __global__ void __launch_bounds__(32) cache_inplace_tma_kernel(const InplacePara
   extern __shared__ __align__(128) unsigned char tsm[];
   __shared__ __align__(8) unsigned long long bar[2];
   const int K = p.k, lane = threadIdx.x;
-  int* par_s = reinterpret_cast<int*>(tsm + 2 * (size_t)kIpTmaStage);
+  const int STAGE = p.stage_bytes;  // each of the two staging buffers
+  int* par_s = reinterpret_cast<int*>(tsm + 2 * (size_t)STAGE);
   grid_launch_dependents();
   grid_dependency_wait();  // the parents come from the beam step just before
   for (int i = lane; i < p.batch * K; i += 32) par_s[i] = __ldg(p.parent + i);
@@ -187,7 +188,7 @@ __global__ void __launch_bounds__(32) cache_inplace_tma_kernel(const InplacePara
       return;
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    const unsigned char* src = tsm + (size_t)pv_buf * kIpTmaStage;
+    const unsigned char* src = tsm + (size_t)pv_buf * STAGE;
     for (int j = 0; j < K; ++j) {
       if (!((pv_changed >> j) & 1ull)) continue;
       const int q = par_s[pv_b * K + j];
@@ -231,7 +232,7 @@ __global__ void __launch_bounds__(32) cache_inplace_tma_kernel(const InplacePara
     const int tb = (int)min((long long)p.tile_bytes, p.slab_bytes - t0);
     // a step moves as many of the item's heads as the needed parents' slabs fit a buffer
     const int nn = __popcll(needed);
-    const int hsub = max(1, min(hg, kIpTmaStage / (nn * tb)));
+    const int hsub = max(1, min(hg, STAGE / (nn * tb)));
     for (int hs = 0; hs < hg && !aborted; hs += hsub) {
       const int hn = min(hsub, hg - hs);
       unsigned char* base = p.cache + (size_t)l * p.layer_stride + (size_t)b * K * p.row_stride +
@@ -240,7 +241,7 @@ __global__ void __launch_bounds__(32) cache_inplace_tma_kernel(const InplacePara
       bulk_wait_read<0>();
       const uint32_t b_addr = smem_addr(&bar[cur]);
       mbar_arrive_expect_tx(b_addr, (uint32_t)(nn * hn * tb));
-      unsigned char* dst = tsm + (size_t)cur * kIpTmaStage;
+      unsigned char* dst = tsm + (size_t)cur * STAGE;
       int slot = 0;
       for (int q = 0; q < K; ++q) {
         if (!((needed >> q) & 1ull)) continue;
@@ -391,17 +392,17 @@ cudaError_t config_u(size_t smem, int* occ) {
 
 }  // namespace
 
-size_t cache_inplace_tma_smem(int batch, int k) {
-  return 2 * (size_t)kIpTmaStage + align_up((size_t)batch * k * sizeof(int32_t), 16);
+size_t cache_inplace_tma_smem(int stage_bytes, int batch, int k) {
+  return 2 * (size_t)stage_bytes + align_up((size_t)batch * k * sizeof(int32_t), 16);
 }
 
 cudaError_t launch_cache_inplace_tma(const InplaceParams& p, int grid, cudaStream_t stream) {
-  PdlLaunch l(dim3((unsigned)grid), dim3(32), cache_inplace_tma_smem(p.batch, p.k), stream);
+  PdlLaunch l(dim3((unsigned)grid), dim3(32), cache_inplace_tma_smem(p.stage_bytes, p.batch, p.k), stream);
   return cudaLaunchKernelEx(&l.cfg, cache_inplace_tma_kernel, p);
 }
 
-cudaError_t cache_inplace_tma_occupancy(int batch, int k, int* occ) {
-  const size_t smem = cache_inplace_tma_smem(batch, k);
+cudaError_t cache_inplace_tma_occupancy(int stage_bytes, int batch, int k, int* occ) {
+  const size_t smem = cache_inplace_tma_smem(stage_bytes, batch, k);
   cudaError_t e = cudaFuncSetAttribute(cache_inplace_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, cache_inplace_tma_kernel, 32, smem);

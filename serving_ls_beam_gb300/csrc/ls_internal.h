@@ -249,7 +249,7 @@ struct SampleParams {
 // In-place cache refresh (cache_inplace.cu): staging space per CTA of the plain kernel, per
 // stage of the bulk-copy kernel (two stages), and the parents the bulk-copy kernel stages.
 constexpr int kIpStageBytes = 48 * 1024;
-constexpr int kIpTmaStage = 32 * 1024;
+constexpr int kIpTmaStage = 32 * 1024;  // bulk-copy kernel: each of its two staging buffers (default)
 constexpr int kIpWorkOff = 64;  // byte offset of the bulk-copy kernel's work counter in a workspace
 constexpr int kIpTmaMaxParents = 8192;
 
@@ -263,6 +263,7 @@ struct InplaceParams {
   uint32_t* work;         // bulk-copy kernel: {next item, CTAs done}, zero between launches; or null
   int tile_bytes;         // positions staged at a time, in bytes (<= stage / k)
   int heads_per_item;     // bulk-copy kernel: heads of one (layer, batch) moved together
+  int stage_bytes;        // bulk-copy kernel: bytes of each of its two staging buffers
   int batch, k, heads, layers;
   long long units;        // layers * batch * heads
   // word kernel: an item is heads [h0, h0 + word_heads) of one (layer, batch); its words are
@@ -336,8 +337,8 @@ constexpr int kIpWordThreads = 256;
 cudaError_t launch_cache_inplace_words(const InplaceParams& p, int unit, int grid, cudaStream_t stream);
 // every batch's parents are staged in shared memory: batch * k <= kIpTmaMaxParents
 cudaError_t cache_inplace_words_occupancy(int unit, int batch, int k, int* occupancy);
-size_t cache_inplace_tma_smem(int batch, int k);
+size_t cache_inplace_tma_smem(int stage_bytes, int batch, int k);
 cudaError_t launch_cache_inplace_tma(const InplaceParams& p, int grid, cudaStream_t stream);
-cudaError_t cache_inplace_tma_occupancy(int batch, int k, int* occupancy);
+cudaError_t cache_inplace_tma_occupancy(int stage_bytes, int batch, int k, int* occupancy);
 
 }  // namespace lsb
