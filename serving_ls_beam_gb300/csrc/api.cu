@@ -789,16 +789,17 @@ ls_status ls_cache_refresh_inplace(void* cache, ls_dtype dtype, const int32_t* p
   p.layers = layers;
   p.units = units;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // short slabs (< 1 KB: the first decode steps) and k <= 8: the word kernel (a warp per
-  // item, a lane per word position), about 256 words per item.  Measured at c5 against the
-  // bulk-copy kernel: 9-15 us against 18-19 us at len 1-4, even at len 8, 10% slower from
-  // len 16 on.  Without bulk copies (unaligned slabs) it serves every length.
+  // short slabs (up to 2 KB: the first 16 decode steps at c5) and k <= 8: the word kernel (a
+  // warp per item, a lane per word position), about 256 words per item.  Measured at c5
+  // against the bulk-copy kernel, one launch: len 1-4 9-15 us against 18-19 us, len 8-10
+  // 27-33 us against 40-45 us, len 11-16 40-49 us against 43-51 us, about even at len 18-26.
+  // Without bulk copies (unaligned slabs) it serves every length.
   const long long slab_words = slab_bytes / unit;
   const bool words_fit = k <= kIpWordMaxK && (long long)heads * slab_words < (1ll << 31) &&
                          (long long)batch * k <= kIpTmaMaxParents;
   const bool tma_fit = unit == 16 && (long long)batch * k <= kIpTmaMaxParents;
   const bool words = words_fit && !(dbg.flags & (kFlagPlainInplace | kFlagTmaInplace)) &&
-                     (slab_bytes < 1024 || !tma_fit || (dbg.flags & kFlagWordInplace));
+                     (slab_bytes <= 2048 || !tma_fit || (dbg.flags & kFlagWordInplace));
   if (words) {
     long long wh = (dbg.ipw > 0 ? dbg.ipw : 256) / slab_words;
     wh = wh < 1 ? 1 : (wh > heads ? heads : wh);
