@@ -433,20 +433,26 @@ static ls_status beam_step_impl(const void* logits, ls_dtype logit_dtype, const 
 
   const int dtype = (int)logit_dtype;
   const long long rows = (long long)batch * k;
-  // K3 (the whole step of a batch in one CTA) when the batches fill the GPU by themselves and
-  // every strip's block maxima fit its shared memory
+  // K3 (the whole step of a batch in one CTA) when the batches fill the GPU by themselves, or
+  // when the rows are more than the cluster form runs in one wave (two CTAs per SM), and every
+  // strip's block maxima fit its shared memory
   int fu_parts = (kFuThreads / 32) / k;
   if (dbg.parts > 0 && dbg.parts * k <= kFuThreads / 32) fu_parts = dbg.parts;
   const int fu_vpl = (dtype == LS_DTYPE_F32 || bias) ? 4 : 8;
   const long long fu_ns = ((15 + (long long)vocab * es + 15) / 16 + 32ll * fu_vpl - 1) / (32ll * fu_vpl);
   const bool fused = !(dbg.flags & kFlagNoFused) && k <= kFuMaxK && fu_parts >= 1 &&
                      (fu_ns + fu_parts - 1) / fu_parts <= kFuMaxStages &&
-                     ((dbg.flags & kFlagFused) || 2ll * batch >= di->sms);
-  // otherwise K3's cluster form for k a power of two up to 8: a CTA (eight strips) per row,
-  // a batch's k CTAs one cluster
+                     ((dbg.flags & kFlagFused) || 2ll * batch >= di->sms || rows > 2ll * di->sms);
+  // otherwise K3's cluster form for k a power of two up to 8 (a CTA of eight strips per row, a
+  // batch's k CTAs one cluster) when the rows are at least a third of the SMs; fewer rows take
+  // the two-kernel path, whose strips spread a row over more warps.  One launch, f16 unless
+  // noted: 64 x 8 x 40000 K3 26.6 us, cluster 36.9 (two waves); 32 x 8 x 40000 cluster 22.5,
+  // K3 26.6, two kernels 32.8; 8 x 8 x 120000 f32 cluster 25.2, two kernels 41.6; 8 x 4 x 250000
+  // two kernels 22.6, cluster 24.6; 8 x 1 x 50257 two kernels 12.3, cluster 14.3
   constexpr int kClParts = kFuThreads / 32;
   const bool cluster = (!fused || (dbg.flags & kFlagCluster)) && !(dbg.flags & (kFlagNoFused | kFlagNoCluster)) &&
-                       k <= kFuMaxK && (k & (k - 1)) == 0 && (fu_ns + kClParts - 1) / kClParts <= kFuMaxStages;
+                       k <= kFuMaxK && (k & (k - 1)) == 0 && (fu_ns + kClParts - 1) / kClParts <= kFuMaxStages &&
+                       ((dbg.flags & kFlagCluster) || 3ll * rows >= di->sms);
   if (fused || cluster) {
     if (!fused_configured(di)) return cuda_fail(cudaErrorUnknown);
     unsigned char* ws = static_cast<unsigned char*>(workspace);
