@@ -44,7 +44,7 @@ extern "C" {
 typedef enum {
   LS_OK = 0,
   LS_ERR_INVALID_ARG = 1, /* bad argument, found on the host; nothing enqueued */
-  LS_ERR_UNSUPPORTED = 2, /* valid request outside what this build supports */
+  LS_ERR_UNSUPPORTED = 2, /* valid request outside what the library supports */
   LS_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
   LS_ERR_TIMEOUT = 4,     /* a bounded device wait ran out (reported by ls_read_status) */
   LS_ERR_INTERNAL = 5     /* device-detected inconsistency, e.g. a parent index out of range */
